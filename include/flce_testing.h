@@ -1,0 +1,45 @@
+/*
+ * flce_testing.h — test hook of the fused linear cross-entropy library.
+ *
+ * Not part of the loss API: it exposes the library's tcgen05 GEMM core so that
+ * each operand layout it uses (K-major and MN-major A and B, ragged tails) can
+ * be checked in isolation.  The paper pages have no counterpart; the GEMM is
+ * the "matmul with fp32 accumulation" step of the logit chain (TRL PR #6859,
+ * review, "verified" bullet 2) and of the gradient products.
+ *
+ * C[m, n] = sum_k A(m, k) * B(n, k), bf16 inputs, fp32 accumulation and output.
+ *   a_mn_major = 0: A is [M rows][K] with row stride lda (elements)
+ *   a_mn_major = 1: A is [K rows][M] with row stride lda
+ *   b_mn_major = 0: B is [N rows][K] with row stride ldb
+ *   b_mn_major = 1: B is [K rows][N] with row stride ldb
+ *   C is [M][N] fp32 with row stride ldc.
+ * Device pointers, 16-byte aligned; lda, ldb multiples of 8, ldc of 4.
+ * Asynchronous on `stream`.  Returns an FLCE_* status code.
+ */
+#ifndef FLCE_TESTING_H_
+#define FLCE_TESTING_H_
+
+#include "flce.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Process-wide override of two backward planning choices, for tests and tuning
+ * sweeps (0 restores the automatic choice):
+ *   chunk_cols  vocabulary columns per backward chunk (rounded up to 256)
+ *   dh_ksplit   K splits of the dh product, 1..16
+ * flce_workspace_size follows the override, so query it after setting.  Not
+ * thread-safe with respect to calls in flight on other threads.
+ */
+FLCE_API int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit);
+
+FLCE_API int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int64_t K, const void* A,
+                      int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc, flce_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_TESTING_H_ */

@@ -1,0 +1,555 @@
+// flce_api.cu — the C ABI: argument validation, workspace layout, tensor-map
+// encoding, tile/split planning and the launch sequence of the forward and
+// the backward.  Host code only; every step of the computation runs in the
+// kernels of flce_fwd.cu and flce_bwd.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "flce.h"
+#include "flce_launch.h"
+#include "flce_testing.h"
+
+namespace flce {
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr int kMaxSplits = 64;                     // forward vocabulary splits
+constexpr int kMaxKSplit = 16;                     // dh K splits
+constexpr size_t kGChunkBudget = size_t(1) << 30;  // bytes of the bf16 G chunk
+constexpr int kMaxDevices = 64;
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct DeviceInfo {
+  bool init = false;
+  int num_sms = 0;
+  int major = 0, minor = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_device(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FLCE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    d.init = true;
+  }
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return FLCE_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = d;
+  if (d.major != 10 || d.minor != 3) return FLCE_ERR_UNSUPPORTED_DEVICE;
+  return FLCE_OK;
+}
+
+// 2-D bf16 tensor map with 128-byte swizzle; out-of-range elements read as 0.
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+             uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FLCE_OK : FLCE_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int validate(const flce_problem* p) {
+  if (!p) return FLCE_ERR_INVALID_ARG;
+  if (p->n_tokens < 0 || p->n_tokens > INT32_MAX - 256) return FLCE_ERR_INVALID_ARG;
+  if (p->vocab < 1 || p->vocab > INT32_MAX - 256) return FLCE_ERR_INVALID_ARG;
+  if (p->hidden < 8 || p->hidden > (int64_t(1) << 20)) return FLCE_ERR_INVALID_ARG;
+  if (p->reduction < FLCE_RED_NONE || p->reduction > FLCE_RED_MEAN) return FLCE_ERR_INVALID_ARG;
+  if (!std::isfinite(p->logit_scale) || !std::isfinite(p->final_logit_softcapping)) return FLCE_ERR_INVALID_ARG;
+  if (p->hidden_dtype != FLCE_BF16 && p->hidden_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED_DTYPE;
+  if (p->weight_dtype != FLCE_BF16) {
+    if (p->weight_dtype == FLCE_F32 && p->hidden_dtype == FLCE_BF16) return FLCE_ERR_DTYPE_MISMATCH;
+    return FLCE_ERR_UNSUPPORTED_DTYPE;
+  }
+  if (p->hidden % 8 != 0) return FLCE_ERR_MISALIGNED;
+  return FLCE_OK;
+}
+
+int check_bias_dtype(const flce_problem* p, const void* bias) {
+  if (bias && p->bias_dtype != FLCE_BF16 && p->bias_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED_DTYPE;
+  return FLCE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout.  Sizes use upper bounds that do not depend on the SM
+// count, so flce_workspace_size needs no device.
+// ---------------------------------------------------------------------------
+struct Layout {
+  size_t status = 0;
+  size_t hi = 0, lo = 0;
+  size_t part_m = 0, part_s = 0, part_a = 0, part_best = 0, part_idx = 0, z_target = 0, blocks = 0;
+  size_t g = 0, dbias_part = 0, dh_part = 0;
+  size_t total = 0;
+  // backward geometry
+  int64_t vc = 0;        // vocabulary chunk width (multiple of 256) = row stride of G
+  int64_t n_chunks = 0;
+  int ksplit_max = 1;
+  bool need_dh_part = false;
+};
+
+// Test/tuning overrides (flce_testing_set_tuning); 0 = automatic.
+std::atomic<int64_t> g_force_chunk_cols{0};
+std::atomic<int> g_force_dh_ksplit{0};
+
+int64_t chunk_width(int64_t n_tokens, int64_t vocab) {
+  const int64_t forced = g_force_chunk_cols.load();
+  if (forced > 0) return std::min(cdiv(forced, kBN) * kBN, cdiv(vocab, kBN) * kBN);
+  const int64_t rows = std::max<int64_t>(1, n_tokens);
+  int64_t vc_max = static_cast<int64_t>(kGChunkBudget / (static_cast<size_t>(rows) * 2));
+  vc_max = std::max<int64_t>(kBN, vc_max / kBN * kBN);
+  // At least two chunks whenever the vocabulary spans more than one tile, so
+  // that the G scratch never holds the whole (tokens x vocab) matrix.
+  const int64_t n_chunks = std::max<int64_t>(cdiv(vocab, vc_max), vocab > kBN ? 2 : 1);
+  return cdiv(cdiv(vocab, n_chunks), kBN) * kBN;
+}
+
+int dh_ksplit_bound(int64_t n_tokens, int64_t hidden, int64_t vc) {
+  const int forced = g_force_dh_ksplit.load();
+  if (forced > 0) return std::min(forced, kMaxKSplit);
+  const int64_t tiles = cdiv(n_tokens, kBM) * cdiv(hidden, kBN);
+  if (tiles >= 128) return 1;
+  const int64_t kb = cdiv(vc, kBK);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxKSplit, kb / 8)));
+}
+
+Layout make_layout(const flce_problem* p, bool backward, bool has_bias) {
+  Layout L;
+  const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
+  size_t off = 256;  // status word + padding
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  if (p->hidden_dtype == FLCE_F32) {
+    L.hi = take(size_t(N) * D * 2);
+    L.lo = take(size_t(N) * D * 2);
+  }
+  if (!backward) {
+    const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN));
+    const size_t part = size_t(splits) * N * 4;
+    L.part_m = take(part);
+    L.part_s = take(part);
+    L.part_a = take(part);
+    L.part_best = take(part);
+    L.part_idx = take(part);
+    L.z_target = take(size_t(N) * 4);
+    L.blocks = take(size_t(cdiv(N, kMergeThreads)) * sizeof(BlockPartial));
+  } else {
+    L.vc = chunk_width(N, V);
+    L.n_chunks = cdiv(V, L.vc);
+    L.ksplit_max = dh_ksplit_bound(N, D, L.vc);
+    L.g = take(size_t(N) * L.vc * 2);
+    if (has_bias) L.dbias_part = take(size_t(cdiv(N, kBM)) * L.vc * 4);
+    L.need_dh_part = L.n_chunks > 1 || L.ksplit_max > 1;
+    if (L.need_dh_part) L.dh_part = take(size_t(L.ksplit_max) * N * D * 4);
+  }
+  L.total = off;
+  return L;
+}
+
+GemmSched base_sched(int64_t m_rows, int64_t n_cols, int64_t k, int nseg, int seg_a) {
+  GemmSched s{};
+  s.m_tiles = static_cast<int32_t>(cdiv(m_rows, kBM));
+  s.n_tiles = static_cast<int32_t>(cdiv(n_cols, kBN));
+  s.k_blocks = static_cast<int32_t>(cdiv(k, kBK));
+  s.nseg = nseg;
+  s.seg_a = seg_a;
+  s.ksplit = 1;
+  s.kb_per_split = s.k_blocks;
+  s.n_per_unit = 1;
+  s.n_units = s.n_tiles;
+  s.group_m = 1;
+  return s;
+}
+
+void finish_sched(GemmSched& s) {
+  s.n_units = static_cast<int32_t>(cdiv(s.n_tiles, s.n_per_unit));
+  s.group_m = std::max(1, std::min(s.group_m, s.m_tiles));
+  s.total_units = s.m_tiles * s.n_units * s.ksplit;
+}
+
+// Forward vocabulary split: the split count (<= kMaxSplits) that best fills
+// the SMs with equal units; ties go to fewer splits.
+int choose_splits(int64_t m_tiles, int64_t n_tiles, int num_sms, int* per_unit) {
+  double best_eff = -1.0;
+  int best_s = 1, best_per = static_cast<int>(n_tiles);
+  const int64_t max_s = std::min<int64_t>(kMaxSplits, n_tiles);
+  for (int64_t s = 1; s <= max_s; ++s) {
+    const int64_t per = cdiv(n_tiles, s);
+    const int64_t splits = cdiv(n_tiles, per);
+    if (splits != s) continue;
+    const int64_t units = m_tiles * splits;
+    const int64_t waves = cdiv(units, num_sms);
+    const double eff = double(m_tiles * n_tiles) / double(waves * num_sms * per);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best_s = static_cast<int>(s);
+      best_per = static_cast<int>(per);
+    }
+  }
+  *per_unit = best_per;
+  return best_s;
+}
+
+int fail(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
+
+#define FLCE_TRY(expr)               \
+  do {                               \
+    const int rc_ = (expr);          \
+    if (rc_ != FLCE_OK) return rc_;  \
+  } while (0)
+
+}  // namespace
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+int flce_abi_version(void) { return kAbiVersion; }
+
+const char* flce_status_string(int status) {
+  switch (status) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_INVALID_ARG: return "invalid argument";
+    case FLCE_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case FLCE_ERR_DTYPE_MISMATCH: return "hidden and weight dtypes do not match";
+    case FLCE_ERR_MISALIGNED: return "misaligned pointer or hidden size not a multiple of 8";
+    case FLCE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FLCE_ERR_CUDA: return "CUDA runtime error";
+    case FLCE_ERR_TARGET_OUT_OF_RANGE: return "a target is outside [0, vocab) and is not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    case FLCE_ERR_UNSUPPORTED_DEVICE: return "the current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+int flce_workspace_size(const flce_problem* problem, int for_backward, size_t* bytes) {
+  if (!bytes) return FLCE_ERR_INVALID_ARG;
+  FLCE_TRY(validate(problem));
+  // The bias-dependent part is included whenever a bias could be passed.
+  *bytes = make_layout(problem, for_backward != 0, true).total;
+  return FLCE_OK;
+}
+
+int flce_read_device_status(const void* workspace, flce_stream_t stream, int* status) {
+  if (!workspace || !status) return FLCE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_CUDA;
+  *status = v;
+  return FLCE_OK;
+}
+
+int flce_forward(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
+                 const int64_t* targets, float* loss, float* lse, float* entropy, int64_t* correct,
+                 int64_t* n_valid, float* entropy_sum, void* workspace, size_t workspace_bytes,
+                 flce_stream_t stream) {
+  FLCE_TRY(validate(p));
+  FLCE_TRY(check_bias_dtype(p, bias));
+  const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
+  if (!weight || !loss || !correct || !n_valid || !entropy_sum || !workspace) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!hidden || !targets || !lse)) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(weight, 16) || (N > 0 && !aligned(hidden, 16)) || !aligned(workspace, 256) ||
+      (targets && !aligned(targets, 8)))
+    return FLCE_ERR_MISALIGNED;
+  const Layout L = make_layout(p, false, true);
+  if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  FLCE_TRY(get_device(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
+
+  BlockPartial* blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
+  ReduceParams rp{};
+  rp.blocks = blocks;
+  rp.n_blocks = static_cast<int32_t>(cdiv(N, kMergeThreads));
+  rp.reduction = p->reduction;
+  rp.loss = loss;
+  rp.correct = correct;
+  rp.n_valid = n_valid;
+  rp.entropy_sum = entropy_sum;
+  if (N == 0) return fail(launch_fwd_reduce(rp, st));
+
+  const bool h32 = p->hidden_dtype == FLCE_F32;
+  const void* a_main = hidden;
+  if (h32) {
+    uint16_t* hi = reinterpret_cast<uint16_t*>(ws + L.hi);
+    uint16_t* lo = reinterpret_cast<uint16_t*>(ws + L.lo);
+    FLCE_TRY(fail(launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st)));
+    a_main = hi;
+  }
+  TmaMaps maps;
+  FLCE_TRY(make_map(&maps.a0, a_main, D, N, D * 2, kBK, kBM));
+  maps.a1 = maps.a0;
+  if (h32) FLCE_TRY(make_map(&maps.a1, ws + L.lo, D, N, D * 2, kBK, kBM));
+  FLCE_TRY(make_map(&maps.b0, weight, D, V, D * 2, kBK, kBN));
+  maps.b1 = maps.b0;
+
+  GemmSched sc = base_sched(N, V, D, h32 ? 2 : 1, 1);
+  int per_unit = 1;
+  const int splits = choose_splits(sc.m_tiles, sc.n_tiles, dev.num_sms, &per_unit);
+  sc.n_per_unit = per_unit;
+  sc.group_m = 32;
+  finish_sched(sc);
+
+  const bool softcap = p->final_logit_softcapping > 0.f;
+  FwdParams fp{};
+  fp.n_tokens = N;
+  fp.vocab = V;
+  fp.bias = bias;
+  fp.bias_f32 = p->bias_dtype == FLCE_F32;
+  fp.n_splits = splits;
+  fp.scale = p->logit_scale;
+  fp.softcap = softcap ? p->final_logit_softcapping : 0.f;
+  fp.inv_softcap = softcap ? 1.f / p->final_logit_softcapping : 0.f;
+  fp.ignore_index = p->ignore_index;
+  fp.targets = targets;
+  fp.part_m = reinterpret_cast<float*>(ws + L.part_m);
+  fp.part_s = reinterpret_cast<float*>(ws + L.part_s);
+  fp.part_a = reinterpret_cast<float*>(ws + L.part_a);
+  fp.part_best = reinterpret_cast<float*>(ws + L.part_best);
+  fp.part_idx = reinterpret_cast<int32_t*>(ws + L.part_idx);
+  fp.z_target = reinterpret_cast<float*>(ws + L.z_target);
+  const int grid = std::min(sc.total_units, dev.num_sms);
+  FLCE_TRY(fail(launch_fwd_gemm(bias != nullptr, softcap, maps, sc, fp, status, grid, st)));
+
+  MergeParams mp{};
+  mp.n_tokens = N;
+  mp.vocab = V;
+  mp.n_splits = splits;
+  mp.reduction = p->reduction;
+  mp.ignore_index = p->ignore_index;
+  mp.part_m = fp.part_m;
+  mp.part_s = fp.part_s;
+  mp.part_a = fp.part_a;
+  mp.part_best = fp.part_best;
+  mp.part_idx = fp.part_idx;
+  mp.z_target = fp.z_target;
+  mp.targets = targets;
+  mp.lse = lse;
+  mp.entropy = entropy;
+  mp.loss_tok = p->reduction == FLCE_RED_NONE ? loss : nullptr;
+  mp.blocks = blocks;
+  FLCE_TRY(fail(launch_fwd_merge(mp, status, st)));
+  return fail(launch_fwd_reduce(rp, st));
+}
+
+int flce_backward(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
+                  const int64_t* targets, const float* lse, const int64_t* n_valid, const float* dloss,
+                  void* dhidden, void* dweight, void* dbias, void* workspace, size_t workspace_bytes,
+                  flce_stream_t stream) {
+  FLCE_TRY(validate(p));
+  FLCE_TRY(check_bias_dtype(p, bias));
+  const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
+  if (!weight || !dweight || !workspace || !n_valid || !dloss) return FLCE_ERR_INVALID_ARG;
+  if ((bias == nullptr) != (dbias == nullptr)) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!hidden || !targets || !lse || !dhidden)) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(weight, 16) || !aligned(dweight, 16) || !aligned(workspace, 256) ||
+      (N > 0 && (!aligned(hidden, 16) || !aligned(dhidden, 16))) || (targets && !aligned(targets, 8)))
+    return FLCE_ERR_MISALIGNED;
+  const Layout L = make_layout(p, true, true);
+  if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  FLCE_TRY(get_device(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  const size_t bias_elem = p->bias_dtype == FLCE_F32 ? 4 : 2;
+  if (N == 0) {
+    FLCE_TRY(fail(cudaMemsetAsync(dweight, 0, size_t(V) * D * 2, st)));
+    if (dbias) FLCE_TRY(fail(cudaMemsetAsync(dbias, 0, size_t(V) * bias_elem, st)));
+    return FLCE_OK;
+  }
+
+  const bool h32 = p->hidden_dtype == FLCE_F32;
+  const void* h_main = hidden;
+  if (h32) {
+    uint16_t* hi = reinterpret_cast<uint16_t*>(ws + L.hi);
+    uint16_t* lo = reinterpret_cast<uint16_t*>(ws + L.lo);
+    FLCE_TRY(fail(launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st)));
+    h_main = hi;
+  }
+  const bool softcap = p->final_logit_softcapping > 0.f;
+  uint16_t* g = reinterpret_cast<uint16_t*>(ws + L.g);
+  float* dbias_part = bias ? reinterpret_cast<float*>(ws + L.dbias_part) : nullptr;
+  float* dh_part = L.need_dh_part ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
+
+  // Maps that do not change across chunks.
+  TmaMaps rec;  // recompute: A = h (K-major), B = W (K-major)
+  FLCE_TRY(make_map(&rec.a0, h_main, D, N, D * 2, kBK, kBM));
+  rec.a1 = rec.a0;
+  if (h32) FLCE_TRY(make_map(&rec.a1, ws + L.lo, D, N, D * 2, kBK, kBM));
+  FLCE_TRY(make_map(&rec.b0, weight, D, V, D * 2, kBK, kBN));
+  rec.b1 = rec.b0;
+  CUtensorMap h_mn, lo_mn, w_mn;  // MN-major views: h for dW, W for dh
+  FLCE_TRY(make_map(&h_mn, h_main, D, N, D * 2, 64, kBK));
+  lo_mn = h_mn;
+  if (h32) FLCE_TRY(make_map(&lo_mn, ws + L.lo, D, N, D * 2, 64, kBK));
+  FLCE_TRY(make_map(&w_mn, weight, D, V, D * 2, 64, kBK));
+
+  // dh K split for this device (bounded by the layout's slot count).
+  const int64_t dh_tiles = cdiv(N, kBM) * cdiv(D, kBN);
+  int ksplit = 1;
+  if (g_force_dh_ksplit.load() > 0) {
+    ksplit = L.ksplit_max;
+  } else if (L.ksplit_max > 1) {
+    ksplit = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(L.ksplit_max, dev.num_sms / dh_tiles)));
+  }
+
+  for (int64_t c = 0; c < L.n_chunks; ++c) {
+    const int64_t v0 = c * L.vc;
+    const int64_t width = std::min<int64_t>(L.vc, V - v0);
+    const bool first = c == 0, last = c == L.n_chunks - 1;
+
+    // (1) recompute the logits of the chunk and form G (bf16) + dbias partials
+    GemmSched s1 = base_sched(N, width, D, h32 ? 2 : 1, 1);
+    s1.b_mn_off = static_cast<int32_t>(v0);
+    s1.group_m = 32;
+    finish_sched(s1);
+    GradParams gp{};
+    gp.n_tokens = N;
+    gp.vocab = V;
+    gp.v0 = v0;
+    gp.bias = bias;
+    gp.bias_f32 = p->bias_dtype == FLCE_F32;
+    gp.reduction = p->reduction;
+    gp.scale = p->logit_scale;
+    gp.softcap = softcap ? p->final_logit_softcapping : 0.f;
+    gp.inv_softcap = softcap ? 1.f / p->final_logit_softcapping : 0.f;
+    gp.ignore_index = p->ignore_index;
+    gp.targets = targets;
+    gp.lse = lse;
+    gp.dloss = dloss;
+    gp.n_valid = n_valid;
+    gp.g = g;
+    gp.ldg = L.vc;
+    gp.dbias_part = dbias_part;
+    FLCE_TRY(fail(launch_grad_gemm(bias != nullptr, softcap, rec, s1, gp, status,
+                                   std::min(s1.total_units, dev.num_sms), st)));
+    if (bias) {
+      FLCE_TRY(fail(launch_dbias_reduce(dbias_part, L.vc, s1.m_tiles, width,
+                                        static_cast<uint8_t*>(dbias) + v0 * bias_elem,
+                                        p->bias_dtype == FLCE_F32, st)));
+    }
+
+    // (2) dW[v0 : v0+width] = G^T h    (A = G MN-major, B = h MN-major, K = N)
+    TmaMaps mw;
+    FLCE_TRY(make_map(&mw.a0, g, width, N, L.vc * 2, 64, kBK));
+    mw.a1 = mw.a0;
+    mw.b0 = h_mn;
+    mw.b1 = lo_mn;
+    GemmSched s2 = base_sched(width, D, N, h32 ? 2 : 1, 0);
+    s2.a_mn = 1;
+    s2.b_mn = 1;
+    s2.group_m = std::max(1, dev.num_sms / std::max(1, s2.n_tiles));
+    finish_sched(s2);
+    StoreParams sp{};
+    sp.rows = width;
+    sp.cols = D;
+    sp.out = static_cast<uint8_t*>(dweight) + size_t(v0) * D * 2;
+    sp.ldo = D;
+    sp.out_f32 = 0;
+    FLCE_TRY(fail(launch_store_gemm(mw, s2, sp, status, std::min(s2.total_units, dev.num_sms), st)));
+
+    // (3) dh (+)= G W[v0 : v0+width]   (A = G K-major, B = W MN-major, K = width)
+    TmaMaps mh;
+    FLCE_TRY(make_map(&mh.a0, g, width, N, L.vc * 2, kBK, kBM));
+    mh.a1 = mh.a0;
+    mh.b0 = w_mn;
+    mh.b1 = w_mn;
+    GemmSched s3 = base_sched(N, D, width, 1, 0);
+    s3.b_mn = 1;
+    s3.b_k_off = static_cast<int32_t>(v0);
+    s3.ksplit = ksplit;
+    s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
+    s3.group_m = std::max(1, dev.num_sms / std::max(1, s3.n_tiles * ksplit));
+    finish_sched(s3);
+    AccumParams ap{};
+    ap.rows = N;
+    ap.cols = D;
+    ap.part = dh_part;
+    ap.part_stride = N * D;
+    ap.accumulate = first ? 0 : 1;
+    ap.write_final = (ksplit == 1 && last) ? 1 : 0;
+    ap.out = dhidden;
+    ap.out_f32 = h32 ? 1 : 0;
+    FLCE_TRY(fail(launch_accum_gemm(mh, s3, ap, status, std::min(s3.total_units, dev.num_sms), st)));
+  }
+  if (ksplit > 1) {
+    FLCE_TRY(fail(launch_dh_finalize(dh_part, N * D, ksplit, N * D, dhidden, h32 ? 1 : 0, dev.num_sms * 4, st)));
+  }
+  return FLCE_OK;
+}
+
+int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit) {
+  if (chunk_cols < 0 || dh_ksplit < 0 || dh_ksplit > kMaxKSplit) return FLCE_ERR_INVALID_ARG;
+  g_force_chunk_cols.store(chunk_cols);
+  g_force_dh_ksplit.store(dh_ksplit);
+  return FLCE_OK;
+}
+
+int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, float* C, int64_t ldc, flce_stream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C) return FLCE_ERR_INVALID_ARG;
+  if (lda % 8 || ldb % 8 || ldc % 4 || !aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16))
+    return FLCE_ERR_MISALIGNED;
+  DeviceInfo dev;
+  FLCE_TRY(get_device(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  TmaMaps m;
+  if (!a_mn_major) FLCE_TRY(make_map(&m.a0, A, K, M, lda * 2, kBK, kBM));
+  else FLCE_TRY(make_map(&m.a0, A, M, K, lda * 2, 64, kBK));
+  if (!b_mn_major) FLCE_TRY(make_map(&m.b0, B, K, N, ldb * 2, kBK, kBN));
+  else FLCE_TRY(make_map(&m.b0, B, N, K, ldb * 2, 64, kBK));
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  GemmSched s = base_sched(M, N, K, 1, 0);
+  s.a_mn = a_mn_major ? 1 : 0;
+  s.b_mn = b_mn_major ? 1 : 0;
+  finish_sched(s);
+  StoreParams sp{};
+  sp.rows = M;
+  sp.cols = N;
+  sp.out = C;
+  sp.ldo = ldc;
+  sp.out_f32 = 1;
+  return fail(launch_store_gemm(m, s, sp, nullptr, std::min(s.total_units, dev.num_sms), st));
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// flce_bwd.cu — backward kernels: the recompute GEMM with the logit-gradient
+// epilogue (four variants: bias x soft cap), the dW store GEMM, the dh
+// accumulate GEMM, the ordered dbias reduction and the dh K-split finalize.
+#include <cuda_runtime.h>
+
+#include "flce_gemm.cuh"
+#include "flce_launch.h"
+
+namespace flce {
+
+template <class Epi>
+static cudaError_t launch_gemm_impl(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
+                                    int* status, int grid, cudaStream_t stream) {
+  auto kern = gemm_kernel<Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, kGemmSmemBytes, stream>>>(m.a0, m.a1, m.b0, m.b1, sc, p, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_gemm(bool bias, bool softcap, const TmaMaps& maps, const GemmSched& sc,
+                             const GradParams& p, int* status, int grid, cudaStream_t stream) {
+  if (bias && softcap) return launch_gemm_impl<EpiGrad<true, true>>(maps, sc, p, status, grid, stream);
+  if (bias) return launch_gemm_impl<EpiGrad<true, false>>(maps, sc, p, status, grid, stream);
+  if (softcap) return launch_gemm_impl<EpiGrad<false, true>>(maps, sc, p, status, grid, stream);
+  return launch_gemm_impl<EpiGrad<false, false>>(maps, sc, p, status, grid, stream);
+}
+
+cudaError_t launch_store_gemm(const TmaMaps& maps, const GemmSched& sc, const StoreParams& p, int* status,
+                              int grid, cudaStream_t stream) {
+  return launch_gemm_impl<EpiStore>(maps, sc, p, status, grid, stream);
+}
+
+cudaError_t launch_accum_gemm(const TmaMaps& maps, const GemmSched& sc, const AccumParams& p, int* status,
+                              int grid, cudaStream_t stream) {
+  return launch_gemm_impl<EpiAccum>(maps, sc, p, status, grid, stream);
+}
+
+// dbias[j] = sum over m tiles of the per-tile column sums, in m order.
+__global__ void dbias_reduce_kernel(const float* __restrict__ part, int64_t ldg, int m_tiles, int64_t cols,
+                                    void* dbias, int bias_f32) {
+  const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (j >= cols) return;
+  float s = 0.f;
+  for (int m = 0; m < m_tiles; ++m) s += part[static_cast<int64_t>(m) * ldg + j];
+  if (bias_f32) {
+    reinterpret_cast<float*>(dbias)[j] = s;
+  } else {
+    reinterpret_cast<uint16_t*>(dbias)[j] = static_cast<uint16_t>(pack_bf16x2(s, 0.f) & 0xFFFFu);
+  }
+}
+
+cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int64_t cols, void* dbias,
+                                int bias_f32, cudaStream_t stream) {
+  const int64_t blocks = (cols + 255) / 256;
+  if (blocks == 0) return cudaSuccess;
+  dbias_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, ldg, m_tiles, cols, dbias, bias_f32);
+  return cudaGetLastError();
+}
+
+// dh = sum over K-split slots, in slot order, cast to the output dtype.
+__global__ void dh_finalize_kernel(const float4* __restrict__ part, int64_t stride4, int ksplit, int64_t n4,
+                                   void* out, int out_f32) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 s = part[i];
+    for (int k = 1; k < ksplit; ++k) {
+      const float4 o = part[k * stride4 + i];
+      s.x += o.x;
+      s.y += o.y;
+      s.z += o.z;
+      s.w += o.w;
+    }
+    if (out_f32) {
+      reinterpret_cast<float4*>(out)[i] = s;
+    } else {
+      reinterpret_cast<uint2*>(out)[i] = make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+    }
+  }
+}
+
+cudaError_t launch_dh_finalize(const float* part, int64_t stride, int ksplit, int64_t n, void* out, int out_f32,
+                               int grid, cudaStream_t stream) {
+  dh_finalize_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(part), stride / 4, ksplit, n / 4,
+                                               out, out_f32);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

@@ -1,0 +1,186 @@
+// flce_fwd.cu — forward kernels: the logit GEMM with the online-statistics
+// epilogue (four variants: bias x soft cap), the split-partial merge, the final
+// deterministic reduction, and the fp32-hidden hi/lo split.
+#include <cuda_runtime.h>
+
+#include "flce_gemm.cuh"
+#include "flce_launch.h"
+
+namespace flce {
+
+template <class Epi>
+static cudaError_t launch_gemm_impl(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
+                                    int* status, int grid, cudaStream_t stream) {
+  auto kern = gemm_kernel<Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, kGemmSmemBytes, stream>>>(m.a0, m.a1, m.b0, m.b1, sc, p, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_gemm(bool bias, bool softcap, const TmaMaps& maps, const GemmSched& sc,
+                            const FwdParams& p, int* status, int grid, cudaStream_t stream) {
+  if (bias && softcap) return launch_gemm_impl<EpiFwd<true, true>>(maps, sc, p, status, grid, stream);
+  if (bias) return launch_gemm_impl<EpiFwd<true, false>>(maps, sc, p, status, grid, stream);
+  if (softcap) return launch_gemm_impl<EpiFwd<false, true>>(maps, sc, p, status, grid, stream);
+  return launch_gemm_impl<EpiFwd<false, false>>(maps, sc, p, status, grid, stream);
+}
+
+// ---------------------------------------------------------------------------
+// fp32 hidden -> bf16 hi + bf16 lo, hi = rn(h), lo = rn(h - hi).  hi + lo
+// carries about 16 bits of the 24-bit mantissa.
+// ---------------------------------------------------------------------------
+__global__ void split_hidden_kernel(const float4* __restrict__ h, uint2* __restrict__ hi, uint2* __restrict__ lo,
+                                    int64_t n4) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 x = h[i];
+    const uint32_t h01 = pack_bf16x2(x.x, x.y);
+    const uint32_t h23 = pack_bf16x2(x.z, x.w);
+    const float r0 = x.x - __uint_as_float(h01 << 16);
+    const float r1 = x.y - __uint_as_float(h01 & 0xFFFF0000u);
+    const float r2 = x.z - __uint_as_float(h23 << 16);
+    const float r3 = x.w - __uint_as_float(h23 & 0xFFFF0000u);
+    hi[i] = make_uint2(h01, h23);
+    lo[i] = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
+  }
+}
+
+cudaError_t launch_split_hidden(const float* h, uint16_t* hi, uint16_t* lo, int64_t n, int grid,
+                                cudaStream_t stream) {
+  const int64_t n4 = n / 4;
+  split_hidden_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(h), reinterpret_cast<uint2*>(hi),
+                                                reinterpret_cast<uint2*>(lo), n4);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Merge of the split partials (one thread per token) and block partial sums.
+//   M = max_s m_s, S = sum_s s_s e^(m_s - M), A = sum_s a_s e^(m_s - M)
+//   lse = M + ln S, sum p z = A / S, entropy = lse - A / S
+//   argmax: largest best_s, the earliest split on ties (lowest index)
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p, int* status) {
+  const int64_t row = blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x;
+  double loss_d = 0.0, ent_d = 0.0;
+  long long corr = 0, val = 0;
+  if (row < p.n_tokens) {
+    const int64_t N = p.n_tokens;
+    float M = -INFINITY;
+    for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, p.part_m[s * N + row]);
+    float S = 0.f, A = 0.f, best = -INFINITY;
+    int32_t best_idx = 0;
+    for (int s = 0; s < p.n_splits; ++s) {
+      const float ms = p.part_m[s * N + row];
+      const float f = expf(ms - M);
+      S = fmaf(p.part_s[s * N + row], f, S);
+      A = fmaf(p.part_a[s * N + row], f, A);
+      const float b = p.part_best[s * N + row];
+      if (b > best) {
+        best = b;
+        best_idx = p.part_idx[s * N + row];
+      }
+    }
+    const float lse = M + logf(S);
+    const float ent = lse - A / S;
+    const int64_t t = p.targets[row];
+    const bool in_range = t >= 0 && t < p.vocab;
+    const bool valid = in_range && t != p.ignore_index;
+    if (t != p.ignore_index && !in_range) atomicCAS(status, 0, kStatusTargetOutOfRange);
+    const float loss = valid ? lse - p.z_target[row] : 0.f;
+    p.lse[row] = lse;
+    if (p.entropy) p.entropy[row] = ent;
+    if (p.loss_tok) p.loss_tok[row] = loss;
+    loss_d = loss;
+    ent_d = valid ? ent : 0.0;
+    corr = (valid && best_idx == t) ? 1 : 0;
+    val = valid ? 1 : 0;
+  }
+  __shared__ double s_loss[kMergeThreads / 32], s_ent[kMergeThreads / 32];
+  __shared__ long long s_corr[kMergeThreads / 32], s_val[kMergeThreads / 32];
+  loss_d = warp_sum(loss_d);
+  ent_d = warp_sum(ent_d);
+  corr = warp_sum(corr);
+  val = warp_sum(val);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    s_loss[w] = loss_d;
+    s_ent[w] = ent_d;
+    s_corr[w] = corr;
+    s_val[w] = val;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    BlockPartial bp{0.0, 0.0, 0, 0};
+    for (int i = 0; i < kMergeThreads / 32; ++i) {
+      bp.loss += s_loss[i];
+      bp.entropy += s_ent[i];
+      bp.correct += s_corr[i];
+      bp.valid += s_val[i];
+    }
+    p.blocks[blockIdx.x] = bp;
+  }
+}
+
+cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream) {
+  const int64_t blocks = (p.n_tokens + kMergeThreads - 1) / kMergeThreads;
+  if (blocks == 0) return cudaSuccess;
+  fwd_merge_kernel<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(p, status);
+  return cudaGetLastError();
+}
+
+// Final scalars from the block partials, in a fixed order (one block).
+__global__ void __launch_bounds__(256) fwd_reduce_kernel(ReduceParams p) {
+  double loss_d = 0.0, ent_d = 0.0;
+  long long corr = 0, val = 0;
+  for (int i = threadIdx.x; i < p.n_blocks; i += blockDim.x) {
+    const BlockPartial b = p.blocks[i];
+    loss_d += b.loss;
+    ent_d += b.entropy;
+    corr += b.correct;
+    val += b.valid;
+  }
+  __shared__ double s_loss[8], s_ent[8];
+  __shared__ long long s_corr[8], s_val[8];
+  loss_d = warp_sum(loss_d);
+  ent_d = warp_sum(ent_d);
+  corr = warp_sum(corr);
+  val = warp_sum(val);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    s_loss[w] = loss_d;
+    s_ent[w] = ent_d;
+    s_corr[w] = corr;
+    s_val[w] = val;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double L = 0.0, E = 0.0;
+    long long C = 0, V = 0;
+    for (int i = 0; i < 8; ++i) {
+      L += s_loss[i];
+      E += s_ent[i];
+      C += s_corr[i];
+      V += s_val[i];
+    }
+    if (p.reduction == 2) p.loss[0] = V > 0 ? static_cast<float>(L / static_cast<double>(V)) : 0.f;
+    if (p.reduction == 1) p.loss[0] = static_cast<float>(L);
+    p.correct[0] = C;
+    p.n_valid[0] = V;
+    p.entropy_sum[0] = static_cast<float>(E);
+  }
+}
+
+cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream) {
+  fwd_reduce_kernel<<<1, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

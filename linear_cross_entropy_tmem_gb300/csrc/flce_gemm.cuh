@@ -1,0 +1,668 @@
+// flce_gemm.cuh — the persistent, warp-specialised tcgen05 GEMM that every
+// product of the fused linear cross-entropy runs on, and its epilogues.
+//
+//   warp 4      TMA producer: fills a 4-stage shared-memory ring with 128-byte
+//               swizzled bf16 tiles of A (128 x 64) and B (256 x 64).
+//   warp 5      MMA issuer: one elected thread issues tcgen05.mma (M=128,
+//               N=256, K=16) into one of two TMEM accumulators (2 x 256 fp32
+//               columns) and commits stage releases / accumulator-ready
+//               signals to mbarriers.  The whole warp owns the TMEM allocation.
+//   warps 0-3   epilogue: thread i owns TMEM lane i (one output row), reads 32
+//               columns at a time with tcgen05.ld and runs the epilogue policy
+//               while the MMA of the next tile fills the other accumulator.
+//
+// Epilogue policies:
+//   EpiFwd    logits -> bias, scale, soft cap -> online (max, sum exp,
+//             sum exp*z, argmax, target logit) per token across a vocabulary
+//             split; one partial record per (split, token).
+//   EpiGrad   recomputed logits -> G = w_n (softmax - onehot) dz/dacc in bf16
+//             for one vocabulary chunk, plus per-tile dbias column sums.
+//   EpiStore  accumulator -> bf16 / fp32 store (dW; the test GEMM).
+//   EpiAccum  accumulator -> fp32 K-split slot (=, +=) or the final dh store.
+//
+// Every wait is bounded (see mbar_wait); a role that gives up raises a
+// CTA-wide abort flag, the others stop at their next wait, in-flight copies
+// and MMAs are drained, TMEM is freed and the kernel returns with
+// FLCE_ERR_TIMEOUT in the device status word.
+#pragma once
+
+#include <cuda.h>
+#include <cfloat>
+
+#include "flce_device.cuh"
+#include "flce_internal.h"
+
+namespace flce {
+
+struct Unit {
+  int m_blk, n_unit, n_first, n_count, kb_first, kb_count, ks;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u) {
+  const int per_m = sc.n_units * sc.ksplit;
+  const int per_group = sc.group_m * per_m;
+  const int g = u / per_group;
+  const int r = u - g * per_group;
+  const int m0 = g * sc.group_m;
+  const int gm = min(sc.group_m, sc.m_tiles - m0);
+  const int m_local = r % gm;
+  const int rest = r / gm;
+  Unit t;
+  t.m_blk = m0 + m_local;
+  t.ks = rest % sc.ksplit;
+  t.n_unit = rest / sc.ksplit;
+  t.n_first = t.n_unit * sc.n_per_unit;
+  t.n_count = min(sc.n_per_unit, sc.n_tiles - t.n_first);
+  t.kb_first = t.ks * sc.kb_per_split;
+  t.kb_count = max(0, min(sc.kb_per_split, sc.k_blocks - t.kb_first));
+  return t;
+}
+
+__device__ __forceinline__ float load_bias(const void* bias, int bias_f32, int64_t v) {
+  if (bias_f32) return __ldg(reinterpret_cast<const float*>(bias) + v);
+  const unsigned short raw = __ldg(reinterpret_cast<const unsigned short*>(bias) + v);
+  return __uint_as_float(static_cast<uint32_t>(raw) << 16);
+}
+
+// All 128 epilogue threads agree on a predicate (named barrier 1, AND).
+__device__ __forceinline__ bool epilogue_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(ok)), "n"(kEpilogueThreads)
+      : "memory");
+  return r != 0;
+}
+
+// ============================================================================
+// Epilogue: forward statistics over one vocabulary split
+// ============================================================================
+template <bool kBias, bool kSoftcap>
+struct EpiFwd {
+  using Params = FwdParams;
+  struct State {
+    int64_t row, target;
+    float m, s, a, best, zt;
+    int32_t best_idx;
+  };
+
+  __device__ static void begin_unit(const Params& p, const Unit& u, State& st) {
+    st.row = static_cast<int64_t>(u.m_blk) * kBM + threadIdx.x;
+    st.target = st.row < p.n_tokens ? __ldg(p.targets + st.row) : p.ignore_index;
+    st.m = -INFINITY;
+    st.s = 0.f;
+    st.a = 0.f;
+    st.best = -INFINITY;
+    st.best_idx = 0;
+    st.zt = 0.f;
+  }
+
+  __device__ static void tile(const Params& p, const Unit& /*u*/, int n_tile, uint32_t taddr, State& st,
+                              float* /*epi_smem*/) {
+    const int64_t v_tile = static_cast<int64_t>(n_tile) * kBN;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int64_t vc = v_tile + c * 32;
+      if (vc >= p.vocab) break;  // warp-uniform: the rest of the tile is past the vocabulary
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait();
+      const bool ragged = vc + 32 > p.vocab;
+      float z[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float x = __uint_as_float(r[j]);
+        if (kBias) x += (!ragged || vc + j < p.vocab) ? load_bias(p.bias, p.bias_f32, vc + j) : 0.f;
+        x *= p.scale;
+        if (kSoftcap) x = p.softcap * tanh_exp(x * p.inv_softcap);
+        z[j] = x;
+      }
+      if (ragged) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (vc + j >= p.vocab) z[j] = -FLT_MAX;
+      }
+      float cmax = z[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, z[j]);
+      if (cmax > st.best) {  // strict: the lowest index wins ties, across chunks and tiles
+        int jj = 31;
+#pragma unroll
+        for (int j = 31; j >= 0; --j)
+          if (z[j] == cmax) jj = j;
+        st.best = cmax;
+        st.best_idx = static_cast<int32_t>(vc + jj);
+      }
+      if (cmax > st.m) {  // lazy rescale of the running sums to the new maximum
+        const float f = ex2_approx((st.m - cmax) * kLog2e);
+        st.s *= f;
+        st.a *= f;
+        st.m = cmax;
+      }
+      const float mb = st.m * kLog2e;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float e = ex2_approx(fmaf(z[j], kLog2e, -mb));
+        st.s += e;
+        st.a = fmaf(e, z[j], st.a);
+      }
+      const int64_t tl = st.target - vc;
+      if (tl >= 0 && tl < 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j == tl) st.zt = z[j];
+      }
+    }
+  }
+
+  __device__ static void end_unit(const Params& p, const Unit& u, State& st) {
+    if (st.row >= p.n_tokens) return;
+    const size_t o = static_cast<size_t>(u.n_unit) * static_cast<size_t>(p.n_tokens) + st.row;
+    p.part_m[o] = st.m;
+    p.part_s[o] = st.s;
+    p.part_a[o] = st.a;
+    p.part_best[o] = st.best;
+    p.part_idx[o] = st.best_idx;
+    const int64_t v_lo = static_cast<int64_t>(u.n_first) * kBN;
+    const int64_t v_hi = min(static_cast<int64_t>(u.n_first + u.n_count) * kBN, p.vocab);
+    if (st.target >= v_lo && st.target < v_hi) p.z_target[st.row] = st.zt;
+  }
+};
+
+// ============================================================================
+// Epilogue: backward logit gradient G for one vocabulary chunk
+// ============================================================================
+// Reduce 32 per-lane column values over the 32 lanes of the warp; afterwards
+// lane l holds the sum of column l over the warp's 32 rows (fixed order).
+__device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+template <bool kBias, bool kSoftcap>
+struct EpiGrad {
+  using Params = GradParams;
+  struct State {
+    int64_t row, target;
+    float lse2;  // lse * log2(e)
+    float w;     // per-token weight (0 for ignored tokens and rows past N)
+  };
+
+  __device__ static void begin_unit(const Params& p, const Unit& u, State& st) {
+    st.row = static_cast<int64_t>(u.m_blk) * kBM + threadIdx.x;
+    st.target = p.ignore_index;
+    st.lse2 = 0.f;
+    st.w = 0.f;
+    if (st.row < p.n_tokens) {
+      st.target = __ldg(p.targets + st.row);
+      st.lse2 = __ldg(p.lse + st.row) * kLog2e;
+      const bool valid = st.target != p.ignore_index && st.target >= 0 && st.target < p.vocab;
+      if (valid) {
+        if (p.reduction == 0) {
+          st.w = __ldg(p.dloss + st.row);
+        } else if (p.reduction == 1) {
+          st.w = __ldg(p.dloss);
+        } else {
+          const int64_t nv = __ldg(reinterpret_cast<const long long*>(p.n_valid));
+          st.w = nv > 0 ? __ldg(p.dloss) / static_cast<float>(nv) : 0.f;
+        }
+      }
+    }
+  }
+
+  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st,
+                              float* epi_smem) {
+    const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;  // chunk-local column
+    const int64_t v_tile = p.v0 + col_tile;                       // vocabulary row
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
+    const float wd = st.w * p.scale;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int64_t vc = v_tile + c * 32;
+      if (vc >= p.vocab) {  // warp-uniform: no vocabulary rows left in this tile
+        if (kBias) epi_smem[warp * kBN + c * 32 + lane] = 0.f;
+        continue;
+      }
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait();
+      const bool ragged = vc + 32 > p.vocab;
+      float g[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float x = __uint_as_float(r[j]);
+        if (kBias) x += (!ragged || vc + j < p.vocab) ? load_bias(p.bias, p.bias_f32, vc + j) : 0.f;
+        x *= p.scale;
+        float z, d;
+        if (kSoftcap) {
+          const float th = tanh_exp(x * p.inv_softcap);
+          z = p.softcap * th;
+          d = wd * fmaf(-th, th, 1.f);
+        } else {
+          z = x;
+          d = wd;
+        }
+        const float pr = ex2_approx(fmaf(z, kLog2e, -st.lse2));
+        const float oh = (vc + j == st.target) ? 1.f : 0.f;
+        g[j] = d * (pr - oh);
+      }
+      if (ragged) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (vc + j >= p.vocab) g[j] = 0.f;
+      }
+      if (st.row < p.n_tokens) {
+        uint4* dst = reinterpret_cast<uint4*>(p.g + st.row * p.ldg + col_tile + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 pk;
+          pk.x = pack_bf16x2(g[8 * q + 0], g[8 * q + 1]);
+          pk.y = pack_bf16x2(g[8 * q + 2], g[8 * q + 3]);
+          pk.z = pack_bf16x2(g[8 * q + 4], g[8 * q + 5]);
+          pk.w = pack_bf16x2(g[8 * q + 6], g[8 * q + 7]);
+          dst[q] = pk;
+        }
+      }
+      if (kBias) epi_smem[warp * kBN + c * 32 + lane] = warp_column_sums(g);
+    }
+    if (kBias) {
+      epilogue_bar_sync();
+#pragma unroll
+      for (int h = 0; h < kBN / kEpilogueThreads; ++h) {
+        const int col = threadIdx.x + h * kEpilogueThreads;
+        const float s = epi_smem[col] + epi_smem[kBN + col] + epi_smem[2 * kBN + col] + epi_smem[3 * kBN + col];
+        if (v_tile + col < p.vocab)
+          p.dbias_part[static_cast<int64_t>(u.m_blk) * p.ldg + col_tile + col] = s;
+      }
+      epilogue_bar_sync();
+    }
+  }
+
+  __device__ static void end_unit(const Params&, const Unit&, State&) {}
+};
+
+// ============================================================================
+// Epilogue: plain store (dW rows of one chunk; the test GEMM)
+// ============================================================================
+struct EpiStore {
+  using Params = StoreParams;
+  struct State {
+    int64_t row;
+  };
+  __device__ static void begin_unit(const Params&, const Unit& u, State& st) {
+    st.row = static_cast<int64_t>(u.m_blk) * kBM + threadIdx.x;
+  }
+  __device__ static void tile(const Params& p, const Unit&, int n_tile, uint32_t taddr, State& st, float*) {
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int64_t col = static_cast<int64_t>(n_tile) * kBN + c * 32;
+      if (col >= p.cols) break;  // warp-uniform
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait();
+      if (st.row >= p.rows) continue;
+      if (p.out_f32) {
+        float* dst = reinterpret_cast<float*>(p.out) + st.row * p.ldo + col;
+        if (col + 32 <= p.cols) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<uint4*>(dst)[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        } else {
+          const int64_t n = p.cols - col;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < n) dst[j] = __uint_as_float(r[j]);
+        }
+      } else {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + st.row * p.ldo + col;
+        if (col + 32 <= p.cols) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 pk;
+            pk.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
+            pk.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
+            pk.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
+            pk.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+            reinterpret_cast<uint4*>(dst)[q] = pk;
+          }
+        } else {
+          const int64_t n = p.cols - col;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < n) dst[j] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]), 0.f) & 0xFFFFu);
+        }
+      }
+    }
+  }
+  __device__ static void end_unit(const Params&, const Unit&, State&) {}
+};
+
+// ============================================================================
+// Epilogue: dh accumulation (K-split slot, or the final store)
+// ============================================================================
+struct EpiAccum {
+  using Params = AccumParams;
+  struct State {
+    int64_t row;
+  };
+  __device__ static void begin_unit(const Params&, const Unit& u, State& st) {
+    st.row = static_cast<int64_t>(u.m_blk) * kBM + threadIdx.x;
+  }
+  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*) {
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int64_t col = static_cast<int64_t>(n_tile) * kBN + c * 32;
+      if (col >= p.cols) break;  // warp-uniform
+      float v[32];
+      if (u.kb_count > 0) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      } else {  // a K split with no K blocks contributes zero
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
+      if (st.row >= p.rows) continue;
+      float* slot = p.part + static_cast<int64_t>(u.ks) * p.part_stride + st.row * p.cols + col;
+      const int64_t rem = p.cols - col;
+      const int n = rem < 32 ? static_cast<int>(rem) : 32;
+      if (n == 32) {
+        if (p.accumulate) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 o = reinterpret_cast<const float4*>(slot)[q];
+            v[4 * q] += o.x;
+            v[4 * q + 1] += o.y;
+            v[4 * q + 2] += o.z;
+            v[4 * q + 3] += o.w;
+          }
+        }
+        if (!p.write_final) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(slot)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else if (p.out_f32) {
+          float* dst = reinterpret_cast<float*>(p.out) + st.row * p.cols + col;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+          uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + st.row * p.cols + col;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 pk;
+            pk.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+            pk.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+            pk.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+            pk.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+            reinterpret_cast<uint4*>(dst)[q] = pk;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j >= n) continue;
+          float x = v[j];
+          if (p.accumulate) x += slot[j];
+          if (!p.write_final) {
+            slot[j] = x;
+          } else if (p.out_f32) {
+            reinterpret_cast<float*>(p.out)[st.row * p.cols + col + j] = x;
+          } else {
+            reinterpret_cast<uint16_t*>(p.out)[st.row * p.cols + col + j] =
+                static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
+          }
+        }
+      }
+    }
+  }
+  __device__ static void end_unit(const Params&, const Unit&, State&) {}
+};
+
+// ============================================================================
+// The kernel
+// ============================================================================
+struct GemmSmem {
+  uint8_t* a;          // kStages x kATileBytes
+  uint8_t* b;          // kStages x kBTileBytes
+  uint64_t* full;      // [kStages]  TMA -> MMA
+  uint64_t* empty;     // [kStages]  MMA -> TMA
+  uint64_t* tfull;     // [kAccBufs] MMA -> epilogue
+  uint64_t* tempty;    // [kAccBufs] epilogue -> MMA
+  uint64_t* drain;     // MMA teardown
+  uint32_t* tmem_slot;
+  CtaControl* ctl;
+  float* epi;          // kEpiSmemBytes
+};
+
+__device__ __forceinline__ GemmSmem carve_smem(uint8_t* raw) {
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  GemmSmem s;
+  s.a = base;
+  s.b = base + kStages * kATileBytes;
+  uint8_t* bar = s.b + kStages * kBTileBytes;
+  s.full = reinterpret_cast<uint64_t*>(bar);
+  s.empty = s.full + kStages;
+  s.tfull = s.empty + kStages;
+  s.tempty = s.tfull + kAccBufs;
+  s.drain = s.tempty + kAccBufs;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+  s.ctl = reinterpret_cast<CtaControl*>(s.tmem_slot + 2);
+  s.epi = reinterpret_cast<float*>(bar + kBarrierBytes);
+  return s;
+}
+
+// Bounded wait used only while tearing down: waits for a copy that was issued
+// to land, regardless of the abort flag.
+__device__ __forceinline__ void mbar_wait_teardown(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(addr, parity)) {
+    if (global_timer_ns() - t0 > kWaitTimeoutNs / 8) return;
+  }
+}
+
+template <class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
+                const __grid_constant__ CUtensorMap map_b0, const __grid_constant__ CUtensorMap map_b1,
+                const GemmSched sc, const typename Epi::Params ep, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  GemmSmem sm = carve_smem(smem_raw);
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == kTmaWarp * 32) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(&sm.tfull[b], 1);
+      mbar_init(&sm.tempty[b], kEpilogueWarps);
+    }
+    mbar_init(sm.drain, 1);
+    sm.ctl->abort = 0u;
+    fence_mbar_init();
+    tma_prefetch_map(&map_a0);
+    tma_prefetch_map(&map_b0);
+    if (sc.nseg > 1) {
+      tma_prefetch_map(sc.seg_a ? &map_a1 : &map_b1);
+    }
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(sm.tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ---------------------------------------------------------------- producer
+    if (elect_one()) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_phase[kStages];
+      bool issued[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) {
+        issued[s] = false;
+        issued_phase[s] = 0;
+      }
+      for (int uu = blockIdx.x; uu < sc.total_units; uu += gridDim.x) {
+        const Unit u = decode_unit(sc, uu);
+        bool ok = true;
+        for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
+          for (int seg = 0; ok && seg < sc.nseg; ++seg) {
+            const CUtensorMap* ma = (seg && sc.seg_a) ? &map_a1 : &map_a0;
+            const CUtensorMap* mb = (seg && !sc.seg_a) ? &map_b1 : &map_b0;
+            for (int kb = u.kb_first; kb < u.kb_first + u.kb_count; ++kb) {
+              if (!mbar_wait(&sm.empty[stage], phase ^ 1u, sm.ctl, status)) {
+                ok = false;
+                break;
+              }
+              uint64_t* fb = &sm.full[stage];
+              mbar_arrive_expect_tx(fb, kStageBytes);
+              uint8_t* sa = sm.a + stage * kATileBytes;
+              uint8_t* sb = sm.b + stage * kBTileBytes;
+              const int k = kb * kBK;
+              if (!sc.a_mn) {
+                tma_load_2d(sa, ma, fb, sc.a_k_off + k, sc.a_mn_off + u.m_blk * kBM);
+              } else {
+#pragma unroll
+                for (int j = 0; j < kBM / 64; ++j)
+                  tma_load_2d(sa + j * kMnAtomBytes, ma, fb, sc.a_mn_off + u.m_blk * kBM + 64 * j, sc.a_k_off + k);
+              }
+              if (!sc.b_mn) {
+                tma_load_2d(sb, mb, fb, sc.b_k_off + k, sc.b_mn_off + n * kBN);
+              } else {
+#pragma unroll
+                for (int j = 0; j < kBN / 64; ++j)
+                  tma_load_2d(sb + j * kMnAtomBytes, mb, fb, sc.b_mn_off + n * kBN + 64 * j, sc.b_k_off + k);
+              }
+              issued[stage] = true;
+              issued_phase[stage] = phase;
+              if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+        }
+        if (!ok) break;
+      }
+      // Every copy this thread issued must land before the CTA may exit.
+#pragma unroll
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) mbar_wait_teardown(&sm.full[s], issued_phase[s]);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (elect_one()) {
+      const uint32_t idesc = instr_desc_bf16(kBM, kBN, sc.a_mn, sc.b_mn);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int uu = blockIdx.x; ok && uu < sc.total_units; uu += gridDim.x) {
+        const Unit u = decode_unit(sc, uu);
+        for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
+          if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, sm.ctl, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kBN;
+          uint32_t accumulate = 0;
+          for (int seg = 0; ok && seg < sc.nseg; ++seg) {
+            for (int kb = 0; kb < u.kb_count; ++kb) {
+              if (!mbar_wait(&sm.full[stage], phase, sm.ctl, status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a_base = smem_u32(sm.a + stage * kATileBytes);
+              const uint32_t b_base = smem_u32(sm.b + stage * kBTileBytes);
+#pragma unroll
+              for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                const uint64_t ad = sc.a_mn ? smem_desc_sw128(a_base + kk * 2048, kMnAtomBytes, 1024)
+                                            : smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                const uint64_t bd = sc.b_mn ? smem_desc_sw128(b_base + kk * 2048, kMnAtomBytes, 1024)
+                                            : smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+                accumulate = 1;
+              }
+              umma_commit(&sm.empty[stage]);  // stage free once these MMAs have read it
+              if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+          if (!ok) break;
+          umma_commit(&sm.tfull[acc]);  // accumulator ready for the epilogue
+          if (++acc == kAccBufs) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+      }
+      // Wait for every MMA this thread issued before TMEM can be released.
+      umma_commit(sm.drain);
+      mbar_wait_teardown(sm.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    uint32_t acc = 0, acc_phase = 0;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+    for (int uu = blockIdx.x; ok && uu < sc.total_units; uu += gridDim.x) {
+      const Unit u = decode_unit(sc, uu);
+      typename Epi::State st;
+      Epi::begin_unit(ep, u, st);
+      for (int n = u.n_first; n < u.n_first + u.n_count; ++n) {
+        const bool got = mbar_wait(&sm.tfull[acc], acc_phase, sm.ctl, status);
+        if (!epilogue_all(got)) {
+          sm.ctl->abort = 1u;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        Epi::tile(ep, u, n, tmem_base + lane_base + acc * kBN, st, sm.epi);
+        tc_fence_before();
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&sm.tempty[acc]);
+        if (++acc == kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (ok) Epi::end_unit(ep, u, st);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace flce

@@ -1,0 +1,121 @@
+// flce_internal.h — constants and parameter blocks shared by the host launcher
+// and the sm_103a kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+namespace flce {
+
+// ---- GEMM tiling (one CTA per SM, warp-specialised) ------------------------
+constexpr int kBM = 128;          // tile rows = TMEM lanes (tokens, or vocab rows for dW)
+constexpr int kBN = 256;          // tile columns = TMEM columns of one accumulator
+constexpr int kBK = 64;           // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;        // K of one tcgen05.mma.kind::f16
+constexpr int kStages = 4;        // shared-memory ring depth
+constexpr int kAccBufs = 2;       // TMEM accumulators (2 x 256 columns = all 512)
+constexpr int kTmemCols = 512;
+
+constexpr int kATileBytes = kBM * kBK * 2;         // 16 KB
+constexpr int kBTileBytes = kBN * kBK * 2;         // 32 KB
+constexpr int kMnAtomBytes = 64 * kBK * 2;         // 8 KB: 64 MN elements x 64 K rows
+constexpr int kStageBytes = kATileBytes + kBTileBytes;
+
+constexpr int kEpilogueWarps = 4;                   // warps 0..3: one TMEM lane quarter each
+constexpr int kEpilogueThreads = kEpilogueWarps * 32;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+
+constexpr int kEpiSmemBytes = kEpilogueWarps * kBN * 4;   // column-sum staging (dbias)
+constexpr int kBarrierBytes = 256;
+constexpr int kGemmSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarrierBytes + kEpiSmemBytes;
+
+// A bounded wait inside a kernel gives up after this much wall time.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+// Device status codes (same values as the public FLCE_ERR_* codes).
+constexpr int kStatusTargetOutOfRange = 7;
+constexpr int kStatusTimeout = 8;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- Persistent tile schedule ----------------------------------------------
+// Work is a list of units; CTA b takes units b, b + gridDim.x, ...  A unit is
+// one m tile, a run of `n_per_unit` consecutive n tiles and one K split.
+// Units are rasterised in groups of `group_m` m tiles so that CTAs running at
+// the same time share operand tiles through L2.
+struct GemmSched {
+  int32_t m_tiles, n_tiles;
+  int32_t k_blocks;       // 64-wide K blocks over the whole K range
+  int32_t nseg;           // 1, or 2 when the fp32 hidden state is split into hi + lo
+  int32_t seg_a;          // 1: segment 1 switches the A map; 0: it switches the B map
+  int32_t ksplit;         // K splits per output tile
+  int32_t kb_per_split;
+  int32_t n_per_unit;
+  int32_t n_units;        // ceil(n_tiles / n_per_unit)
+  int32_t group_m;
+  int32_t total_units;
+  int32_t a_mn, b_mn;     // operand majorness: 0 = K-major, 1 = MN-major
+  int32_t a_mn_off, a_k_off;   // coordinate offsets into the A tensor map
+  int32_t b_mn_off, b_k_off;   // coordinate offsets into the B tensor map
+};
+
+// ---- Epilogue parameter blocks --------------------------------------------
+// Forward: online per-token statistics over each unit's vocabulary range
+// (one unit = one vocabulary split of one m tile).
+struct FwdParams {
+  int64_t n_tokens, vocab;
+  const void* bias;       // nullptr, bf16 or fp32 [V]
+  int32_t bias_f32;
+  int32_t n_splits;
+  float scale, softcap, inv_softcap;
+  int64_t ignore_index;
+  const int64_t* targets;
+  // partials, [n_splits][n_tokens] each
+  float* part_m;          // running max of z
+  float* part_s;          // sum exp(z - m)
+  float* part_a;          // sum exp(z - m) * z
+  float* part_best;       // largest z
+  int32_t* part_idx;      // its lowest vocabulary index
+  float* z_target;        // [n_tokens] z at the target, written by the owning split
+};
+
+// Backward recompute: G = w_n (softmax - onehot) * dz/dacc for one vocabulary
+// chunk, written as bf16; optional per-m-tile column sums for dbias.
+struct GradParams {
+  int64_t n_tokens, vocab;
+  int64_t v0;             // first vocabulary row of the chunk
+  const void* bias;
+  int32_t bias_f32;
+  int32_t reduction;      // FLCE_RED_*
+  float scale, softcap, inv_softcap;
+  int64_t ignore_index;
+  const int64_t* targets;
+  const float* lse;
+  const float* dloss;
+  const int64_t* n_valid;
+  uint16_t* g;            // bf16 [n_tokens][ldg]
+  int64_t ldg;
+  float* dbias_part;      // [m_tiles][ldg] or nullptr
+};
+
+// Plain store of the accumulator (dW, and the test GEMM).
+struct StoreParams {
+  int64_t rows, cols;     // valid extent of the output
+  void* out;
+  int64_t ldo;
+  int32_t out_f32;
+};
+
+// dh accumulation over vocabulary chunks and K splits.
+struct AccumParams {
+  int64_t rows, cols;
+  float* part;            // [ksplit][rows][cols] fp32
+  int64_t part_stride;    // elements between K-split slots
+  int32_t accumulate;     // add the slot's previous value
+  int32_t write_final;    // write `out` in its dtype instead of the slot (ksplit == 1)
+  void* out;
+  int32_t out_f32;
+};
+
+}  // namespace flce

@@ -1,0 +1,68 @@
+// flce_launch.h — host-side launchers for the kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "flce_internal.h"
+
+namespace flce {
+
+struct TmaMaps {
+  CUtensorMap a0, a1, b0, b1;
+};
+
+// Per-token merge of the split partials, with per-block partial sums.
+struct BlockPartial {
+  double loss;
+  double entropy;
+  long long correct;
+  long long valid;
+};
+
+struct MergeParams {
+  int64_t n_tokens, vocab;
+  int32_t n_splits;
+  int32_t reduction;
+  int64_t ignore_index;
+  const float *part_m, *part_s, *part_a, *part_best;
+  const int32_t* part_idx;
+  const float* z_target;
+  const int64_t* targets;
+  float* lse;
+  float* entropy;     // nullable
+  float* loss_tok;    // the loss output when reduction is 'none', else nullptr
+  BlockPartial* blocks;
+};
+
+struct ReduceParams {
+  const BlockPartial* blocks;
+  int32_t n_blocks;
+  int32_t reduction;
+  float* loss;        // [1] for mean / sum
+  int64_t* correct;
+  int64_t* n_valid;
+  float* entropy_sum;
+};
+
+constexpr int kMergeThreads = 256;
+
+cudaError_t launch_fwd_gemm(bool bias, bool softcap, const TmaMaps& maps, const GemmSched& sc,
+                            const FwdParams& p, int* status, int grid, cudaStream_t stream);
+cudaError_t launch_grad_gemm(bool bias, bool softcap, const TmaMaps& maps, const GemmSched& sc,
+                             const GradParams& p, int* status, int grid, cudaStream_t stream);
+cudaError_t launch_store_gemm(const TmaMaps& maps, const GemmSched& sc, const StoreParams& p, int* status,
+                              int grid, cudaStream_t stream);
+cudaError_t launch_accum_gemm(const TmaMaps& maps, const GemmSched& sc, const AccumParams& p, int* status,
+                              int grid, cudaStream_t stream);
+
+cudaError_t launch_split_hidden(const float* h, uint16_t* hi, uint16_t* lo, int64_t n, int grid,
+                                cudaStream_t stream);
+cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream);
+cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream);
+cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int64_t cols, void* dbias,
+                                int bias_f32, cudaStream_t stream);
+cudaError_t launch_dh_finalize(const float* part, int64_t stride, int ksplit, int64_t n, void* out, int out_f32,
+                               int grid, cudaStream_t stream);
+
+}  // namespace flce

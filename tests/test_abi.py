@@ -1,0 +1,163 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+validation returns the documented status codes.  CPU only: no kernel runs."""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from linear_cross_entropy_tmem_gb300 import binding as B
+from linear_cross_entropy_tmem_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        names.update(re.findall(r"FLCE_API\s+[\w\s\*]+?\b(flce_\w+)\s*\(", open(h).read()))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"flce_forward", "flce_backward", "flce_workspace_size", "flce_read_device_status",
+            "flce_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(B.SIGNATURES), "binding signatures and headers disagree"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.flce_abi_version() == 1
+    for code in range(0, 10):
+        assert lib.flce_status_string(code).decode() not in ("", "unknown status")
+    assert lib.flce_status_string(12345).decode() == "unknown status"
+
+
+def test_problem_struct_layout_matches_header():
+    # int64 x3, int32 x4, float x2, int64  ->  56 bytes with natural alignment
+    assert ctypes.sizeof(B.FlceProblem) == 56
+    assert B.FlceProblem.ignore_index.offset == 48
+
+
+def _problem(**kw):
+    base = dict(n_tokens=512, hidden=128, vocab=4096, hidden_dtype=B.FLCE_BF16, weight_dtype=B.FLCE_BF16,
+                bias_dtype=B.FLCE_BF16, reduction=B.FLCE_RED_MEAN, logit_scale=1.0,
+                final_logit_softcapping=0.0, ignore_index=-100)
+    base.update(kw)
+    return B.FlceProblem(**base)
+
+
+def _ws(lib, prob, bwd):
+    n = ctypes.c_size_t()
+    st = lib.flce_workspace_size(ctypes.byref(prob), bwd, ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_size_needs_no_gpu_and_never_scales_with_n_times_v(lib):
+    for (N, D, V) in [(512, 128, 4096), (16384, 640, 262144), (256, 2048, 248320), (16384, 4096, 151936),
+                      (8192, 2048, 128256)]:
+        for bwd in (0, 1):
+            st, n = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V), bwd)
+            assert st == B.FLCE_OK
+            assert n > 0
+        st, fw = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V), 0)
+        st, bw = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, hidden_dtype=B.FLCE_F32), 1)
+        # forward: O(N * splits); backward: one bf16 G chunk of at most 1 GiB,
+        # its per-tile dbias sums (1/64 of it in fp32 per 128 rows), the fp32 hi/lo
+        # split and the fp32 dh accumulator (4 N D bytes each at most)
+        assert fw <= 21 * N * 64 + (1 << 20)
+        assert bw <= (1 << 30) + (1 << 30) // 64 + 3 * 4 * N * D + (1 << 20)
+        # the G chunk covers at most about half of the vocabulary
+        assert bw <= N * (V // 2 + 256) * 2 * (1 + 1 / 32) + 16 * 4 * N * D + 4 * N * D + (1 << 20)
+        if N * V >= 1 << 28:
+            assert bw < 2 * N * V  # far below a full (tokens x vocab) bf16 buffer
+    st, n = _ws(lib, _problem(n_tokens=0), 1)
+    assert st == B.FLCE_OK
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(vocab=0), B.FLCE_ERR_INVALID_ARG),
+    (dict(n_tokens=-1), B.FLCE_ERR_INVALID_ARG),
+    (dict(hidden=4), B.FLCE_ERR_INVALID_ARG),
+    (dict(hidden=130), B.FLCE_ERR_MISALIGNED),
+    (dict(reduction=7), B.FLCE_ERR_INVALID_ARG),
+    (dict(weight_dtype=B.FLCE_F32), B.FLCE_ERR_DTYPE_MISMATCH),
+    (dict(weight_dtype=B.FLCE_F32, hidden_dtype=B.FLCE_F32), B.FLCE_ERR_UNSUPPORTED_DTYPE),
+    (dict(hidden_dtype=5), B.FLCE_ERR_UNSUPPORTED_DTYPE),
+    (dict(logit_scale=float("nan")), B.FLCE_ERR_INVALID_ARG),
+])
+def test_problem_validation(lib, kw, code):
+    assert _ws(lib, _problem(**kw), 0)[0] == code
+    assert _ws(lib, _problem(**kw), 1)[0] == code
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+def test_call_validation_without_gpu(lib):
+    """Argument errors are reported before any CUDA call, so no GPU is needed."""
+    p = _problem()
+    _, ws = _ws(lib, p, 0)
+    good = [_fake(0x10000 * (i + 1)) for i in range(12)]
+    h, w, b, t, loss, lse, ent, corr, nv, es, wsp = good[:11]
+    fwd = lib.flce_forward
+    # null weight
+    assert fwd(ctypes.byref(p), h, None, None, t, loss, lse, ent, corr, nv, es, wsp, ws, None) == B.FLCE_ERR_INVALID_ARG
+    # null loss output
+    assert fwd(ctypes.byref(p), h, w, None, t, None, lse, ent, corr, nv, es, wsp, ws, None) == B.FLCE_ERR_INVALID_ARG
+    # misaligned hidden / workspace
+    assert fwd(ctypes.byref(p), _fake(0x10008), w, None, t, loss, lse, ent, corr, nv, es, wsp, ws, None) \
+        == B.FLCE_ERR_MISALIGNED
+    assert fwd(ctypes.byref(p), h, w, None, t, loss, lse, ent, corr, nv, es, _fake(0x10080), ws, None) \
+        == B.FLCE_ERR_MISALIGNED
+    # workspace too small
+    assert fwd(ctypes.byref(p), h, w, None, t, loss, lse, ent, corr, nv, es, wsp, ws - 1, None) \
+        == B.FLCE_ERR_WORKSPACE_TOO_SMALL
+    # bad bias dtype only matters when a bias is passed
+    pb = _problem(bias_dtype=9)
+    assert fwd(ctypes.byref(pb), h, w, b, t, loss, lse, ent, corr, nv, es, wsp, ws, None) \
+        == B.FLCE_ERR_UNSUPPORTED_DTYPE
+    bwd = lib.flce_backward
+    _, wsb = _ws(lib, p, 1)
+    dh, dw, db = good[8], good[9], good[10]
+    # bias and dbias must be both present or both absent
+    assert bwd(ctypes.byref(p), h, w, b, t, lse, nv, loss, dh, dw, None, wsp, wsb, None) == B.FLCE_ERR_INVALID_ARG
+    assert bwd(ctypes.byref(p), h, w, None, t, lse, nv, loss, dh, dw, db, wsp, wsb, None) == B.FLCE_ERR_INVALID_ARG
+    assert bwd(ctypes.byref(p), h, w, None, t, lse, nv, loss, dh, dw, None, wsp, wsb - 1, None) \
+        == B.FLCE_ERR_WORKSPACE_TOO_SMALL
+    assert lib.flce_read_device_status(None, None, None) == B.FLCE_ERR_INVALID_ARG
+    assert lib.flce_testing_set_tuning(-1, 0) == B.FLCE_ERR_INVALID_ARG
+    assert lib.flce_testing_set_tuning(0, 17) == B.FLCE_ERR_INVALID_ARG
+    assert lib.flce_testing_set_tuning(0, 0) == B.FLCE_OK
+
+
+def test_python_binding_refuses_cpu_tensors():
+    """The product path has no CPU fallback: CPU inputs raise."""
+    import torch
+
+    import linear_cross_entropy_tmem_gb300 as F
+    h = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(5, 8, dtype=torch.bfloat16)
+    t = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(RuntimeError, match="CUDA"):
+        F.flce_forward(h, W, t)
+
+
+def test_oracle_is_not_imported_by_the_product_path():
+    """No module of the package imports the oracle."""
+    pkg = os.path.join(ROOT, "linear_cross_entropy_tmem_gb300")
+    for f in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True):
+        src = open(f).read()
+        assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), f

@@ -1,0 +1,178 @@
+"""GPU parity of flce_forward / flce_backward (through the C ABI) against the fp64
+oracle on the same seeded inputs, at sizes the oracle finishes in seconds that
+still span several tiles and ragged tails, plus the edge cases of the method."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_cross_entropy_tmem_gb300.synthetic import TINY, Workload, make_inputs
+from tests.parity import compare_backward, compare_forward, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+# name -> (workload, tuning override (chunk columns, dh K splits))
+CASES = {
+    "tiny N512 D128 V4096 mean": (TINY, (0, 0)),
+    "ragged N300 D200 V1000 bias-bf16 s0.7 c5 sum": (
+        Workload("r", 300, 200, 1000, sigma_w=0.15, bias=True, logit_scale=0.7, softcap=5.0, reduction="sum",
+                 seed=1), (0, 0)),
+    "fp32-h N257 D136 V777 bias s0.0625 c30 none": (
+        Workload("h32", 257, 136, 777, sigma_w=0.3, hidden_dtype=torch.float32, bias=True, logit_scale=0.0625,
+                 softcap=30.0, reduction="none", seed=2), (0, 0)),
+    "multi-chunk ksplit3 N384 D256 V3000 bias mean": (
+        Workload("mc", 384, 256, 3000, sigma_w=0.1, bias=True, seed=3), (1024, 3)),
+    "multi-chunk ksplit1 N640 D512 V2560 none": (
+        Workload("mc1", 640, 512, 2560, sigma_w=0.08, reduction="none", seed=4), (768, 1)),
+    "fp32-h multi-chunk N200 D64 V1500 softcap sum": (
+        Workload("h32mc", 200, 64, 1500, sigma_w=0.4, hidden_dtype=torch.float32, softcap=8.0,
+                 reduction="sum", seed=5), (512, 2)),
+    "single tile vocab N130 D64 V200 softcap": (
+        Workload("v200", 130, 64, 200, sigma_w=0.3, softcap=3.0, seed=6), (0, 0)),
+    "minimum D8 V1": (Workload("d8v1", 33, 8, 1, ignore_every=5, seed=7), (0, 0)),
+    "D8 V300 mean": (Workload("d8", 70, 8, 300, sigma_w=1.0, seed=8), (0, 0)),
+}
+
+
+@pytest.fixture(autouse=True)
+def _reset_tuning():
+    from linear_cross_entropy_tmem_gb300.api import testing_set_tuning
+    yield
+    testing_set_tuning(0, 0)
+
+
+def _run_case(w: Workload, tuning):
+    from linear_cross_entropy_tmem_gb300.api import testing_set_tuning
+    testing_set_tuning(*tuning)
+    h, W, b, t, dloss = make_inputs(w, "cpu")
+    dev = [x.cuda() if x is not None else None for x in (h, W, b, t, dloss)]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    gpu = run_gpu(*dev, **kw)
+    assert gpu["status"] == 0
+    ref_f = oracle.forward(h, W, b, t, **kw)
+    ref_b = oracle.backward(h, W, b, t, dloss=dloss, **kw)
+    z = oracle.logits(h, W, b, logit_scale=w.logit_scale, softcap=w.softcap)
+    compare_forward(gpu["fwd"], ref_f, reduction=w.reduction, z=z, t=t.numpy())
+    compare_backward(gpu["bwd"], ref_b)
+    return gpu, dev
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_parity_small(name):
+    w, tuning = CASES[name]
+    _run_case(w, tuning)
+
+
+def test_bitwise_deterministic_across_runs():
+    w = CASES["multi-chunk ksplit3 N384 D256 V3000 bias mean"][0]
+    from linear_cross_entropy_tmem_gb300.api import testing_set_tuning
+    testing_set_tuning(1024, 3)
+    h, W, b, t, dloss = [x.cuda() if x is not None else None for x in make_inputs(w, "cpu")]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    a = run_gpu(h, W, b, t, dloss, **kw)
+    c = run_gpu(h, W, b, t, dloss, **kw)
+    for x, y in zip((a["fwd"].loss, a["fwd"].lse, a["fwd"].entropy, a["fwd"].correct, a["fwd"].entropy_sum),
+                    (c["fwd"].loss, c["fwd"].lse, c["fwd"].entropy, c["fwd"].correct, c["fwd"].entropy_sum)):
+        assert torch.equal(x, y)
+    for x, y in zip(a["bwd"], c["bwd"]):
+        assert torch.equal(x, y)
+
+
+def test_all_ignored_gives_zero_loss_and_exact_zero_grads():
+    w = Workload("ign", 100, 64, 500, sigma_w=0.2, bias=True, seed=9)
+    for red in ("mean", "sum", "none"):
+        h, W, b, t, _ = make_inputs(w, "cuda")
+        t[:] = -100
+        dloss = torch.ones(100 if red == "none" else 1, device="cuda")
+        g = run_gpu(h, W, b, t, dloss, logit_scale=1.0, softcap=0.0, reduction=red)
+        f = g["fwd"]
+        assert int(f.n_valid) == 0 and int(f.correct) == 0 and float(f.entropy_sum) == 0.0
+        assert torch.all(f.loss == 0)
+        for x in g["bwd"]:
+            assert torch.all(x == 0)
+
+
+def test_empty_batch():
+    import linear_cross_entropy_tmem_gb300 as F
+    W = torch.randn(300, 64, device="cuda").to(torch.bfloat16)
+    b = torch.randn(300, device="cuda").to(torch.bfloat16)
+    h = torch.empty(0, 64, device="cuda", dtype=torch.bfloat16)
+    t = torch.empty(0, dtype=torch.int64, device="cuda")
+    for red in ("mean", "sum"):
+        f = F.flce_forward(h, W, t, b, reduction=red)
+        dh, dW, db = F.flce_backward(h, W, t, f.lse, f.n_valid, torch.ones(1, device="cuda"), b, reduction=red)
+        torch.cuda.synchronize()
+        assert float(f.loss) == 0.0 and int(f.n_valid) == 0 and int(f.correct) == 0
+        assert dh.numel() == 0 and torch.all(dW == 0) and torch.all(db == 0)
+
+
+def test_out_of_range_target_sets_status_and_is_ignored():
+    w = Workload("oor", 64, 64, 300, sigma_w=0.2, seed=10, ignore_every=0)
+    h, W, b, t, dloss = make_inputs(w, "cpu")
+    t[5] = 300
+    t[9] = -7
+    g = run_gpu(h.cuda(), W.cuda(), None, t.cuda(), dloss.cuda(), logit_scale=1.0, softcap=0.0, reduction="mean")
+    assert g["status"] == 7
+    ref = oracle.forward(h, W, None, t)
+    assert ref["status"] == oracle.STATUS_TARGET_OUT_OF_RANGE
+    compare_forward(g["fwd"], ref, reduction="mean")
+    compare_backward(g["bwd"], oracle.backward(h, W, None, t, dloss=dloss))
+
+
+def test_targets_at_argmax_give_exact_accuracy():
+    """TRL PR #6859, "Correctness": with targets at the argmax, accuracy is exact."""
+    for V in (32000, 150000, 200000):
+        w = Workload("am", 96, 64, V, sigma_w=0.5, seed=V)
+        h, W, b, t, dloss = make_inputs(w, "cpu")
+        z = oracle.logits(h, W)
+        zs = np.sort(z, axis=1)
+        keep = (zs[:, -1] - zs[:, -2]) >= 1e-3          # exclude near-ties
+        t = torch.from_numpy(z.argmax(axis=1))
+        t[~torch.from_numpy(keep)] = -100
+        g = run_gpu(h.cuda(), W.cuda(), None, t.cuda(), dloss.cuda(), logit_scale=1.0, softcap=0.0,
+                    reduction="mean", backward=False)
+        f = g["fwd"]
+        assert int(f.correct) == int(f.n_valid) == int(keep.sum())
+
+
+def test_ties_go_to_lowest_index():
+    """Duplicate head rows give bitwise-equal logits; the lowest index must win.
+
+    Rows 3 and 650 (and 399, 400) are made identical and three times larger than
+    the rest, so they hold the maximum for a sizeable share of the tokens.
+    """
+    w = Workload("tie", 128, 64, 700, sigma_w=0.3, seed=11, ignore_every=0)
+    h, W, b, t, dloss = make_inputs(w, "cpu")
+    W[3] = (W[3].float() * 3).to(torch.bfloat16)
+    W[650] = W[3]
+    W[399] = (W[399].float() * 3).to(torch.bfloat16)
+    W[400] = W[399]
+    z = oracle.logits(h, W)
+    am = z.argmax(axis=1)  # first maximum
+    zs = np.sort(z, axis=1)
+    gap = zs[:, -1] - zs[:, -2]
+    exact = np.isin(am, [3, 399])
+    assert exact.sum() >= 10 and np.all(gap[exact] == 0.0)
+    t = torch.from_numpy(am)
+    g = run_gpu(h.cuda(), W.cuda(), None, t.cuda(), dloss.cuda(), logit_scale=1.0, softcap=0.0,
+                reduction="sum", backward=False)
+    may_flip = int(((gap > 0) & (gap < 1e-3)).sum())
+    assert 128 - may_flip <= int(g["fwd"].correct) <= 128
+
+
+def test_autograd_wrapper_matches_direct_calls():
+    import linear_cross_entropy_tmem_gb300 as F
+    w = CASES["ragged N300 D200 V1000 bias-bf16 s0.7 c5 sum"][0]
+    h, W, b, t, _ = [x.cuda() if x is not None else None for x in make_inputs(w, "cpu")]
+    hh, WW, bb = (x.clone().requires_grad_(True) for x in (h, W, b))
+    loss, correct, n_valid, ent = F.linear_cross_entropy(hh, WW, t, bb, logit_scale=0.7, softcap=5.0,
+                                                         reduction="sum")
+    (2.0 * loss).backward()
+    f = F.flce_forward(h, W, t, b, logit_scale=0.7, softcap=5.0, reduction="sum")
+    dh, dW, db = F.flce_backward(h, W, t, f.lse, f.n_valid, torch.full((1,), 2.0, device="cuda"), b,
+                                 logit_scale=0.7, softcap=5.0, reduction="sum")
+    torch.cuda.synchronize()
+    assert torch.equal(loss, f.loss)
+    assert torch.equal(hh.grad, dh) and torch.equal(WW.grad, dW) and torch.equal(bb.grad, db)
