@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the fused linear cross-entropy (forward + backward) on GB300.
+
+One step = flce_forward + flce_backward over one batch of the Qwen3-8B-like head
+(N=16384 tokens, D=4096, V=151936, bf16, mean reduction) -- the workload the
+headline metric is quoted on.  Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qwen8b]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides, CUDA events on the launching stream,
+max over ranks.  The inputs are larger than L2 (the 1.25 GB head alone is ten
+times the 129 MB L2), so no flush is needed between steps.  For N > 1 every
+rank runs its own replica of the workload (independent batches; the loss needs
+no exchange), so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s (% of GB300 bf16 tensor peak)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+# ----------------------------------------------------------------------------- utilities
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["flce", "reference"], default="flce")
+    ap.add_argument("--workload", default="qwen8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = automatic)")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Max of a scalar over all ranks (timing only; no data-path exchange)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.out = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(index)], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        for line in self.out.read().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample_step(h_rows, W, b, t_rows, dloss, w):
+    """One oracle forward + backward over a sample of tokens (the oracle as it stands)."""
+    import oracle
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    f = oracle.forward(h_rows, W, b, t_rows, **kw)
+    g = oracle.backward(h_rows, W, b, t_rows, dloss=dloss, **kw)
+    return f, g
+
+
+def cpu_inputs(w, rows):
+    """The workload's tensors restricted to a token sample, on the CPU."""
+    import torch
+
+    from linear_cross_entropy_tmem_gb300.synthetic import make_inputs
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    sample = w.scaled(n_tokens=max(rows, 1))
+    h, W, b, t, dloss = make_inputs(sample, dev)
+    out = [x.cpu() if x is not None else None for x in (h, W, b, t, dloss)]
+    del h, W, b, t, dloss
+    if dev == "cuda":
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(w, rows=0, budget_s=15.0):
+    """Time the oracle on a bounded sample of the workload (tokens/s on host cores)."""
+    rows = rows or 32
+    h, W, b, t, dloss = cpu_inputs(w, rows)
+    t0 = time.perf_counter()
+    oracle_sample_step(h, W, b, t, dloss, w)
+    dt = time.perf_counter() - t0
+    reps = 1
+    while dt * (reps + 1) / reps < budget_s and dt < budget_s / 2 and reps < 4:
+        t1 = time.perf_counter()
+        oracle_sample_step(h, W, b, t, dloss, w)
+        dt += time.perf_counter() - t1
+        reps += 1
+    value = rows * reps / dt
+    return {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{rows} tokens x {reps} runs of the fp64 oracle forward+backward at full V={w.vocab}, "
+                      f"D={w.hidden} ({dt:.1f} s)"}
+
+
+def reference_arm(args):
+    from linear_cross_entropy_tmem_gb300.synthetic import WORKLOADS
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    rows = args.cpu_rows or 16
+    h, W, b, t, dloss = cpu_inputs(w, rows)
+    for _ in range(args.warmup):
+        oracle_sample_step(h, W, b, t, dloss, w)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(h, W, b, t, dloss, w)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "n_tokens": w.n_tokens, "hidden": w.hidden, "vocab": w.vocab,
+                   "sample_tokens_per_step": rows, "l2": "n/a (host)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{rows} tokens per step at full V and D, fp64 oracle forward+backward"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class Runner:
+    """Preallocated buffers and raw C-ABI calls for one forward + backward step."""
+
+    def __init__(self, w, device, seed_offset=0):
+        import torch
+
+        import linear_cross_entropy_tmem_gb300.api as api
+        from linear_cross_entropy_tmem_gb300 import binding as B
+        from linear_cross_entropy_tmem_gb300.synthetic import make_inputs
+        self.B = B
+        self.lib = B.load()
+        self.w = w
+        self.device = device
+        self.h, self.W, self.b, self.t, self.dloss = make_inputs(w.scaled(seed=w.seed + seed_offset), device)
+        N, D, V = w.n_tokens, w.hidden, w.vocab
+        self.prob = api.make_problem(N, D, V, hidden_dtype=self.h.dtype, bias_dtype=torch.bfloat16,
+                                     logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.loss = torch.empty(N if w.reduction == "none" else 1, **f32)
+        self.lse = torch.empty(N, **f32)
+        self.correct = torch.empty(1, dtype=torch.int64, device=device)
+        self.n_valid = torch.empty(1, dtype=torch.int64, device=device)
+        self.ent_sum = torch.empty(1, **f32)
+        self.dh = torch.empty_like(self.h)
+        self.dW = torch.empty_like(self.W)
+        self.db = torch.empty_like(self.b) if self.b is not None else None
+        self.ws_f = torch.empty(api.flce_workspace_size(self.prob, False), dtype=torch.uint8, device=device)
+        self.ws_b = torch.empty(api.flce_workspace_size(self.prob, True), dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.current_stream(device)
+        p = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
+        s = ctypes.c_void_p(self.stream.cuda_stream)
+        self.fwd_args = (ctypes.byref(self.prob), p(self.h), p(self.W), p(self.b), p(self.t), p(self.loss),
+                         p(self.lse), None, p(self.correct), p(self.n_valid), p(self.ent_sum), p(self.ws_f),
+                         self.ws_f.numel(), s)
+        self.bwd_args = (ctypes.byref(self.prob), p(self.h), p(self.W), p(self.b), p(self.t), p(self.lse),
+                         p(self.n_valid), p(self.dloss), p(self.dh), p(self.dW), p(self.db), p(self.ws_b),
+                         self.ws_b.numel(), s)
+
+    def step(self):
+        self.B.check(self.lib.flce_forward(*self.fwd_args), "flce_forward")
+        self.B.check(self.lib.flce_backward(*self.bwd_args), "flce_backward")
+
+    def input_bytes(self):
+        return sum(x.numel() * x.element_size() for x in (self.h, self.W, self.b, self.t, self.dloss) if x is not None)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_cross_entropy_tmem_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kind, workload):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(workload, {}).get(kind)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def flce_arm(args):
+    import torch
+
+    from linear_cross_entropy_tmem_gb300 import binding as B
+    from linear_cross_entropy_tmem_gb300.synthetic import WORKLOADS
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist("nccl")
+    w = WORKLOADS[args.workload]
+    run = Runner(w, device, seed_offset=rank)
+    lib = run.lib
+
+    for _ in range(args.warmup):
+        run.step()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region, with the launch log bracketing every kernel
+    n_launch_per_step = 64
+    cap = n_launch_per_step * args.steps
+    recs = (B.FlceLaunchRecord * cap)()
+    events = []
+    for i in range(cap):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()  # torch creates the CUDA event on its first record
+        e1.record()
+        events.append((e0, e1))
+        recs[i].begin_event = ctypes.c_void_p(e0.cuda_event)
+        recs[i].end_event = ctypes.c_void_p(e1.cuda_event)
+    count = ctypes.c_int32(0)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    launches0 = lib.flce_testing_launch_count()
+    B.check(lib.flce_testing_set_launch_log(recs, cap, ctypes.byref(count)), "launch log")
+    start.record()
+    for _ in range(args.steps):
+        run.step()
+    end.record()
+    torch.cuda.synchronize()
+    B.check(lib.flce_testing_set_launch_log(None, 0, None), "launch log")
+    launches = lib.flce_testing_launch_count() - launches0
+    barrier(dist, device)
+    clock = clocks.stop()
+    ms = start.elapsed_time(end) / args.steps
+    status = ctypes.c_int(0)
+    B.check(lib.flce_read_device_status(ctypes.c_void_p(run.ws_b.data_ptr()), None, ctypes.byref(status)), "status")
+    if status.value != 0:
+        raise RuntimeError(f"device status {status.value} during the timed region")
+
+    per_kind = {}
+    for i in range(count.value):
+        k = B.LAUNCH_KINDS[recs[i].kind]
+        d = per_kind.setdefault(k, [0, 0.0])
+        d[0] += 1
+        d[1] += events[i][0].elapsed_time(events[i][1])
+    flops_kind = 2.0 * w.n_tokens * w.vocab * w.hidden  # per step, for each GEMM kind
+    gemm_kinds = [k for k in per_kind if k != "other"]
+    dominant = max(gemm_kinds, key=lambda k: per_kind[k][1])
+    n_l, t_ms = per_kind[dominant]
+    achieved = flops_kind * args.steps / (t_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    ms_max = max_over_ranks(dist, ms, device)
+    tokens = w.n_tokens * world
+    value = tokens / (ms_max * 1e-3)
+    tflops = w.flops() * world / (ms_max * 1e-3) / 1e12
+
+    # ---- end to end through host buffers: H2D inputs, step, D2H loss + metrics
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(run, k).to("cpu").pin_memory() for k in ("h", "W", "t", "dloss")
+                if getattr(run, k) is not None}
+        if run.b is not None:
+            host["b"] = run.b.to("cpu").pin_memory()
+        out_host = torch.empty(4, dtype=torch.float64).pin_memory()
+        res = torch.empty(4, dtype=torch.float64, device=device)
+
+        def e2e_step():
+            for k, v in host.items():
+                getattr(run, k).copy_(v, non_blocking=True)
+            run.step()
+            res[0] = run.loss[0]
+            res[1] = run.correct[0]
+            res[2] = run.n_valid[0]
+            res[3] = run.ent_sum[0]
+            out_host.copy_(res, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(dist, device)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        s1.record()
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(dist, s0.elapsed_time(s1) / args.steps, device)
+        e2e = {"value": tokens / (e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in host.values())),
+               "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()),
+               "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_rows)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.hidden_dtype == torch.bfloat16 else "f32+bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "n_tokens": w.n_tokens, "hidden": w.hidden, "vocab": w.vocab,
+                       "reduction": w.reduction, "parallelism": f"replicas x{world}" if world > 1 else "none",
+                       "l2": "inputs larger than L2 (1.25 GB head), no flush"},
+            "tflops": tflops,
+            "pct_of_peak": {"of_burst": tflops / peak_burst, "of_sustained": tflops / peak, "source": peak_src},
+            "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
+                         "peak_kind": f"bf16 sustained ({peak_src})", "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": committed_traffic(dominant, args.workload),
+                         "launches": n_l, "avg_launch_ms": t_ms / n_l},
+            "kernels": {k: {"launches": v[0], "ms_per_step": v[1] / args.steps,
+                            "tflops": (flops_kind * args.steps / (v[1] * 1e-3) / 1e12) if k != "other" else None}
+                        for k, v in sorted(per_kind.items())},
+            "gpu_launches": int(launches),
+            "clocks": clock,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return reference_arm(args)
+    return flce_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

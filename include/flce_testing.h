@@ -35,6 +35,37 @@ extern "C" {
  */
 FLCE_API int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit);
 
+/* Kinds of launch recorded by the launch log. */
+enum {
+  FLCE_LAUNCH_FWD_LOGITS = 0,   /* forward logit GEMM + online statistics        */
+  FLCE_LAUNCH_BWD_RECOMPUTE = 1,/* backward logit recompute + G                   */
+  FLCE_LAUNCH_BWD_DWEIGHT = 2,  /* dW = G^T h                                     */
+  FLCE_LAUNCH_BWD_DHIDDEN = 3,  /* dh += G W                                      */
+  FLCE_LAUNCH_OTHER = 4         /* split, merge, reduce, dbias, dh finalize        */
+};
+
+/* One logged launch: two caller-created CUDA events (cudaEvent_t, timing
+ * enabled) that the library records on the call's stream right before and
+ * right after the kernel, and the kind of the kernel (written by the library). */
+typedef struct {
+  void* begin_event;
+  void* end_event;
+  int32_t kind;
+  int32_t reserved;
+} flce_launch_record;
+
+/*
+ * Profiling hook: while set, every kernel launch of flce_forward /
+ * flce_backward is bracketed by the events of records[*count], its kind is
+ * stored and *count is incremented, until *count reaches capacity.  Pass NULL
+ * records to switch it off.  `records` and `count` are host memory owned by the
+ * caller and must stay valid while the hook is set.  Not thread-safe.
+ */
+FLCE_API int flce_testing_set_launch_log(flce_launch_record* records, int32_t capacity, int32_t* count);
+
+/* Number of kernels this process has launched through the library so far. */
+FLCE_API int64_t flce_testing_launch_count(void);
+
 FLCE_API int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int64_t K, const void* A,
                       int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc, flce_stream_t stream);
 

@@ -28,6 +28,14 @@ FLCE_ERR_TIMEOUT = 8
 FLCE_ERR_UNSUPPORTED_DEVICE = 9
 
 
+class FlceLaunchRecord(ctypes.Structure):
+    """Mirror of ``flce_launch_record``."""
+    _fields_ = [("begin_event", c_void_p), ("end_event", c_void_p), ("kind", c_int32), ("reserved", c_int32)]
+
+
+LAUNCH_KINDS = {0: "fwd_logits", 1: "bwd_recompute", 2: "bwd_dweight", 3: "bwd_dhidden", 4: "other"}
+
+
 class FlceProblem(ctypes.Structure):
     """Mirror of ``flce_problem``."""
     _fields_ = [
@@ -57,6 +65,8 @@ SIGNATURES = {
     "flce_status_string": (c_char_p, [c_int]),
     "flce_abi_version": (c_int, []),
     "flce_testing_set_tuning": (c_int, [c_int64, c_int]),
+    "flce_testing_set_launch_log": (c_int, [c_void_p, c_int32, POINTER(c_int32)]),
+    "flce_testing_launch_count": (c_int64, []),
     "flce_testing_gemm": (c_int, [c_int, c_int, c_int64, c_int64, c_int64, c_void_p, c_int64, c_void_p, c_int64,
                                   c_void_p, c_int64, c_void_p]),
 }

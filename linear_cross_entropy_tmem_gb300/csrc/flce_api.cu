@@ -224,6 +224,30 @@ int choose_splits(int64_t m_tiles, int64_t n_tiles, int num_sms, int* per_unit) 
 
 int fail(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
 
+// Launch log (flce_testing_set_launch_log) and launch counter.
+flce_launch_record* g_log = nullptr;
+int32_t g_log_cap = 0;
+int32_t* g_log_count = nullptr;
+std::atomic<int64_t> g_launches{0};
+
+// Runs `launch` (returning cudaError_t) on `st`, bracketed by logged events
+// when the launch log is on; counts the launch.
+template <class F>
+int logged(int kind, cudaStream_t st, F&& launch) {
+  flce_launch_record* rec = nullptr;
+  if (g_log && g_log_count && *g_log_count < g_log_cap) rec = &g_log[*g_log_count];
+  if (rec && cudaEventRecord(static_cast<cudaEvent_t>(rec->begin_event), st) != cudaSuccess) return FLCE_ERR_CUDA;
+  const cudaError_t e = launch();
+  if (e != cudaSuccess) return FLCE_ERR_CUDA;
+  g_launches.fetch_add(1);
+  if (rec) {
+    if (cudaEventRecord(static_cast<cudaEvent_t>(rec->end_event), st) != cudaSuccess) return FLCE_ERR_CUDA;
+    rec->kind = kind;
+    ++*g_log_count;
+  }
+  return FLCE_OK;
+}
+
 #define FLCE_TRY(expr)               \
   do {                               \
     const int rc_ = (expr);          \
@@ -303,14 +327,16 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   rp.correct = correct;
   rp.n_valid = n_valid;
   rp.entropy_sum = entropy_sum;
-  if (N == 0) return fail(launch_fwd_reduce(rp, st));
+  if (N == 0) return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
 
   const bool h32 = p->hidden_dtype == FLCE_F32;
   const void* a_main = hidden;
   if (h32) {
     uint16_t* hi = reinterpret_cast<uint16_t*>(ws + L.hi);
     uint16_t* lo = reinterpret_cast<uint16_t*>(ws + L.lo);
-    FLCE_TRY(fail(launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st)));
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+      return launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st);
+    }));
     a_main = hi;
   }
   TmaMaps maps;
@@ -346,7 +372,8 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   fp.part_idx = reinterpret_cast<int32_t*>(ws + L.part_idx);
   fp.z_target = reinterpret_cast<float*>(ws + L.z_target);
   const int grid = std::min(sc.total_units, dev.num_sms);
-  FLCE_TRY(fail(launch_fwd_gemm(bias != nullptr, softcap, maps, sc, fp, status, grid, st)));
+  FLCE_TRY(logged(FLCE_LAUNCH_FWD_LOGITS, st,
+                   [&] { return launch_fwd_gemm(bias != nullptr, softcap, maps, sc, fp, status, grid, st); }));
 
   MergeParams mp{};
   mp.n_tokens = N;
@@ -365,8 +392,8 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   mp.entropy = entropy;
   mp.loss_tok = p->reduction == FLCE_RED_NONE ? loss : nullptr;
   mp.blocks = blocks;
-  FLCE_TRY(fail(launch_fwd_merge(mp, status, st)));
-  return fail(launch_fwd_reduce(rp, st));
+  FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_merge(mp, status, st); }));
+  return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
 }
 
 int flce_backward(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
@@ -402,7 +429,9 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   if (h32) {
     uint16_t* hi = reinterpret_cast<uint16_t*>(ws + L.hi);
     uint16_t* lo = reinterpret_cast<uint16_t*>(ws + L.lo);
-    FLCE_TRY(fail(launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st)));
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+      return launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st);
+    }));
     h_main = hi;
   }
   const bool softcap = p->final_logit_softcapping > 0.f;
@@ -460,12 +489,15 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     gp.g = g;
     gp.ldg = L.vc;
     gp.dbias_part = dbias_part;
-    FLCE_TRY(fail(launch_grad_gemm(bias != nullptr, softcap, rec, s1, gp, status,
-                                   std::min(s1.total_units, dev.num_sms), st)));
+    FLCE_TRY(logged(FLCE_LAUNCH_BWD_RECOMPUTE, st, [&] {
+      return launch_grad_gemm(bias != nullptr, softcap, rec, s1, gp, status, std::min(s1.total_units, dev.num_sms),
+                              st);
+    }));
     if (bias) {
-      FLCE_TRY(fail(launch_dbias_reduce(dbias_part, L.vc, s1.m_tiles, width,
-                                        static_cast<uint8_t*>(dbias) + v0 * bias_elem,
-                                        p->bias_dtype == FLCE_F32, st)));
+      FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+        return launch_dbias_reduce(dbias_part, L.vc, s1.m_tiles, width, static_cast<uint8_t*>(dbias) + v0 * bias_elem,
+                                   p->bias_dtype == FLCE_F32, st);
+      }));
     }
 
     // (2) dW[v0 : v0+width] = G^T h    (A = G MN-major, B = h MN-major, K = N)
@@ -485,7 +517,8 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     sp.out = static_cast<uint8_t*>(dweight) + size_t(v0) * D * 2;
     sp.ldo = D;
     sp.out_f32 = 0;
-    FLCE_TRY(fail(launch_store_gemm(mw, s2, sp, status, std::min(s2.total_units, dev.num_sms), st)));
+    FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
+                    [&] { return launch_store_gemm(mw, s2, sp, status, std::min(s2.total_units, dev.num_sms), st); }));
 
     // (3) dh (+)= G W[v0 : v0+width]   (A = G K-major, B = W MN-major, K = width)
     TmaMaps mh;
@@ -509,10 +542,13 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     ap.write_final = (ksplit == 1 && last) ? 1 : 0;
     ap.out = dhidden;
     ap.out_f32 = h32 ? 1 : 0;
-    FLCE_TRY(fail(launch_accum_gemm(mh, s3, ap, status, std::min(s3.total_units, dev.num_sms), st)));
+    FLCE_TRY(logged(FLCE_LAUNCH_BWD_DHIDDEN, st,
+                    [&] { return launch_accum_gemm(mh, s3, ap, status, std::min(s3.total_units, dev.num_sms), st); }));
   }
   if (ksplit > 1) {
-    FLCE_TRY(fail(launch_dh_finalize(dh_part, N * D, ksplit, N * D, dhidden, h32 ? 1 : 0, dev.num_sms * 4, st)));
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+      return launch_dh_finalize(dh_part, N * D, ksplit, N * D, dhidden, h32 ? 1 : 0, dev.num_sms * 4, st);
+    }));
   }
   return FLCE_OK;
 }
@@ -523,6 +559,16 @@ int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit) {
   g_force_dh_ksplit.store(dh_ksplit);
   return FLCE_OK;
 }
+
+int flce_testing_set_launch_log(flce_launch_record* records, int32_t capacity, int32_t* count) {
+  if (records && (capacity < 0 || !count)) return FLCE_ERR_INVALID_ARG;
+  g_log = records;
+  g_log_cap = records ? capacity : 0;
+  g_log_count = records ? count : nullptr;
+  return FLCE_OK;
+}
+
+int64_t flce_testing_launch_count(void) { return g_launches.load(); }
 
 int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                       const void* B, int64_t ldb, float* C, int64_t ldc, flce_stream_t stream) {
