@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = automatic)")
+    ap.add_argument("--tokens", type=int, default=0, help="override N (profiling captures of a small case)")
+    ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures of a small case)")
     return ap.parse_args(argv)
 
 
@@ -200,7 +202,7 @@ def reference_arm(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    w = WORKLOADS[args.workload]
+    w = pick_workload(args)
     rows = args.cpu_rows or 16
     h, W, b, t, dloss = cpu_inputs(w, rows)
     for _ in range(args.warmup):
@@ -295,6 +297,19 @@ def committed_traffic(kind, workload):
     return e.get("dram_bytes_per_launch")
 
 
+def pick_workload(args):
+    from linear_cross_entropy_tmem_gb300.synthetic import WORKLOADS
+    w = WORKLOADS[args.workload]
+    kw = {}
+    if args.tokens:
+        kw["n_tokens"] = args.tokens
+    if args.vocab:
+        kw["vocab"] = args.vocab
+    if kw:
+        w = w.scaled(name=f"{w.name} (N={kw.get('n_tokens', w.n_tokens)}, V={kw.get('vocab', w.vocab)})", **kw)
+    return w
+
+
 def flce_arm(args):
     import torch
 
@@ -306,7 +321,7 @@ def flce_arm(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist = init_dist("nccl")
-    w = WORKLOADS[args.workload]
+    w = pick_workload(args)
     run = Runner(w, device, seed_offset=rank)
     lib = run.lib
 

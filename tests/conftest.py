@@ -15,6 +15,8 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def lib():
-    """The loaded C-ABI library (built in-tree by ``__graft_entry__.build()``)."""
+    """The loaded C-ABI library (built in-tree first if missing or stale)."""
     from linear_cross_entropy_tmem_gb300 import binding
+    from linear_cross_entropy_tmem_gb300.build import build
+    build()
     return binding.load()
