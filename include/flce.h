@@ -172,6 +172,36 @@ FLCE_API int flce_backward(const flce_problem* problem, const void* hidden, cons
  */
 FLCE_API int flce_read_device_status(const void* workspace, flce_stream_t stream, int* status);
 
+/*
+ * Forward without any allocation, for callers that cannot call cudaMalloc
+ * (for example a plugin inside a host application that owns the device-memory
+ * budget and gives its plugins no allocator, or latency-critical code that
+ * cannot accept cudaMalloc's implicit device synchronisation).  The pages have
+ * no counterpart: it is flce_forward with the same arguments minus the
+ * workspace, whose scratch lives instead in a static device array of
+ * FLCE_NOALLOC_SCRATCH_BYTES that each GPU loading the library holds until the
+ * process exits.
+ *   - Problems whose forward workspace (flce_workspace_size(problem, 0)) is
+ *     larger than FLCE_NOALLOC_SCRATCH_BYTES are rejected with
+ *     FLCE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  With bf16
+ *     hidden states that admits about 26K tokens; fp32 hidden states need
+ *     4*N*D more bytes.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - All calls share the one array, which keeps the last call's contents; the
+ *     call clears what must start at zero.  Calls whose GPU work overlaps in
+ *     time race on the array.
+ *   - The caller holds no workspace, so flce_read_device_status cannot be
+ *     used: a target outside [0, V) that is not ignore_index is still treated
+ *     as ignored, but it is not reported.
+ */
+#define FLCE_NOALLOC_SCRATCH_BYTES (32u << 20)
+FLCE_API int flce_forward_noalloc(const flce_problem* problem, const void* hidden, const void* weight,
+                                  const void* bias, const int64_t* targets, float* loss, float* lse,
+                                  float* entropy, int64_t* correct, int64_t* n_valid, float* entropy_sum,
+                                  flce_stream_t stream);
+
 /* Static English description of a status code (never NULL). */
 FLCE_API const char* flce_status_string(int status);
 

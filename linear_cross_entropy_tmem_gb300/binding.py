@@ -61,6 +61,8 @@ SIGNATURES = {
                              c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "flce_backward": (c_int, [POINTER(FlceProblem), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "flce_forward_noalloc": (c_int, [POINTER(FlceProblem), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "flce_read_device_status": (c_int, [c_void_p, c_void_p, POINTER(c_int)]),
     "flce_status_string": (c_char_p, [c_int]),
     "flce_abi_version": (c_int, []),

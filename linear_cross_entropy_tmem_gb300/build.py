@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libflce.so")
-SOURCES = ["flce_api.cu", "flce_fwd.cu", "flce_bwd.cu"]
+SOURCES = ["flce_api.cu", "flce_fwd.cu", "flce_bwd.cu", "flce_noalloc.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
