@@ -84,3 +84,40 @@ def compare_backward(gpu_b, ref):
             continue
         err = oracle.relative_frobenius(g, r)
         assert err <= TOL_GRAD, (name, err)
+
+
+def oracle_forward_rowblocks(h, W, b, t, *, row_block=256, **kw):
+    """The oracle's forward applied to consecutive groups of tokens (every output
+    is per token; the scalar reductions are sums over the groups).  Inputs are
+    widened to fp64 once so that each group only pays for its own logits."""
+    hf = oracle.widen(h)
+    Wf = oracle.widen(W)
+    bf = None if b is None else oracle.widen(b)
+    tt = np.asarray(t.cpu().numpy() if hasattr(t, "cpu") else t)
+    red = kw.pop("reduction", "mean")
+    parts = [oracle.forward(hf[r:r + row_block], Wf, bf, tt[r:r + row_block], reduction="none", **kw)
+             for r in range(0, hf.shape[0], row_block)]
+    out = {k: np.concatenate([p[k] for p in parts]) for k in ("loss_tok", "lse", "entropy", "argmax", "valid")}
+    out["n_valid"] = int(sum(p["n_valid"] for p in parts))
+    out["correct"] = int(sum(p["correct"] for p in parts))
+    out["entropy_sum"] = float(sum(p["entropy_sum"] for p in parts))
+    total = float(out["loss_tok"].sum())
+    out["loss"] = {"sum": total, "mean": total / out["n_valid"] if out["n_valid"] else 0.0,
+                   "none": out["loss_tok"]}[red]
+    out["status"] = max(p["status"] for p in parts)
+    return out
+
+
+def near_tie_bounds_rowblocks(h, W, b, t, ref, *, row_block=256, logit_scale=1.0, softcap=0.0):
+    """correct_bounds() over groups of tokens (only needed when the counts differ)."""
+    hf = oracle.widen(h)
+    Wf = oracle.widen(W)
+    bf = None if b is None else oracle.widen(b)
+    tt = np.asarray(t.cpu().numpy() if hasattr(t, "cpu") else t)
+    lo = hi = 0
+    for r in range(0, hf.shape[0], row_block):
+        z = oracle.logits(hf[r:r + row_block], Wf, bf, logit_scale=logit_scale, softcap=softcap)
+        a, c = correct_bounds(z, tt[r:r + row_block], ref["valid"][r:r + row_block], ref["argmax"][r:r + row_block])
+        lo += a
+        hi += c
+    return lo, hi
