@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = automatic)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling captures of a small case)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures of a small case)")
+    ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 1, 2],
+                    help="GEMM kernel: 0 automatic, 1 single CTA, 2 CTA pair (A/B timing)")
     return ap.parse_args(argv)
 
 
@@ -324,6 +326,7 @@ def flce_arm(args):
     w = pick_workload(args)
     run = Runner(w, device, seed_offset=rank)
     lib = run.lib
+    B.check(lib.flce_testing_set_gemm_mode(args.gemm_mode), "gemm mode")
 
     for _ in range(args.warmup):
         run.step()
@@ -432,6 +435,7 @@ def flce_arm(args):
             "data": "synthetic",
             "config": {"workload": w.name, "n_tokens": w.n_tokens, "hidden": w.hidden, "vocab": w.vocab,
                        "reduction": w.reduction, "parallelism": f"replicas x{world}" if world > 1 else "none",
+                       "gemm_mode": ["auto", "single-cta", "cta-pair"][args.gemm_mode],
                        "l2": "inputs larger than L2 (1.25 GB head), no flush"},
             "tflops": tflops,
             "pct_of_peak": {"of_burst": tflops / peak_burst, "of_sustained": tflops / peak, "source": peak_src},

@@ -35,6 +35,13 @@ extern "C" {
  */
 FLCE_API int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit);
 
+/*
+ * Process-wide choice of GEMM kernel, for tests and A/B timing: 0 automatic
+ * (CTA pairs with 256-row tiles when there are at least 256 rows and enough
+ * tiles, else single CTAs), 1 single-CTA kernel only, 2 CTA-pair kernel only.
+ */
+FLCE_API int flce_testing_set_gemm_mode(int mode);
+
 /* Kinds of launch recorded by the launch log. */
 enum {
   FLCE_LAUNCH_FWD_LOGITS = 0,   /* forward logit GEMM + online statistics        */

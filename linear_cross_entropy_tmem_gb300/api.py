@@ -195,3 +195,8 @@ def testing_gemm(A: torch.Tensor, B_: torch.Tensor, *, a_mn_major: bool, b_mn_ma
 
 def testing_set_tuning(chunk_cols: int = 0, dh_ksplit: int = 0) -> None:
     B.check(B.load().flce_testing_set_tuning(int(chunk_cols), int(dh_ksplit)), "flce_testing_set_tuning")
+
+
+def testing_set_gemm_mode(mode: int = 0) -> None:
+    """0 automatic, 1 single-CTA GEMM kernel only, 2 CTA-pair kernel only (tests, A/B timing)."""
+    B.check(B.load().flce_testing_set_gemm_mode(int(mode)), "flce_testing_set_gemm_mode")

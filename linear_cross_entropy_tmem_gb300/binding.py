@@ -67,6 +67,7 @@ SIGNATURES = {
     "flce_status_string": (c_char_p, [c_int]),
     "flce_abi_version": (c_int, []),
     "flce_testing_set_tuning": (c_int, [c_int64, c_int]),
+    "flce_testing_set_gemm_mode": (c_int, [c_int]),
     "flce_testing_set_launch_log": (c_int, [c_void_p, c_int32, POINTER(c_int32)]),
     "flce_testing_launch_count": (c_int64, []),
     "flce_testing_gemm": (c_int, [c_int, c_int, c_int64, c_int64, c_int64, c_void_p, c_int64, c_void_p, c_int64,

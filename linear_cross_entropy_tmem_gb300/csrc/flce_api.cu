@@ -117,9 +117,19 @@ struct Layout {
   bool need_dh_part = false;
 };
 
-// Test/tuning overrides (flce_testing_set_tuning); 0 = automatic.
+// Test/tuning overrides (flce_testing_set_tuning, flce_testing_set_gemm_mode); 0 = automatic.
 std::atomic<int64_t> g_force_chunk_cols{0};
 std::atomic<int> g_force_dh_ksplit{0};
+std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel
+
+// CTA pairs (256-row tiles) when there are at least 256 rows and enough units
+// to give every cluster work; otherwise single CTAs (128-row tiles).
+bool use_pair(int64_t m_rows, int64_t units_per_pair_row, int num_sms) {
+  const int mode = g_gemm_mode.load();
+  if (mode == 1) return false;
+  if (mode == 2) return true;
+  return m_rows >= kPairRows && cdiv(m_rows, kPairRows) * units_per_pair_row >= num_sms / 2;
+}
 
 int64_t chunk_width(int64_t n_tokens, int64_t vocab) {
   const int64_t forced = g_force_chunk_cols.load();
@@ -178,9 +188,9 @@ Layout make_layout(const flce_problem* p, bool backward, bool has_bias) {
   return L;
 }
 
-GemmSched base_sched(int64_t m_rows, int64_t n_cols, int64_t k, int nseg, int seg_a) {
+GemmSched base_sched(int64_t m_rows, int64_t n_cols, int64_t k, int nseg, int seg_a, bool pair = false) {
   GemmSched s{};
-  s.m_tiles = static_cast<int32_t>(cdiv(m_rows, kBM));
+  s.m_tiles = static_cast<int32_t>(cdiv(m_rows, pair ? kPairRows : kBM));
   s.n_tiles = static_cast<int32_t>(cdiv(n_cols, kBN));
   s.k_blocks = static_cast<int32_t>(cdiv(k, kBK));
   s.nseg = nseg;
@@ -339,18 +349,19 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
     }));
     a_main = hi;
   }
+  const bool pair = use_pair(N, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
   TmaMaps maps;
   FLCE_TRY(make_map(&maps.a0, a_main, D, N, D * 2, kBK, kBM));
   maps.a1 = maps.a0;
   if (h32) FLCE_TRY(make_map(&maps.a1, ws + L.lo, D, N, D * 2, kBK, kBM));
-  FLCE_TRY(make_map(&maps.b0, weight, D, V, D * 2, kBK, kBN));
+  FLCE_TRY(make_map(&maps.b0, weight, D, V, D * 2, kBK, pair ? kBN / 2 : kBN));
   maps.b1 = maps.b0;
 
-  GemmSched sc = base_sched(N, V, D, h32 ? 2 : 1, 1);
+  GemmSched sc = base_sched(N, V, D, h32 ? 2 : 1, 1, pair);
   int per_unit = 1;
-  const int splits = choose_splits(sc.m_tiles, sc.n_tiles, dev.num_sms, &per_unit);
+  const int splits = choose_splits(sc.m_tiles, sc.n_tiles, pair ? dev.num_sms / 2 : dev.num_sms, &per_unit);
   sc.n_per_unit = per_unit;
-  sc.group_m = 32;
+  sc.group_m = pair ? 16 : 32;
   finish_sched(sc);
 
   const bool softcap = p->final_logit_softcapping > 0.f;
@@ -371,9 +382,8 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   fp.part_best = reinterpret_cast<float*>(ws + L.part_best);
   fp.part_idx = reinterpret_cast<int32_t*>(ws + L.part_idx);
   fp.z_target = reinterpret_cast<float*>(ws + L.z_target);
-  const int grid = std::min(sc.total_units, dev.num_sms);
   FLCE_TRY(logged(FLCE_LAUNCH_FWD_LOGITS, st,
-                   [&] { return launch_fwd_gemm(bias != nullptr, softcap, maps, sc, fp, status, grid, st); }));
+                   [&] { return launch_fwd_gemm(bias != nullptr, softcap, pair, maps, sc, fp, status, dev.num_sms, st); }));
 
   MergeParams mp{};
   mp.n_tokens = N;
@@ -440,11 +450,12 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   float* dh_part = L.need_dh_part ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
 
   // Maps that do not change across chunks.
+  const bool pair_rec = use_pair(N, cdiv(L.vc, kBN), dev.num_sms);
   TmaMaps rec;  // recompute: A = h (K-major), B = W (K-major)
   FLCE_TRY(make_map(&rec.a0, h_main, D, N, D * 2, kBK, kBM));
   rec.a1 = rec.a0;
   if (h32) FLCE_TRY(make_map(&rec.a1, ws + L.lo, D, N, D * 2, kBK, kBM));
-  FLCE_TRY(make_map(&rec.b0, weight, D, V, D * 2, kBK, kBN));
+  FLCE_TRY(make_map(&rec.b0, weight, D, V, D * 2, kBK, pair_rec ? kBN / 2 : kBN));
   rec.b1 = rec.b0;
   CUtensorMap h_mn, lo_mn, w_mn;  // MN-major views: h for dW, W for dh
   FLCE_TRY(make_map(&h_mn, h_main, D, N, D * 2, 64, kBK));
@@ -452,13 +463,16 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   if (h32) FLCE_TRY(make_map(&lo_mn, ws + L.lo, D, N, D * 2, 64, kBK));
   FLCE_TRY(make_map(&w_mn, weight, D, V, D * 2, 64, kBK));
 
-  // dh K split for this device (bounded by the layout's slot count).
-  const int64_t dh_tiles = cdiv(N, kBM) * cdiv(D, kBN);
+  // dh: CTA pairs or single CTAs, and the K split for this device (bounded by
+  // the layout's slot count).
+  const bool pair_dh = use_pair(N, cdiv(D, kBN), dev.num_sms);
+  const int dh_ctas = pair_dh ? dev.num_sms / 2 : dev.num_sms;
+  const int64_t dh_tiles = cdiv(N, pair_dh ? kPairRows : kBM) * cdiv(D, kBN);
   int ksplit = 1;
   if (g_force_dh_ksplit.load() > 0) {
     ksplit = L.ksplit_max;
   } else if (L.ksplit_max > 1) {
-    ksplit = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(L.ksplit_max, dev.num_sms / dh_tiles)));
+    ksplit = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(L.ksplit_max, dh_ctas / dh_tiles)));
   }
 
   for (int64_t c = 0; c < L.n_chunks; ++c) {
@@ -467,9 +481,9 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     const bool first = c == 0, last = c == L.n_chunks - 1;
 
     // (1) recompute the logits of the chunk and form G (bf16) + dbias partials
-    GemmSched s1 = base_sched(N, width, D, h32 ? 2 : 1, 1);
+    GemmSched s1 = base_sched(N, width, D, h32 ? 2 : 1, 1, pair_rec);
     s1.b_mn_off = static_cast<int32_t>(v0);
-    s1.group_m = 32;
+    s1.group_m = pair_rec ? 16 : 32;
     finish_sched(s1);
     GradParams gp{};
     gp.n_tokens = N;
@@ -490,12 +504,12 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     gp.ldg = L.vc;
     gp.dbias_part = dbias_part;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_RECOMPUTE, st, [&] {
-      return launch_grad_gemm(bias != nullptr, softcap, rec, s1, gp, status, std::min(s1.total_units, dev.num_sms),
-                              st);
+      return launch_grad_gemm(bias != nullptr, softcap, pair_rec, rec, s1, gp, status, dev.num_sms, st);
     }));
     if (bias) {
       FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-        return launch_dbias_reduce(dbias_part, L.vc, s1.m_tiles, width, static_cast<uint8_t*>(dbias) + v0 * bias_elem,
+        return launch_dbias_reduce(dbias_part, L.vc, static_cast<int>(cdiv(N, kBM)), width,
+                                   static_cast<uint8_t*>(dbias) + v0 * bias_elem,
                                    p->bias_dtype == FLCE_F32, st);
       }));
     }
@@ -506,10 +520,11 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     mw.a1 = mw.a0;
     mw.b0 = h_mn;
     mw.b1 = lo_mn;
-    GemmSched s2 = base_sched(width, D, N, h32 ? 2 : 1, 0);
+    const bool pair_dw = use_pair(width, cdiv(D, kBN), dev.num_sms);
+    GemmSched s2 = base_sched(width, D, N, h32 ? 2 : 1, 0, pair_dw);
     s2.a_mn = 1;
     s2.b_mn = 1;
-    s2.group_m = std::max(1, dev.num_sms / std::max(1, s2.n_tiles));
+    s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
     finish_sched(s2);
     StoreParams sp{};
     sp.rows = width;
@@ -518,7 +533,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     sp.ldo = D;
     sp.out_f32 = 0;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
-                    [&] { return launch_store_gemm(mw, s2, sp, status, std::min(s2.total_units, dev.num_sms), st); }));
+                    [&] { return launch_store_gemm(pair_dw, mw, s2, sp, status, dev.num_sms, st); }));
 
     // (3) dh (+)= G W[v0 : v0+width]   (A = G K-major, B = W MN-major, K = width)
     TmaMaps mh;
@@ -526,12 +541,12 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     mh.a1 = mh.a0;
     mh.b0 = w_mn;
     mh.b1 = w_mn;
-    GemmSched s3 = base_sched(N, D, width, 1, 0);
+    GemmSched s3 = base_sched(N, D, width, 1, 0, pair_dh);
     s3.b_mn = 1;
     s3.b_k_off = static_cast<int32_t>(v0);
     s3.ksplit = ksplit;
     s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
-    s3.group_m = std::max(1, dev.num_sms / std::max(1, s3.n_tiles * ksplit));
+    s3.group_m = std::max(1, dh_ctas / std::max(1, s3.n_tiles * ksplit));
     finish_sched(s3);
     AccumParams ap{};
     ap.rows = N;
@@ -543,7 +558,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     ap.out = dhidden;
     ap.out_f32 = h32 ? 1 : 0;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_DHIDDEN, st,
-                    [&] { return launch_accum_gemm(mh, s3, ap, status, std::min(s3.total_units, dev.num_sms), st); }));
+                    [&] { return launch_accum_gemm(pair_dh, mh, s3, ap, status, dev.num_sms, st); }));
   }
   if (ksplit > 1) {
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
@@ -557,6 +572,12 @@ int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit) {
   if (chunk_cols < 0 || dh_ksplit < 0 || dh_ksplit > kMaxKSplit) return FLCE_ERR_INVALID_ARG;
   g_force_chunk_cols.store(chunk_cols);
   g_force_dh_ksplit.store(dh_ksplit);
+  return FLCE_OK;
+}
+
+int flce_testing_set_gemm_mode(int mode) {
+  if (mode < 0 || mode > 2) return FLCE_ERR_INVALID_ARG;
+  g_gemm_mode.store(mode);
   return FLCE_OK;
 }
 
@@ -578,14 +599,15 @@ int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int6
   DeviceInfo dev;
   FLCE_TRY(get_device(&dev));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool pair = use_pair(M, cdiv(N, kBN), dev.num_sms);
   TmaMaps m;
   if (!a_mn_major) FLCE_TRY(make_map(&m.a0, A, K, M, lda * 2, kBK, kBM));
   else FLCE_TRY(make_map(&m.a0, A, M, K, lda * 2, 64, kBK));
-  if (!b_mn_major) FLCE_TRY(make_map(&m.b0, B, K, N, ldb * 2, kBK, kBN));
+  if (!b_mn_major) FLCE_TRY(make_map(&m.b0, B, K, N, ldb * 2, kBK, pair ? kBN / 2 : kBN));
   else FLCE_TRY(make_map(&m.b0, B, N, K, ldb * 2, 64, kBK));
   m.a1 = m.a0;
   m.b1 = m.b0;
-  GemmSched s = base_sched(M, N, K, 1, 0);
+  GemmSched s = base_sched(M, N, K, 1, 0, pair);
   s.a_mn = a_mn_major ? 1 : 0;
   s.b_mn = b_mn_major ? 1 : 0;
   finish_sched(s);
@@ -595,7 +617,7 @@ int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int6
   sp.out = C;
   sp.ldo = ldc;
   sp.out_f32 = 1;
-  return fail(launch_store_gemm(m, s, sp, nullptr, std::min(s.total_units, dev.num_sms), st));
+  return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_store_gemm(pair, m, s, sp, nullptr, dev.num_sms, st); });
 }
 
 }  // extern "C"

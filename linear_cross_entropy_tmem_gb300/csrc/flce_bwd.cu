@@ -3,37 +3,26 @@
 // accumulate GEMM, the ordered dbias reduction and the dh K-split finalize.
 #include <cuda_runtime.h>
 
-#include "flce_gemm.cuh"
-#include "flce_launch.h"
+#include "flce_gemm_launch.cuh"
 
 namespace flce {
 
-template <class Epi>
-static cudaError_t launch_gemm_impl(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
-                                    int* status, int grid, cudaStream_t stream) {
-  auto kern = gemm_kernel<Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, kGemmSmemBytes, stream>>>(m.a0, m.a1, m.b0, m.b1, sc, p, status);
-  return cudaGetLastError();
+cudaError_t launch_grad_gemm(bool bias, bool softcap, bool pair, const TmaMaps& maps, const GemmSched& sc,
+                             const GradParams& p, int* status, int num_sms, cudaStream_t stream) {
+  if (bias && softcap) return launch_gemm<EpiGrad<true, true>>(pair, maps, sc, p, status, num_sms, stream);
+  if (bias) return launch_gemm<EpiGrad<true, false>>(pair, maps, sc, p, status, num_sms, stream);
+  if (softcap) return launch_gemm<EpiGrad<false, true>>(pair, maps, sc, p, status, num_sms, stream);
+  return launch_gemm<EpiGrad<false, false>>(pair, maps, sc, p, status, num_sms, stream);
 }
 
-cudaError_t launch_grad_gemm(bool bias, bool softcap, const TmaMaps& maps, const GemmSched& sc,
-                             const GradParams& p, int* status, int grid, cudaStream_t stream) {
-  if (bias && softcap) return launch_gemm_impl<EpiGrad<true, true>>(maps, sc, p, status, grid, stream);
-  if (bias) return launch_gemm_impl<EpiGrad<true, false>>(maps, sc, p, status, grid, stream);
-  if (softcap) return launch_gemm_impl<EpiGrad<false, true>>(maps, sc, p, status, grid, stream);
-  return launch_gemm_impl<EpiGrad<false, false>>(maps, sc, p, status, grid, stream);
+cudaError_t launch_store_gemm(bool pair, const TmaMaps& maps, const GemmSched& sc, const StoreParams& p,
+                              int* status, int num_sms, cudaStream_t stream) {
+  return launch_gemm<EpiStore>(pair, maps, sc, p, status, num_sms, stream);
 }
 
-cudaError_t launch_store_gemm(const TmaMaps& maps, const GemmSched& sc, const StoreParams& p, int* status,
-                              int grid, cudaStream_t stream) {
-  return launch_gemm_impl<EpiStore>(maps, sc, p, status, grid, stream);
-}
-
-cudaError_t launch_accum_gemm(const TmaMaps& maps, const GemmSched& sc, const AccumParams& p, int* status,
-                              int grid, cudaStream_t stream) {
-  return launch_gemm_impl<EpiAccum>(maps, sc, p, status, grid, stream);
+cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& sc, const AccumParams& p,
+                              int* status, int num_sms, cudaStream_t stream) {
+  return launch_gemm<EpiAccum>(pair, maps, sc, p, status, num_sms, stream);
 }
 
 // dbias[j] = sum over m tiles of the per-tile column sums, in m order.

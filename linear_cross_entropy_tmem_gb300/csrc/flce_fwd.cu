@@ -3,27 +3,16 @@
 // deterministic reduction, and the fp32-hidden hi/lo split.
 #include <cuda_runtime.h>
 
-#include "flce_gemm.cuh"
-#include "flce_launch.h"
+#include "flce_gemm_launch.cuh"
 
 namespace flce {
 
-template <class Epi>
-static cudaError_t launch_gemm_impl(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
-                                    int* status, int grid, cudaStream_t stream) {
-  auto kern = gemm_kernel<Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, kGemmSmemBytes, stream>>>(m.a0, m.a1, m.b0, m.b1, sc, p, status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_fwd_gemm(bool bias, bool softcap, const TmaMaps& maps, const GemmSched& sc,
-                            const FwdParams& p, int* status, int grid, cudaStream_t stream) {
-  if (bias && softcap) return launch_gemm_impl<EpiFwd<true, true>>(maps, sc, p, status, grid, stream);
-  if (bias) return launch_gemm_impl<EpiFwd<true, false>>(maps, sc, p, status, grid, stream);
-  if (softcap) return launch_gemm_impl<EpiFwd<false, true>>(maps, sc, p, status, grid, stream);
-  return launch_gemm_impl<EpiFwd<false, false>>(maps, sc, p, status, grid, stream);
+cudaError_t launch_fwd_gemm(bool bias, bool softcap, bool pair, const TmaMaps& maps, const GemmSched& sc,
+                            const FwdParams& p, int* status, int num_sms, cudaStream_t stream) {
+  if (bias && softcap) return launch_gemm<EpiFwd<true, true>>(pair, maps, sc, p, status, num_sms, stream);
+  if (bias) return launch_gemm<EpiFwd<true, false>>(pair, maps, sc, p, status, num_sms, stream);
+  if (softcap) return launch_gemm<EpiFwd<false, true>>(pair, maps, sc, p, status, num_sms, stream);
+  return launch_gemm<EpiFwd<false, false>>(pair, maps, sc, p, status, num_sms, stream);
 }
 
 // ---------------------------------------------------------------------------

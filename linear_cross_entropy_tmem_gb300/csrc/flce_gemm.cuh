@@ -36,9 +36,11 @@ namespace flce {
 
 struct Unit {
   int m_blk, n_unit, n_first, n_count, kb_first, kb_count, ks;
+  int64_t row0;  // first output row of this CTA's 128-row slice of the tile
 };
 
-__device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u) {
+__device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u, int rows_per_tile = kBM,
+                                            uint32_t rank = 0) {
   const int per_m = sc.n_units * sc.ksplit;
   const int per_group = sc.group_m * per_m;
   const int g = u / per_group;
@@ -55,6 +57,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u) {
   t.n_count = min(sc.n_per_unit, sc.n_tiles - t.n_first);
   t.kb_first = t.ks * sc.kb_per_split;
   t.kb_count = max(0, min(sc.kb_per_split, sc.k_blocks - t.kb_first));
+  t.row0 = static_cast<int64_t>(t.m_blk) * rows_per_tile + static_cast<int64_t>(rank) * kBM;
   return t;
 }
 
@@ -91,7 +94,7 @@ struct EpiFwd {
   };
 
   __device__ static void begin_unit(const Params& p, const Unit& u, State& st) {
-    st.row = static_cast<int64_t>(u.m_blk) * kBM + threadIdx.x;
+    st.row = u.row0 + threadIdx.x;
     st.target = st.row < p.n_tokens ? __ldg(p.targets + st.row) : p.ignore_index;
     st.m = -INFINITY;
     st.s = 0.f;
@@ -203,7 +206,7 @@ struct EpiGrad {
   };
 
   __device__ static void begin_unit(const Params& p, const Unit& u, State& st) {
-    st.row = static_cast<int64_t>(u.m_blk) * kBM + threadIdx.x;
+    st.row = u.row0 + threadIdx.x;
     st.target = p.ignore_index;
     st.lse2 = 0.f;
     st.w = 0.f;
@@ -287,7 +290,7 @@ struct EpiGrad {
         const int col = threadIdx.x + h * kEpilogueThreads;
         const float s = epi_smem[col] + epi_smem[kBN + col] + epi_smem[2 * kBN + col] + epi_smem[3 * kBN + col];
         if (v_tile + col < p.vocab)
-          p.dbias_part[static_cast<int64_t>(u.m_blk) * p.ldg + col_tile + col] = s;
+          p.dbias_part[(u.row0 / kBM) * p.ldg + col_tile + col] = s;
       }
       epilogue_bar_sync();
     }
@@ -305,7 +308,7 @@ struct EpiStore {
     int64_t row;
   };
   __device__ static void begin_unit(const Params&, const Unit& u, State& st) {
-    st.row = static_cast<int64_t>(u.m_blk) * kBM + threadIdx.x;
+    st.row = u.row0 + threadIdx.x;
   }
   __device__ static void tile(const Params& p, const Unit&, int n_tile, uint32_t taddr, State& st, float*) {
 #pragma unroll 1
@@ -361,7 +364,7 @@ struct EpiAccum {
     int64_t row;
   };
   __device__ static void begin_unit(const Params&, const Unit& u, State& st) {
-    st.row = static_cast<int64_t>(u.m_blk) * kBM + threadIdx.x;
+    st.row = u.row0 + threadIdx.x;
   }
   __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*) {
 #pragma unroll 1
@@ -662,6 +665,238 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+
+// ============================================================================
+// The CTA-pair kernel (cta_group::2): a cluster of two CTAs computes a 256 x 256
+// tile.  Each CTA loads its own 128 rows of A and its own half of B (no TMA
+// multicast); the leader CTA's MMA thread issues M=256 MMAs that read both
+// CTAs' shared memory and write 128 x 256 fp32 into each CTA's TMEM.
+//   full[s]    in the leader: both CTAs' copies of stage s complete on it
+//   empty[s]   in each CTA: multicast commit from the leader's MMA thread
+//   tfull[b]   in each CTA: multicast commit, accumulator b ready
+//   tempty[b]  in the leader: 4 epilogue warps of each CTA arrive (8 total)
+// ============================================================================
+__device__ __forceinline__ GemmSmem carve_smem_pair(uint8_t* raw) {
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  GemmSmem s;
+  s.a = base;
+  s.b = base + kStagesPair * kATileBytes;
+  uint8_t* bar = s.b + kStagesPair * kBHalfBytes;
+  s.full = reinterpret_cast<uint64_t*>(bar);
+  s.empty = s.full + kStagesPair;
+  s.tfull = s.empty + kStagesPair;
+  s.tempty = s.tfull + kAccBufs;
+  s.drain = s.tempty + kAccBufs;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+  s.ctl = reinterpret_cast<CtaControl*>(s.tmem_slot + 2);
+  s.epi = reinterpret_cast<float*>(bar + kBarrierBytes);
+  return s;
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
+}
+
+template <class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
+                     const __grid_constant__ CUtensorMap map_b0, const __grid_constant__ CUtensorMap map_b1,
+                     const GemmSched sc, const typename Epi::Params ep, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  GemmSmem sm = carve_smem_pair(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == kTmaWarp * 32) {
+    for (int s = 0; s < kStagesPair; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(&sm.tfull[b], 1);
+      mbar_init(&sm.tempty[b], 2 * kEpilogueWarps);
+    }
+    mbar_init(sm.drain, 1);
+    sm.ctl->abort = 0u;
+    fence_mbar_init();
+    tma_prefetch_map(&map_a0);
+    tma_prefetch_map(&map_b0);
+    if (sc.nseg > 1) tma_prefetch_map(sc.seg_a ? &map_a1 : &map_b1);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(sm.tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised, TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = *sm.tmem_slot;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+  bool aborted = false;
+
+  if (warp == kTmaWarp) {
+    // ---------------------------------------------------------------- producers (both CTAs)
+    if (elect_one()) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_phase[kStagesPair];
+      bool issued[kStagesPair];
+#pragma unroll
+      for (int s = 0; s < kStagesPair; ++s) {
+        issued[s] = false;
+        issued_phase[s] = 0;
+      }
+      bool ok = true;
+      for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
+        const Unit u = decode_unit(sc, uu, kPairRows, rank);
+        const int a_row = sc.a_mn_off + static_cast<int>(u.row0);
+        for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
+          const int b_col = sc.b_mn_off + n * kBN + static_cast<int>(rank) * (kBN / 2);
+          for (int seg = 0; ok && seg < sc.nseg; ++seg) {
+            const CUtensorMap* ma = (seg && sc.seg_a) ? &map_a1 : &map_a0;
+            const CUtensorMap* mb = (seg && !sc.seg_a) ? &map_b1 : &map_b0;
+            for (int kb = u.kb_first; kb < u.kb_first + u.kb_count; ++kb) {
+              if (!mbar_wait(&sm.empty[stage], phase ^ 1u, sm.ctl, status)) {
+                ok = false;
+                break;
+              }
+              const uint32_t fb = map_to_cta(smem_u32(&sm.full[stage]), 0);
+              if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * kStagePairBytes);
+              uint8_t* sa = sm.a + stage * kATileBytes;
+              uint8_t* sb = sm.b + stage * kBHalfBytes;
+              const int k = kb * kBK;
+              if (!sc.a_mn) {
+                tma_load_2d_pair(sa, ma, fb, sc.a_k_off + k, a_row);
+              } else {
+#pragma unroll
+                for (int j = 0; j < kBM / 64; ++j)
+                  tma_load_2d_pair(sa + j * kMnAtomBytes, ma, fb, a_row + 64 * j, sc.a_k_off + k);
+              }
+              if (!sc.b_mn) {
+                tma_load_2d_pair(sb, mb, fb, sc.b_k_off + k, b_col);
+              } else {
+#pragma unroll
+                for (int j = 0; j < kBN / 128; ++j)
+                  tma_load_2d_pair(sb + j * kMnAtomBytes, mb, fb, b_col + 64 * j, sc.b_k_off + k);
+              }
+              issued[stage] = true;
+              issued_phase[stage] = phase;
+              if (++stage == kStagesPair) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+        }
+      }
+      if (!ok) aborted = true;
+      // The leader's full barriers count both CTAs' copies: wait for them to land.
+      if (leader) {
+#pragma unroll
+        for (int s = 0; s < kStagesPair; ++s)
+          if (issued[s]) mbar_wait_teardown(&sm.full[s], issued_phase[s]);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer (leader only)
+    if (leader && elect_one()) {
+      const uint32_t idesc = instr_desc_bf16(kPairRows, kBN, sc.a_mn, sc.b_mn);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
+        const Unit u = decode_unit(sc, uu, kPairRows, rank);
+        for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
+          if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, sm.ctl, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kBN;
+          uint32_t accumulate = 0;
+          for (int seg = 0; ok && seg < sc.nseg; ++seg) {
+            for (int kb = 0; kb < u.kb_count; ++kb) {
+              if (!mbar_wait(&sm.full[stage], phase, sm.ctl, status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a_base = smem_u32(sm.a + stage * kATileBytes);
+              const uint32_t b_base = smem_u32(sm.b + stage * kBHalfBytes);
+#pragma unroll
+              for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                const uint64_t ad = sc.a_mn ? smem_desc_sw128(a_base + kk * 2048, kMnAtomBytes, 1024)
+                                            : smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                const uint64_t bd = sc.b_mn ? smem_desc_sw128(b_base + kk * 2048, kMnAtomBytes, 1024)
+                                            : smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+                accumulate = 1;
+              }
+              umma_commit_pair(&sm.empty[stage], 0x3);  // stage free in both CTAs
+              if (++stage == kStagesPair) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+          if (!ok) break;
+          umma_commit_pair(&sm.tfull[acc], 0x3);  // accumulator ready in both CTAs
+          if (++acc == kAccBufs) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) aborted = true;
+      umma_commit_pair(sm.drain, 0x1);
+      mbar_wait_teardown(sm.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    uint32_t acc = 0, acc_phase = 0;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+    for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
+      const Unit u = decode_unit(sc, uu, kPairRows, rank);
+      typename Epi::State st;
+      Epi::begin_unit(ep, u, st);
+      for (int n = u.n_first; n < u.n_first + u.n_count; ++n) {
+        const bool got = mbar_wait(&sm.tfull[acc], acc_phase, sm.ctl, status);
+        if (!epilogue_all(got)) {
+          sm.ctl->abort = 1u;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        Epi::tile(ep, u, n, tmem_base + lane_base + acc * kBN, st, sm.epi);
+        tc_fence_before();
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&sm.tempty[acc]), 0));
+        if (++acc == kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (ok) Epi::end_unit(ep, u, st);
+    }
+    if (!ok) aborted = true;
+  }
+
+  // After an abort, copies the other CTA issued may still be in flight toward
+  // this CTA's shared memory or barriers: give them time to land.
+  if (aborted || sm.ctl->abort) spin_ns(100000);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 

@@ -1,0 +1,65 @@
+// flce_gemm_launch.cuh — launch helpers for the two GEMM kernels (single CTA
+// and CTA pair), shared by flce_fwd.cu and flce_bwd.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "flce_gemm.cuh"
+#include "flce_launch.h"
+
+namespace flce {
+
+template <class Epi>
+static cudaError_t launch_gemm_single(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
+                                      int* status, int num_sms, cudaStream_t stream) {
+  auto kern = gemm_kernel<Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(sc.total_units, num_sms));
+  kern<<<grid, kThreads, kGemmSmemBytes, stream>>>(m.a0, m.a1, m.b0, m.b1, sc, p, status);
+  return cudaGetLastError();
+}
+
+template <class Epi>
+static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
+                                    int* status, int num_sms, cudaStream_t stream) {
+  auto kern = gemm_pair_kernel<Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmPairSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kGemmPairSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Clusters that can be resident at once (one CTA per SM), cached per device.
+  static int resident[64] = {0};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (resident[dev] == 0) {
+    cfg.gridDim = dim3(2 * std::max(1, num_sms / 2));
+    int n = 0;
+    if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
+    resident[dev] = std::max(1, n);
+  }
+  const int clusters = std::max(1, std::min(std::min(sc.total_units, num_sms / 2), resident[dev]));
+  cfg.gridDim = dim3(2 * clusters);
+  return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.b0, m.b1, sc, p, status);
+}
+
+template <class Epi>
+static cudaError_t launch_gemm(bool pair, const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
+                               int* status, int num_sms, cudaStream_t stream) {
+  return pair ? launch_gemm_pair<Epi>(m, sc, p, status, num_sms, stream)
+              : launch_gemm_single<Epi>(m, sc, p, status, num_sms, stream);
+}
+
+}  // namespace flce

@@ -20,6 +20,13 @@ constexpr int kBTileBytes = kBN * kBK * 2;         // 32 KB
 constexpr int kMnAtomBytes = 64 * kBK * 2;         // 8 KB: 64 MN elements x 64 K rows
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
 
+// CTA-pair (cta_group::2) tiles: each CTA holds its 128 rows of A and its half
+// (128 of 256 columns) of B, so a stage is 32 KB per CTA and six fit.
+constexpr int kPairRows = 2 * kBM;                  // tile rows per CTA pair
+constexpr int kStagesPair = 6;
+constexpr int kBHalfBytes = (kBN / 2) * kBK * 2;    // 16 KB
+constexpr int kStagePairBytes = kATileBytes + kBHalfBytes;
+
 constexpr int kEpilogueWarps = 4;                   // warps 0..3: one TMEM lane quarter each
 constexpr int kEpilogueThreads = kEpilogueWarps * 32;
 constexpr int kTmaWarp = 4;
@@ -29,6 +36,8 @@ constexpr int kThreads = 6 * 32;
 constexpr int kEpiSmemBytes = kEpilogueWarps * kBN * 4;   // column-sum staging (dbias)
 constexpr int kBarrierBytes = 256;
 constexpr int kGemmSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarrierBytes + kEpiSmemBytes;
+constexpr int kGemmPairSmemBytes =
+    1024 /*alignment slack*/ + kStagesPair * kStagePairBytes + kBarrierBytes + kEpiSmemBytes;
 
 // A bounded wait inside a kernel gives up after this much wall time.
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;

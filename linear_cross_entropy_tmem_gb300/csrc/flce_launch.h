@@ -47,14 +47,16 @@ struct ReduceParams {
 
 constexpr int kMergeThreads = 256;
 
-cudaError_t launch_fwd_gemm(bool bias, bool softcap, const TmaMaps& maps, const GemmSched& sc,
-                            const FwdParams& p, int* status, int grid, cudaStream_t stream);
-cudaError_t launch_grad_gemm(bool bias, bool softcap, const TmaMaps& maps, const GemmSched& sc,
-                             const GradParams& p, int* status, int grid, cudaStream_t stream);
-cudaError_t launch_store_gemm(const TmaMaps& maps, const GemmSched& sc, const StoreParams& p, int* status,
-                              int grid, cudaStream_t stream);
-cudaError_t launch_accum_gemm(const TmaMaps& maps, const GemmSched& sc, const AccumParams& p, int* status,
-                              int grid, cudaStream_t stream);
+// GEMM launches.  `pair` selects the CTA-pair kernel (clusters of two CTAs,
+// 256-row tiles); `num_sms` bounds the persistent grid (CTAs, or 2 x clusters).
+cudaError_t launch_fwd_gemm(bool bias, bool softcap, bool pair, const TmaMaps& maps, const GemmSched& sc,
+                            const FwdParams& p, int* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_grad_gemm(bool bias, bool softcap, bool pair, const TmaMaps& maps, const GemmSched& sc,
+                             const GradParams& p, int* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_store_gemm(bool pair, const TmaMaps& maps, const GemmSched& sc, const StoreParams& p,
+                              int* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& sc, const AccumParams& p,
+                              int* status, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_split_hidden(const float* h, uint16_t* hi, uint16_t* lo, int64_t n, int grid,
                                 cudaStream_t stream);

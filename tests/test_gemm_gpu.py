@@ -20,10 +20,19 @@ def _store(x: torch.Tensor, mn_major: bool) -> torch.Tensor:
     return s
 
 
+@pytest.fixture
+def gemm_mode(request):
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode
+    testing_set_gemm_mode(request.param)
+    yield request.param
+    testing_set_gemm_mode(0)
+
+
+@pytest.mark.parametrize("gemm_mode", [1, 2], indirect=True, ids=["single-cta", "cta-pair"])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (1, 1), (0, 1), (1, 0)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 200), (1, 8, 8), (257, 1000, 1032),
                                    (640, 768, 4096)])
-def test_gemm_layouts_match_fp64(lib, a_mn, b_mn, M, N, K):
+def test_gemm_layouts_match_fp64(lib, gemm_mode, a_mn, b_mn, M, N, K):
     from linear_cross_entropy_tmem_gb300.api import testing_gemm
     g = torch.Generator().manual_seed(M * 7 + N * 3 + K)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)

@@ -38,9 +38,10 @@ CASES = {
 
 @pytest.fixture(autouse=True)
 def _reset_tuning():
-    from linear_cross_entropy_tmem_gb300.api import testing_set_tuning
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_tuning
     yield
     testing_set_tuning(0, 0)
+    testing_set_gemm_mode(0)
 
 
 def _run_case(w: Workload, tuning):
@@ -59,8 +60,11 @@ def _run_case(w: Workload, tuning):
     return gpu, dev
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["auto", "single-cta", "cta-pair"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_parity_small(name):
+def test_parity_small(name, mode):
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode
+    testing_set_gemm_mode(mode)
     w, tuning = CASES[name]
     _run_case(w, tuning)
 
