@@ -285,12 +285,15 @@ struct EpiGrad {
     }
     if (kBias) {
       epilogue_bar_sync();
+      // A CTA-pair tile can have its second 128-row half entirely past the
+      // last token: that half has no slot in the per-tile partial sums.
+      if (u.row0 < p.n_tokens) {
 #pragma unroll
-      for (int h = 0; h < kBN / kEpilogueThreads; ++h) {
-        const int col = threadIdx.x + h * kEpilogueThreads;
-        const float s = epi_smem[col] + epi_smem[kBN + col] + epi_smem[2 * kBN + col] + epi_smem[3 * kBN + col];
-        if (v_tile + col < p.vocab)
-          p.dbias_part[(u.row0 / kBM) * p.ldg + col_tile + col] = s;
+        for (int h = 0; h < kBN / kEpilogueThreads; ++h) {
+          const int col = threadIdx.x + h * kEpilogueThreads;
+          const float s = epi_smem[col] + epi_smem[kBN + col] + epi_smem[2 * kBN + col] + epi_smem[3 * kBN + col];
+          if (v_tile + col < p.vocab) p.dbias_part[(u.row0 / kBM) * p.ldg + col_tile + col] = s;
+        }
       }
       epilogue_bar_sync();
     }
