@@ -370,6 +370,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   fp.vocab = V;
   fp.bias = bias;
   fp.bias_f32 = p->bias_dtype == FLCE_F32;
+  fp.bias_vec = bias != nullptr && aligned(bias, 16);
   fp.n_splits = splits;
   fp.scale = p->logit_scale;
   fp.softcap = softcap ? p->final_logit_softcapping : 0.f;
@@ -491,6 +492,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     gp.v0 = v0;
     gp.bias = bias;
     gp.bias_f32 = p->bias_dtype == FLCE_F32;
+    gp.bias_vec = bias != nullptr && aligned(bias, 16);
     gp.reduction = p->reduction;
     gp.scale = p->logit_scale;
     gp.softcap = softcap ? p->final_logit_softcapping : 0.f;

@@ -53,15 +53,12 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// tanh from the identity tanh(u) = 1 - 2 / (exp(2u) + 1), with exp(2u) taken as
-// 2^(2u*log2 e).  Absolute error ~1e-7: the soft cap multiplies it by c, well
-// inside the loss tolerance.  exp overflow gives +inf and 2/inf = 0, so the
-// result saturates to +-1 correctly.
-__device__ __forceinline__ float tanh_exp(float u) {
-  const float e = ex2_approx(u * 2.8853900817779268f);  // 2*log2(e)
-  return 1.0f - 2.0f * rcp_approx(e + 1.0f);
+// tanh(u) from t = 2 u log2(e): tanh(u) = 1 - 2 / (2^t + 1), with the
+// hardware 2^x and reciprocal.  Absolute error about 1e-7; 2^t overflowing to
+// +inf gives rcp 0 and tanh 1, 2^t underflowing to 0 gives tanh -1.
+__device__ __forceinline__ float tanh_from_exp2_arg(float t) {
+  return fmaf(-2.0f, rcp_approx(ex2_approx(t) + 1.0f), 1.0f);
 }
-
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
@@ -192,6 +189,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Wait for outstanding tcgen05.ld and tie `r` to the wait, so that no use of
+// the loaded registers can be scheduled above it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+        "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+        "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+        "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
 //   start : shared address of the tile (1024-byte aligned swizzle atoms; a

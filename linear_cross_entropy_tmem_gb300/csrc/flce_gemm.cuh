@@ -67,6 +67,71 @@ __device__ __forceinline__ float load_bias(const void* bias, int bias_f32, int64
   return __uint_as_float(static_cast<uint32_t>(raw) << 16);
 }
 
+// The 32 bias values of columns [vc, vc+32) (0 past the vocabulary).  Every
+// lane reads the same addresses, so each load is one broadcast transaction;
+// 16-byte vectors when the bias is aligned and the chunk is whole.
+__device__ __forceinline__ void load_bias_chunk(const void* bias, int bias_f32, int bias_vec, int64_t vc,
+                                                int64_t vocab, float (&b)[32]) {
+  if (bias_vec && vc + 32 <= vocab) {
+    if (bias_f32) {
+      const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(bias) + vc);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 v = __ldg(src + q);
+        b[4 * q] = v.x;
+        b[4 * q + 1] = v.y;
+        b[4 * q + 2] = v.z;
+        b[4 * q + 3] = v.w;
+      }
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(bias) + vc);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = __ldg(src + q);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          b[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+          b[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) b[j] = (vc + j < vocab) ? load_bias(bias, bias_f32, vc + j) : 0.f;
+  }
+}
+
+// Runs f(r, c) over the first `nch` 32-column chunks of this warp's TMEM
+// lanes, loading chunk c+1 while chunk c is processed.  nch is warp-uniform.
+template <class F>
+__device__ __forceinline__ void for_each_tmem_chunk(uint32_t taddr, int nch, F&& f) {
+  if (nch <= 0) return;
+  uint32_t ra[32], rb[32];
+  tmem_ld32(taddr, ra);
+  tmem_ld_wait(ra);
+#pragma unroll 1
+  for (int c = 0; c < nch; c += 2) {
+    const bool has1 = c + 1 < nch;
+    if (has1) tmem_ld32(taddr + (c + 1) * 32, rb);
+    f(ra, c);
+    if (has1) {
+      tmem_ld_wait(rb);
+      const bool has2 = c + 2 < nch;
+      if (has2) tmem_ld32(taddr + (c + 2) * 32, ra);
+      f(rb, c + 1);
+      if (has2) tmem_ld_wait(ra);
+    }
+  }
+}
+
+// Number of 32-column chunks of a tile that start inside [0, limit).
+__device__ __forceinline__ int chunks_below(int64_t col0, int64_t limit) {
+  const int64_t rem = limit - col0;
+  if (rem <= 0) return 0;
+  return rem >= kBN ? kBN / 32 : static_cast<int>((rem + 31) / 32);
+}
+
 // All 128 epilogue threads agree on a predicate (named barrier 1, AND).
 __device__ __forceinline__ bool epilogue_all(bool ok) {
   uint32_t r;
@@ -79,6 +144,17 @@ __device__ __forceinline__ bool epilogue_all(bool ok) {
       : "r"(static_cast<uint32_t>(ok)), "n"(kEpilogueThreads)
       : "memory");
   return r != 0;
+}
+
+__device__ __forceinline__ float max32(const float (&z)[32]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = fmaxf(z[i], z[i + 16]);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) t[i] = fmaxf(t[i], t[i + 8]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t[i] = fmaxf(t[i], t[i + 4]);
+  return fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
 }
 
 // ============================================================================
@@ -107,31 +183,26 @@ struct EpiFwd {
   __device__ static void tile(const Params& p, const Unit& /*u*/, int n_tile, uint32_t taddr, State& st,
                               float* /*epi_smem*/) {
     const int64_t v_tile = static_cast<int64_t>(n_tile) * kBN;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    // z = c tanh(s x / c): tanh takes t = 2 (s x / c) log2 e = x k_t
+    const float k_t = p.scale * p.inv_softcap * 2.0f * kLog2e;
+    for_each_tmem_chunk(taddr, chunks_below(v_tile, p.vocab), [&](const uint32_t (&r)[32], int c) {
       const int64_t vc = v_tile + c * 32;
-      if (vc >= p.vocab) break;  // warp-uniform: the rest of the tile is past the vocabulary
-      uint32_t r[32];
-      tmem_ld32(taddr + c * 32, r);
-      tmem_ld_wait();
       const bool ragged = vc + 32 > p.vocab;
+      float bch[32];
+      if (kBias) load_bias_chunk(p.bias, p.bias_f32, p.bias_vec, vc, p.vocab, bch);
       float z[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float x = __uint_as_float(r[j]);
-        if (kBias) x += (!ragged || vc + j < p.vocab) ? load_bias(p.bias, p.bias_f32, vc + j) : 0.f;
-        x *= p.scale;
-        if (kSoftcap) x = p.softcap * tanh_exp(x * p.inv_softcap);
-        z[j] = x;
+        if (kBias) x += bch[j];
+        z[j] = kSoftcap ? p.softcap * tanh_from_exp2_arg(x * k_t) : x * p.scale;
       }
       if (ragged) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (vc + j >= p.vocab) z[j] = -FLT_MAX;
       }
-      float cmax = z[0];
-#pragma unroll
-      for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, z[j]);
+      const float cmax = max32(z);
       if (cmax > st.best) {  // strict: the lowest index wins ties, across chunks and tiles
         int jj = 31;
 #pragma unroll
@@ -147,19 +218,22 @@ struct EpiFwd {
         st.m = cmax;
       }
       const float mb = st.m * kLog2e;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f}, a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float e = ex2_approx(fmaf(z[j], kLog2e, -mb));
-        st.s += e;
-        st.a = fmaf(e, z[j], st.a);
+        s4[j & 3] += e;
+        a4[j & 3] = fmaf(e, z[j], a4[j & 3]);
       }
+      st.s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      st.a += (a4[0] + a4[1]) + (a4[2] + a4[3]);
       const int64_t tl = st.target - vc;
       if (tl >= 0 && tl < 32) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (j == tl) st.zt = z[j];
       }
-    }
+    });
   }
 
   __device__ static void end_unit(const Params& p, const Unit& u, State& st) {
@@ -227,6 +301,19 @@ struct EpiGrad {
     }
   }
 
+  // dz/dacc-weighted factor and probability of one logit (acc + bias = x).
+  __device__ static void grad_terms(const Params& p, float x, float wd, float k_t, float k_p, const State& st,
+                                    float& d, float& pr) {
+    if (kSoftcap) {
+      const float th = tanh_from_exp2_arg(x * k_t);
+      pr = ex2_approx(fmaf(th, k_p, -st.lse2));          // e^(z - lse), z = c th
+      d = wd * fmaf(-th, th, 1.f);                        // w s (1 - (z/c)^2)
+    } else {
+      pr = ex2_approx(fmaf(x, k_p, -st.lse2));            // e^(s x - lse)
+      d = wd;
+    }
+  }
+
   __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st,
                               float* epi_smem) {
     const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;  // chunk-local column
@@ -234,35 +321,35 @@ struct EpiGrad {
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
     const float wd = st.w * p.scale;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    const float k_t = p.scale * p.inv_softcap * 2.0f * kLog2e;
+    const float k_p = kSoftcap ? p.softcap * kLog2e : p.scale * kLog2e;
+    const int nch = chunks_below(v_tile, p.vocab);
+    for_each_tmem_chunk(taddr, nch, [&](const uint32_t (&r)[32], int c) {
       const int64_t vc = v_tile + c * 32;
-      if (vc >= p.vocab) {  // warp-uniform: no vocabulary rows left in this tile
-        if (kBias) epi_smem[warp * kBN + c * 32 + lane] = 0.f;
-        continue;
-      }
-      uint32_t r[32];
-      tmem_ld32(taddr + c * 32, r);
-      tmem_ld_wait();
       const bool ragged = vc + 32 > p.vocab;
+      float bch[32];
+      if (kBias) load_bias_chunk(p.bias, p.bias_f32, p.bias_vec, vc, p.vocab, bch);
       float g[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float x = __uint_as_float(r[j]);
-        if (kBias) x += (!ragged || vc + j < p.vocab) ? load_bias(p.bias, p.bias_f32, vc + j) : 0.f;
-        x *= p.scale;
-        float z, d;
-        if (kSoftcap) {
-          const float th = tanh_exp(x * p.inv_softcap);
-          z = p.softcap * th;
-          d = wd * fmaf(-th, th, 1.f);
-        } else {
-          z = x;
-          d = wd;
+        if (kBias) x += bch[j];
+        float d, pr;
+        grad_terms(p, x, wd, k_t, k_p, st, d, pr);
+        g[j] = d * pr;
+      }
+      const int64_t tl = st.target - vc;
+      if (tl >= 0 && tl < 32) {  // the target column: subtract the one-hot term
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j == tl) {
+            float x = __uint_as_float(r[j]);
+            if (kBias) x += bch[j];
+            float d, pr;
+            grad_terms(p, x, wd, k_t, k_p, st, d, pr);
+            g[j] = d * (pr - 1.f);
+          }
         }
-        const float pr = ex2_approx(fmaf(z, kLog2e, -st.lse2));
-        const float oh = (vc + j == st.target) ? 1.f : 0.f;
-        g[j] = d * (pr - oh);
       }
       if (ragged) {
 #pragma unroll
@@ -282,8 +369,9 @@ struct EpiGrad {
         }
       }
       if (kBias) epi_smem[warp * kBN + c * 32 + lane] = warp_column_sums(g);
-    }
+    });
     if (kBias) {
+      for (int c = nch; c < kBN / 32; ++c) epi_smem[warp * kBN + c * 32 + lane] = 0.f;
       epilogue_bar_sync();
       // A CTA-pair tile can have its second 128-row half entirely past the
       // last token: that half has no slot in the per-tile partial sums.
@@ -310,33 +398,27 @@ struct EpiStore {
   struct State {
     int64_t row;
   };
-  __device__ static void begin_unit(const Params&, const Unit& u, State& st) {
-    st.row = u.row0 + threadIdx.x;
-  }
+  __device__ static void begin_unit(const Params&, const Unit& u, State& st) { st.row = u.row0 + threadIdx.x; }
   __device__ static void tile(const Params& p, const Unit&, int n_tile, uint32_t taddr, State& st, float*) {
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      const int64_t col = static_cast<int64_t>(n_tile) * kBN + c * 32;
-      if (col >= p.cols) break;  // warp-uniform
-      uint32_t r[32];
-      tmem_ld32(taddr + c * 32, r);
-      tmem_ld_wait();
-      if (st.row >= p.rows) continue;
+    const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;
+    for_each_tmem_chunk(taddr, chunks_below(col_tile, p.cols), [&](const uint32_t (&r)[32], int c) {
+      if (st.row >= p.rows) return;
+      const int64_t col = col_tile + c * 32;
+      const int64_t n = p.cols - col;
       if (p.out_f32) {
         float* dst = reinterpret_cast<float*>(p.out) + st.row * p.ldo + col;
-        if (col + 32 <= p.cols) {
+        if (n >= 32) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             reinterpret_cast<uint4*>(dst)[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
         } else {
-          const int64_t n = p.cols - col;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j < n) dst[j] = __uint_as_float(r[j]);
         }
       } else {
         uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + st.row * p.ldo + col;
-        if (col + 32 <= p.cols) {
+        if (n >= 32) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 pk;
@@ -347,13 +429,12 @@ struct EpiStore {
             reinterpret_cast<uint4*>(dst)[q] = pk;
           }
         } else {
-          const int64_t n = p.cols - col;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j < n) dst[j] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]), 0.f) & 0xFFFFu);
         }
       }
-    }
+    });
   }
   __device__ static void end_unit(const Params&, const Unit&, State&) {}
 };
@@ -366,76 +447,79 @@ struct EpiAccum {
   struct State {
     int64_t row;
   };
-  __device__ static void begin_unit(const Params&, const Unit& u, State& st) {
-    st.row = u.row0 + threadIdx.x;
+  __device__ static void begin_unit(const Params&, const Unit& u, State& st) { st.row = u.row0 + threadIdx.x; }
+
+  __device__ static void store(const Params& p, const Unit& u, const State& st, int64_t col, float (&v)[32]) {
+    if (st.row >= p.rows) return;
+    float* slot = p.part + static_cast<int64_t>(u.ks) * p.part_stride + st.row * p.cols + col;
+    const int64_t rem = p.cols - col;
+    if (rem >= 32) {
+      if (p.accumulate) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 o = reinterpret_cast<const float4*>(slot)[q];
+          v[4 * q] += o.x;
+          v[4 * q + 1] += o.y;
+          v[4 * q + 2] += o.z;
+          v[4 * q + 3] += o.w;
+        }
+      }
+      if (!p.write_final) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<float4*>(slot)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      } else if (p.out_f32) {
+        float* dst = reinterpret_cast<float*>(p.out) + st.row * p.cols + col;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      } else {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + st.row * p.cols + col;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 pk;
+          pk.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+          pk.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+          pk.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+          pk.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+          reinterpret_cast<uint4*>(dst)[q] = pk;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j >= rem) continue;
+        float x = v[j];
+        if (p.accumulate) x += slot[j];
+        if (!p.write_final) {
+          slot[j] = x;
+        } else if (p.out_f32) {
+          reinterpret_cast<float*>(p.out)[st.row * p.cols + col + j] = x;
+        } else {
+          reinterpret_cast<uint16_t*>(p.out)[st.row * p.cols + col + j] =
+              static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
+        }
+      }
+    }
   }
+
   __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*) {
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      const int64_t col = static_cast<int64_t>(n_tile) * kBN + c * 32;
-      if (col >= p.cols) break;  // warp-uniform
-      float v[32];
-      if (u.kb_count > 0) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
+    const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;
+    const int nch = chunks_below(col_tile, p.cols);
+    if (u.kb_count > 0) {
+      for_each_tmem_chunk(taddr, nch, [&](const uint32_t (&r)[32], int c) {
+        float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-      } else {  // a K split with no K blocks contributes zero
+        store(p, u, st, col_tile + c * 32, v);
+      });
+    } else {  // a K split with no K blocks contributes zero
+#pragma unroll 1
+      for (int c = 0; c < nch; ++c) {
+        float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
-      }
-      if (st.row >= p.rows) continue;
-      float* slot = p.part + static_cast<int64_t>(u.ks) * p.part_stride + st.row * p.cols + col;
-      const int64_t rem = p.cols - col;
-      const int n = rem < 32 ? static_cast<int>(rem) : 32;
-      if (n == 32) {
-        if (p.accumulate) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 o = reinterpret_cast<const float4*>(slot)[q];
-            v[4 * q] += o.x;
-            v[4 * q + 1] += o.y;
-            v[4 * q + 2] += o.z;
-            v[4 * q + 3] += o.w;
-          }
-        }
-        if (!p.write_final) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(slot)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else if (p.out_f32) {
-          float* dst = reinterpret_cast<float*>(p.out) + st.row * p.cols + col;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-          uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + st.row * p.cols + col;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 pk;
-            pk.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-            pk.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-            pk.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-            pk.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-            reinterpret_cast<uint4*>(dst)[q] = pk;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j >= n) continue;
-          float x = v[j];
-          if (p.accumulate) x += slot[j];
-          if (!p.write_final) {
-            slot[j] = x;
-          } else if (p.out_f32) {
-            reinterpret_cast<float*>(p.out)[st.row * p.cols + col + j] = x;
-          } else {
-            reinterpret_cast<uint16_t*>(p.out)[st.row * p.cols + col + j] =
-                static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
-          }
-        }
+        store(p, u, st, col_tile + c * 32, v);
       }
     }
   }

@@ -76,6 +76,7 @@ struct FwdParams {
   int64_t n_tokens, vocab;
   const void* bias;       // nullptr, bf16 or fp32 [V]
   int32_t bias_f32;
+  int32_t bias_vec;       // bias is 16-byte aligned: load it as 16-byte vectors
   int32_t n_splits;
   float scale, softcap, inv_softcap;
   int64_t ignore_index;
@@ -96,6 +97,7 @@ struct GradParams {
   int64_t v0;             // first vocabulary row of the chunk
   const void* bias;
   int32_t bias_f32;
+  int32_t bias_vec;
   int32_t reduction;      // FLCE_RED_*
   float scale, softcap, inv_softcap;
   int64_t ignore_index;
