@@ -91,7 +91,7 @@ def _logsumexp_rows(z: np.ndarray) -> np.ndarray:
 
 
 def forward(h, W, b=None, targets=None, *, logit_scale=1.0, softcap=0.0,
-            ignore_index=-100, reduction="mean") -> dict:
+            ignore_index=-100, reduction="mean", num_items_in_batch=0.0) -> dict:
     """Forward of the fused linear cross-entropy: the 4-tuple plus per-token values.
 
     TRL PR #6859, "What it supports": the helper returns the same 4-tuple as the
@@ -107,6 +107,10 @@ def forward(h, W, b=None, targets=None, *, logit_scale=1.0, softcap=0.0,
     ``n_valid``     count of tokens whose target is not ignore_index
     ``entropy_sum`` sum of the per-token entropy over valid tokens
     ``status``      STATUS_OK or STATUS_TARGET_OUT_OF_RANGE
+
+    ``num_items_in_batch`` > 0 replaces n_valid as the mean's denominator (the
+    count of valid tokens over a whole accumulated batch; TRL PR #6859 review,
+    "Test coverage" item 10, test_num_items_in_batch_reduction).
     """
     if reduction not in ("mean", "sum", "none"):
         raise ValueError(f"reduction must be mean, sum or none, not {reduction!r}")
@@ -133,7 +137,8 @@ def forward(h, W, b=None, targets=None, *, logit_scale=1.0, softcap=0.0,
     if reduction == "sum":
         loss = total
     elif reduction == "mean":
-        loss = total / n_valid if n_valid > 0 else 0.0
+        denom = float(num_items_in_batch) if num_items_in_batch > 0 else n_valid
+        loss = total / denom if denom > 0 else 0.0
     else:
         loss = loss_tok.copy()
     return {
@@ -145,18 +150,21 @@ def forward(h, W, b=None, targets=None, *, logit_scale=1.0, softcap=0.0,
 
 
 def token_weights(targets, vocab, *, reduction="mean", dloss=1.0, ignore_index=-100,
-                  n_valid=None) -> np.ndarray:
+                  n_valid=None, num_items_in_batch=0.0) -> np.ndarray:
     """Per-token weight ``w_n`` that multiplies the softmax gradient.
 
     mean: ``g / n_valid`` (0 when n_valid is 0); sum: ``g``; none: ``dloss[n]``
     (Liger-Kernel PR #1574, Summary item 2: each row scaled by its own upstream
     gradient).  Ignored tokens get 0 (TRL PR #6859 review, "Correctness" item 2).
-    ``n_valid`` may be given for a subset of tokens whose mean runs over more.
+    ``n_valid`` may be given for a subset of tokens whose mean runs over more;
+    ``num_items_in_batch`` > 0 replaces it as the mean's denominator.
     """
     t = _targets(targets)
     valid = (t >= 0) & (t < vocab) & (t != ignore_index)
     if n_valid is None:
         n_valid = int(valid.sum())
+    if num_items_in_batch > 0:
+        n_valid = float(num_items_in_batch)
     if reduction == "none":
         g = widen(dloss).reshape(-1)
         if g.shape[0] != t.shape[0]:
@@ -175,7 +183,7 @@ def token_weights(targets, vocab, *, reduction="mean", dloss=1.0, ignore_index=-
 
 def grad_logits(h, W, b=None, targets=None, *, logit_scale=1.0, softcap=0.0,
                 ignore_index=-100, reduction="mean", dloss=1.0, lse=None,
-                n_valid=None, vocab_rows=None) -> np.ndarray:
+                n_valid=None, vocab_rows=None, num_items_in_batch=0.0) -> np.ndarray:
     """``G = dL/d(acc)``: ``w_n (softmax - onehot) * s * (1 - (z/c)^2)``.
 
     The derivative of ``c*tanh(s*(acc+b)/c)`` with respect to ``acc`` is
@@ -197,13 +205,13 @@ def grad_logits(h, W, b=None, targets=None, *, logit_scale=1.0, softcap=0.0,
     p = np.exp(z - np.asarray(lse, dtype=np.float64)[:, None])
     onehot = (t[:, None] == cols[None, :]).astype(np.float64)
     w = token_weights(t, vocab, reduction=reduction, dloss=dloss,
-                      ignore_index=ignore_index, n_valid=n_valid)
+                      ignore_index=ignore_index, n_valid=n_valid, num_items_in_batch=num_items_in_batch)
     dz_dacc = float(logit_scale) * ((1.0 - (z / float(softcap)) ** 2) if softcap > 0.0 else 1.0)
     return w[:, None] * (p - onehot) * dz_dacc
 
 
 def backward(h, W, b=None, targets=None, *, logit_scale=1.0, softcap=0.0,
-             ignore_index=-100, reduction="mean", dloss=1.0) -> dict:
+             ignore_index=-100, reduction="mean", dloss=1.0, num_items_in_batch=0.0) -> dict:
     """Backward: ``dh = G W``, ``dW = G^T h``, ``db = sum_n G`` (float64, G unrounded).
 
     TRL PR #6859 review, "Correctness" item 2: the weight gradient is the
@@ -213,7 +221,8 @@ def backward(h, W, b=None, targets=None, *, logit_scale=1.0, softcap=0.0,
     hf = widen(h)
     Wf = widen(W)
     G = grad_logits(hf, Wf, b, targets, logit_scale=logit_scale, softcap=softcap,
-                    ignore_index=ignore_index, reduction=reduction, dloss=dloss)
+                    ignore_index=ignore_index, reduction=reduction, dloss=dloss,
+                    num_items_in_batch=num_items_in_batch)
     return {
         "dh": G @ Wf,
         "dW": G.T @ hf,
@@ -245,17 +254,17 @@ def lse_all(h, W, b=None, *, logit_scale=1.0, softcap=0.0, row_block=256) -> np.
 
 
 def dweight_rows(h, W, b, targets, vocab_rows, lse, *, logit_scale=1.0, softcap=0.0,
-                 ignore_index=-100, reduction="mean", dloss=1.0):
+                 ignore_index=-100, reduction="mean", dloss=1.0, num_items_in_batch=0.0):
     """Rows ``vocab_rows`` of dW and db, given the oracle's own full lse of every token."""
     hf = widen(h)
     G = grad_logits(hf, W, b, targets, logit_scale=logit_scale, softcap=softcap,
                     ignore_index=ignore_index, reduction=reduction, dloss=dloss,
-                    lse=lse, vocab_rows=vocab_rows)
+                    lse=lse, vocab_rows=vocab_rows, num_items_in_batch=num_items_in_batch)
     return G.T @ hf, G.sum(axis=0)
 
 
 def dhidden_rows(h, W, b, targets, rows, *, n_valid, logit_scale=1.0, softcap=0.0,
-                 ignore_index=-100, reduction="mean", dloss=1.0) -> np.ndarray:
+                 ignore_index=-100, reduction="mean", dloss=1.0, num_items_in_batch=0.0) -> np.ndarray:
     """Rows ``rows`` of dh (each needs only its own token's logits)."""
     rows = np.asarray(rows)
     t = _targets(targets)
@@ -263,7 +272,7 @@ def dhidden_rows(h, W, b, targets, rows, *, n_valid, logit_scale=1.0, softcap=0.
     g_rows = g[rows] if reduction == "none" else g[:1]
     G = grad_logits(widen(h)[rows], W, b, t[rows], logit_scale=logit_scale,
                     softcap=softcap, ignore_index=ignore_index, reduction=reduction,
-                    dloss=g_rows, n_valid=n_valid)
+                    dloss=g_rows, n_valid=n_valid, num_items_in_batch=num_items_in_batch)
     return G @ widen(W)
 
 

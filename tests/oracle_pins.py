@@ -317,10 +317,37 @@ def check_out_of_range_target(o):
     assert o.forward(h, W, b, t, reduction="none")["status"] == o.STATUS_OK
 
 
+def check_num_items_in_batch(o):
+    """The mean over num_items_in_batch equals the summed loss divided by it; its
+    gradient is pinned by central differences of that forward."""
+    h, W, b, t = _rand_case(19, n=4, d=3, v=5, bias=True, ignore=(1,))
+    kw = dict(logit_scale=0.8, softcap=2.0)
+    total = o.forward(h, W, b, t, reduction="sum", **kw)["loss"]
+    for items in (3.0, 7.0, 64.0):
+        m = o.forward(h, W, b, t, reduction="mean", num_items_in_batch=items, **kw)["loss"]
+        assert abs(m - total / items) <= 1e-15 * max(1.0, abs(total))
+        g = o.backward(h, W, b, t, reduction="mean", dloss=np.array([1.5]), num_items_in_batch=items, **kw)
+        eps = 1e-6
+        for name, arr in (("dh", h), ("dW", W), ("db", b)):
+            num = np.zeros_like(arr)
+            for idx in np.ndindex(arr.shape):
+                old = arr[idx]
+                arr[idx] = old + eps
+                lp = o.forward(h, W, b, t, reduction="mean", num_items_in_batch=items, **kw)["loss"]
+                arr[idx] = old - eps
+                lm = o.forward(h, W, b, t, reduction="mean", num_items_in_batch=items, **kw)["loss"]
+                arr[idx] = old
+                num[idx] = 1.5 * (lp - lm) / (2 * eps)
+            np.testing.assert_allclose(g[name], num, rtol=1e-6, atol=1e-9, err_msg=f"{name} items={items}")
+    # 0 means "use n_valid"
+    a = o.forward(h, W, b, t, reduction="mean", num_items_in_batch=0.0, **kw)["loss"]
+    assert abs(a - total / 3) <= 1e-15 * max(1.0, abs(total))
+
+
 ALL_CHECKS = [
     check_forward_matches_torch, check_entropy_matches_scipy, check_softcap_limits,
     check_gradients_finite_difference, check_zero_head_closed_form, check_invariants,
     check_all_ignored, check_vocab_one, check_argmax_targets_exact_accuracy,
     check_ties_lowest_index, check_brute_force_python, check_sympy_exact,
-    check_subset_helpers, check_out_of_range_target,
+    check_subset_helpers, check_out_of_range_target, check_num_items_in_batch,
 ]

@@ -35,7 +35,8 @@ MUTANTS = {
     "argmax ties to highest": [("argmax = z.argmax(axis=1)",
                                 "argmax = z.shape[1] - 1 - z[:, ::-1].argmax(axis=1)")],
     "ignored rows in loss": [("loss_tok = np.where(valid, lse - z_t, 0.0)", "loss_tok = lse - z_t")],
-    "mean over all tokens": [("loss = total / n_valid if n_valid > 0 else 0.0", "loss = total / n_tok")],
+    "mean over all tokens": [("denom = float(num_items_in_batch) if num_items_in_batch > 0 else n_valid",
+                              "denom = float(num_items_in_batch) if num_items_in_batch > 0 else n_tok")],
     "entropy sum over ignored": [("entropy_sum = float(entropy[valid].sum())",
                                   "entropy_sum = float(entropy.sum())")],
     "grad sign": [("return w[:, None] * (p - onehot) * dz_dacc",
@@ -50,6 +51,9 @@ MUTANTS = {
     "bias grad averaged": [('"db": None if b is None else G.sum(axis=0)',
                             '"db": None if b is None else G.sum(axis=0) / G.shape[0]')],
     "hidden grad transposed head": [('"dh": G @ Wf', '"dh": G @ Wf[::-1]')],
+    "num_items ignored in the forward": [("denom = float(num_items_in_batch) if num_items_in_batch > 0 else n_valid",
+                                          "denom = n_valid")],
+    "num_items ignored in the backward": [("        n_valid = float(num_items_in_batch)", "        pass")],
 }
 
 
