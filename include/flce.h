@@ -65,6 +65,19 @@ enum { FLCE_F32 = 0, FLCE_BF16 = 1 };
 /* Reduction of the per-token losses. */
 enum { FLCE_RED_NONE = 0, FLCE_RED_SUM = 1, FLCE_RED_MEAN = 2 };
 
+/* Bits of flce_problem.flags. */
+enum {
+  /*
+   * Gather the tokens whose target is valid before any product, so that the
+   * cost scales with the number of valid tokens instead of N (TRL PR #6859,
+   * review "Correctness" item 2: gather before the call).  Loss, metrics and
+   * gradients are unchanged (up to summation order); ignored tokens then get
+   * lse = 0 and entropy = 0 instead of their values over the vocabulary, and a
+   * zero dhidden row.
+   */
+  FLCE_FLAG_COMPACT_VALID = 1u
+};
+
 /* Status codes returned by every call (and stored in the device status word). */
 enum {
   FLCE_OK = 0,
@@ -96,6 +109,13 @@ enum {
  *   ignore_index  targets equal to it contribute nothing (usually -100)
  *   reduction     FLCE_RED_MEAN (divide by the number of valid tokens; 0 when
  *                 there are none), FLCE_RED_SUM or FLCE_RED_NONE.
+ *   num_items_in_batch  0, or the count of valid tokens of a whole accumulated
+ *                 batch: the mean then divides by it, in the forward and the
+ *                 backward (TRL PR #6859 review, "Test coverage" item 10).
+ *                 Finite and >= 0.
+ *   flags         FLCE_FLAG_COMPACT_VALID or 0.
+ *   reserved      0.
+ * (ABI version 2: num_items_in_batch, flags and reserved were added.)
  */
 typedef struct {
   int64_t n_tokens;
@@ -108,6 +128,9 @@ typedef struct {
   float logit_scale;
   float final_logit_softcapping;
   int64_t ignore_index;
+  double num_items_in_batch;  /* > 0: FLCE_RED_MEAN divides by it instead of n_valid */
+  uint32_t flags;             /* FLCE_FLAG_* */
+  uint32_t reserved;          /* must be 0 */
 } flce_problem;
 
 /*

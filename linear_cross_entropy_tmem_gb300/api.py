@@ -32,14 +32,17 @@ def _stream(device: torch.device):
 
 def make_problem(n_tokens: int, hidden: int, vocab: int, *, hidden_dtype=torch.bfloat16,
                  weight_dtype=torch.bfloat16, bias_dtype=torch.bfloat16, logit_scale: float = 1.0,
-                 softcap: float = 0.0, ignore_index: int = -100, reduction: str = "mean") -> B.FlceProblem:
+                 softcap: float = 0.0, ignore_index: int = -100, reduction: str = "mean",
+                 num_items_in_batch: float = 0.0, compact: bool = False) -> B.FlceProblem:
     if reduction not in B.REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(B.REDUCTIONS)}")
     return B.FlceProblem(
         n_tokens=n_tokens, hidden=hidden, vocab=vocab,
         hidden_dtype=_dtype_code(hidden_dtype, "hidden"), weight_dtype=_dtype_code(weight_dtype, "weight"),
         bias_dtype=_dtype_code(bias_dtype, "bias"), reduction=B.REDUCTIONS[reduction],
-        logit_scale=float(logit_scale), final_logit_softcapping=float(softcap), ignore_index=int(ignore_index))
+        logit_scale=float(logit_scale), final_logit_softcapping=float(softcap), ignore_index=int(ignore_index),
+        num_items_in_batch=float(num_items_in_batch), flags=B.FLCE_FLAG_COMPACT_VALID if compact else 0,
+        reserved=0)
 
 
 def flce_workspace_size(problem: B.FlceProblem, for_backward: bool) -> int:
@@ -81,6 +84,7 @@ class ForwardResult(NamedTuple):
 def flce_forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
                  bias: Optional[torch.Tensor] = None, *, logit_scale: float = 1.0, softcap: float = 0.0,
                  ignore_index: int = -100, reduction: str = "mean", entropy: bool = False,
+                 num_items_in_batch: float = 0.0, compact: bool = False,
                  workspace: Optional[torch.Tensor] = None) -> ForwardResult:
     """Forward of the fused linear cross-entropy (see ``flce_forward`` in include/flce.h)."""
     _require_cuda(hidden, weight, targets, bias)
@@ -93,7 +97,7 @@ def flce_forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tens
     prob = make_problem(N, D, V, hidden_dtype=hidden.dtype, weight_dtype=weight.dtype,
                         bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
                         logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
-                        reduction=reduction)
+                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact)
     dev = hidden.device
     ws = _workspace(flce_workspace_size(prob, False), dev, workspace)
     f32 = dict(dtype=torch.float32, device=dev)
@@ -115,7 +119,8 @@ def flce_forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tens
 def flce_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
                   n_valid: torch.Tensor, dloss: torch.Tensor, bias: Optional[torch.Tensor] = None, *,
                   logit_scale: float = 1.0, softcap: float = 0.0, ignore_index: int = -100,
-                  reduction: str = "mean", workspace: Optional[torch.Tensor] = None, outputs=None):
+                  reduction: str = "mean", num_items_in_batch: float = 0.0, compact: bool = False,
+                  workspace: Optional[torch.Tensor] = None, outputs=None):
     """Backward (see ``flce_backward`` in include/flce.h); returns (dhidden, dweight, dbias)."""
     _require_cuda(hidden, weight, targets, lse, n_valid, dloss, bias)
     for t, n in ((hidden, "hidden"), (weight, "weight"), (targets, "targets"), (bias, "bias"), (lse, "lse")):
@@ -125,7 +130,7 @@ def flce_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Ten
     prob = make_problem(N, D, V, hidden_dtype=hidden.dtype, weight_dtype=weight.dtype,
                         bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
                         logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
-                        reduction=reduction)
+                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact)
     dev = hidden.device
     ws = _workspace(flce_workspace_size(prob, True), dev, workspace)
     dloss = dloss.to(dtype=torch.float32).contiguous().reshape(-1)
@@ -159,28 +164,31 @@ class LinearCrossEntropy(torch.autograd.Function):
     """Autograd wrapper: loss of ``hidden @ weight.T (+ bias)`` against ``targets``."""
 
     @staticmethod
-    def forward(ctx, hidden, weight, bias, targets, logit_scale, softcap, ignore_index, reduction):
+    def forward(ctx, hidden, weight, bias, targets, logit_scale, softcap, ignore_index, reduction,
+                num_items_in_batch=0.0, compact=False):
         r = flce_forward(hidden, weight, targets, bias, logit_scale=logit_scale, softcap=softcap,
-                         ignore_index=ignore_index, reduction=reduction)
+                         ignore_index=ignore_index, reduction=reduction, num_items_in_batch=num_items_in_batch,
+                         compact=compact)
         ctx.save_for_backward(hidden, weight, bias, targets, r.lse, r.n_valid)
-        ctx.cfg = (logit_scale, softcap, ignore_index, reduction)
+        ctx.cfg = (logit_scale, softcap, ignore_index, reduction, num_items_in_batch, compact)
         ctx.mark_non_differentiable(r.correct, r.n_valid, r.entropy_sum)
         return r.loss, r.correct, r.n_valid, r.entropy_sum
 
     @staticmethod
     def backward(ctx, dloss, _dc, _dn, _de):
         hidden, weight, bias, targets, lse, n_valid = ctx.saved_tensors
-        s, c, ig, red = ctx.cfg
+        s, c, ig, red, items, cmp = ctx.cfg
         dh, dW, db = flce_backward(hidden, weight, targets, lse, n_valid, dloss.contiguous(), bias,
-                                   logit_scale=s, softcap=c, ignore_index=ig, reduction=red)
-        return dh, dW, db, None, None, None, None, None
+                                   logit_scale=s, softcap=c, ignore_index=ig, reduction=red,
+                                   num_items_in_batch=items, compact=cmp)
+        return dh, dW, db, None, None, None, None, None, None, None
 
 
 def linear_cross_entropy(hidden, weight, targets, bias=None, *, logit_scale=1.0, softcap=0.0,
-                         ignore_index=-100, reduction="mean"):
+                         ignore_index=-100, reduction="mean", num_items_in_batch=0.0, compact=False):
     """Returns (loss, correct, n_valid, entropy_sum); only ``loss`` carries gradients."""
     return LinearCrossEntropy.apply(hidden, weight, bias, targets, float(logit_scale), float(softcap),
-                                    int(ignore_index), reduction)
+                                    int(ignore_index), reduction, float(num_items_in_batch), bool(compact))
 
 
 def testing_gemm(A: torch.Tensor, B_: torch.Tensor, *, a_mn_major: bool, b_mn_major: bool, M: int, N: int,

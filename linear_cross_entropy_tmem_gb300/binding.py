@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 
 FLCE_F32, FLCE_BF16 = 0, 1
 FLCE_RED_NONE, FLCE_RED_SUM, FLCE_RED_MEAN = 0, 1, 2
+FLCE_FLAG_COMPACT_VALID = 1
 REDUCTIONS = {"none": FLCE_RED_NONE, "sum": FLCE_RED_SUM, "mean": FLCE_RED_MEAN}
 
 FLCE_OK = 0
@@ -49,6 +50,9 @@ class FlceProblem(ctypes.Structure):
         ("logit_scale", c_float),
         ("final_logit_softcapping", c_float),
         ("ignore_index", c_int64),
+        ("num_items_in_batch", ctypes.c_double),
+        ("flags", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
     ]
 
 

@@ -19,7 +19,7 @@
 namespace flce {
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr int kMaxSplits = 64;                     // forward vocabulary splits
 constexpr int kMaxKSplit = 16;                     // dh K splits
 constexpr size_t kGChunkBudget = size_t(1) << 30;  // bytes of the bf16 G chunk
@@ -91,9 +91,14 @@ int validate(const flce_problem* p) {
     if (p->weight_dtype == FLCE_F32 && p->hidden_dtype == FLCE_BF16) return FLCE_ERR_DTYPE_MISMATCH;
     return FLCE_ERR_UNSUPPORTED_DTYPE;
   }
+  if (!std::isfinite(p->num_items_in_batch) || p->num_items_in_batch < 0.0) return FLCE_ERR_INVALID_ARG;
+  if ((p->flags & ~static_cast<uint32_t>(FLCE_FLAG_COMPACT_VALID)) != 0 || p->reserved != 0)
+    return FLCE_ERR_INVALID_ARG;
   if (p->hidden % 8 != 0) return FLCE_ERR_MISALIGNED;
   return FLCE_OK;
 }
+
+bool compact(const flce_problem* p) { return (p->flags & FLCE_FLAG_COMPACT_VALID) != 0; }
 
 int check_bias_dtype(const flce_problem* p, const void* bias) {
   if (bias && p->bias_dtype != FLCE_BF16 && p->bias_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED_DTYPE;
@@ -109,6 +114,8 @@ struct Layout {
   size_t hi = 0, lo = 0;
   size_t part_m = 0, part_s = 0, part_a = 0, part_best = 0, part_idx = 0, z_target = 0, blocks = 0;
   size_t g = 0, dbias_part = 0, dh_part = 0;
+  // valid-token compaction
+  size_t c_count = 0, c_blocks = 0, c_offsets = 0, c_map = 0, c_targets = 0, c_hidden = 0, c_lse = 0, c_dloss = 0;
   size_t total = 0;
   // backward geometry
   int64_t vc = 0;        // vocabulary chunk width (multiple of 256) = row stride of G
@@ -164,6 +171,19 @@ Layout make_layout(const flce_problem* p, bool backward, bool has_bias) {
   if (p->hidden_dtype == FLCE_F32) {
     L.hi = take(size_t(N) * D * 2);
     L.lo = take(size_t(N) * D * 2);
+  }
+  if (compact(p)) {
+    const size_t blocks = size_t(cdiv(N, kCompactBlock));
+    L.c_count = take(4);
+    L.c_blocks = take(blocks * 4);
+    L.c_offsets = take(blocks * 4);
+    L.c_map = take(size_t(N) * 4);
+    L.c_targets = take(size_t(N) * 8);
+    if (p->hidden_dtype != FLCE_F32) L.c_hidden = take(size_t(N) * D * 2);  // fp32 input compacts into hi / lo
+    if (backward) {
+      L.c_lse = take(size_t(N) * 4);
+      L.c_dloss = take(size_t(N) * 4);
+    }
   }
   if (!backward) {
     const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN));
@@ -333,6 +353,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   rp.blocks = blocks;
   rp.n_blocks = static_cast<int32_t>(cdiv(N, kMergeThreads));
   rp.reduction = p->reduction;
+  rp.num_items = p->num_items_in_batch;
   rp.loss = loss;
   rp.correct = correct;
   rp.n_valid = n_valid;
@@ -340,10 +361,38 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   if (N == 0) return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
 
   const bool h32 = p->hidden_dtype == FLCE_F32;
+  const bool cmp = compact(p);
+  const int32_t* row_count = nullptr;
+  const int32_t* row_map = nullptr;
+  const int64_t* tgt = targets;
   const void* a_main = hidden;
-  if (h32) {
-    uint16_t* hi = reinterpret_cast<uint16_t*>(ws + L.hi);
-    uint16_t* lo = reinterpret_cast<uint16_t*>(ws + L.lo);
+  uint16_t* hi = h32 ? reinterpret_cast<uint16_t*>(ws + L.hi) : nullptr;
+  uint16_t* lo = h32 ? reinterpret_cast<uint16_t*>(ws + L.lo) : nullptr;
+  if (cmp) {
+    CompactParams cp{};
+    cp.n_tokens = N;
+    cp.hidden = D;
+    cp.vocab = V;
+    cp.ignore_index = p->ignore_index;
+    cp.targets = targets;
+    cp.hidden_in = hidden;
+    cp.hidden_f32 = h32;
+    cp.block_counts = reinterpret_cast<int32_t*>(ws + L.c_blocks);
+    cp.block_offsets = reinterpret_cast<int32_t*>(ws + L.c_offsets);
+    cp.count = reinterpret_cast<int32_t*>(ws + L.c_count);
+    cp.row_map = reinterpret_cast<int32_t*>(ws + L.c_map);
+    cp.targets_out = reinterpret_cast<int64_t*>(ws + L.c_targets);
+    cp.hc = h32 ? hi : reinterpret_cast<uint16_t*>(ws + L.c_hidden);
+    cp.lo = lo;
+    cp.lse_default = lse;
+    cp.entropy_default = entropy;
+    cp.loss_default = p->reduction == FLCE_RED_NONE ? loss : nullptr;
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, st); }));
+    row_count = cp.count;
+    row_map = cp.row_map;
+    tgt = cp.targets_out;
+    a_main = cp.hc;
+  } else if (h32) {
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
       return launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st);
     }));
@@ -353,7 +402,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   TmaMaps maps;
   FLCE_TRY(make_map(&maps.a0, a_main, D, N, D * 2, kBK, kBM));
   maps.a1 = maps.a0;
-  if (h32) FLCE_TRY(make_map(&maps.a1, ws + L.lo, D, N, D * 2, kBK, kBM));
+  if (h32) FLCE_TRY(make_map(&maps.a1, lo, D, N, D * 2, kBK, kBM));
   FLCE_TRY(make_map(&maps.b0, weight, D, V, D * 2, kBK, pair ? kBN / 2 : kBN));
   maps.b1 = maps.b0;
 
@@ -362,6 +411,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   const int splits = choose_splits(sc.m_tiles, sc.n_tiles, pair ? dev.num_sms / 2 : dev.num_sms, &per_unit);
   sc.n_per_unit = per_unit;
   sc.group_m = pair ? 16 : 32;
+  sc.m_limit = row_count;
   finish_sched(sc);
 
   const bool softcap = p->final_logit_softcapping > 0.f;
@@ -376,7 +426,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   fp.softcap = softcap ? p->final_logit_softcapping : 0.f;
   fp.inv_softcap = softcap ? 1.f / p->final_logit_softcapping : 0.f;
   fp.ignore_index = p->ignore_index;
-  fp.targets = targets;
+  fp.targets = tgt;
   fp.part_m = reinterpret_cast<float*>(ws + L.part_m);
   fp.part_s = reinterpret_cast<float*>(ws + L.part_s);
   fp.part_a = reinterpret_cast<float*>(ws + L.part_a);
@@ -398,11 +448,13 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   mp.part_best = fp.part_best;
   mp.part_idx = fp.part_idx;
   mp.z_target = fp.z_target;
-  mp.targets = targets;
+  mp.targets = tgt;
   mp.lse = lse;
   mp.entropy = entropy;
   mp.loss_tok = p->reduction == FLCE_RED_NONE ? loss : nullptr;
   mp.blocks = blocks;
+  mp.row_map = row_map;
+  mp.row_count = row_count;
   FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_merge(mp, status, st); }));
   return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
 }
@@ -436,10 +488,46 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   }
 
   const bool h32 = p->hidden_dtype == FLCE_F32;
+  const bool cmp = compact(p);
+  const bool none = p->reduction == FLCE_RED_NONE;
+  const int32_t* row_count = nullptr;
+  const int32_t* row_map = nullptr;
+  const int64_t* tgt = targets;
+  const float* lse_use = lse;
+  const float* dloss_use = dloss;
   const void* h_main = hidden;
-  if (h32) {
-    uint16_t* hi = reinterpret_cast<uint16_t*>(ws + L.hi);
-    uint16_t* lo = reinterpret_cast<uint16_t*>(ws + L.lo);
+  uint16_t* hi = h32 ? reinterpret_cast<uint16_t*>(ws + L.hi) : nullptr;
+  uint16_t* lo = h32 ? reinterpret_cast<uint16_t*>(ws + L.lo) : nullptr;
+  if (cmp) {
+    CompactParams cp{};
+    cp.n_tokens = N;
+    cp.hidden = D;
+    cp.vocab = V;
+    cp.ignore_index = p->ignore_index;
+    cp.targets = targets;
+    cp.hidden_in = hidden;
+    cp.hidden_f32 = h32;
+    cp.block_counts = reinterpret_cast<int32_t*>(ws + L.c_blocks);
+    cp.block_offsets = reinterpret_cast<int32_t*>(ws + L.c_offsets);
+    cp.count = reinterpret_cast<int32_t*>(ws + L.c_count);
+    cp.row_map = reinterpret_cast<int32_t*>(ws + L.c_map);
+    cp.targets_out = reinterpret_cast<int64_t*>(ws + L.c_targets);
+    cp.hc = h32 ? hi : reinterpret_cast<uint16_t*>(ws + L.c_hidden);
+    cp.lo = lo;
+    cp.lse_in = lse;
+    cp.lse_out = reinterpret_cast<float*>(ws + L.c_lse);
+    cp.dloss_in = none ? dloss : nullptr;
+    cp.dloss_out = none ? reinterpret_cast<float*>(ws + L.c_dloss) : nullptr;
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, st); }));
+    row_count = cp.count;
+    row_map = cp.row_map;
+    tgt = cp.targets_out;
+    lse_use = cp.lse_out;
+    if (none) dloss_use = cp.dloss_out;
+    h_main = cp.hc;
+    // ignored tokens get a zero dhidden row; the valid ones are written below
+    FLCE_TRY(fail(cudaMemsetAsync(dhidden, 0, size_t(N) * D * (h32 ? 4 : 2), st)));
+  } else if (h32) {
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
       return launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st);
     }));
@@ -455,13 +543,13 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   TmaMaps rec;  // recompute: A = h (K-major), B = W (K-major)
   FLCE_TRY(make_map(&rec.a0, h_main, D, N, D * 2, kBK, kBM));
   rec.a1 = rec.a0;
-  if (h32) FLCE_TRY(make_map(&rec.a1, ws + L.lo, D, N, D * 2, kBK, kBM));
+  if (h32) FLCE_TRY(make_map(&rec.a1, lo, D, N, D * 2, kBK, kBM));
   FLCE_TRY(make_map(&rec.b0, weight, D, V, D * 2, kBK, pair_rec ? kBN / 2 : kBN));
   rec.b1 = rec.b0;
   CUtensorMap h_mn, lo_mn, w_mn;  // MN-major views: h for dW, W for dh
   FLCE_TRY(make_map(&h_mn, h_main, D, N, D * 2, 64, kBK));
   lo_mn = h_mn;
-  if (h32) FLCE_TRY(make_map(&lo_mn, ws + L.lo, D, N, D * 2, 64, kBK));
+  if (h32) FLCE_TRY(make_map(&lo_mn, lo, D, N, D * 2, 64, kBK));
   FLCE_TRY(make_map(&w_mn, weight, D, V, D * 2, 64, kBK));
 
   // dh: CTA pairs or single CTAs, and the K split for this device (bounded by
@@ -485,6 +573,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     GemmSched s1 = base_sched(N, width, D, h32 ? 2 : 1, 1, pair_rec);
     s1.b_mn_off = static_cast<int32_t>(v0);
     s1.group_m = pair_rec ? 16 : 32;
+    s1.m_limit = row_count;
     finish_sched(s1);
     GradParams gp{};
     gp.n_tokens = N;
@@ -498,10 +587,11 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     gp.softcap = softcap ? p->final_logit_softcapping : 0.f;
     gp.inv_softcap = softcap ? 1.f / p->final_logit_softcapping : 0.f;
     gp.ignore_index = p->ignore_index;
-    gp.targets = targets;
-    gp.lse = lse;
-    gp.dloss = dloss;
+    gp.targets = tgt;
+    gp.lse = lse_use;
+    gp.dloss = dloss_use;
     gp.n_valid = n_valid;
+    gp.num_items = static_cast<float>(p->num_items_in_batch);
     gp.g = g;
     gp.ldg = L.vc;
     gp.dbias_part = dbias_part;
@@ -512,7 +602,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
       FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
         return launch_dbias_reduce(dbias_part, L.vc, static_cast<int>(cdiv(N, kBM)), width,
                                    static_cast<uint8_t*>(dbias) + v0 * bias_elem,
-                                   p->bias_dtype == FLCE_F32, st);
+                                   p->bias_dtype == FLCE_F32, row_count, st);
       }));
     }
 
@@ -527,6 +617,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     s2.a_mn = 1;
     s2.b_mn = 1;
     s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
+    s2.k_limit = row_count;
     finish_sched(s2);
     StoreParams sp{};
     sp.rows = width;
@@ -549,6 +640,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     s3.ksplit = ksplit;
     s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
     s3.group_m = std::max(1, dh_ctas / std::max(1, s3.n_tiles * ksplit));
+    s3.m_limit = row_count;
     finish_sched(s3);
     AccumParams ap{};
     ap.rows = N;
@@ -559,12 +651,15 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     ap.write_final = (ksplit == 1 && last) ? 1 : 0;
     ap.out = dhidden;
     ap.out_f32 = h32 ? 1 : 0;
+    ap.row_map = row_map;
+    ap.row_count = row_count;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_DHIDDEN, st,
                     [&] { return launch_accum_gemm(pair_dh, mh, s3, ap, status, dev.num_sms, st); }));
   }
   if (ksplit > 1) {
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-      return launch_dh_finalize(dh_part, N * D, ksplit, N * D, dhidden, h32 ? 1 : 0, dev.num_sms * 4, st);
+      return launch_dh_finalize(dh_part, N * D, ksplit, N, D, dhidden, h32 ? 1 : 0, row_map, row_count,
+                                dev.num_sms * 4, st);
     }));
   }
   return FLCE_OK;

@@ -60,7 +60,9 @@ __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p,
   const int64_t row = blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x;
   double loss_d = 0.0, ent_d = 0.0;
   long long corr = 0, val = 0;
-  if (row < p.n_tokens) {
+  const int64_t rows = p.row_count ? static_cast<int64_t>(*p.row_count) : p.n_tokens;
+  if (row < rows) {
+    const int64_t orow = p.row_map ? static_cast<int64_t>(p.row_map[row]) : row;
     const int64_t N = p.n_tokens;
     float M = -INFINITY;
     for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, p.part_m[s * N + row]);
@@ -72,9 +74,10 @@ __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p,
       S = fmaf(p.part_s[s * N + row], f, S);
       A = fmaf(p.part_a[s * N + row], f, A);
       const float b = p.part_best[s * N + row];
-      if (b > best) {
+      const int32_t bi = p.part_idx[s * N + row];
+      if (b > best || (b == best && bi < best_idx)) {  // lowest index on ties
         best = b;
-        best_idx = p.part_idx[s * N + row];
+        best_idx = bi;
       }
     }
     const float lse = M + logf(S);
@@ -84,9 +87,9 @@ __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p,
     const bool valid = in_range && t != p.ignore_index;
     if (t != p.ignore_index && !in_range) atomicCAS(status, 0, kStatusTargetOutOfRange);
     const float loss = valid ? lse - p.z_target[row] : 0.f;
-    p.lse[row] = lse;
-    if (p.entropy) p.entropy[row] = ent;
-    if (p.loss_tok) p.loss_tok[row] = loss;
+    p.lse[orow] = lse;
+    if (p.entropy) p.entropy[orow] = ent;
+    if (p.loss_tok) p.loss_tok[orow] = loss;
     loss_d = loss;
     ent_d = valid ? ent : 0.0;
     corr = (valid && best_idx == t) ? 1 : 0;
@@ -159,7 +162,8 @@ __global__ void __launch_bounds__(256) fwd_reduce_kernel(ReduceParams p) {
       C += s_corr[i];
       V += s_val[i];
     }
-    if (p.reduction == 2) p.loss[0] = V > 0 ? static_cast<float>(L / static_cast<double>(V)) : 0.f;
+    const double den = p.num_items > 0.0 ? p.num_items : static_cast<double>(V);
+    if (p.reduction == 2) p.loss[0] = den > 0.0 ? static_cast<float>(L / den) : 0.f;
     if (p.reduction == 1) p.loss[0] = static_cast<float>(L);
     p.correct[0] = C;
     p.n_valid[0] = V;
@@ -169,6 +173,137 @@ __global__ void __launch_bounds__(256) fwd_reduce_kernel(ReduceParams p) {
 
 cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream) {
   fwd_reduce_kernel<<<1, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Valid-token compaction: the tokens whose target is valid, in their original
+// order, are gathered into positions [0, count); positions [count, N) get a
+// zero hidden row and the ignore index so that they contribute nothing.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool target_valid(const CompactParams& p, int64_t row, int64_t* t_out) {
+  const int64_t t = p.targets[row];
+  *t_out = t;
+  return t != p.ignore_index && t >= 0 && t < p.vocab;
+}
+
+__global__ void __launch_bounds__(kCompactBlock) compact_count_kernel(CompactParams p, int* status) {
+  const int64_t row = blockIdx.x * static_cast<int64_t>(kCompactBlock) + threadIdx.x;
+  int valid = 0;
+  if (row < p.n_tokens) {
+    int64_t t;
+    valid = target_valid(p, row, &t) ? 1 : 0;
+    if (!valid && t != p.ignore_index) atomicCAS(status, 0, kStatusTargetOutOfRange);
+  }
+  const int n = __syncthreads_count(valid);
+  if (threadIdx.x == 0) p.block_counts[blockIdx.x] = n;
+}
+
+__global__ void compact_scan_kernel(CompactParams p, int n_blocks) {
+  if (threadIdx.x != 0) return;
+  int acc = 0;
+  for (int b = 0; b < n_blocks; ++b) {
+    p.block_offsets[b] = acc;
+    acc += p.block_counts[b];
+  }
+  *p.count = acc;
+}
+
+// Copies hidden row `src` to compacted row `dst` (bf16), or splits it into hi / lo (fp32).
+__device__ __forceinline__ void copy_hidden_row(const CompactParams& p, int64_t src, int64_t dst, uint32_t lane) {
+  const int64_t D = p.hidden;
+  if (!p.hidden_f32) {
+    const uint4* in = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.hidden_in) + src * D);
+    uint4* out = reinterpret_cast<uint4*>(p.hc + dst * D);
+    for (int64_t i = lane; i < D / 8; i += 32) out[i] = in[i];
+  } else {
+    const float4* in = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.hidden_in) + src * D);
+    uint2* hi = reinterpret_cast<uint2*>(p.hc + dst * D);
+    uint2* lo = reinterpret_cast<uint2*>(p.lo + dst * D);
+    for (int64_t i = lane; i < D / 4; i += 32) {
+      const float4 x = in[i];
+      const uint32_t h01 = pack_bf16x2(x.x, x.y);
+      const uint32_t h23 = pack_bf16x2(x.z, x.w);
+      hi[i] = make_uint2(h01, h23);
+      lo[i] = make_uint2(pack_bf16x2(x.x - __uint_as_float(h01 << 16), x.y - __uint_as_float(h01 & 0xFFFF0000u)),
+                         pack_bf16x2(x.z - __uint_as_float(h23 << 16), x.w - __uint_as_float(h23 & 0xFFFF0000u)));
+    }
+  }
+}
+
+__device__ __forceinline__ void zero_hidden_row(const CompactParams& p, int64_t dst, uint32_t lane) {
+  const int64_t D = p.hidden;
+  uint4* out = reinterpret_cast<uint4*>(p.hc + dst * D);
+  for (int64_t i = lane; i < D / 8; i += 32) out[i] = make_uint4(0, 0, 0, 0);
+  if (p.hidden_f32) {
+    uint4* out2 = reinterpret_cast<uint4*>(p.lo + dst * D);
+    for (int64_t i = lane; i < D / 8; i += 32) out2[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactParams p) {
+  __shared__ int s_warp[kCompactBlock / 32];
+  __shared__ int s_pos[kCompactBlock];
+  const int64_t base = blockIdx.x * static_cast<int64_t>(kCompactBlock);
+  const int64_t row = base + threadIdx.x;
+  const uint32_t lane = threadIdx.x & 31u;
+  const int warp = threadIdx.x >> 5;
+  int64_t t = p.ignore_index;
+  const bool valid = row < p.n_tokens && target_valid(p, row, &t);
+  const uint32_t ballot = __ballot_sync(0xffffffffu, valid);
+  if (lane == 0) s_warp[warp] = __popc(ballot);
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the per-warp counts
+    const int c = s_warp[lane];
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= static_cast<uint32_t>(o)) incl += y;
+    }
+    s_warp[lane] = incl - c;
+  }
+  __syncthreads();
+  const int pos = valid ? p.block_offsets[blockIdx.x] + s_warp[warp] + __popc(ballot & ((1u << lane) - 1u)) : -1;
+  s_pos[threadIdx.x] = pos;
+  if (valid) {
+    p.row_map[pos] = static_cast<int32_t>(row);
+    p.targets_out[pos] = t;
+    if (p.lse_in) p.lse_out[pos] = p.lse_in[row];
+    if (p.dloss_in) p.dloss_out[pos] = p.dloss_in[row];
+  } else if (row < p.n_tokens) {  // ignored token: its per-token outputs are 0
+    if (p.lse_default) p.lse_default[row] = 0.f;
+    if (p.entropy_default) p.entropy_default[row] = 0.f;
+    if (p.loss_default) p.loss_default[row] = 0.f;
+  }
+  const int64_t count = *p.count;
+  const int64_t q = base + threadIdx.x;  // a compacted position in this block's window
+  if (q >= count && q < p.n_tokens) {
+    p.row_map[q] = 0;
+    p.targets_out[q] = p.ignore_index;
+    if (p.lse_out) p.lse_out[q] = 0.f;
+    if (p.dloss_out) p.dloss_out[q] = 0.f;
+  }
+  __syncthreads();
+  for (int i = 0; i < 32; ++i) {
+    const int r_local = warp * 32 + i;
+    const int64_t r = base + r_local;
+    if (r >= p.n_tokens) break;
+    const int dst = s_pos[r_local];
+    if (dst >= 0) copy_hidden_row(p, r, dst, lane);
+    if (r >= count) zero_hidden_row(p, r, lane);
+  }
+}
+
+cudaError_t launch_compact(const CompactParams& p, int* status, cudaStream_t stream) {
+  const int64_t blocks = (p.n_tokens + kCompactBlock - 1) / kCompactBlock;
+  if (blocks == 0) return cudaSuccess;
+  compact_count_kernel<<<static_cast<unsigned>(blocks), kCompactBlock, 0, stream>>>(p, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  compact_scan_kernel<<<1, 32, 0, stream>>>(p, static_cast<int>(blocks));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  compact_gather_kernel<<<static_cast<unsigned>(blocks), kCompactBlock, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -37,10 +37,23 @@ namespace flce {
 struct Unit {
   int m_blk, n_unit, n_first, n_count, kb_first, kb_count, ks;
   int64_t row0;  // first output row of this CTA's 128-row slice of the tile
+  bool skip;     // the tile starts past the device-side row limit: no work
 };
 
+// Device-side limits of a launch (valid-token compaction), read once.
+struct Limits {
+  int32_t m_rows;   // units whose first row is at or past this are skipped
+  int32_t k_blocks; // K blocks past this are not loaded or multiplied
+};
+__device__ __forceinline__ Limits read_limits(const GemmSched& sc) {
+  Limits l;
+  l.m_rows = sc.m_limit ? *reinterpret_cast<const volatile int32_t*>(sc.m_limit) : 0x7fffffff;
+  l.k_blocks = sc.k_limit ? (*reinterpret_cast<const volatile int32_t*>(sc.k_limit) + kBK - 1) / kBK : 0x7fffffff;
+  return l;
+}
+
 __device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u, int rows_per_tile = kBM,
-                                            uint32_t rank = 0) {
+                                            uint32_t rank = 0, Limits lim = Limits{0x7fffffff, 0x7fffffff}) {
   const int per_m = sc.n_units * sc.ksplit;
   const int per_group = sc.group_m * per_m;
   const int g = u / per_group;
@@ -56,8 +69,9 @@ __device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u, int rows
   t.n_first = t.n_unit * sc.n_per_unit;
   t.n_count = min(sc.n_per_unit, sc.n_tiles - t.n_first);
   t.kb_first = t.ks * sc.kb_per_split;
-  t.kb_count = max(0, min(sc.kb_per_split, sc.k_blocks - t.kb_first));
+  t.kb_count = max(0, min(sc.kb_per_split, min(sc.k_blocks, lim.k_blocks) - t.kb_first));
   t.row0 = static_cast<int64_t>(t.m_blk) * rows_per_tile + static_cast<int64_t>(rank) * kBM;
+  t.skip = static_cast<int64_t>(t.m_blk) * rows_per_tile >= lim.m_rows;
   return t;
 }
 
@@ -294,8 +308,10 @@ struct EpiGrad {
         } else if (p.reduction == 1) {
           st.w = __ldg(p.dloss);
         } else {
-          const int64_t nv = __ldg(reinterpret_cast<const long long*>(p.n_valid));
-          st.w = nv > 0 ? __ldg(p.dloss) / static_cast<float>(nv) : 0.f;
+          const float den = p.num_items > 0.f
+                                ? p.num_items
+                                : static_cast<float>(__ldg(reinterpret_cast<const long long*>(p.n_valid)));
+          st.w = den > 0.f ? __ldg(p.dloss) / den : 0.f;
         }
       }
     }
@@ -399,11 +415,24 @@ struct EpiStore {
     int64_t row;
   };
   __device__ static void begin_unit(const Params&, const Unit& u, State& st) { st.row = u.row0 + threadIdx.x; }
-  __device__ static void tile(const Params& p, const Unit&, int n_tile, uint32_t taddr, State& st, float*) {
+  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*) {
     const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;
-    for_each_tmem_chunk(taddr, chunks_below(col_tile, p.cols), [&](const uint32_t (&r)[32], int c) {
+    if (u.kb_count == 0) {  // no K blocks (all tokens ignored under compaction): the product is zero
+      uint32_t zero[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) zero[j] = 0u;
+      const int nch = chunks_below(col_tile, p.cols);
+#pragma unroll 1
+      for (int c = 0; c < nch; ++c) store(p, st, col_tile + c * 32, zero);
+      return;
+    }
+    for_each_tmem_chunk(taddr, chunks_below(col_tile, p.cols),
+                        [&](const uint32_t (&r)[32], int c) { store(p, st, col_tile + c * 32, r); });
+  }
+
+  __device__ static void store(const Params& p, const State& st, int64_t col, const uint32_t (&r)[32]) {
+    {
       if (st.row >= p.rows) return;
-      const int64_t col = col_tile + c * 32;
       const int64_t n = p.cols - col;
       if (p.out_f32) {
         float* dst = reinterpret_cast<float*>(p.out) + st.row * p.ldo + col;
@@ -434,7 +463,7 @@ struct EpiStore {
             if (j < n) dst[j] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]), 0.f) & 0xFFFFu);
         }
       }
-    });
+    }
   }
   __device__ static void end_unit(const Params&, const Unit&, State&) {}
 };
@@ -451,6 +480,8 @@ struct EpiAccum {
 
   __device__ static void store(const Params& p, const Unit& u, const State& st, int64_t col, float (&v)[32]) {
     if (st.row >= p.rows) return;
+    if (p.row_count && st.row >= *p.row_count) return;
+    const int64_t orow = p.row_map ? static_cast<int64_t>(__ldg(p.row_map + st.row)) : st.row;
     float* slot = p.part + static_cast<int64_t>(u.ks) * p.part_stride + st.row * p.cols + col;
     const int64_t rem = p.cols - col;
     if (rem >= 32) {
@@ -469,12 +500,12 @@ struct EpiAccum {
         for (int q = 0; q < 8; ++q)
           reinterpret_cast<float4*>(slot)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       } else if (p.out_f32) {
-        float* dst = reinterpret_cast<float*>(p.out) + st.row * p.cols + col;
+        float* dst = reinterpret_cast<float*>(p.out) + orow * p.cols + col;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       } else {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + st.row * p.cols + col;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + orow * p.cols + col;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 pk;
@@ -494,9 +525,9 @@ struct EpiAccum {
         if (!p.write_final) {
           slot[j] = x;
         } else if (p.out_f32) {
-          reinterpret_cast<float*>(p.out)[st.row * p.cols + col + j] = x;
+          reinterpret_cast<float*>(p.out)[orow * p.cols + col + j] = x;
         } else {
-          reinterpret_cast<uint16_t*>(p.out)[st.row * p.cols + col + j] =
+          reinterpret_cast<uint16_t*>(p.out)[orow * p.cols + col + j] =
               static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
         }
       }
@@ -604,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot;
+  const Limits lim = read_limits(sc);
 
   if (warp == kTmaWarp) {
     // ---------------------------------------------------------------- producer
@@ -617,7 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued_phase[s] = 0;
       }
       for (int uu = blockIdx.x; uu < sc.total_units; uu += gridDim.x) {
-        const Unit u = decode_unit(sc, uu);
+        const Unit u = decode_unit(sc, uu, kBM, 0, lim);
+        if (u.skip) continue;
         bool ok = true;
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
           for (int seg = 0; ok && seg < sc.nseg; ++seg) {
@@ -670,7 +703,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int uu = blockIdx.x; ok && uu < sc.total_units; uu += gridDim.x) {
-        const Unit u = decode_unit(sc, uu);
+        const Unit u = decode_unit(sc, uu, kBM, 0, lim);
+        if (u.skip) continue;
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
           if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, sm.ctl, status)) {
             ok = false;
@@ -723,7 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok = true;
     for (int uu = blockIdx.x; ok && uu < sc.total_units; uu += gridDim.x) {
-      const Unit u = decode_unit(sc, uu);
+      const Unit u = decode_unit(sc, uu, kBM, 0, lim);
+        if (u.skip) continue;
       typename Epi::State st;
       Epi::begin_unit(ep, u, st);
       for (int n = u.n_first; n < u.n_first + u.n_count; ++n) {
@@ -824,6 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot;
+  const Limits lim = read_limits(sc);
   const int cid = blockIdx.x >> 1;
   const int ncl = gridDim.x >> 1;
   bool aborted = false;
@@ -841,7 +877,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
-        const Unit u = decode_unit(sc, uu, kPairRows, rank);
+        const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
+        if (u.skip) continue;
         const int a_row = sc.a_mn_off + static_cast<int>(u.row0);
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
           const int b_col = sc.b_mn_off + n * kBN + static_cast<int>(rank) * (kBN / 2);
@@ -897,7 +934,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
-        const Unit u = decode_unit(sc, uu, kPairRows, rank);
+        const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
+        if (u.skip) continue;
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
           if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, sm.ctl, status)) {
             ok = false;
@@ -950,7 +988,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok = true;
     for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
-      const Unit u = decode_unit(sc, uu, kPairRows, rank);
+      const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
+        if (u.skip) continue;
       typename Epi::State st;
       Epi::begin_unit(ep, u, st);
       for (int n = u.n_first; n < u.n_first + u.n_count; ++n) {

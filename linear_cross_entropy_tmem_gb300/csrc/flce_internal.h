@@ -67,6 +67,11 @@ struct GemmSched {
   int32_t a_mn, b_mn;     // operand majorness: 0 = K-major, 1 = MN-major
   int32_t a_mn_off, a_k_off;   // coordinate offsets into the A tensor map
   int32_t b_mn_off, b_k_off;   // coordinate offsets into the B tensor map
+  // Optional device-side limits (valid-token compaction): units whose first
+  // row is at or past *m_limit are skipped, and the K range stops at *k_limit
+  // elements.  nullptr = no limit.
+  const int32_t* m_limit;
+  const int32_t* k_limit;
 };
 
 // ---- Epilogue parameter blocks --------------------------------------------
@@ -105,6 +110,7 @@ struct GradParams {
   const float* lse;
   const float* dloss;
   const int64_t* n_valid;
+  float num_items;        // > 0: the mean divides by it instead of *n_valid
   uint16_t* g;            // bf16 [n_tokens][ldg]
   int64_t ldg;
   float* dbias_part;      // [m_tiles][ldg] or nullptr
@@ -127,6 +133,31 @@ struct AccumParams {
   int32_t write_final;    // write `out` in its dtype instead of the slot (ksplit == 1)
   void* out;
   int32_t out_f32;
+  const int32_t* row_map;   // compacted row -> output row, or nullptr
+  const int32_t* row_count; // rows at or past *row_count are not written, or nullptr
+};
+
+// Valid-token compaction.
+constexpr int kCompactBlock = 1024;  // rows per block of the count / gather kernels
+struct CompactParams {
+  int64_t n_tokens, hidden, vocab, ignore_index;
+  const int64_t* targets;
+  const void* hidden_in;   // [N][D] bf16 or fp32
+  int32_t hidden_f32;
+  int32_t* block_counts;   // [blocks]
+  int32_t* block_offsets;  // [blocks]
+  int32_t* count;          // [1] number of valid tokens
+  int32_t* row_map;        // [N] compacted position -> original row
+  int64_t* targets_out;    // [N] compacted targets (ignore_index past the count)
+  uint16_t* hc;            // [N][D] bf16 compacted hidden (bf16 input), or hi part (fp32 input)
+  uint16_t* lo;            // [N][D] lo part (fp32 input), else nullptr
+  const float* lse_in;     // backward: [N] lse to compact, or nullptr
+  float* lse_out;
+  const float* dloss_in;   // backward, reduction none: [N] upstream grads to compact, or nullptr
+  float* dloss_out;
+  float* lse_default;      // forward: write 0 at ignored rows of these outputs (nullable)
+  float* entropy_default;
+  float* loss_default;
 };
 
 }  // namespace flce

@@ -33,12 +33,15 @@ struct MergeParams {
   float* entropy;     // nullable
   float* loss_tok;    // the loss output when reduction is 'none', else nullptr
   BlockPartial* blocks;
+  const int32_t* row_map;    // compacted row -> output row, or nullptr
+  const int32_t* row_count;  // rows at or past *row_count are skipped, or nullptr
 };
 
 struct ReduceParams {
   const BlockPartial* blocks;
   int32_t n_blocks;
   int32_t reduction;
+  double num_items;   // > 0: the mean divides by it instead of the valid count
   float* loss;        // [1] for mean / sum
   int64_t* correct;
   int64_t* n_valid;
@@ -63,8 +66,11 @@ cudaError_t launch_split_hidden(const float* h, uint16_t* hi, uint16_t* lo, int6
 cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream);
 cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream);
 cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int64_t cols, void* dbias,
-                                int bias_f32, cudaStream_t stream);
-cudaError_t launch_dh_finalize(const float* part, int64_t stride, int ksplit, int64_t n, void* out, int out_f32,
-                               int grid, cudaStream_t stream);
+                                int bias_f32, const int32_t* row_count, cudaStream_t stream);
+cudaError_t launch_dh_finalize(const float* part, int64_t stride, int ksplit, int64_t rows, int64_t cols, void* out,
+                               int out_f32, const int32_t* row_map, const int32_t* row_count, int grid,
+                               cudaStream_t stream);
+// Valid-token compaction: count, scan, gather (see CompactParams).
+cudaError_t launch_compact(const CompactParams& p, int* status, cudaStream_t stream);
 
 }  // namespace flce

@@ -23,14 +23,15 @@ TOL_GRAD = 1e-2
 NEAR_TIE = 1e-3
 
 
-def run_gpu(h, W, b, t, dloss, *, logit_scale, softcap, reduction, ignore_index=-100, backward=True):
+def run_gpu(h, W, b, t, dloss, *, logit_scale, softcap, reduction, ignore_index=-100, backward=True,
+            num_items_in_batch=0.0, compact=False):
     import linear_cross_entropy_tmem_gb300 as F
-    f = F.flce_forward(h, W, t, b, logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
-                       reduction=reduction, entropy=True)
+    kw = dict(logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index, reduction=reduction,
+              num_items_in_batch=num_items_in_batch, compact=compact)
+    f = F.flce_forward(h, W, t, b, entropy=True, **kw)
     out = {"fwd": f}
     if backward:
-        out["bwd"] = F.flce_backward(h, W, t, f.lse, f.n_valid, dloss, b, logit_scale=logit_scale,
-                                     softcap=softcap, ignore_index=ignore_index, reduction=reduction)
+        out["bwd"] = F.flce_backward(h, W, t, f.lse, f.n_valid, dloss, b, **kw)
     torch.cuda.synchronize()
     out["status"] = F.flce_read_device_status(f.workspace)
     return out

@@ -38,16 +38,18 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.flce_abi_version() == 1
+    assert lib.flce_abi_version() == 2
     for code in range(0, 10):
         assert lib.flce_status_string(code).decode() not in ("", "unknown status")
     assert lib.flce_status_string(12345).decode() == "unknown status"
 
 
 def test_problem_struct_layout_matches_header():
-    # int64 x3, int32 x4, float x2, int64  ->  56 bytes with natural alignment
-    assert ctypes.sizeof(B.FlceProblem) == 56
+    # int64 x3, int32 x4, float x2, int64, double, uint32 x2 -> 72 bytes, natural alignment
+    assert ctypes.sizeof(B.FlceProblem) == 72
     assert B.FlceProblem.ignore_index.offset == 48
+    assert B.FlceProblem.num_items_in_batch.offset == 56
+    assert B.FlceProblem.flags.offset == 64
 
 
 def _problem(**kw):
@@ -96,6 +98,10 @@ def test_workspace_size_needs_no_gpu_and_never_scales_with_n_times_v(lib):
     (dict(weight_dtype=B.FLCE_F32, hidden_dtype=B.FLCE_F32), B.FLCE_ERR_UNSUPPORTED_DTYPE),
     (dict(hidden_dtype=5), B.FLCE_ERR_UNSUPPORTED_DTYPE),
     (dict(logit_scale=float("nan")), B.FLCE_ERR_INVALID_ARG),
+    (dict(num_items_in_batch=-1.0), B.FLCE_ERR_INVALID_ARG),
+    (dict(num_items_in_batch=float("inf")), B.FLCE_ERR_INVALID_ARG),
+    (dict(flags=8), B.FLCE_ERR_INVALID_ARG),
+    (dict(reserved=1), B.FLCE_ERR_INVALID_ARG),
 ])
 def test_problem_validation(lib, kw, code):
     assert _ws(lib, _problem(**kw), 0)[0] == code

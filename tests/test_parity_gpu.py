@@ -180,3 +180,98 @@ def test_autograd_wrapper_matches_direct_calls():
     torch.cuda.synchronize()
     assert torch.equal(loss, f.loss)
     assert torch.equal(hh.grad, dh) and torch.equal(WW.grad, dW) and torch.equal(bb.grad, db)
+
+
+# ---------------------------------------------------------------------------
+# num_items_in_batch and valid-token compaction
+# ---------------------------------------------------------------------------
+def test_num_items_in_batch_matches_oracle():
+    """TRL PR #6859 review, "Test coverage" item 10: the mean over a caller-given count."""
+    w = CASES["ragged N300 D200 V1000 bias-bf16 s0.7 c5 sum"][0].scaled(reduction="mean")
+    h, W, b, t, dloss = make_inputs(w, "cpu")
+    dloss = torch.full((1,), 0.7)
+    dev = [x.cuda() if x is not None else None for x in (h, W, b, t, dloss)]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction="mean")
+    for items in (1000.0, 37.0):
+        g = run_gpu(*dev, num_items_in_batch=items, **kw)
+        ref_f = oracle.forward(h, W, b, t, num_items_in_batch=items, **kw)
+        ref_b = oracle.backward(h, W, b, t, dloss=dloss, num_items_in_batch=items, **kw)
+        compare_forward(g["fwd"], ref_f, reduction="mean")
+        compare_backward(g["bwd"], ref_b)
+
+
+def _compare_compacted(gpu, ref_f, ref_b, t, reduction):
+    valid = ref_f["valid"]
+    f = gpu["fwd"]
+    lse = f.lse.double().cpu().numpy()
+    ent = f.entropy.double().cpu().numpy()
+    np.testing.assert_allclose(lse[valid], ref_f["lse"][valid], atol=2e-3, rtol=0)
+    np.testing.assert_allclose(ent[valid], ref_f["entropy"][valid], atol=5e-3, rtol=0)
+    assert np.all(lse[~valid] == 0.0) and np.all(ent[~valid] == 0.0)
+    nv = int(f.n_valid)
+    assert nv == ref_f["n_valid"]
+    if reduction == "none":
+        np.testing.assert_allclose(f.loss.double().cpu().numpy(), ref_f["loss"], atol=2e-3, rtol=0)
+    else:
+        tol = 2e-3 * (nv if reduction == "sum" else 1)
+        assert abs(float(f.loss) - ref_f["loss"]) <= tol
+    assert abs(float(f.entropy_sum) - ref_f["entropy_sum"]) <= 5e-3 * max(1, nv)
+    assert int(f.correct) == ref_f["correct"]
+    dh, dW, db = gpu["bwd"]
+    assert torch.all(dh[torch.from_numpy(~valid).cuda()] == 0)
+    assert oracle.relative_frobenius(dh, ref_b["dh"]) <= 1e-2
+    assert oracle.relative_frobenius(dW, ref_b["dW"]) <= 1e-2
+    if db is not None:
+        assert oracle.relative_frobenius(db, ref_b["db"]) <= 1e-2
+
+
+COMPACT_CASES = ["tiny N512 D128 V4096 mean", "ragged N300 D200 V1000 bias-bf16 s0.7 c5 sum",
+                 "fp32-h N257 D136 V777 bias s0.0625 c30 none", "multi-chunk ksplit3 N384 D256 V3000 bias mean",
+                 "multi-chunk ksplit1 N640 D512 V2560 none", "fp32-h multi-chunk N200 D64 V1500 softcap sum"]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["auto", "single-cta", "cta-pair"])
+@pytest.mark.parametrize("name", COMPACT_CASES)
+@pytest.mark.parametrize("ignore_every", [17, 3])
+def test_compaction_matches_oracle(name, mode, ignore_every):
+    """FLCE_FLAG_COMPACT_VALID: valid tokens match the oracle; ignored ones get 0."""
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_tuning
+    w, tuning = CASES[name]
+    w = w.scaled(ignore_every=ignore_every)
+    testing_set_gemm_mode(mode)
+    testing_set_tuning(*tuning)
+    h, W, b, t, dloss = make_inputs(w, "cpu")
+    dev = [x.cuda() if x is not None else None for x in (h, W, b, t, dloss)]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    gpu = run_gpu(*dev, compact=True, **kw)
+    assert gpu["status"] == 0
+    _compare_compacted(gpu, oracle.forward(h, W, b, t, **kw), oracle.backward(h, W, b, t, dloss=dloss, **kw),
+                       t, w.reduction)
+
+
+def test_compaction_all_ignored_and_out_of_range():
+    w = Workload("cign", 300, 64, 700, sigma_w=0.2, bias=True, seed=12)
+    h, W, b, t, _ = make_inputs(w, "cuda")
+    t[:] = -100
+    g = run_gpu(h, W, b, t, torch.ones(1, device="cuda"), logit_scale=1.0, softcap=0.0, reduction="mean",
+                compact=True)
+    assert int(g["fwd"].n_valid) == 0 and float(g["fwd"].loss) == 0.0
+    for x in g["bwd"]:
+        assert torch.all(x == 0)
+    t[:] = 5
+    t[7] = 700  # out of range: reported and treated as ignored
+    g = run_gpu(h, W, b, t, torch.ones(1, device="cuda"), logit_scale=1.0, softcap=0.0, reduction="mean",
+                compact=True)
+    assert g["status"] == 7 and int(g["fwd"].n_valid) == 299
+
+
+def test_compaction_is_deterministic():
+    from linear_cross_entropy_tmem_gb300.api import testing_set_tuning
+    w, tuning = CASES["multi-chunk ksplit3 N384 D256 V3000 bias mean"]
+    testing_set_tuning(*tuning)
+    h, W, b, t, dloss = [x.cuda() if x is not None else None for x in make_inputs(w.scaled(ignore_every=3), "cpu")]
+    a = run_gpu(h, W, b, t, dloss, logit_scale=1.0, softcap=0.0, reduction="mean", compact=True)
+    c = run_gpu(h, W, b, t, dloss, logit_scale=1.0, softcap=0.0, reduction="mean", compact=True)
+    assert torch.equal(a["fwd"].lse, c["fwd"].lse) and torch.equal(a["fwd"].loss, c["fwd"].loss)
+    for x, y in zip(a["bwd"], c["bwd"]):
+        assert torch.equal(x, y)
