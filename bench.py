@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = automatic)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling captures of a small case)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures of a small case)")
+    ap.add_argument("--compact", action="store_true",
+                    help="gather the valid tokens first (FLCE_FLAG_COMPACT_VALID)")
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM kernel: 0 automatic, 1 single CTA, 2 CTA pair (A/B timing)")
     return ap.parse_args(argv)
@@ -232,7 +234,7 @@ def reference_arm(args):
 class Runner:
     """Preallocated buffers and raw C-ABI calls for one forward + backward step."""
 
-    def __init__(self, w, device, seed_offset=0):
+    def __init__(self, w, device, seed_offset=0, compact=False):
         import torch
 
         import linear_cross_entropy_tmem_gb300.api as api
@@ -245,7 +247,8 @@ class Runner:
         self.h, self.W, self.b, self.t, self.dloss = make_inputs(w.scaled(seed=w.seed + seed_offset), device)
         N, D, V = w.n_tokens, w.hidden, w.vocab
         self.prob = api.make_problem(N, D, V, hidden_dtype=self.h.dtype, bias_dtype=torch.bfloat16,
-                                     logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+                                     logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction,
+                                     compact=compact)
         f32 = dict(dtype=torch.float32, device=device)
         self.loss = torch.empty(N if w.reduction == "none" else 1, **f32)
         self.lse = torch.empty(N, **f32)
@@ -324,7 +327,7 @@ def flce_arm(args):
     device = torch.device("cuda", local)
     dist = init_dist("nccl")
     w = pick_workload(args)
-    run = Runner(w, device, seed_offset=rank)
+    run = Runner(w, device, seed_offset=rank, compact=args.compact)
     lib = run.lib
     B.check(lib.flce_testing_set_gemm_mode(args.gemm_mode), "gemm mode")
 
@@ -436,6 +439,7 @@ def flce_arm(args):
             "config": {"workload": w.name, "n_tokens": w.n_tokens, "hidden": w.hidden, "vocab": w.vocab,
                        "reduction": w.reduction, "parallelism": f"replicas x{world}" if world > 1 else "none",
                        "gemm_mode": ["auto", "single-cta", "cta-pair"][args.gemm_mode],
+                       "compact_valid_tokens": bool(args.compact),
                        "l2": "inputs larger than L2 (1.25 GB head), no flush"},
             "tflops": tflops,
             "pct_of_peak": {"of_burst": tflops / peak_burst, "of_sustained": tflops / peak, "source": peak_src},

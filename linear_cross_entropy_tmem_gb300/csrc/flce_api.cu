@@ -387,7 +387,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
     cp.lse_default = lse;
     cp.entropy_default = entropy;
     cp.loss_default = p->reduction == FLCE_RED_NONE ? loss : nullptr;
-    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, st); }));
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, dev.num_sms, st); }));
     row_count = cp.count;
     row_map = cp.row_map;
     tgt = cp.targets_out;
@@ -518,7 +518,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     cp.lse_out = reinterpret_cast<float*>(ws + L.c_lse);
     cp.dloss_in = none ? dloss : nullptr;
     cp.dloss_out = none ? reinterpret_cast<float*>(ws + L.c_dloss) : nullptr;
-    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, st); }));
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, dev.num_sms, st); }));
     row_count = cp.count;
     row_map = cp.row_map;
     tgt = cp.targets_out;

@@ -243,7 +243,6 @@ __device__ __forceinline__ void zero_hidden_row(const CompactParams& p, int64_t 
 
 __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactParams p) {
   __shared__ int s_warp[kCompactBlock / 32];
-  __shared__ int s_pos[kCompactBlock];
   const int64_t base = blockIdx.x * static_cast<int64_t>(kCompactBlock);
   const int64_t row = base + threadIdx.x;
   const uint32_t lane = threadIdx.x & 31u;
@@ -265,7 +264,6 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
   }
   __syncthreads();
   const int pos = valid ? p.block_offsets[blockIdx.x] + s_warp[warp] + __popc(ballot & ((1u << lane) - 1u)) : -1;
-  s_pos[threadIdx.x] = pos;
   if (valid) {
     p.row_map[pos] = static_cast<int32_t>(row);
     p.targets_out[pos] = t;
@@ -284,18 +282,25 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
     if (p.lse_out) p.lse_out[q] = 0.f;
     if (p.dloss_out) p.dloss_out[q] = 0.f;
   }
-  __syncthreads();
-  for (int i = 0; i < 32; ++i) {
-    const int r_local = warp * 32 + i;
-    const int64_t r = base + r_local;
-    if (r >= p.n_tokens) break;
-    const int dst = s_pos[r_local];
-    if (dst >= 0) copy_hidden_row(p, r, dst, lane);
-    if (r >= count) zero_hidden_row(p, r, lane);
+}
+
+// Compacted row q <- hidden row row_map[q] (q < count), or a zero row; one warp
+// per row, grid-stride, so that the copy runs on every SM.
+__global__ void __launch_bounds__(256) compact_copy_kernel(CompactParams p) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t count = *p.count;
+  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); q < p.n_tokens;
+       q += warps) {
+    if (q < count) {
+      copy_hidden_row(p, p.row_map[q], q, lane);
+    } else {
+      zero_hidden_row(p, q, lane);
+    }
   }
 }
 
-cudaError_t launch_compact(const CompactParams& p, int* status, cudaStream_t stream) {
+cudaError_t launch_compact(const CompactParams& p, int* status, int num_sms, cudaStream_t stream) {
   const int64_t blocks = (p.n_tokens + kCompactBlock - 1) / kCompactBlock;
   if (blocks == 0) return cudaSuccess;
   compact_count_kernel<<<static_cast<unsigned>(blocks), kCompactBlock, 0, stream>>>(p, status);
@@ -304,6 +309,8 @@ cudaError_t launch_compact(const CompactParams& p, int* status, cudaStream_t str
   compact_scan_kernel<<<1, 32, 0, stream>>>(p, static_cast<int>(blocks));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   compact_gather_kernel<<<static_cast<unsigned>(blocks), kCompactBlock, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  compact_copy_kernel<<<num_sms * 4, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

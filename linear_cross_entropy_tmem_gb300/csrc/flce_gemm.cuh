@@ -40,26 +40,37 @@ struct Unit {
   bool skip;     // the tile starts past the device-side row limit: no work
 };
 
-// Device-side limits of a launch (valid-token compaction), read once.
+// Device-side limits of a launch (valid-token compaction), read once.  With a
+// row limit the units are enumerated over the m tiles that hold a valid row
+// only, so the persistent CTAs stay balanced.
 struct Limits {
-  int32_t m_rows;   // units whose first row is at or past this are skipped
-  int32_t k_blocks; // K blocks past this are not loaded or multiplied
+  int32_t m_rows;       // rows at or past this hold no work
+  int32_t m_tiles;      // m tiles enumerated
+  int32_t total_units;  // units enumerated
+  int32_t k_blocks;     // K blocks past this are not loaded or multiplied
 };
-__device__ __forceinline__ Limits read_limits(const GemmSched& sc) {
+__device__ __forceinline__ Limits read_limits(const GemmSched& sc, int rows_per_tile) {
   Limits l;
-  l.m_rows = sc.m_limit ? *reinterpret_cast<const volatile int32_t*>(sc.m_limit) : 0x7fffffff;
+  l.m_rows = 0x7fffffff;
+  l.m_tiles = sc.m_tiles;
+  l.total_units = sc.total_units;
+  if (sc.m_limit) {
+    l.m_rows = *reinterpret_cast<const volatile int32_t*>(sc.m_limit);
+    l.m_tiles = min(sc.m_tiles, (l.m_rows + rows_per_tile - 1) / rows_per_tile);
+    l.total_units = l.m_tiles * sc.n_units * sc.ksplit;
+  }
   l.k_blocks = sc.k_limit ? (*reinterpret_cast<const volatile int32_t*>(sc.k_limit) + kBK - 1) / kBK : 0x7fffffff;
   return l;
 }
 
-__device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u, int rows_per_tile = kBM,
-                                            uint32_t rank = 0, Limits lim = Limits{0x7fffffff, 0x7fffffff}) {
+__device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u, int rows_per_tile, uint32_t rank,
+                                            const Limits& lim) {
   const int per_m = sc.n_units * sc.ksplit;
   const int per_group = sc.group_m * per_m;
   const int g = u / per_group;
   const int r = u - g * per_group;
   const int m0 = g * sc.group_m;
-  const int gm = min(sc.group_m, sc.m_tiles - m0);
+  const int gm = min(sc.group_m, lim.m_tiles - m0);
   const int m_local = r % gm;
   const int rest = r / gm;
   Unit t;
@@ -635,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot;
-  const Limits lim = read_limits(sc);
+  const Limits lim = read_limits(sc, kBM);
 
   if (warp == kTmaWarp) {
     // ---------------------------------------------------------------- producer
@@ -648,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued[s] = false;
         issued_phase[s] = 0;
       }
-      for (int uu = blockIdx.x; uu < sc.total_units; uu += gridDim.x) {
+      for (int uu = blockIdx.x; uu < lim.total_units; uu += gridDim.x) {
         const Unit u = decode_unit(sc, uu, kBM, 0, lim);
         if (u.skip) continue;
         bool ok = true;
@@ -702,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = instr_desc_bf16(kBM, kBN, sc.a_mn, sc.b_mn);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int uu = blockIdx.x; ok && uu < sc.total_units; uu += gridDim.x) {
+      for (int uu = blockIdx.x; ok && uu < lim.total_units; uu += gridDim.x) {
         const Unit u = decode_unit(sc, uu, kBM, 0, lim);
         if (u.skip) continue;
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
@@ -756,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc = 0, acc_phase = 0;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok = true;
-    for (int uu = blockIdx.x; ok && uu < sc.total_units; uu += gridDim.x) {
+    for (int uu = blockIdx.x; ok && uu < lim.total_units; uu += gridDim.x) {
       const Unit u = decode_unit(sc, uu, kBM, 0, lim);
         if (u.skip) continue;
       typename Epi::State st;
@@ -859,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot;
-  const Limits lim = read_limits(sc);
+  const Limits lim = read_limits(sc, kPairRows);
   const int cid = blockIdx.x >> 1;
   const int ncl = gridDim.x >> 1;
   bool aborted = false;
@@ -876,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued_phase[s] = 0;
       }
       bool ok = true;
-      for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
+      for (int uu = cid; ok && uu < lim.total_units; uu += ncl) {
         const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
         if (u.skip) continue;
         const int a_row = sc.a_mn_off + static_cast<int>(u.row0);
@@ -933,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = instr_desc_bf16(kPairRows, kBN, sc.a_mn, sc.b_mn);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
+      for (int uu = cid; ok && uu < lim.total_units; uu += ncl) {
         const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
         if (u.skip) continue;
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
@@ -987,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc = 0, acc_phase = 0;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok = true;
-    for (int uu = cid; ok && uu < sc.total_units; uu += ncl) {
+    for (int uu = cid; ok && uu < lim.total_units; uu += ncl) {
       const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
         if (u.skip) continue;
       typename Epi::State st;

@@ -71,6 +71,6 @@ cudaError_t launch_dh_finalize(const float* part, int64_t stride, int ksplit, in
                                int out_f32, const int32_t* row_map, const int32_t* row_count, int grid,
                                cudaStream_t stream);
 // Valid-token compaction: count, scan, gather (see CompactParams).
-cudaError_t launch_compact(const CompactParams& p, int* status, cudaStream_t stream);
+cudaError_t launch_compact(const CompactParams& p, int* status, int num_sms, cudaStream_t stream);
 
 }  // namespace flce

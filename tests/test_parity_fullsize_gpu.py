@@ -20,12 +20,14 @@ from tests.parity import (TOL_ENT, TOL_GRAD, TOL_LOSS, TOL_LSE, near_tie_bounds_
 pytestmark = [pytest.mark.gpu, pytest.mark.fullsize]
 
 
-@pytest.mark.parametrize("name", ["tiny", "chunk", "commandr", "gemma", "qwen8b"])
-def test_parity_full_size(name):
+@pytest.mark.parametrize("name,compact", [("tiny", False), ("chunk", False), ("commandr", False), ("gemma", False),
+                                          ("qwen8b", False), ("commandr", True)],
+                         ids=["tiny", "chunk", "commandr", "gemma", "qwen8b", "commandr-compact"])
+def test_parity_full_size(name, compact):
     w = WORKLOADS[name]
     h, W, b, t, dloss = make_inputs(w, "cuda")
     kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
-    gpu = run_gpu(h, W, b, t, dloss, **kw)
+    gpu = run_gpu(h, W, b, t, dloss, compact=compact, **kw)
     assert gpu["status"] == 0
     f = gpu["fwd"]
     dh, dW, db = gpu["bwd"]
@@ -44,8 +46,11 @@ def test_parity_full_size(name):
     torch.cuda.empty_cache()
 
     ref = oracle_forward_rowblocks(hc, Wc, bc, tc, **kw)
-    np.testing.assert_allclose(lse_g, ref["lse"], atol=TOL_LSE, rtol=0)
-    np.testing.assert_allclose(ent_g, ref["entropy"], atol=TOL_ENT, rtol=0)
+    v = ref["valid"] if compact else np.ones_like(ref["valid"])
+    np.testing.assert_allclose(lse_g[v], ref["lse"][v], atol=TOL_LSE, rtol=0)
+    np.testing.assert_allclose(ent_g[v], ref["entropy"][v], atol=TOL_ENT, rtol=0)
+    if compact:  # ignored tokens are not computed: lse = entropy = 0
+        assert np.all(lse_g[~v] == 0.0) and np.all(ent_g[~v] == 0.0)
     nv = ref["n_valid"]
     assert int(f.n_valid) == nv
     if w.reduction == "none":
