@@ -50,6 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = automatic)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling captures of a small case)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures of a small case)")
+    ap.add_argument("--fused", action="store_true", help="one flce_forward_backward call per step")
     ap.add_argument("--compact", action="store_true",
                     help="gather the valid tokens first (FLCE_FLAG_COMPACT_VALID)")
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 1, 2],
@@ -234,7 +235,7 @@ def reference_arm(args):
 class Runner:
     """Preallocated buffers and raw C-ABI calls for one forward + backward step."""
 
-    def __init__(self, w, device, seed_offset=0, compact=False):
+    def __init__(self, w, device, seed_offset=0, compact=False, fused=False):
         import torch
 
         import linear_cross_entropy_tmem_gb300.api as api
@@ -260,6 +261,9 @@ class Runner:
         self.db = torch.empty_like(self.b) if self.b is not None else None
         self.ws_f = torch.empty(api.flce_workspace_size(self.prob, False), dtype=torch.uint8, device=device)
         self.ws_b = torch.empty(api.flce_workspace_size(self.prob, True), dtype=torch.uint8, device=device)
+        self.fused = fused
+        self.ws_fb = torch.empty(api.flce_workspace_size(self.prob, 2) if fused else 256, dtype=torch.uint8,
+                                 device=device)
         self.stream = torch.cuda.current_stream(device)
         p = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
         s = ctypes.c_void_p(self.stream.cuda_stream)
@@ -270,7 +274,14 @@ class Runner:
                          p(self.n_valid), p(self.dloss), p(self.dh), p(self.dW), p(self.db), p(self.ws_b),
                          self.ws_b.numel(), s)
 
+        self.fb_args = (ctypes.byref(self.prob), p(self.h), p(self.W), p(self.b), p(self.t), p(self.dloss),
+                        p(self.loss), p(self.lse), None, p(self.correct), p(self.n_valid), p(self.ent_sum),
+                        p(self.dh), p(self.dW), p(self.db), p(self.ws_fb), self.ws_fb.numel(), s)
+
     def step(self):
+        if self.fused:
+            self.B.check(self.lib.flce_forward_backward(*self.fb_args), "flce_forward_backward")
+            return
         self.B.check(self.lib.flce_forward(*self.fwd_args), "flce_forward")
         self.B.check(self.lib.flce_backward(*self.bwd_args), "flce_backward")
 
@@ -327,7 +338,7 @@ def flce_arm(args):
     device = torch.device("cuda", local)
     dist = init_dist("nccl")
     w = pick_workload(args)
-    run = Runner(w, device, seed_offset=rank, compact=args.compact)
+    run = Runner(w, device, seed_offset=rank, compact=args.compact, fused=args.fused)
     lib = run.lib
     B.check(lib.flce_testing_set_gemm_mode(args.gemm_mode), "gemm mode")
 
@@ -440,6 +451,7 @@ def flce_arm(args):
                        "reduction": w.reduction, "parallelism": f"replicas x{world}" if world > 1 else "none",
                        "gemm_mode": ["auto", "single-cta", "cta-pair"][args.gemm_mode],
                        "compact_valid_tokens": bool(args.compact),
+                       "entry": "flce_forward_backward" if args.fused else "flce_forward + flce_backward",
                        "l2": "inputs larger than L2 (1.25 GB head), no flush"},
             "tflops": tflops,
             "pct_of_peak": {"of_burst": tflops / peak_burst, "of_sustained": tflops / peak, "source": peak_src},

@@ -134,8 +134,9 @@ typedef struct {
 } flce_problem;
 
 /*
- * Bytes of device workspace flce_forward (for_backward = 0) or flce_backward
- * (for_backward = 1) needs for `problem`, written to *bytes.  The size grows
+ * Bytes of device workspace flce_forward (for_backward = 0), flce_backward
+ * (for_backward = 1) or flce_forward_backward (for_backward = 2) needs for
+ * `problem`, written to *bytes.  The size grows
  * with N * (number of vocabulary splits) for the forward and with
  * N * (vocabulary chunk) + N * D for the backward; it never grows with N * V.
  * The size is an upper bound that does not depend on the device, so the call
@@ -187,6 +188,24 @@ FLCE_API int flce_backward(const flce_problem* problem, const void* hidden, cons
                   const void* bias, const int64_t* targets, const float* lse,
                   const int64_t* n_valid, const float* dloss, void* dhidden, void* dweight,
                   void* dbias, void* workspace, size_t workspace_bytes, flce_stream_t stream);
+
+/*
+ * Forward and backward in one call, for callers that know the upstream
+ * gradient before the forward runs (a training step whose loss is used as is).
+ * Same arguments and results as flce_forward followed by flce_backward with
+ * `lse` and `n_valid` passed from one to the other, bit for bit; the two halves
+ * share argument checks, planning, the fp32 hidden split and the valid-token
+ * compaction, and their scratch shares one workspace of
+ * flce_workspace_size(problem, 2) bytes.
+ *   dloss    fp32 upstream gradient, [1] (mean / sum) or [N] (none), on the
+ *            device before the call's work reaches the backward
+ *   lse, n_valid: outputs of the forward half, read by the backward half
+ */
+FLCE_API int flce_forward_backward(const flce_problem* problem, const void* hidden, const void* weight,
+                                   const void* bias, const int64_t* targets, const float* dloss, float* loss,
+                                   float* lse, float* entropy, int64_t* correct, int64_t* n_valid,
+                                   float* entropy_sum, void* dhidden, void* dweight, void* dbias, void* workspace,
+                                   size_t workspace_bytes, flce_stream_t stream);
 
 /*
  * Synchronises `stream`, then copies the device status word at the start of

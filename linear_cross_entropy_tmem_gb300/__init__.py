@@ -5,6 +5,6 @@ an optional bias, logit scale and soft cap), forward and backward, without
 materialising the (tokens x vocab) logits.  See ``include/flce.h``.
 """
 from .api import (  # noqa: F401
-    ForwardResult, LinearCrossEntropy, flce_backward, flce_forward, flce_read_device_status,
+    ForwardResult, LinearCrossEntropy, flce_backward, flce_forward, flce_forward_backward, flce_read_device_status,
     flce_status_string, flce_workspace_size, linear_cross_entropy, make_problem,
 )

@@ -45,9 +45,10 @@ def make_problem(n_tokens: int, hidden: int, vocab: int, *, hidden_dtype=torch.b
         reserved=0)
 
 
-def flce_workspace_size(problem: B.FlceProblem, for_backward: bool) -> int:
+def flce_workspace_size(problem: B.FlceProblem, for_backward) -> int:
+    """Bytes for flce_forward (0 / False), flce_backward (1 / True) or flce_forward_backward (2)."""
     out = ctypes.c_size_t(0)
-    B.check(B.load().flce_workspace_size(ctypes.byref(problem), int(bool(for_backward)), ctypes.byref(out)),
+    B.check(B.load().flce_workspace_size(ctypes.byref(problem), int(for_backward), ctypes.byref(out)),
             "flce_workspace_size")
     return int(out.value)
 
@@ -146,6 +147,48 @@ def flce_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Ten
                                 ws.numel(), _stream(dev))
     B.check(st, "flce_backward")
     return dh, dW, db
+
+
+def flce_forward_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, dloss: torch.Tensor,
+                          bias: Optional[torch.Tensor] = None, *, logit_scale: float = 1.0, softcap: float = 0.0,
+                          ignore_index: int = -100, reduction: str = "mean", entropy: bool = False,
+                          num_items_in_batch: float = 0.0, compact: bool = False,
+                          workspace: Optional[torch.Tensor] = None):
+    """Forward and backward in one call (see ``flce_forward_backward`` in include/flce.h).
+
+    Returns ``(ForwardResult, (dhidden, dweight, dbias))``."""
+    _require_cuda(hidden, weight, targets, dloss, bias)
+    for t, n in ((hidden, "hidden"), (weight, "weight"), (targets, "targets"), (bias, "bias")):
+        _contig(t, n)
+    if targets.dtype != torch.int64:
+        raise TypeError("flce: targets must be int64")
+    N, D = hidden.shape
+    V = weight.shape[0]
+    prob = make_problem(N, D, V, hidden_dtype=hidden.dtype, weight_dtype=weight.dtype,
+                        bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
+                        logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
+                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact)
+    dev = hidden.device
+    ws = _workspace(flce_workspace_size(prob, 2), dev, workspace)
+    f32 = dict(dtype=torch.float32, device=dev)
+    loss = torch.empty(N if reduction == "none" else 1, **f32)
+    lse = torch.empty(N, **f32)
+    ent = torch.empty(N, **f32) if entropy else None
+    correct = torch.empty(1, dtype=torch.int64, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    ent_sum = torch.empty(1, **f32)
+    dloss = dloss.to(dtype=torch.float32).contiguous().reshape(-1)
+    dh = torch.empty_like(hidden)
+    dW = torch.empty_like(weight)
+    db = torch.empty_like(bias) if bias is not None else None
+    st = B.load().flce_forward_backward(ctypes.byref(prob), _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets),
+                                        _ptr(dloss), _ptr(loss), _ptr(lse), _ptr(ent), _ptr(correct),
+                                        _ptr(n_valid), _ptr(ent_sum), _ptr(dh), _ptr(dW), _ptr(db), _ptr(ws),
+                                        ws.numel(), _stream(dev))
+    B.check(st, "flce_forward_backward")
+    if reduction != "none":
+        loss = loss.view(())
+    return (ForwardResult(loss, lse, correct.view(()), n_valid.view(()), ent_sum.view(()), ent, ws), (dh, dW, db))
 
 
 def flce_read_device_status(workspace: torch.Tensor) -> int:

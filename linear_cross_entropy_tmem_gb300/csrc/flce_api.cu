@@ -159,7 +159,12 @@ int dh_ksplit_bound(int64_t n_tokens, int64_t hidden, int64_t vc) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxKSplit, kb / 8)));
 }
 
-Layout make_layout(const flce_problem* p, bool backward, bool has_bias) {
+enum LayoutKind { kForward = 0, kBackward = 1, kFused = 2 };
+
+// [status][hi, lo][compaction][forward region | backward region]; in the fused
+// call the forward and backward regions overlap (the forward's scratch is dead
+// before the backward starts, in stream order).
+Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
   Layout L;
   const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
   size_t off = 256;  // status word + padding
@@ -180,12 +185,14 @@ Layout make_layout(const flce_problem* p, bool backward, bool has_bias) {
     L.c_map = take(size_t(N) * 4);
     L.c_targets = take(size_t(N) * 8);
     if (p->hidden_dtype != FLCE_F32) L.c_hidden = take(size_t(N) * D * 2);  // fp32 input compacts into hi / lo
-    if (backward) {
+    if (kind != kForward) {
       L.c_lse = take(size_t(N) * 4);
       L.c_dloss = take(size_t(N) * 4);
     }
   }
-  if (!backward) {
+  const size_t region = off;
+  size_t end = off;
+  if (kind != kBackward) {
     const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN));
     const size_t part = size_t(splits) * N * 4;
     L.part_m = take(part);
@@ -195,7 +202,10 @@ Layout make_layout(const flce_problem* p, bool backward, bool has_bias) {
     L.part_idx = take(part);
     L.z_target = take(size_t(N) * 4);
     L.blocks = take(size_t(cdiv(N, kMergeThreads)) * sizeof(BlockPartial));
-  } else {
+    end = std::max(end, off);
+  }
+  if (kind != kForward) {
+    off = region;
     L.vc = chunk_width(N, V);
     L.n_chunks = cdiv(V, L.vc);
     L.ksplit_max = dh_ksplit_bound(N, D, L.vc);
@@ -203,8 +213,9 @@ Layout make_layout(const flce_problem* p, bool backward, bool has_bias) {
     if (has_bias) L.dbias_part = take(size_t(cdiv(N, kBM)) * L.vc * 4);
     L.need_dh_part = L.n_chunks > 1 || L.ksplit_max > 1;
     if (L.need_dh_part) L.dh_part = take(size_t(L.ksplit_max) * N * D * 4);
+    end = std::max(end, off);
   }
-  L.total = off;
+  L.total = end;
   return L;
 }
 
@@ -313,7 +324,8 @@ int flce_workspace_size(const flce_problem* problem, int for_backward, size_t* b
   if (!bytes) return FLCE_ERR_INVALID_ARG;
   FLCE_TRY(validate(problem));
   // The bias-dependent part is included whenever a bias could be passed.
-  *bytes = make_layout(problem, for_backward != 0, true).total;
+  if (for_backward < 0 || for_backward > 2) return FLCE_ERR_INVALID_ARG;
+  *bytes = make_layout(problem, for_backward, true).total;
   return FLCE_OK;
 }
 
@@ -327,91 +339,113 @@ int flce_read_device_status(const void* workspace, flce_stream_t stream, int* st
   return FLCE_OK;
 }
 
-int flce_forward(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
-                 const int64_t* targets, float* loss, float* lse, float* entropy, int64_t* correct,
-                 int64_t* n_valid, float* entropy_sum, void* workspace, size_t workspace_bytes,
-                 flce_stream_t stream) {
-  FLCE_TRY(validate(p));
-  FLCE_TRY(check_bias_dtype(p, bias));
-  const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
-  if (!weight || !loss || !correct || !n_valid || !entropy_sum || !workspace) return FLCE_ERR_INVALID_ARG;
-  if (N > 0 && (!hidden || !targets || !lse)) return FLCE_ERR_INVALID_ARG;
-  if (!aligned(weight, 16) || (N > 0 && !aligned(hidden, 16)) || !aligned(workspace, 256) ||
-      (targets && !aligned(targets, 8)))
-    return FLCE_ERR_MISALIGNED;
-  const Layout L = make_layout(p, false, true);
-  if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  DeviceInfo dev;
-  FLCE_TRY(get_device(&dev));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int* status = reinterpret_cast<int*>(ws + L.status);
-  FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
+}  // extern "C"
 
-  BlockPartial* blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
+namespace flce {
+namespace {
+
+// Inputs of the products after the shared preparation: the bf16 view of the
+// hidden states the GEMMs read, and (under compaction) the row count, row map
+// and compacted per-token arrays.
+struct Prep {
+  bool h32 = false, cmp = false;
+  const void* a_main = nullptr;
+  uint16_t* lo = nullptr;
+  const int32_t* row_count = nullptr;
+  const int32_t* row_map = nullptr;
+  const int64_t* tgt = nullptr;
+  float* c_lse = nullptr;
+  const float* c_dloss = nullptr;
+};
+
+int prepare(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
+            cudaStream_t st, const void* hidden, const int64_t* targets, const float* lse_in, const float* dloss,
+            float* lse_def, float* ent_def, float* loss_def, Prep* out) {
+  const int64_t N = p->n_tokens, D = p->hidden;
+  Prep r;
+  r.h32 = p->hidden_dtype == FLCE_F32;
+  r.cmp = compact(p);
+  r.tgt = targets;
+  r.a_main = hidden;
+  uint16_t* hi = r.h32 ? reinterpret_cast<uint16_t*>(ws + L.hi) : nullptr;
+  r.lo = r.h32 ? reinterpret_cast<uint16_t*>(ws + L.lo) : nullptr;
+  const bool none = p->reduction == FLCE_RED_NONE;
+  if (r.cmp) {
+    CompactParams cp{};
+    cp.n_tokens = N;
+    cp.hidden = D;
+    cp.vocab = p->vocab;
+    cp.ignore_index = p->ignore_index;
+    cp.targets = targets;
+    cp.hidden_in = hidden;
+    cp.hidden_f32 = r.h32;
+    cp.block_counts = reinterpret_cast<int32_t*>(ws + L.c_blocks);
+    cp.block_offsets = reinterpret_cast<int32_t*>(ws + L.c_offsets);
+    cp.count = reinterpret_cast<int32_t*>(ws + L.c_count);
+    cp.row_map = reinterpret_cast<int32_t*>(ws + L.c_map);
+    cp.targets_out = reinterpret_cast<int64_t*>(ws + L.c_targets);
+    cp.hc = r.h32 ? hi : reinterpret_cast<uint16_t*>(ws + L.c_hidden);
+    cp.lo = r.lo;
+    if (L.c_lse) {
+      cp.lse_in = lse_in;
+      cp.lse_out = reinterpret_cast<float*>(ws + L.c_lse);
+      r.c_lse = cp.lse_out;
+    }
+    if (L.c_dloss && none && dloss) {
+      cp.dloss_in = dloss;
+      cp.dloss_out = reinterpret_cast<float*>(ws + L.c_dloss);
+      r.c_dloss = cp.dloss_out;
+    }
+    cp.lse_default = lse_def;
+    cp.entropy_default = ent_def;
+    cp.loss_default = loss_def;
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, dev.num_sms, st); }));
+    r.row_count = cp.count;
+    r.row_map = cp.row_map;
+    r.tgt = cp.targets_out;
+    r.a_main = cp.hc;
+  } else if (r.h32) {
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+      return launch_split_hidden(static_cast<const float*>(hidden), hi, r.lo, N * D, dev.num_sms * 4, st);
+    }));
+    r.a_main = hi;
+  }
+  *out = r;
+  return FLCE_OK;
+}
+
+ReduceParams reduce_params(const flce_problem* p, const Layout& L, uint8_t* ws, float* loss, int64_t* correct,
+                           int64_t* n_valid, float* entropy_sum) {
   ReduceParams rp{};
-  rp.blocks = blocks;
-  rp.n_blocks = static_cast<int32_t>(cdiv(N, kMergeThreads));
+  rp.blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
+  rp.n_blocks = static_cast<int32_t>(cdiv(p->n_tokens, kMergeThreads));
   rp.reduction = p->reduction;
   rp.num_items = p->num_items_in_batch;
   rp.loss = loss;
   rp.correct = correct;
   rp.n_valid = n_valid;
   rp.entropy_sum = entropy_sum;
-  if (N == 0) return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
+  return rp;
+}
 
-  const bool h32 = p->hidden_dtype == FLCE_F32;
-  const bool cmp = compact(p);
-  const int32_t* row_count = nullptr;
-  const int32_t* row_map = nullptr;
-  const int64_t* tgt = targets;
-  const void* a_main = hidden;
-  uint16_t* hi = h32 ? reinterpret_cast<uint16_t*>(ws + L.hi) : nullptr;
-  uint16_t* lo = h32 ? reinterpret_cast<uint16_t*>(ws + L.lo) : nullptr;
-  if (cmp) {
-    CompactParams cp{};
-    cp.n_tokens = N;
-    cp.hidden = D;
-    cp.vocab = V;
-    cp.ignore_index = p->ignore_index;
-    cp.targets = targets;
-    cp.hidden_in = hidden;
-    cp.hidden_f32 = h32;
-    cp.block_counts = reinterpret_cast<int32_t*>(ws + L.c_blocks);
-    cp.block_offsets = reinterpret_cast<int32_t*>(ws + L.c_offsets);
-    cp.count = reinterpret_cast<int32_t*>(ws + L.c_count);
-    cp.row_map = reinterpret_cast<int32_t*>(ws + L.c_map);
-    cp.targets_out = reinterpret_cast<int64_t*>(ws + L.c_targets);
-    cp.hc = h32 ? hi : reinterpret_cast<uint16_t*>(ws + L.c_hidden);
-    cp.lo = lo;
-    cp.lse_default = lse;
-    cp.entropy_default = entropy;
-    cp.loss_default = p->reduction == FLCE_RED_NONE ? loss : nullptr;
-    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, dev.num_sms, st); }));
-    row_count = cp.count;
-    row_map = cp.row_map;
-    tgt = cp.targets_out;
-    a_main = cp.hc;
-  } else if (h32) {
-    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-      return launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st);
-    }));
-    a_main = hi;
-  }
+int run_forward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
+                cudaStream_t st, const void* weight, const void* bias, const Prep& pr, float* loss, float* lse,
+                float* entropy, int64_t* correct, int64_t* n_valid, float* entropy_sum, float* lse_compact) {
+  const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
   const bool pair = use_pair(N, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
   TmaMaps maps;
-  FLCE_TRY(make_map(&maps.a0, a_main, D, N, D * 2, kBK, kBM));
+  FLCE_TRY(make_map(&maps.a0, pr.a_main, D, N, D * 2, kBK, kBM));
   maps.a1 = maps.a0;
-  if (h32) FLCE_TRY(make_map(&maps.a1, lo, D, N, D * 2, kBK, kBM));
+  if (pr.h32) FLCE_TRY(make_map(&maps.a1, pr.lo, D, N, D * 2, kBK, kBM));
   FLCE_TRY(make_map(&maps.b0, weight, D, V, D * 2, kBK, pair ? kBN / 2 : kBN));
   maps.b1 = maps.b0;
 
-  GemmSched sc = base_sched(N, V, D, h32 ? 2 : 1, 1, pair);
+  GemmSched sc = base_sched(N, V, D, pr.h32 ? 2 : 1, 1, pair);
   int per_unit = 1;
   const int splits = choose_splits(sc.m_tiles, sc.n_tiles, pair ? dev.num_sms / 2 : dev.num_sms, &per_unit);
   sc.n_per_unit = per_unit;
   sc.group_m = pair ? 16 : 32;
-  sc.m_limit = row_count;
+  sc.m_limit = pr.row_count;
   finish_sched(sc);
 
   const bool softcap = p->final_logit_softcapping > 0.f;
@@ -426,7 +460,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   fp.softcap = softcap ? p->final_logit_softcapping : 0.f;
   fp.inv_softcap = softcap ? 1.f / p->final_logit_softcapping : 0.f;
   fp.ignore_index = p->ignore_index;
-  fp.targets = tgt;
+  fp.targets = pr.tgt;
   fp.part_m = reinterpret_cast<float*>(ws + L.part_m);
   fp.part_s = reinterpret_cast<float*>(ws + L.part_s);
   fp.part_a = reinterpret_cast<float*>(ws + L.part_a);
@@ -448,90 +482,27 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   mp.part_best = fp.part_best;
   mp.part_idx = fp.part_idx;
   mp.z_target = fp.z_target;
-  mp.targets = tgt;
+  mp.targets = pr.tgt;
   mp.lse = lse;
   mp.entropy = entropy;
   mp.loss_tok = p->reduction == FLCE_RED_NONE ? loss : nullptr;
-  mp.blocks = blocks;
-  mp.row_map = row_map;
-  mp.row_count = row_count;
+  mp.blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
+  mp.row_map = pr.row_map;
+  mp.row_count = pr.row_count;
+  mp.lse_compact = lse_compact;
   FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_merge(mp, status, st); }));
+  const ReduceParams rp = reduce_params(p, L, ws, loss, correct, n_valid, entropy_sum);
   return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
 }
 
-int flce_backward(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
-                  const int64_t* targets, const float* lse, const int64_t* n_valid, const float* dloss,
-                  void* dhidden, void* dweight, void* dbias, void* workspace, size_t workspace_bytes,
-                  flce_stream_t stream) {
-  FLCE_TRY(validate(p));
-  FLCE_TRY(check_bias_dtype(p, bias));
+int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
+                 cudaStream_t st, const void* weight, const void* bias, const Prep& pr, const float* lse_use,
+                 const int64_t* n_valid, const float* dloss_use, void* dhidden, void* dweight, void* dbias) {
   const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
-  if (!weight || !dweight || !workspace || !n_valid || !dloss) return FLCE_ERR_INVALID_ARG;
-  if ((bias == nullptr) != (dbias == nullptr)) return FLCE_ERR_INVALID_ARG;
-  if (N > 0 && (!hidden || !targets || !lse || !dhidden)) return FLCE_ERR_INVALID_ARG;
-  if (!aligned(weight, 16) || !aligned(dweight, 16) || !aligned(workspace, 256) ||
-      (N > 0 && (!aligned(hidden, 16) || !aligned(dhidden, 16))) || (targets && !aligned(targets, 8)))
-    return FLCE_ERR_MISALIGNED;
-  const Layout L = make_layout(p, true, true);
-  if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  DeviceInfo dev;
-  FLCE_TRY(get_device(&dev));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int* status = reinterpret_cast<int*>(ws + L.status);
-  FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  const bool h32 = pr.h32;
   const size_t bias_elem = p->bias_dtype == FLCE_F32 ? 4 : 2;
-  if (N == 0) {
-    FLCE_TRY(fail(cudaMemsetAsync(dweight, 0, size_t(V) * D * 2, st)));
-    if (dbias) FLCE_TRY(fail(cudaMemsetAsync(dbias, 0, size_t(V) * bias_elem, st)));
-    return FLCE_OK;
-  }
-
-  const bool h32 = p->hidden_dtype == FLCE_F32;
-  const bool cmp = compact(p);
-  const bool none = p->reduction == FLCE_RED_NONE;
-  const int32_t* row_count = nullptr;
-  const int32_t* row_map = nullptr;
-  const int64_t* tgt = targets;
-  const float* lse_use = lse;
-  const float* dloss_use = dloss;
-  const void* h_main = hidden;
-  uint16_t* hi = h32 ? reinterpret_cast<uint16_t*>(ws + L.hi) : nullptr;
-  uint16_t* lo = h32 ? reinterpret_cast<uint16_t*>(ws + L.lo) : nullptr;
-  if (cmp) {
-    CompactParams cp{};
-    cp.n_tokens = N;
-    cp.hidden = D;
-    cp.vocab = V;
-    cp.ignore_index = p->ignore_index;
-    cp.targets = targets;
-    cp.hidden_in = hidden;
-    cp.hidden_f32 = h32;
-    cp.block_counts = reinterpret_cast<int32_t*>(ws + L.c_blocks);
-    cp.block_offsets = reinterpret_cast<int32_t*>(ws + L.c_offsets);
-    cp.count = reinterpret_cast<int32_t*>(ws + L.c_count);
-    cp.row_map = reinterpret_cast<int32_t*>(ws + L.c_map);
-    cp.targets_out = reinterpret_cast<int64_t*>(ws + L.c_targets);
-    cp.hc = h32 ? hi : reinterpret_cast<uint16_t*>(ws + L.c_hidden);
-    cp.lo = lo;
-    cp.lse_in = lse;
-    cp.lse_out = reinterpret_cast<float*>(ws + L.c_lse);
-    cp.dloss_in = none ? dloss : nullptr;
-    cp.dloss_out = none ? reinterpret_cast<float*>(ws + L.c_dloss) : nullptr;
-    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_compact(cp, status, dev.num_sms, st); }));
-    row_count = cp.count;
-    row_map = cp.row_map;
-    tgt = cp.targets_out;
-    lse_use = cp.lse_out;
-    if (none) dloss_use = cp.dloss_out;
-    h_main = cp.hc;
-    // ignored tokens get a zero dhidden row; the valid ones are written below
+  if (pr.cmp) {  // ignored tokens get a zero dhidden row; the valid ones are written below
     FLCE_TRY(fail(cudaMemsetAsync(dhidden, 0, size_t(N) * D * (h32 ? 4 : 2), st)));
-  } else if (h32) {
-    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-      return launch_split_hidden(static_cast<const float*>(hidden), hi, lo, N * D, dev.num_sms * 4, st);
-    }));
-    h_main = hi;
   }
   const bool softcap = p->final_logit_softcapping > 0.f;
   uint16_t* g = reinterpret_cast<uint16_t*>(ws + L.g);
@@ -541,15 +512,15 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   // Maps that do not change across chunks.
   const bool pair_rec = use_pair(N, cdiv(L.vc, kBN), dev.num_sms);
   TmaMaps rec;  // recompute: A = h (K-major), B = W (K-major)
-  FLCE_TRY(make_map(&rec.a0, h_main, D, N, D * 2, kBK, kBM));
+  FLCE_TRY(make_map(&rec.a0, pr.a_main, D, N, D * 2, kBK, kBM));
   rec.a1 = rec.a0;
-  if (h32) FLCE_TRY(make_map(&rec.a1, lo, D, N, D * 2, kBK, kBM));
+  if (h32) FLCE_TRY(make_map(&rec.a1, pr.lo, D, N, D * 2, kBK, kBM));
   FLCE_TRY(make_map(&rec.b0, weight, D, V, D * 2, kBK, pair_rec ? kBN / 2 : kBN));
   rec.b1 = rec.b0;
   CUtensorMap h_mn, lo_mn, w_mn;  // MN-major views: h for dW, W for dh
-  FLCE_TRY(make_map(&h_mn, h_main, D, N, D * 2, 64, kBK));
+  FLCE_TRY(make_map(&h_mn, pr.a_main, D, N, D * 2, 64, kBK));
   lo_mn = h_mn;
-  if (h32) FLCE_TRY(make_map(&lo_mn, lo, D, N, D * 2, 64, kBK));
+  if (h32) FLCE_TRY(make_map(&lo_mn, pr.lo, D, N, D * 2, 64, kBK));
   FLCE_TRY(make_map(&w_mn, weight, D, V, D * 2, 64, kBK));
 
   // dh: CTA pairs or single CTAs, and the K split for this device (bounded by
@@ -573,7 +544,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     GemmSched s1 = base_sched(N, width, D, h32 ? 2 : 1, 1, pair_rec);
     s1.b_mn_off = static_cast<int32_t>(v0);
     s1.group_m = pair_rec ? 16 : 32;
-    s1.m_limit = row_count;
+    s1.m_limit = pr.row_count;
     finish_sched(s1);
     GradParams gp{};
     gp.n_tokens = N;
@@ -587,7 +558,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     gp.softcap = softcap ? p->final_logit_softcapping : 0.f;
     gp.inv_softcap = softcap ? 1.f / p->final_logit_softcapping : 0.f;
     gp.ignore_index = p->ignore_index;
-    gp.targets = tgt;
+    gp.targets = pr.tgt;
     gp.lse = lse_use;
     gp.dloss = dloss_use;
     gp.n_valid = n_valid;
@@ -602,7 +573,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
       FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
         return launch_dbias_reduce(dbias_part, L.vc, static_cast<int>(cdiv(N, kBM)), width,
                                    static_cast<uint8_t*>(dbias) + v0 * bias_elem,
-                                   p->bias_dtype == FLCE_F32, row_count, st);
+                                   p->bias_dtype == FLCE_F32, pr.row_count, st);
       }));
     }
 
@@ -617,7 +588,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     s2.a_mn = 1;
     s2.b_mn = 1;
     s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
-    s2.k_limit = row_count;
+    s2.k_limit = pr.row_count;
     finish_sched(s2);
     StoreParams sp{};
     sp.rows = width;
@@ -640,7 +611,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     s3.ksplit = ksplit;
     s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
     s3.group_m = std::max(1, dh_ctas / std::max(1, s3.n_tiles * ksplit));
-    s3.m_limit = row_count;
+    s3.m_limit = pr.row_count;
     finish_sched(s3);
     AccumParams ap{};
     ap.rows = N;
@@ -651,18 +622,139 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
     ap.write_final = (ksplit == 1 && last) ? 1 : 0;
     ap.out = dhidden;
     ap.out_f32 = h32 ? 1 : 0;
-    ap.row_map = row_map;
-    ap.row_count = row_count;
+    ap.row_map = pr.row_map;
+    ap.row_count = pr.row_count;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_DHIDDEN, st,
                     [&] { return launch_accum_gemm(pair_dh, mh, s3, ap, status, dev.num_sms, st); }));
   }
   if (ksplit > 1) {
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-      return launch_dh_finalize(dh_part, N * D, ksplit, N, D, dhidden, h32 ? 1 : 0, row_map, row_count,
+      return launch_dh_finalize(dh_part, N * D, ksplit, N, D, dhidden, h32 ? 1 : 0, pr.row_map, pr.row_count,
                                 dev.num_sms * 4, st);
     }));
   }
   return FLCE_OK;
+}
+
+int check_forward_args(const flce_problem* p, const void* hidden, const void* weight, const int64_t* targets,
+                       const float* loss, const float* lse, const int64_t* correct, const int64_t* n_valid,
+                       const float* entropy_sum, const void* workspace) {
+  const int64_t N = p->n_tokens;
+  if (!weight || !loss || !correct || !n_valid || !entropy_sum || !workspace) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!hidden || !targets || !lse)) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(weight, 16) || (N > 0 && !aligned(hidden, 16)) || !aligned(workspace, 256) ||
+      (targets && !aligned(targets, 8)))
+    return FLCE_ERR_MISALIGNED;
+  return FLCE_OK;
+}
+
+int check_backward_args(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
+                        const int64_t* targets, const float* lse, const int64_t* n_valid, const float* dloss,
+                        const void* dhidden, const void* dweight, const void* dbias, const void* workspace) {
+  const int64_t N = p->n_tokens;
+  if (!weight || !dweight || !workspace || !n_valid || !dloss) return FLCE_ERR_INVALID_ARG;
+  if ((bias == nullptr) != (dbias == nullptr)) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!hidden || !targets || !lse || !dhidden)) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(weight, 16) || !aligned(dweight, 16) || !aligned(workspace, 256) ||
+      (N > 0 && (!aligned(hidden, 16) || !aligned(dhidden, 16))) || (targets && !aligned(targets, 8)))
+    return FLCE_ERR_MISALIGNED;
+  return FLCE_OK;
+}
+
+int zero_grads_for_empty(const flce_problem* p, void* dweight, void* dbias, cudaStream_t st) {
+  const size_t bias_elem = p->bias_dtype == FLCE_F32 ? 4 : 2;
+  FLCE_TRY(fail(cudaMemsetAsync(dweight, 0, size_t(p->vocab) * p->hidden * 2, st)));
+  if (dbias) FLCE_TRY(fail(cudaMemsetAsync(dbias, 0, size_t(p->vocab) * bias_elem, st)));
+  return FLCE_OK;
+}
+
+}  // namespace
+}  // namespace flce
+
+extern "C" {
+
+int flce_forward(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
+                 const int64_t* targets, float* loss, float* lse, float* entropy, int64_t* correct,
+                 int64_t* n_valid, float* entropy_sum, void* workspace, size_t workspace_bytes,
+                 flce_stream_t stream) {
+  FLCE_TRY(validate(p));
+  FLCE_TRY(check_bias_dtype(p, bias));
+  FLCE_TRY(check_forward_args(p, hidden, weight, targets, loss, lse, correct, n_valid, entropy_sum, workspace));
+  const Layout L = make_layout(p, kForward, true);
+  if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  FLCE_TRY(get_device(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  if (p->n_tokens == 0) {
+    const ReduceParams rp = reduce_params(p, L, ws, loss, correct, n_valid, entropy_sum);
+    return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
+  }
+  Prep pr;
+  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, targets, nullptr, nullptr, lse, entropy,
+                   p->reduction == FLCE_RED_NONE ? loss : nullptr, &pr));
+  return run_forward(p, L, dev, ws, status, st, weight, bias, pr, loss, lse, entropy, correct, n_valid, entropy_sum,
+                     nullptr);
+}
+
+int flce_backward(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
+                  const int64_t* targets, const float* lse, const int64_t* n_valid, const float* dloss,
+                  void* dhidden, void* dweight, void* dbias, void* workspace, size_t workspace_bytes,
+                  flce_stream_t stream) {
+  FLCE_TRY(validate(p));
+  FLCE_TRY(check_bias_dtype(p, bias));
+  FLCE_TRY(check_backward_args(p, hidden, weight, bias, targets, lse, n_valid, dloss, dhidden, dweight, dbias,
+                               workspace));
+  const Layout L = make_layout(p, kBackward, true);
+  if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  FLCE_TRY(get_device(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  if (p->n_tokens == 0) return zero_grads_for_empty(p, dweight, dbias, st);
+  Prep pr;
+  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, targets, lse, dloss, nullptr, nullptr, nullptr, &pr));
+  const float* lse_use = pr.cmp ? pr.c_lse : lse;
+  const float* dloss_use = pr.c_dloss ? pr.c_dloss : dloss;
+  return run_backward(p, L, dev, ws, status, st, weight, bias, pr, lse_use, n_valid, dloss_use, dhidden, dweight,
+                      dbias);
+}
+
+int flce_forward_backward(const flce_problem* p, const void* hidden, const void* weight, const void* bias,
+                          const int64_t* targets, const float* dloss, float* loss, float* lse, float* entropy,
+                          int64_t* correct, int64_t* n_valid, float* entropy_sum, void* dhidden, void* dweight,
+                          void* dbias, void* workspace, size_t workspace_bytes, flce_stream_t stream) {
+  FLCE_TRY(validate(p));
+  FLCE_TRY(check_bias_dtype(p, bias));
+  FLCE_TRY(check_forward_args(p, hidden, weight, targets, loss, lse, correct, n_valid, entropy_sum, workspace));
+  FLCE_TRY(check_backward_args(p, hidden, weight, bias, targets, lse, n_valid, dloss, dhidden, dweight, dbias,
+                               workspace));
+  const Layout L = make_layout(p, kFused, true);
+  if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  FLCE_TRY(get_device(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  if (p->n_tokens == 0) {
+    const ReduceParams rp = reduce_params(p, L, ws, loss, correct, n_valid, entropy_sum);
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); }));
+    return zero_grads_for_empty(p, dweight, dbias, st);
+  }
+  Prep pr;
+  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, targets, nullptr, dloss, lse, entropy,
+                   p->reduction == FLCE_RED_NONE ? loss : nullptr, &pr));
+  FLCE_TRY(run_forward(p, L, dev, ws, status, st, weight, bias, pr, loss, lse, entropy, correct, n_valid,
+                       entropy_sum, pr.cmp ? pr.c_lse : nullptr));
+  const float* lse_use = pr.cmp ? pr.c_lse : lse;
+  const float* dloss_use = pr.c_dloss ? pr.c_dloss : dloss;
+  return run_backward(p, L, dev, ws, status, st, weight, bias, pr, lse_use, n_valid, dloss_use, dhidden, dweight,
+                      dbias);
 }
 
 int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit) {

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p,
     if (t != p.ignore_index && !in_range) atomicCAS(status, 0, kStatusTargetOutOfRange);
     const float loss = valid ? lse - p.z_target[row] : 0.f;
     p.lse[orow] = lse;
+    if (p.lse_compact) p.lse_compact[row] = lse;
     if (p.entropy) p.entropy[orow] = ent;
     if (p.loss_tok) p.loss_tok[orow] = loss;
     loss_d = loss;

@@ -35,6 +35,7 @@ struct MergeParams {
   BlockPartial* blocks;
   const int32_t* row_map;    // compacted row -> output row, or nullptr
   const int32_t* row_count;  // rows at or past *row_count are skipped, or nullptr
+  float* lse_compact;        // also write lse at the compacted row, or nullptr
 };
 
 struct ReduceParams {

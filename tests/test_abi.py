@@ -86,6 +86,13 @@ def test_workspace_size_needs_no_gpu_and_never_scales_with_n_times_v(lib):
             assert bw < 2 * N * V  # far below a full (tokens x vocab) bf16 buffer
     st, n = _ws(lib, _problem(n_tokens=0), 1)
     assert st == B.FLCE_OK
+    # the fused call's scratch regions overlap: it needs no more than the larger of the two plus
+    # the shared part
+    for kw in (dict(), dict(hidden_dtype=B.FLCE_F32), dict(flags=B.FLCE_FLAG_COMPACT_VALID)):
+        pr = _problem(n_tokens=4096, hidden=1024, vocab=50000, **kw)
+        fw, bw, fu = (_ws(lib, pr, k)[1] for k in (0, 1, 2))
+        assert max(fw, bw) <= fu <= fw + bw
+    assert _ws(lib, _problem(), 3)[0] == B.FLCE_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("kw,code", [

@@ -275,3 +275,37 @@ def test_compaction_is_deterministic():
     assert torch.equal(a["fwd"].lse, c["fwd"].lse) and torch.equal(a["fwd"].loss, c["fwd"].loss)
     for x, y in zip(a["bwd"], c["bwd"]):
         assert torch.equal(x, y)
+
+
+# ---------------------------------------------------------------------------
+# flce_forward_backward: one call, same results as forward then backward
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["auto", "single-cta", "cta-pair"])
+@pytest.mark.parametrize("compact", [False, True], ids=["all-tokens", "compact"])
+@pytest.mark.parametrize("name", ["ragged N300 D200 V1000 bias-bf16 s0.7 c5 sum",
+                                  "fp32-h N257 D136 V777 bias s0.0625 c30 none",
+                                  "multi-chunk ksplit3 N384 D256 V3000 bias mean"])
+def test_fused_call_equals_separate_calls(name, compact, mode):
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_tuning
+    w, tuning = CASES[name]
+    testing_set_gemm_mode(mode)
+    testing_set_tuning(*tuning)
+    h, W, b, t, dloss = [x.cuda() if x is not None else None for x in make_inputs(w, "cpu")]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction, compact=compact,
+              num_items_in_batch=500.0 if w.reduction == "mean" else 0.0)
+    sep = run_gpu(h, W, b, t, dloss, **kw)
+    fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, **kw)
+    torch.cuda.synchronize()
+    assert F.flce_read_device_status(fwd.workspace) == 0
+    for x, y in ((fwd.loss, sep["fwd"].loss), (fwd.lse, sep["fwd"].lse), (fwd.entropy, sep["fwd"].entropy),
+                 (fwd.correct, sep["fwd"].correct), (fwd.n_valid, sep["fwd"].n_valid),
+                 (fwd.entropy_sum, sep["fwd"].entropy_sum)):
+        assert torch.equal(x, y)
+    for x, y in zip(grads, sep["bwd"]):
+        assert (x is None and y is None) or torch.equal(x, y)
+    if not compact:
+        ref_f = oracle.forward(h.cpu(), W.cpu(), None if b is None else b.cpu(), t.cpu(),
+                               logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction,
+                               num_items_in_batch=kw["num_items_in_batch"])
+        compare_forward(fwd, ref_f, reduction=w.reduction)
