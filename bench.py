@@ -377,7 +377,9 @@ def flce_arm(args):
     clock = clocks.stop()
     ms = start.elapsed_time(end) / args.steps
     status = ctypes.c_int(0)
-    B.check(lib.flce_read_device_status(ctypes.c_void_p(run.ws_b.data_ptr()), None, ctypes.byref(status)), "status")
+    ws_status = run.ws_fb if run.fused else run.ws_b
+    B.check(lib.flce_read_device_status(ctypes.c_void_p(ws_status.data_ptr()), None, ctypes.byref(status)),
+            "status")
     if status.value != 0:
         raise RuntimeError(f"device status {status.value} during the timed region")
 
