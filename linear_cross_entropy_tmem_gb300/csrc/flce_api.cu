@@ -193,7 +193,7 @@ Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
   const size_t region = off;
   size_t end = off;
   if (kind != kBackward) {
-    const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN));
+    const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN)) * kEpilogueGroups;
     const size_t part = size_t(splits) * N * 4;
     L.part_m = take(part);
     L.part_s = take(part);
@@ -473,7 +473,7 @@ int run_forward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, u
   MergeParams mp{};
   mp.n_tokens = N;
   mp.vocab = V;
-  mp.n_splits = splits;
+  mp.n_splits = splits * kEpilogueGroups;  // one record per split and epilogue group
   mp.reduction = p->reduction;
   mp.ignore_index = p->ignore_index;
   mp.part_m = fp.part_m;

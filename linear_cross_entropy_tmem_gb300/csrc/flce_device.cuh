@@ -35,9 +35,10 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-// Named barrier among the epilogue warps only (barrier 0 is __syncthreads).
-__device__ __forceinline__ void epilogue_bar_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
+// Named barrier among the 128 threads of one epilogue group (ids 1 and 2;
+// barrier 0 is __syncthreads).
+__device__ __forceinline__ void epilogue_bar_sync(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kEpilogueThreads) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -128,10 +128,22 @@ __device__ __forceinline__ void load_bias_chunk(const void* bias, int bias_f32, 
 }
 
 // Runs f(r, c) over the first `nch` 32-column chunks of this warp's TMEM
-// lanes, loading chunk c+1 while chunk c is processed.  nch is warp-uniform.
-template <class F>
+// lanes.  kPipelined: chunk c+1 is loaded while chunk c is processed (for the
+// light epilogues; the heavy ones leave the registers to the math and rely on
+// the other epilogue group for overlap).  nch is warp-uniform.
+template <bool kPipelined = true, class F>
 __device__ __forceinline__ void for_each_tmem_chunk(uint32_t taddr, int nch, F&& f) {
   if (nch <= 0) return;
+  if (!kPipelined) {
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait(r);
+      f(r, c);
+    }
+    return;
+  }
   uint32_t ra[32], rb[32];
   tmem_ld32(taddr, ra);
   tmem_ld_wait(ra);
@@ -157,19 +169,23 @@ __device__ __forceinline__ int chunks_below(int64_t col0, int64_t limit) {
   return rem >= kBN ? kBN / 32 : static_cast<int>((rem + 31) / 32);
 }
 
-// All 128 epilogue threads agree on a predicate (named barrier 1, AND).
-__device__ __forceinline__ bool epilogue_all(bool ok) {
+// The 128 threads of one epilogue group agree on a predicate (named barrier
+// `id`, AND).
+__device__ __forceinline__ bool epilogue_all(bool ok, int id) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, 1, %2, q;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(ok)), "n"(kEpilogueThreads)
+      : "r"(static_cast<uint32_t>(ok)), "r"(id), "n"(kEpilogueThreads)
       : "memory");
   return r != 0;
 }
+
+// Thread index within its epilogue group (its TMEM lane, i.e. its tile row).
+__device__ __forceinline__ int epi_tid() { return static_cast<int>(threadIdx.x) & (kEpilogueThreads - 1); }
 
 __device__ __forceinline__ float max32(const float (&z)[32]) {
   float t[16];
@@ -192,10 +208,11 @@ struct EpiFwd {
     int64_t row, target;
     float m, s, a, best, zt;
     int32_t best_idx;
+    bool has_zt;  // this group processed the tile holding the target
   };
 
-  __device__ static void begin_unit(const Params& p, const Unit& u, State& st) {
-    st.row = u.row0 + threadIdx.x;
+  __device__ static void begin_unit(const Params& p, const Unit& u, State& st, int /*grp*/) {
+    st.row = u.row0 + epi_tid();
     st.target = st.row < p.n_tokens ? __ldg(p.targets + st.row) : p.ignore_index;
     st.m = -INFINITY;
     st.s = 0.f;
@@ -203,14 +220,15 @@ struct EpiFwd {
     st.best = -INFINITY;
     st.best_idx = 0;
     st.zt = 0.f;
+    st.has_zt = false;
   }
 
   __device__ static void tile(const Params& p, const Unit& /*u*/, int n_tile, uint32_t taddr, State& st,
-                              float* /*epi_smem*/) {
+                              float* /*epi_smem*/, int /*grp*/) {
     const int64_t v_tile = static_cast<int64_t>(n_tile) * kBN;
     // z = c tanh(s x / c): tanh takes t = 2 (s x / c) log2 e = x k_t
     const float k_t = p.scale * p.inv_softcap * 2.0f * kLog2e;
-    for_each_tmem_chunk(taddr, chunks_below(v_tile, p.vocab), [&](const uint32_t (&r)[32], int c) {
+    for_each_tmem_chunk<false>(taddr, chunks_below(v_tile, p.vocab), [&](const uint32_t (&r)[32], int c) {
       const int64_t vc = v_tile + c * 32;
       const bool ragged = vc + 32 > p.vocab;
       float bch[32];
@@ -257,21 +275,21 @@ struct EpiFwd {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (j == tl) st.zt = z[j];
+        st.has_zt = true;
       }
     });
   }
 
-  __device__ static void end_unit(const Params& p, const Unit& u, State& st) {
+  __device__ static void end_unit(const Params& p, const Unit& u, State& st, int grp) {
     if (st.row >= p.n_tokens) return;
-    const size_t o = static_cast<size_t>(u.n_unit) * static_cast<size_t>(p.n_tokens) + st.row;
+    const size_t rec = static_cast<size_t>(u.n_unit) * kEpilogueGroups + grp;
+    const size_t o = rec * static_cast<size_t>(p.n_tokens) + st.row;
     p.part_m[o] = st.m;
     p.part_s[o] = st.s;
     p.part_a[o] = st.a;
     p.part_best[o] = st.best;
     p.part_idx[o] = st.best_idx;
-    const int64_t v_lo = static_cast<int64_t>(u.n_first) * kBN;
-    const int64_t v_hi = min(static_cast<int64_t>(u.n_first + u.n_count) * kBN, p.vocab);
-    if (st.target >= v_lo && st.target < v_hi) p.z_target[st.row] = st.zt;
+    if (st.has_zt) p.z_target[st.row] = st.zt;
   }
 };
 
@@ -304,8 +322,8 @@ struct EpiGrad {
     float w;     // per-token weight (0 for ignored tokens and rows past N)
   };
 
-  __device__ static void begin_unit(const Params& p, const Unit& u, State& st) {
-    st.row = u.row0 + threadIdx.x;
+  __device__ static void begin_unit(const Params& p, const Unit& u, State& st, int /*grp*/) {
+    st.row = u.row0 + epi_tid();
     st.target = p.ignore_index;
     st.lse2 = 0.f;
     st.w = 0.f;
@@ -342,16 +360,16 @@ struct EpiGrad {
   }
 
   __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st,
-                              float* epi_smem) {
+                              float* epi_smem, int grp) {
     const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;  // chunk-local column
     const int64_t v_tile = p.v0 + col_tile;                       // vocabulary row
-    const int warp = threadIdx.x >> 5;
+    const int warp = (threadIdx.x >> 5) & (kEpilogueWarps - 1);
     const uint32_t lane = lane_id();
     const float wd = st.w * p.scale;
     const float k_t = p.scale * p.inv_softcap * 2.0f * kLog2e;
     const float k_p = kSoftcap ? p.softcap * kLog2e : p.scale * kLog2e;
     const int nch = chunks_below(v_tile, p.vocab);
-    for_each_tmem_chunk(taddr, nch, [&](const uint32_t (&r)[32], int c) {
+    for_each_tmem_chunk<false>(taddr, nch, [&](const uint32_t (&r)[32], int c) {
       const int64_t vc = v_tile + c * 32;
       const bool ragged = vc + 32 > p.vocab;
       float bch[32];
@@ -399,22 +417,22 @@ struct EpiGrad {
     });
     if (kBias) {
       for (int c = nch; c < kBN / 32; ++c) epi_smem[warp * kBN + c * 32 + lane] = 0.f;
-      epilogue_bar_sync();
+      epilogue_bar_sync(1 + grp);
       // A CTA-pair tile can have its second 128-row half entirely past the
       // last token: that half has no slot in the per-tile partial sums.
       if (u.row0 < p.n_tokens) {
 #pragma unroll
         for (int h = 0; h < kBN / kEpilogueThreads; ++h) {
-          const int col = threadIdx.x + h * kEpilogueThreads;
+          const int col = epi_tid() + h * kEpilogueThreads;
           const float s = epi_smem[col] + epi_smem[kBN + col] + epi_smem[2 * kBN + col] + epi_smem[3 * kBN + col];
           if (v_tile + col < p.vocab) p.dbias_part[(u.row0 / kBM) * p.ldg + col_tile + col] = s;
         }
       }
-      epilogue_bar_sync();
+      epilogue_bar_sync(1 + grp);
     }
   }
 
-  __device__ static void end_unit(const Params&, const Unit&, State&) {}
+  __device__ static void end_unit(const Params&, const Unit&, State&, int) {}
 };
 
 // ============================================================================
@@ -425,8 +443,9 @@ struct EpiStore {
   struct State {
     int64_t row;
   };
-  __device__ static void begin_unit(const Params&, const Unit& u, State& st) { st.row = u.row0 + threadIdx.x; }
-  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*) {
+  __device__ static void begin_unit(const Params&, const Unit& u, State& st, int) { st.row = u.row0 + epi_tid(); }
+  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*,
+                              int) {
     const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;
     if (u.kb_count == 0) {  // no K blocks (all tokens ignored under compaction): the product is zero
       uint32_t zero[32];
@@ -476,7 +495,7 @@ struct EpiStore {
       }
     }
   }
-  __device__ static void end_unit(const Params&, const Unit&, State&) {}
+  __device__ static void end_unit(const Params&, const Unit&, State&, int) {}
 };
 
 // ============================================================================
@@ -487,7 +506,7 @@ struct EpiAccum {
   struct State {
     int64_t row;
   };
-  __device__ static void begin_unit(const Params&, const Unit& u, State& st) { st.row = u.row0 + threadIdx.x; }
+  __device__ static void begin_unit(const Params&, const Unit& u, State& st, int) { st.row = u.row0 + epi_tid(); }
 
   __device__ static void store(const Params& p, const Unit& u, const State& st, int64_t col, float (&v)[32]) {
     if (st.row >= p.rows) return;
@@ -545,7 +564,8 @@ struct EpiAccum {
     }
   }
 
-  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*) {
+  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*,
+                              int) {
     const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;
     const int nch = chunks_below(col_tile, p.cols);
     if (u.kb_count > 0) {
@@ -565,7 +585,7 @@ struct EpiAccum {
       }
     }
   }
-  __device__ static void end_unit(const Params&, const Unit&, State&) {}
+  __device__ static void end_unit(const Params&, const Unit&, State&, int) {}
 };
 
 // ============================================================================
@@ -763,33 +783,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------------------- epilogue
-    uint32_t acc = 0, acc_phase = 0;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ---------------------------------------------------------------- epilogue (two groups)
+    const int grp = warp / kEpilogueWarps;  // owns TMEM accumulator grp: tiles grp, grp+2, ...
+    const uint32_t lane_base = static_cast<uint32_t>((warp % kEpilogueWarps) * 32) << 16;
+    float* epi = sm.epi + grp * kEpiSmemGroupFloats;
+    uint32_t seq = 0, phase = 0;
     bool ok = true;
     for (int uu = blockIdx.x; ok && uu < lim.total_units; uu += gridDim.x) {
       const Unit u = decode_unit(sc, uu, kBM, 0, lim);
         if (u.skip) continue;
       typename Epi::State st;
-      Epi::begin_unit(ep, u, st);
+      Epi::begin_unit(ep, u, st, grp);
       for (int n = u.n_first; n < u.n_first + u.n_count; ++n) {
-        const bool got = mbar_wait(&sm.tfull[acc], acc_phase, sm.ctl, status);
-        if (!epilogue_all(got)) {
+        const bool mine = static_cast<int>(seq & 1u) == grp;
+        ++seq;
+        if (!mine) continue;
+        const bool got = mbar_wait(&sm.tfull[grp], phase, sm.ctl, status);
+        if (!epilogue_all(got, 1 + grp)) {
           sm.ctl->abort = 1u;
           ok = false;
           break;
         }
         tc_fence_after();
-        Epi::tile(ep, u, n, tmem_base + lane_base + acc * kBN, st, sm.epi);
+        Epi::tile(ep, u, n, tmem_base + lane_base + grp * kBN, st, epi, grp);
         tc_fence_before();
         __syncwarp();
-        if (lane_id() == 0) mbar_arrive(&sm.tempty[acc]);
-        if (++acc == kAccBufs) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
+        if (lane_id() == 0) mbar_arrive(&sm.tempty[grp]);
+        phase ^= 1u;
       }
-      if (ok) Epi::end_unit(ep, u, st);
+      if (ok) Epi::end_unit(ep, u, st, grp);
     }
   }
 
@@ -994,33 +1016,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------------------- epilogue (both CTAs)
-    uint32_t acc = 0, acc_phase = 0;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ---------------------------------------------------------------- epilogue (both CTAs, two groups)
+    const int grp = warp / kEpilogueWarps;  // owns TMEM accumulator grp: tiles grp, grp+2, ...
+    const uint32_t lane_base = static_cast<uint32_t>((warp % kEpilogueWarps) * 32) << 16;
+    float* epi = sm.epi + grp * kEpiSmemGroupFloats;
+    uint32_t seq = 0, phase = 0;
     bool ok = true;
     for (int uu = cid; ok && uu < lim.total_units; uu += ncl) {
       const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
         if (u.skip) continue;
       typename Epi::State st;
-      Epi::begin_unit(ep, u, st);
+      Epi::begin_unit(ep, u, st, grp);
       for (int n = u.n_first; n < u.n_first + u.n_count; ++n) {
-        const bool got = mbar_wait(&sm.tfull[acc], acc_phase, sm.ctl, status);
-        if (!epilogue_all(got)) {
+        const bool mine = static_cast<int>(seq & 1u) == grp;
+        ++seq;
+        if (!mine) continue;
+        const bool got = mbar_wait(&sm.tfull[grp], phase, sm.ctl, status);
+        if (!epilogue_all(got, 1 + grp)) {
           sm.ctl->abort = 1u;
           ok = false;
           break;
         }
         tc_fence_after();
-        Epi::tile(ep, u, n, tmem_base + lane_base + acc * kBN, st, sm.epi);
+        Epi::tile(ep, u, n, tmem_base + lane_base + grp * kBN, st, epi, grp);
         tc_fence_before();
         __syncwarp();
-        if (lane_id() == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&sm.tempty[acc]), 0));
-        if (++acc == kAccBufs) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
+        if (lane_id() == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&sm.tempty[grp]), 0));
+        phase ^= 1u;
       }
-      if (ok) Epi::end_unit(ep, u, st);
+      if (ok) Epi::end_unit(ep, u, st, grp);
     }
     if (!ok) aborted = true;
   }

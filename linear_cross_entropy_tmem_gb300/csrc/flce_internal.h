@@ -27,13 +27,18 @@ constexpr int kStagesPair = 6;
 constexpr int kBHalfBytes = (kBN / 2) * kBK * 2;    // 16 KB
 constexpr int kStagePairBytes = kATileBytes + kBHalfBytes;
 
-constexpr int kEpilogueWarps = 4;                   // warps 0..3: one TMEM lane quarter each
+// Two epilogue warpgroups work in ping-pong: group g owns TMEM accumulator g
+// and processes every other tile, so each group has two mainloops' time per
+// tile.  Within a group, warp w reads TMEM lane quarter w.
+constexpr int kEpilogueGroups = kAccBufs;
+constexpr int kEpilogueWarps = 4;                   // warps per group
 constexpr int kEpilogueThreads = kEpilogueWarps * 32;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kTmaWarp = kEpilogueGroups * kEpilogueWarps;  // warp 8
+constexpr int kMmaWarp = kTmaWarp + 1;                      // warp 9
+constexpr int kThreads = (kMmaWarp + 1) * 32;               // 320
 
-constexpr int kEpiSmemBytes = kEpilogueWarps * kBN * 4;   // column-sum staging (dbias)
+constexpr int kEpiSmemGroupFloats = kEpilogueWarps * kBN;   // dbias column-sum staging per group
+constexpr int kEpiSmemBytes = kEpilogueGroups * kEpiSmemGroupFloats * 4;
 constexpr int kBarrierBytes = 256;
 constexpr int kGemmSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarrierBytes + kEpiSmemBytes;
 constexpr int kGemmPairSmemBytes =
@@ -76,7 +81,9 @@ struct GemmSched {
 
 // ---- Epilogue parameter blocks --------------------------------------------
 // Forward: online per-token statistics over each unit's vocabulary range
-// (one unit = one vocabulary split of one m tile).
+// (one unit = one vocabulary split of one m tile).  Each epilogue group keeps
+// its own statistics over the unit's tiles it processed and writes its own
+// record: record r = split * kEpilogueGroups + group.
 struct FwdParams {
   int64_t n_tokens, vocab;
   const void* bias;       // nullptr, bf16 or fp32 [V]
@@ -86,7 +93,7 @@ struct FwdParams {
   float scale, softcap, inv_softcap;
   int64_t ignore_index;
   const int64_t* targets;
-  // partials, [n_splits][n_tokens] each
+  // partials, [n_splits * kEpilogueGroups][n_tokens] each
   float* part_m;          // running max of z
   float* part_s;          // sum exp(z - m)
   float* part_a;          // sum exp(z - m) * z
