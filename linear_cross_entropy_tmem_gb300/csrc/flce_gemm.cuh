@@ -402,16 +402,14 @@ struct EpiGrad {
           if (vc + j >= p.vocab) g[j] = 0.f;
       }
       if (st.row < p.n_tokens) {
-        uint4* dst = reinterpret_cast<uint4*>(p.g + st.row * p.ldg + col_tile + c * 32);
+        uint16_t* dst = p.g + st.row * p.ldg + col_tile + c * 32;  // 64 B, 32-byte aligned
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 pk;
-          pk.x = pack_bf16x2(g[8 * q + 0], g[8 * q + 1]);
-          pk.y = pack_bf16x2(g[8 * q + 2], g[8 * q + 3]);
-          pk.z = pack_bf16x2(g[8 * q + 4], g[8 * q + 5]);
-          pk.w = pack_bf16x2(g[8 * q + 6], g[8 * q + 7]);
-          dst[q] = pk;
-        }
+        for (int q = 0; q < 2; ++q)
+          st_global_v8(dst + 16 * q, pack_bf16x2(g[16 * q + 0], g[16 * q + 1]),
+                       pack_bf16x2(g[16 * q + 2], g[16 * q + 3]), pack_bf16x2(g[16 * q + 4], g[16 * q + 5]),
+                       pack_bf16x2(g[16 * q + 6], g[16 * q + 7]), pack_bf16x2(g[16 * q + 8], g[16 * q + 9]),
+                       pack_bf16x2(g[16 * q + 10], g[16 * q + 11]), pack_bf16x2(g[16 * q + 12], g[16 * q + 13]),
+                       pack_bf16x2(g[16 * q + 14], g[16 * q + 15]));
       }
       if (kBias) epi_smem[warp * kBN + c * 32 + lane] = warp_column_sums(g);
     });
@@ -466,7 +464,12 @@ struct EpiStore {
       const int64_t n = p.cols - col;
       if (p.out_f32) {
         float* dst = reinterpret_cast<float*>(p.out) + st.row * p.ldo + col;
-        if (n >= 32) {
+        if (n >= 32 && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_global_v8(dst + 8 * q, r[8 * q], r[8 * q + 1], r[8 * q + 2], r[8 * q + 3], r[8 * q + 4], r[8 * q + 5],
+                         r[8 * q + 6], r[8 * q + 7]);
+        } else if (n >= 32) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             reinterpret_cast<uint4*>(dst)[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
@@ -477,14 +480,23 @@ struct EpiStore {
         }
       } else {
         uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + st.row * p.ldo + col;
-        if (n >= 32) {
+        const auto f = [&](int j) { return __uint_as_float(r[j]); };
+        if (n >= 32 && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            st_global_v8(dst + 16 * q, pack_bf16x2(f(16 * q + 0), f(16 * q + 1)),
+                         pack_bf16x2(f(16 * q + 2), f(16 * q + 3)), pack_bf16x2(f(16 * q + 4), f(16 * q + 5)),
+                         pack_bf16x2(f(16 * q + 6), f(16 * q + 7)), pack_bf16x2(f(16 * q + 8), f(16 * q + 9)),
+                         pack_bf16x2(f(16 * q + 10), f(16 * q + 11)), pack_bf16x2(f(16 * q + 12), f(16 * q + 13)),
+                         pack_bf16x2(f(16 * q + 14), f(16 * q + 15)));
+        } else if (n >= 32) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 pk;
-            pk.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1]));
-            pk.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3]));
-            pk.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5]));
-            pk.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7]));
+            pk.x = pack_bf16x2(f(8 * q + 0), f(8 * q + 1));
+            pk.y = pack_bf16x2(f(8 * q + 2), f(8 * q + 3));
+            pk.z = pack_bf16x2(f(8 * q + 4), f(8 * q + 5));
+            pk.w = pack_bf16x2(f(8 * q + 6), f(8 * q + 7));
             reinterpret_cast<uint4*>(dst)[q] = pk;
           }
         } else {
@@ -515,25 +527,29 @@ struct EpiAccum {
     float* slot = p.part + static_cast<int64_t>(u.ks) * p.part_stride + st.row * p.cols + col;
     const int64_t rem = p.cols - col;
     if (rem >= 32) {
+      // rows are cols * 4 bytes apart (cols % 8 == 0) and col % 32 == 0: 32-byte aligned
       if (p.accumulate) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 o = reinterpret_cast<const float4*>(slot)[q];
-          v[4 * q] += o.x;
-          v[4 * q + 1] += o.y;
-          v[4 * q + 2] += o.z;
-          v[4 * q + 3] += o.w;
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[8];
+          ld_global_v8(slot + 8 * q, o);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[8 * q + i] += __uint_as_float(o[i]);
         }
       }
-      if (!p.write_final) {
+      const auto u = [&](int j) { return __float_as_uint(v[j]); };
+      if (!p.write_final || p.out_f32) {
+        float* dst = !p.write_final ? slot : reinterpret_cast<float*>(p.out) + orow * p.cols + col;
+        if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {  // the caller's output is only 16-byte aligned
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<float4*>(slot)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      } else if (p.out_f32) {
-        float* dst = reinterpret_cast<float*>(p.out) + orow * p.cols + col;
+          for (int q = 0; q < 4; ++q)
+            st_global_v8(dst + 8 * q, u(8 * q), u(8 * q + 1), u(8 * q + 2), u(8 * q + 3), u(8 * q + 4),
+                         u(8 * q + 5), u(8 * q + 6), u(8 * q + 7));
+        } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
       } else {
         uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + orow * p.cols + col;
 #pragma unroll
