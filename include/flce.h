@@ -226,7 +226,8 @@ FLCE_API int flce_read_device_status(const void* workspace, flce_stream_t stream
  *   - Problems whose forward workspace (flce_workspace_size(problem, 0)) is
  *     larger than FLCE_NOALLOC_SCRATCH_BYTES are rejected with
  *     FLCE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  With bf16
- *     hidden states that admits about 26K tokens; fp32 hidden states need
+ *     hidden states and a vocabulary of 16K or more that admits about 13K
+ *     tokens (2.6 KB of split records per token); fp32 hidden states need
  *     4*N*D more bytes.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
