@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from linear_cross_entropy_tmem_gb300.synthetic import TINY, Workload, make_inputs
-from tests.parity import compare_backward, compare_forward, run_gpu
+from tests.parity import TOL_LSE, compare_backward, compare_forward, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -309,3 +309,67 @@ def test_fused_call_equals_separate_calls(name, compact, mode):
                                logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction,
                                num_items_in_batch=kw["num_items_in_batch"])
         compare_forward(fwd, ref_f, reduction=w.reduction)
+
+
+# ---------------------------------------------------------------------------
+# Guard regions: no kernel writes past the end of an output or the workspace
+# ---------------------------------------------------------------------------
+CANARY = 0x5A
+
+
+def _guarded(n_bytes):
+    """A device byte buffer with 4 KB of canary after the first n_bytes."""
+    return torch.full((n_bytes + 4096,), CANARY, dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["single-cta", "cta-pair"])
+@pytest.mark.parametrize("compact", [False, True], ids=["all-tokens", "compact"])
+@pytest.mark.parametrize("name", ["ragged N300 D200 V1000 bias-bf16 s0.7 c5 sum",
+                                  "fp32-h N257 D136 V777 bias s0.0625 c30 none",
+                                  "multi-chunk ksplit3 N384 D256 V3000 bias mean"])
+def test_no_writes_past_outputs_or_workspace(name, compact, mode):
+    import ctypes
+
+    import linear_cross_entropy_tmem_gb300.api as api
+    from linear_cross_entropy_tmem_gb300 import binding as B
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_tuning
+    w, tuning = CASES[name]
+    testing_set_gemm_mode(mode)
+    testing_set_tuning(*tuning)
+    h, W, b, t, dloss = [x.cuda() if x is not None else None for x in make_inputs(w, "cpu")]
+    N, D, V = w.n_tokens, w.hidden, w.vocab
+    prob = api.make_problem(N, D, V, hidden_dtype=h.dtype, bias_dtype=b.dtype if b is not None else torch.bfloat16,
+                            logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction, compact=compact)
+    f32, hb = 4, h.element_size()
+    sizes = {"loss": (N if w.reduction == "none" else 1) * f32, "lse": N * f32, "ent": N * f32, "corr": 8, "nv": 8,
+             "es": f32, "ws_f": api.flce_workspace_size(prob, 0), "ws_b": api.flce_workspace_size(prob, 1),
+             "dh": N * D * hb, "dW": V * D * 2, "db": V * b.element_size() if b is not None else 0}
+    bufs = {k: _guarded(v) for k, v in sizes.items()}
+    p = {k: ctypes.c_void_p(v.data_ptr()) for k, v in bufs.items()}
+    ptr = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    lib = B.load()
+    B.check(lib.flce_forward(ctypes.byref(prob), ptr(h), ptr(W), ptr(b), ptr(t), p["loss"], p["lse"], p["ent"],
+                             p["corr"], p["nv"], p["es"], p["ws_f"], sizes["ws_f"], s), "forward")
+    B.check(lib.flce_backward(ctypes.byref(prob), ptr(h), ptr(W), ptr(b), ptr(t), p["lse"], p["nv"], ptr(dloss),
+                              p["dh"], p["dW"], p["db"] if b is not None else None, p["ws_b"], sizes["ws_b"], s),
+            "backward")
+    torch.cuda.synchronize()
+    for k, buf in bufs.items():
+        tail = buf[sizes[k]:]
+        assert torch.all(tail == CANARY), f"write past the end of {k}"
+    # the guarded buffers hold the results the parity tests check
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    hc, Wc, bc, tc, dc = [x.cpu() if x is not None else None for x in (h, W, b, t, dloss)]
+    ref_f = oracle.forward(hc, Wc, bc, tc, **kw)
+    ref_b = oracle.backward(hc, Wc, bc, tc, dloss=dc, **kw)
+    assert int(bufs["nv"][:8].view(torch.int64).item()) == ref_f["n_valid"]
+    lse = bufs["lse"][:sizes["lse"]].view(torch.float32).cpu().double().numpy()
+    valid = ref_f["valid"]
+    assert np.abs(lse[valid] - ref_f["lse"][valid]).max() <= TOL_LSE
+    if compact:  # compaction leaves ignored rows out of the matmul and writes lse 0 for them
+        assert np.all(lse[~valid] == 0.0)
+    dh = bufs["dh"][:sizes["dh"]].view(h.dtype).view(N, D)
+    dW = bufs["dW"][:sizes["dW"]].view(torch.bfloat16).view(V, D)
+    db = None if b is None else bufs["db"][:sizes["db"]].view(b.dtype)
+    compare_backward((dh, dW, db), ref_b)
