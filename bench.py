@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling captures of a small case)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures of a small case)")
     ap.add_argument("--fused", action="store_true", help="one flce_forward_backward call per step")
+    ap.add_argument("--bwd", default="auto", choices=["auto", "recompute", "keep_logits"],
+                    help="backward algorithm of the fused call (FLCE_FLAG_BWD_*)")
     ap.add_argument("--compact", action="store_true",
                     help="gather the valid tokens first (FLCE_FLAG_COMPACT_VALID)")
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 1, 2],
@@ -235,7 +237,7 @@ def reference_arm(args):
 class Runner:
     """Preallocated buffers and raw C-ABI calls for one forward + backward step."""
 
-    def __init__(self, w, device, seed_offset=0, compact=False, fused=False):
+    def __init__(self, w, device, seed_offset=0, compact=False, fused=False, bwd="auto"):
         import torch
 
         import linear_cross_entropy_tmem_gb300.api as api
@@ -249,7 +251,7 @@ class Runner:
         N, D, V = w.n_tokens, w.hidden, w.vocab
         self.prob = api.make_problem(N, D, V, hidden_dtype=self.h.dtype, bias_dtype=torch.bfloat16,
                                      logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction,
-                                     compact=compact)
+                                     compact=compact, bwd=bwd)
         f32 = dict(dtype=torch.float32, device=device)
         self.loss = torch.empty(N if w.reduction == "none" else 1, **f32)
         self.lse = torch.empty(N, **f32)
@@ -338,7 +340,7 @@ def flce_arm(args):
     device = torch.device("cuda", local)
     dist = init_dist("nccl")
     w = pick_workload(args)
-    run = Runner(w, device, seed_offset=rank, compact=args.compact, fused=args.fused)
+    run = Runner(w, device, seed_offset=rank, compact=args.compact, fused=args.fused, bwd=args.bwd)
     lib = run.lib
     B.check(lib.flce_testing_set_gemm_mode(args.gemm_mode), "gemm mode")
 
@@ -347,7 +349,7 @@ def flce_arm(args):
     torch.cuda.synchronize()
 
     # ---- device-timed region, with the launch log bracketing every kernel
-    n_launch_per_step = 64
+    n_launch_per_step = 128
     cap = n_launch_per_step * args.steps
     recs = (B.FlceLaunchRecord * cap)()
     events = []
@@ -390,7 +392,9 @@ def flce_arm(args):
         d[0] += 1
         d[1] += events[i][0].elapsed_time(events[i][1])
     flops_kind = 2.0 * w.n_tokens * w.vocab * w.hidden  # per step, for each GEMM kind
-    gemm_kinds = [k for k in per_kind if k != "other"]
+    gemm_kinds = [k for k in per_kind if k not in ("other", "bwd_logit_grad")]
+    keep = "bwd_logit_grad" in per_kind  # the token-chunked backward ran (6NVD instead of 8NVD)
+    zgrad_bytes = 6.0 * w.n_tokens * w.vocab  # per step: fp32 logits read, bf16 G written
     dominant = max(gemm_kinds, key=lambda k: per_kind[k][1])
     n_l, t_ms = per_kind[dominant]
     achieved = flops_kind * args.steps / (t_ms * 1e-3) / 1e12
@@ -454,15 +458,19 @@ def flce_arm(args):
                        "gemm_mode": ["auto", "single-cta", "cta-pair"][args.gemm_mode],
                        "compact_valid_tokens": bool(args.compact),
                        "entry": "flce_forward_backward" if args.fused else "flce_forward + flce_backward",
+                       "backward": "keep_logits (token chunks, 6NVD)" if keep else "recompute (8NVD)",
                        "l2": "inputs larger than L2 (1.25 GB head), no flush"},
             "tflops": tflops,
+            "tflops_executed": tflops * (0.75 if keep else 1.0),
             "pct_of_peak": {"of_burst": tflops / peak_burst, "of_sustained": tflops / peak, "source": peak_src},
             "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
                          "peak_kind": f"bf16 sustained ({peak_src})", "unit": "TFLOP/s", "frac": achieved / peak,
                          "traffic": committed_traffic(dominant, args.workload),
                          "launches": n_l, "avg_launch_ms": t_ms / n_l},
             "kernels": {k: {"launches": v[0], "ms_per_step": v[1] / args.steps,
-                            "tflops": (flops_kind * args.steps / (v[1] * 1e-3) / 1e12) if k != "other" else None}
+                            "tflops": (flops_kind * args.steps / (v[1] * 1e-3) / 1e12) if k in gemm_kinds else None,
+                            "gbs": (zgrad_bytes * args.steps / (v[1] * 1e-3) / 1e9) if k == "bwd_logit_grad"
+                            else None}
                         for k, v in sorted(per_kind.items())},
             "gpu_launches": int(launches),
             "clocks": clock,

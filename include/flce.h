@@ -75,7 +75,29 @@ enum {
    * lse = 0 and entropy = 0 instead of their values over the vocabulary, and a
    * zero dhidden row.
    */
-  FLCE_FLAG_COMPACT_VALID = 1u
+  FLCE_FLAG_COMPACT_VALID = 1u,
+  /*
+   * Backward algorithm of flce_forward_backward (the other calls ignore these
+   * two bits; setting both is FLCE_ERR_INVALID_ARG).  With neither bit the
+   * library chooses from the problem's sizes alone, and
+   * flce_workspace_size(problem, 2) follows the choice.
+   *
+   * FLCE_FLAG_BWD_RECOMPUTE: every logit tile is recomputed in the backward
+   *   (TRL PR #6859, review "Correctness" item 2: the backward sweeps the
+   *   vocabulary again per row).  8*N*V*D flops; the scratch is bounded (a
+   *   bf16 gradient chunk of at most 1 GiB).
+   * FLCE_FLAG_BWD_KEEP_LOGITS: token-chunked.  The tokens are cut into chunks
+   *   of at most half of N; the forward product of a chunk keeps its fp32
+   *   logits in the workspace, and the chunk's logit gradient, dhidden rows and
+   *   dweight contribution are formed from them before the next chunk starts
+   *   (TRL PR #6863, opening section: token chunks whose logits come from a
+   *   bf16 tensor-core product and are held in fp32).  6*N*V*D flops, at the
+   *   price of about 6 bytes of scratch per logit of a chunk plus a 4*V*D-byte
+   *   fp32 dweight accumulator.  Needs N > 256 (else the recompute runs) and
+   *   cannot be combined with FLCE_FLAG_COMPACT_VALID (FLCE_ERR_INVALID_ARG).
+   */
+  FLCE_FLAG_BWD_RECOMPUTE = 2u,
+  FLCE_FLAG_BWD_KEEP_LOGITS = 4u
 };
 
 /* Status codes returned by every call (and stored in the device status word). */
@@ -113,9 +135,10 @@ enum {
  *                 batch: the mean then divides by it, in the forward and the
  *                 backward (TRL PR #6859 review, "Test coverage" item 10).
  *                 Finite and >= 0.
- *   flags         FLCE_FLAG_COMPACT_VALID or 0.
+ *   flags         an OR of FLCE_FLAG_* bits, or 0.
  *   reserved      0.
- * (ABI version 2: num_items_in_batch, flags and reserved were added.)
+ * (ABI version 2: num_items_in_batch, flags and reserved were added; version
+ * 3: the two backward-algorithm flags.)
  */
 typedef struct {
   int64_t n_tokens;
@@ -193,10 +216,15 @@ FLCE_API int flce_backward(const flce_problem* problem, const void* hidden, cons
  * Forward and backward in one call, for callers that know the upstream
  * gradient before the forward runs (a training step whose loss is used as is).
  * Same arguments and results as flce_forward followed by flce_backward with
- * `lse` and `n_valid` passed from one to the other, bit for bit; the two halves
- * share argument checks, planning, the fp32 hidden split and the valid-token
- * compaction, and their scratch shares one workspace of
- * flce_workspace_size(problem, 2) bytes.
+ * `lse` and `n_valid` passed from one to the other.  With the recompute
+ * backward (FLCE_FLAG_BWD_RECOMPUTE) the results are the same bit for bit; the
+ * two halves share argument checks, planning, the fp32 hidden split and the
+ * valid-token compaction, and their scratch shares one workspace of
+ * flce_workspace_size(problem, 2) bytes.  With the token-chunked backward
+ * (FLCE_FLAG_BWD_KEEP_LOGITS) every output is the same up to the order of the
+ * fp32 sums: the vocabulary splits of the forward are planned per chunk, and
+ * dhidden / dweight are summed over different partitions of the vocabulary /
+ * the tokens.
  *   dloss    fp32 upstream gradient, [1] (mean / sum) or [N] (none), on the
  *            device before the call's work reaches the backward
  *   lse, n_valid: outputs of the forward half, read by the backward half

@@ -42,13 +42,22 @@ FLCE_API int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit);
  */
 FLCE_API int flce_testing_set_gemm_mode(int mode);
 
+/*
+ * Process-wide override of the token-chunk size of the token-chunked backward
+ * (FLCE_FLAG_BWD_KEEP_LOGITS), for tests and tuning: rows per chunk, rounded up
+ * to 256 and capped at half of N rounded up to 256; 0 restores the automatic
+ * size.  flce_workspace_size follows it.  Not thread-safe.
+ */
+FLCE_API int flce_testing_set_token_chunk(int64_t rows);
+
 /* Kinds of launch recorded by the launch log. */
 enum {
   FLCE_LAUNCH_FWD_LOGITS = 0,   /* forward logit GEMM + online statistics        */
   FLCE_LAUNCH_BWD_RECOMPUTE = 1,/* backward logit recompute + G                   */
   FLCE_LAUNCH_BWD_DWEIGHT = 2,  /* dW = G^T h                                     */
   FLCE_LAUNCH_BWD_DHIDDEN = 3,  /* dh += G W                                      */
-  FLCE_LAUNCH_OTHER = 4         /* split, merge, reduce, dbias, dh finalize        */
+  FLCE_LAUNCH_OTHER = 4,        /* split, merge, reduce, dbias, dh finalize        */
+  FLCE_LAUNCH_BWD_LOGIT_GRAD = 5/* token-chunked backward: G from kept logits     */
 };
 
 /* One logged launch: two caller-created CUDA events (cudaEvent_t, timing

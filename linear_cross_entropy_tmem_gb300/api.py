@@ -33,15 +33,21 @@ def _stream(device: torch.device):
 def make_problem(n_tokens: int, hidden: int, vocab: int, *, hidden_dtype=torch.bfloat16,
                  weight_dtype=torch.bfloat16, bias_dtype=torch.bfloat16, logit_scale: float = 1.0,
                  softcap: float = 0.0, ignore_index: int = -100, reduction: str = "mean",
-                 num_items_in_batch: float = 0.0, compact: bool = False) -> B.FlceProblem:
+                 num_items_in_batch: float = 0.0, compact: bool = False,
+                 bwd: str = "auto") -> B.FlceProblem:
+    """``bwd`` picks the backward algorithm of the fused call: "auto", "recompute" or
+    "keep_logits" (token-chunked; see FLCE_FLAG_BWD_KEEP_LOGITS in include/flce.h)."""
     if reduction not in B.REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(B.REDUCTIONS)}")
+    if bwd not in B.BWD_ALGOS:
+        raise ValueError(f"bwd must be one of {sorted(B.BWD_ALGOS)}")
     return B.FlceProblem(
         n_tokens=n_tokens, hidden=hidden, vocab=vocab,
         hidden_dtype=_dtype_code(hidden_dtype, "hidden"), weight_dtype=_dtype_code(weight_dtype, "weight"),
         bias_dtype=_dtype_code(bias_dtype, "bias"), reduction=B.REDUCTIONS[reduction],
         logit_scale=float(logit_scale), final_logit_softcapping=float(softcap), ignore_index=int(ignore_index),
-        num_items_in_batch=float(num_items_in_batch), flags=B.FLCE_FLAG_COMPACT_VALID if compact else 0,
+        num_items_in_batch=float(num_items_in_batch),
+        flags=(B.FLCE_FLAG_COMPACT_VALID if compact else 0) | B.BWD_ALGOS[bwd],
         reserved=0)
 
 
@@ -152,9 +158,10 @@ def flce_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Ten
 def flce_forward_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor, dloss: torch.Tensor,
                           bias: Optional[torch.Tensor] = None, *, logit_scale: float = 1.0, softcap: float = 0.0,
                           ignore_index: int = -100, reduction: str = "mean", entropy: bool = False,
-                          num_items_in_batch: float = 0.0, compact: bool = False,
+                          num_items_in_batch: float = 0.0, compact: bool = False, bwd: str = "auto",
                           workspace: Optional[torch.Tensor] = None):
-    """Forward and backward in one call (see ``flce_forward_backward`` in include/flce.h).
+    """Forward and backward in one call (see ``flce_forward_backward`` in include/flce.h);
+    ``bwd`` as in :func:`make_problem`.
 
     Returns ``(ForwardResult, (dhidden, dweight, dbias))``."""
     _require_cuda(hidden, weight, targets, dloss, bias)
@@ -167,7 +174,7 @@ def flce_forward_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: t
     prob = make_problem(N, D, V, hidden_dtype=hidden.dtype, weight_dtype=weight.dtype,
                         bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
                         logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
-                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact)
+                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact, bwd=bwd)
     dev = hidden.device
     ws = _workspace(flce_workspace_size(prob, 2), dev, workspace)
     f32 = dict(dtype=torch.float32, device=dev)
@@ -246,6 +253,11 @@ def testing_gemm(A: torch.Tensor, B_: torch.Tensor, *, a_mn_major: bool, b_mn_ma
 
 def testing_set_tuning(chunk_cols: int = 0, dh_ksplit: int = 0) -> None:
     B.check(B.load().flce_testing_set_tuning(int(chunk_cols), int(dh_ksplit)), "flce_testing_set_tuning")
+
+
+def testing_set_token_chunk(rows: int = 0) -> None:
+    """Rows per token chunk of the token-chunked backward (0 = automatic; tests and tuning)."""
+    B.check(B.load().flce_testing_set_token_chunk(int(rows)), "flce_testing_set_token_chunk")
 
 
 def testing_set_gemm_mode(mode: int = 0) -> None:

@@ -15,6 +15,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 FLCE_F32, FLCE_BF16 = 0, 1
 FLCE_RED_NONE, FLCE_RED_SUM, FLCE_RED_MEAN = 0, 1, 2
 FLCE_FLAG_COMPACT_VALID = 1
+FLCE_FLAG_BWD_RECOMPUTE = 2
+FLCE_FLAG_BWD_KEEP_LOGITS = 4
+BWD_ALGOS = {"auto": 0, "recompute": FLCE_FLAG_BWD_RECOMPUTE, "keep_logits": FLCE_FLAG_BWD_KEEP_LOGITS}
 REDUCTIONS = {"none": FLCE_RED_NONE, "sum": FLCE_RED_SUM, "mean": FLCE_RED_MEAN}
 
 FLCE_OK = 0
@@ -34,7 +37,8 @@ class FlceLaunchRecord(ctypes.Structure):
     _fields_ = [("begin_event", c_void_p), ("end_event", c_void_p), ("kind", c_int32), ("reserved", c_int32)]
 
 
-LAUNCH_KINDS = {0: "fwd_logits", 1: "bwd_recompute", 2: "bwd_dweight", 3: "bwd_dhidden", 4: "other"}
+LAUNCH_KINDS = {0: "fwd_logits", 1: "bwd_recompute", 2: "bwd_dweight", 3: "bwd_dhidden", 4: "other",
+                5: "bwd_logit_grad"}
 
 
 class FlceProblem(ctypes.Structure):
@@ -75,6 +79,7 @@ SIGNATURES = {
     "flce_abi_version": (c_int, []),
     "flce_testing_set_tuning": (c_int, [c_int64, c_int]),
     "flce_testing_set_gemm_mode": (c_int, [c_int]),
+    "flce_testing_set_token_chunk": (c_int, [c_int64]),
     "flce_testing_set_launch_log": (c_int, [c_void_p, c_int32, POINTER(c_int32)]),
     "flce_testing_launch_count": (c_int64, []),
     "flce_testing_gemm": (c_int, [c_int, c_int, c_int64, c_int64, c_int64, c_void_p, c_int64, c_void_p, c_int64,

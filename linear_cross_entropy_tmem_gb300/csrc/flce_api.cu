@@ -11,6 +11,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "flce.h"
 #include "flce_launch.h"
@@ -19,10 +20,17 @@
 namespace flce {
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 constexpr int kMaxSplits = 64;                     // forward vocabulary splits
 constexpr int kMaxKSplit = 16;                     // dh K splits
 constexpr size_t kGChunkBudget = size_t(1) << 30;  // bytes of the bf16 G chunk
+// Token-chunked backward: bytes of the kept fp32 logits + bf16 G of one chunk,
+// and the smallest hidden size for which the automatic choice keeps logits
+// (below it the recompute's 2*D flops per logit cost less than the 6 bytes per
+// logit of the extra pass over the kept logits).
+constexpr size_t kLogitChunkBudget = size_t(4) << 30;
+constexpr int64_t kKeepLogitsMinHidden = 1024;
+constexpr int64_t kTokenChunkAlign = 256;          // rows; a multiple of kMergeThreads and kZGradRows
 constexpr int kMaxDevices = 64;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -92,8 +100,10 @@ int validate(const flce_problem* p) {
     return FLCE_ERR_UNSUPPORTED_DTYPE;
   }
   if (!std::isfinite(p->num_items_in_batch) || p->num_items_in_batch < 0.0) return FLCE_ERR_INVALID_ARG;
-  if ((p->flags & ~static_cast<uint32_t>(FLCE_FLAG_COMPACT_VALID)) != 0 || p->reserved != 0)
-    return FLCE_ERR_INVALID_ARG;
+  constexpr uint32_t kKnownFlags = FLCE_FLAG_COMPACT_VALID | FLCE_FLAG_BWD_RECOMPUTE | FLCE_FLAG_BWD_KEEP_LOGITS;
+  if ((p->flags & ~kKnownFlags) != 0 || p->reserved != 0) return FLCE_ERR_INVALID_ARG;
+  if ((p->flags & FLCE_FLAG_BWD_RECOMPUTE) && (p->flags & FLCE_FLAG_BWD_KEEP_LOGITS)) return FLCE_ERR_INVALID_ARG;
+  if ((p->flags & FLCE_FLAG_BWD_KEEP_LOGITS) && (p->flags & FLCE_FLAG_COMPACT_VALID)) return FLCE_ERR_INVALID_ARG;
   if (p->hidden % 8 != 0) return FLCE_ERR_MISALIGNED;
   return FLCE_OK;
 }
@@ -122,12 +132,19 @@ struct Layout {
   int64_t n_chunks = 0;
   int ksplit_max = 1;
   bool need_dh_part = false;
+  // token-chunked backward (flce_forward_backward keeping the logits)
+  bool token = false;
+  int64_t nc = 0;         // rows per token chunk (multiple of kTokenChunkAlign)
+  int64_t n_tchunks = 0;
+  int64_t ldz = 0;        // row stride of the kept logits and of G (elements)
+  size_t z = 0, zg = 0, dw_acc = 0;
 };
 
 // Test/tuning overrides (flce_testing_set_tuning, flce_testing_set_gemm_mode); 0 = automatic.
 std::atomic<int64_t> g_force_chunk_cols{0};
 std::atomic<int> g_force_dh_ksplit{0};
 std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel
+std::atomic<int64_t> g_force_token_rows{0};
 
 // CTA pairs (256-row tiles) when there are at least 256 rows and enough units
 // to give every cluster work; otherwise single CTAs (128-row tiles).
@@ -161,10 +178,84 @@ int dh_ksplit_bound(int64_t n_tokens, int64_t hidden, int64_t vc) {
 
 enum LayoutKind { kForward = 0, kBackward = 1, kFused = 2 };
 
+// Backward algorithm of the fused call: keep the logits of token chunks
+// (6NVD) or recompute them (8NVD).  Depends on the problem only, so that
+// flce_workspace_size agrees with the call.
+bool keep_logits(const flce_problem* p) {
+  if (p->flags & FLCE_FLAG_BWD_RECOMPUTE) return false;
+  if (p->n_tokens <= kTokenChunkAlign) return false;  // fewer than two chunks
+  if (p->flags & FLCE_FLAG_BWD_KEEP_LOGITS) return true;
+  if (compact(p)) return false;
+  return p->hidden >= kKeepLogitsMinHidden;
+}
+
+int64_t logit_row_stride(int64_t vocab) { return cdiv(vocab, 32) * 32; }
+
+// Rows per token chunk: as many as the logit budget allows, balanced over the
+// chunks, at most half of N (so that the kept logits never cover all tokens).
+int64_t token_chunk_rows(int64_t n_tokens, int64_t vocab) {
+  const int64_t cap = cdiv(cdiv(n_tokens, 2), kTokenChunkAlign) * kTokenChunkAlign;
+  const int64_t forced = g_force_token_rows.load();
+  if (forced > 0) return std::min(cap, cdiv(forced, kTokenChunkAlign) * kTokenChunkAlign);
+  const size_t per_row = size_t(logit_row_stride(vocab)) * 6;
+  const int64_t max_rows =
+      std::max<int64_t>(kTokenChunkAlign, int64_t(kLogitChunkBudget / per_row) / kTokenChunkAlign * kTokenChunkAlign);
+  const int64_t n_chunks = std::max<int64_t>(2, cdiv(n_tokens, max_rows));
+  return std::min(cap, cdiv(cdiv(n_tokens, n_chunks), kTokenChunkAlign) * kTokenChunkAlign);
+}
+
+// K splits the token-chunked dh product may use (slots in the workspace).
+int token_dh_ksplit_bound(int64_t nc, int64_t hidden) {
+  const int forced = g_force_dh_ksplit.load();
+  if (forced > 0) return std::min(forced, kMaxKSplit);
+  const int64_t tiles = cdiv(nc, kBM) * cdiv(hidden, kBN);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxKSplit, cdiv(2048, tiles))));
+}
+
+// [status][hi, lo][forward records of one chunk][kept logits][G][dbias
+// partials of all row tiles][fp32 dW accumulator][dh K-split slots].
+Layout make_token_layout(const flce_problem* p, bool has_bias) {
+  Layout L;
+  L.token = true;
+  const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
+  size_t off = 256;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  if (p->hidden_dtype == FLCE_F32) {
+    L.hi = take(size_t(N) * D * 2);
+    L.lo = take(size_t(N) * D * 2);
+  }
+  L.nc = token_chunk_rows(N, V);
+  L.n_tchunks = cdiv(N, L.nc);
+  L.ldz = logit_row_stride(V);
+  const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN)) * kEpilogueGroups;
+  const size_t part = size_t(splits) * L.nc * 4;
+  L.part_m = take(part);
+  L.part_s = take(part);
+  L.part_a = take(part);
+  L.part_best = take(part);
+  L.part_idx = take(part);
+  L.z_target = take(size_t(L.nc) * 4);
+  L.blocks = take(size_t(cdiv(N, kMergeThreads)) * sizeof(BlockPartial));
+  L.z = take(size_t(L.nc) * L.ldz * 4);
+  L.zg = take(size_t(L.nc) * L.ldz * 2);
+  if (has_bias) L.dbias_part = take(size_t(cdiv(N, kZGradRows)) * L.ldz * 4);
+  L.dw_acc = take(size_t(V) * D * 4);
+  L.ksplit_max = token_dh_ksplit_bound(L.nc, D);
+  L.need_dh_part = L.ksplit_max > 1;
+  if (L.need_dh_part) L.dh_part = take(size_t(L.ksplit_max) * L.nc * D * 4);
+  L.total = off;
+  return L;
+}
+
 // [status][hi, lo][compaction][forward region | backward region]; in the fused
 // call the forward and backward regions overlap (the forward's scratch is dead
 // before the backward starts, in stream order).
 Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
+  if (kind == kFused && keep_logits(p)) return make_token_layout(p, has_bias);
   Layout L;
   const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
   size_t off = 256;  // status word + padding
@@ -636,6 +727,207 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
   return FLCE_OK;
 }
 
+// K splits of one token chunk's dh product: the fewest that fill the device's
+// CTAs (or clusters) within 2 % of the best wave efficiency.
+int choose_token_ksplit(int64_t tiles, int ctas, int bound) {
+  if (g_force_dh_ksplit.load() > 0) return bound;
+  double best = 0.0;
+  std::vector<double> eff(bound + 1, 0.0);
+  for (int k = 1; k <= bound; ++k) {
+    const int64_t units = tiles * k;
+    eff[k] = double(units) / double(cdiv(units, ctas) * ctas);
+    best = std::max(best, eff[k]);
+  }
+  for (int k = 1; k <= bound; ++k)
+    if (eff[k] >= best - 0.02) return k;
+  return 1;
+}
+
+// Token-chunked forward + backward (FLCE_FLAG_BWD_KEEP_LOGITS).  Per chunk of
+// L.nc tokens: the forward product keeps z (fp32), the merge gives lse and the
+// per-token outputs, zgrad forms G and the dbias partials from the kept z, the
+// chunk's dh rows come from one product over the whole vocabulary, and dW
+// accumulates in fp32 across chunks (the last chunk writes the bf16 result).
+int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
+                     cudaStream_t st, const void* weight, const void* bias, const Prep& pr, const float* dloss,
+                     float* loss, float* lse, float* entropy, int64_t* correct, int64_t* n_valid,
+                     float* entropy_sum, void* dhidden, void* dweight, void* dbias) {
+  const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
+  const bool h32 = pr.h32;
+  const bool none = p->reduction == FLCE_RED_NONE;
+  const bool softcap = p->final_logit_softcapping > 0.f;
+  const size_t out_elem = h32 ? 4 : 2;
+  float* z = reinterpret_cast<float*>(ws + L.z);
+  uint16_t* g = reinterpret_cast<uint16_t*>(ws + L.zg);
+  float* dw_acc = reinterpret_cast<float*>(ws + L.dw_acc);
+  float* dbias_part = bias ? reinterpret_cast<float*>(ws + L.dbias_part) : nullptr;
+  float* dh_part = L.need_dh_part ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
+  BlockPartial* blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
+
+  // The mean's denominator is needed by the first chunk's gradient.
+  if (p->reduction == FLCE_RED_MEAN && !(p->num_items_in_batch > 0.0)) {
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st,
+                    [&] { return launch_count_valid(pr.tgt, N, V, p->ignore_index, n_valid, st); }));
+  }
+  CUtensorMap w_mn;  // W as the MN-major B operand of dh
+  FLCE_TRY(make_map(&w_mn, weight, D, V, D * 2, 64, kBK));
+  const bool pair_dh = use_pair(L.nc, cdiv(D, kBN), dev.num_sms);
+  const int dh_ctas = pair_dh ? dev.num_sms / 2 : dev.num_sms;
+  const int ksplit =
+      choose_token_ksplit(cdiv(L.nc, pair_dh ? kPairRows : kBM) * cdiv(D, kBN), dh_ctas, L.ksplit_max);
+  const bool pair_dw = use_pair(V, cdiv(D, kBN), dev.num_sms);
+  const int dw_ctas = pair_dw ? dev.num_sms / 2 : dev.num_sms;
+
+  for (int64_t c = 0; c < L.n_tchunks; ++c) {
+    const int64_t r0 = c * L.nc;
+    const int64_t rows = std::min<int64_t>(L.nc, N - r0);
+    const bool last = c == L.n_tchunks - 1;
+    const uint8_t* a_main = static_cast<const uint8_t*>(pr.a_main) + size_t(r0) * D * 2;
+    const uint8_t* a_lo = h32 ? reinterpret_cast<const uint8_t*>(pr.lo) + size_t(r0) * D * 2 : nullptr;
+    const int64_t* tgt = pr.tgt + r0;
+
+    // (1) logits of the chunk: online statistics, and z kept in fp32
+    const bool pair_f = use_pair(rows, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
+    TmaMaps fm;
+    FLCE_TRY(make_map(&fm.a0, a_main, D, rows, D * 2, kBK, kBM));
+    fm.a1 = fm.a0;
+    if (h32) FLCE_TRY(make_map(&fm.a1, a_lo, D, rows, D * 2, kBK, kBM));
+    FLCE_TRY(make_map(&fm.b0, weight, D, V, D * 2, kBK, pair_f ? kBN / 2 : kBN));
+    fm.b1 = fm.b0;
+    GemmSched sf = base_sched(rows, V, D, h32 ? 2 : 1, 1, pair_f);
+    int per_unit = 1;
+    const int splits = choose_splits(sf.m_tiles, sf.n_tiles, pair_f ? dev.num_sms / 2 : dev.num_sms, &per_unit);
+    sf.n_per_unit = per_unit;
+    sf.group_m = pair_f ? 16 : 32;
+    finish_sched(sf);
+    FwdParams fp{};
+    fp.n_tokens = rows;
+    fp.vocab = V;
+    fp.bias = bias;
+    fp.bias_f32 = p->bias_dtype == FLCE_F32;
+    fp.bias_vec = bias != nullptr && aligned(bias, 16);
+    fp.n_splits = splits;
+    fp.scale = p->logit_scale;
+    fp.softcap = softcap ? p->final_logit_softcapping : 0.f;
+    fp.inv_softcap = softcap ? 1.f / p->final_logit_softcapping : 0.f;
+    fp.ignore_index = p->ignore_index;
+    fp.targets = tgt;
+    fp.part_m = reinterpret_cast<float*>(ws + L.part_m);
+    fp.part_s = reinterpret_cast<float*>(ws + L.part_s);
+    fp.part_a = reinterpret_cast<float*>(ws + L.part_a);
+    fp.part_best = reinterpret_cast<float*>(ws + L.part_best);
+    fp.part_idx = reinterpret_cast<int32_t*>(ws + L.part_idx);
+    fp.z_target = reinterpret_cast<float*>(ws + L.z_target);
+    fp.z_out = z;
+    fp.ldz = L.ldz;
+    FLCE_TRY(logged(FLCE_LAUNCH_FWD_LOGITS, st, [&] {
+      return launch_fwd_gemm(bias != nullptr, softcap, pair_f, fm, sf, fp, status, dev.num_sms, st);
+    }));
+    MergeParams mp{};
+    mp.n_tokens = rows;
+    mp.vocab = V;
+    mp.n_splits = splits * kEpilogueGroups;
+    mp.reduction = p->reduction;
+    mp.ignore_index = p->ignore_index;
+    mp.part_m = fp.part_m;
+    mp.part_s = fp.part_s;
+    mp.part_a = fp.part_a;
+    mp.part_best = fp.part_best;
+    mp.part_idx = fp.part_idx;
+    mp.z_target = fp.z_target;
+    mp.targets = tgt;
+    mp.lse = lse + r0;
+    mp.entropy = entropy ? entropy + r0 : nullptr;
+    mp.loss_tok = none ? loss + r0 : nullptr;
+    mp.blocks = blocks + r0 / kMergeThreads;  // r0 % kMergeThreads == 0
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_merge(mp, status, st); }));
+
+    // (2) G and the dbias partials from the kept logits
+    ZGradParams zp{};
+    zp.rows = rows;
+    zp.vocab = V;
+    zp.z = z;
+    zp.ldz = L.ldz;
+    zp.g = g;
+    zp.reduction = p->reduction;
+    zp.scale = p->logit_scale;
+    zp.softcap = fp.softcap;
+    zp.inv_softcap = fp.inv_softcap;
+    zp.ignore_index = p->ignore_index;
+    zp.targets = tgt;
+    zp.lse = lse + r0;
+    zp.dloss = none ? dloss + r0 : dloss;
+    zp.n_valid = n_valid;
+    zp.num_items = static_cast<float>(p->num_items_in_batch);
+    zp.dbias_part = dbias_part ? dbias_part + (r0 / kZGradRows) * L.ldz : nullptr;
+    FLCE_TRY(logged(FLCE_LAUNCH_BWD_LOGIT_GRAD, st, [&] { return launch_zgrad(zp, softcap, st); }));
+
+    // (3) dh rows of the chunk = G W   (A = G K-major, B = W MN-major, K = V)
+    TmaMaps mh;
+    FLCE_TRY(make_map(&mh.a0, g, V, rows, L.ldz * 2, kBK, kBM));
+    mh.a1 = mh.a0;
+    mh.b0 = w_mn;
+    mh.b1 = w_mn;
+    GemmSched s3 = base_sched(rows, D, V, 1, 0, pair_dh);
+    s3.b_mn = 1;
+    s3.ksplit = ksplit;
+    s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
+    s3.group_m = std::max(1, dh_ctas / std::max(1, s3.n_tiles * ksplit));
+    finish_sched(s3);
+    uint8_t* dh_out = static_cast<uint8_t*>(dhidden) + size_t(r0) * D * out_elem;
+    AccumParams ap{};
+    ap.rows = rows;
+    ap.cols = D;
+    ap.part = dh_part;
+    ap.part_stride = rows * D;
+    ap.accumulate = 0;
+    ap.write_final = ksplit == 1 ? 1 : 0;
+    ap.out = dh_out;
+    ap.out_f32 = h32 ? 1 : 0;
+    FLCE_TRY(logged(FLCE_LAUNCH_BWD_DHIDDEN, st,
+                    [&] { return launch_accum_gemm(pair_dh, mh, s3, ap, status, dev.num_sms, st); }));
+    if (ksplit > 1) {
+      FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+        return launch_dh_finalize(dh_part, rows * D, ksplit, rows, D, dh_out, h32 ? 1 : 0, nullptr, nullptr,
+                                  dev.num_sms * 4, st);
+      }));
+    }
+
+    // (4) dW (+)= G^T h[chunk]   (A = G MN-major, B = h MN-major, K = chunk rows)
+    TmaMaps mw;
+    FLCE_TRY(make_map(&mw.a0, g, V, rows, L.ldz * 2, 64, kBK));
+    mw.a1 = mw.a0;
+    FLCE_TRY(make_map(&mw.b0, a_main, D, rows, D * 2, 64, kBK));
+    mw.b1 = mw.b0;
+    if (h32) FLCE_TRY(make_map(&mw.b1, a_lo, D, rows, D * 2, 64, kBK));
+    GemmSched s2 = base_sched(V, D, rows, h32 ? 2 : 1, 0, pair_dw);
+    s2.a_mn = 1;
+    s2.b_mn = 1;
+    s2.group_m = std::max(1, dw_ctas / std::max(1, s2.n_tiles));
+    finish_sched(s2);
+    AccumParams aw{};
+    aw.rows = V;
+    aw.cols = D;
+    aw.part = dw_acc;
+    aw.part_stride = V * D;
+    aw.accumulate = c > 0 ? 1 : 0;
+    aw.write_final = last ? 1 : 0;
+    aw.out = dweight;
+    aw.out_f32 = 0;
+    FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
+                    [&] { return launch_accum_gemm(pair_dw, mw, s2, aw, status, dev.num_sms, st); }));
+  }
+  const ReduceParams rp = reduce_params(p, L, ws, loss, correct, n_valid, entropy_sum);
+  FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); }));
+  if (bias) {
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+      return launch_dbias_reduce(dbias_part, L.ldz, static_cast<int>(cdiv(N, kZGradRows)), V, dbias,
+                                 p->bias_dtype == FLCE_F32, nullptr, st);
+    }));
+  }
+  return FLCE_OK;
+}
+
 int check_forward_args(const flce_problem* p, const void* hidden, const void* weight, const int64_t* targets,
                        const float* loss, const float* lse, const int64_t* correct, const int64_t* n_valid,
                        const float* entropy_sum, const void* workspace) {
@@ -749,6 +1041,10 @@ int flce_forward_backward(const flce_problem* p, const void* hidden, const void*
   Prep pr;
   FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, targets, nullptr, dloss, lse, entropy,
                    p->reduction == FLCE_RED_NONE ? loss : nullptr, &pr));
+  if (L.token) {
+    return run_fused_tokens(p, L, dev, ws, status, st, weight, bias, pr, dloss, loss, lse, entropy, correct,
+                            n_valid, entropy_sum, dhidden, dweight, dbias);
+  }
   FLCE_TRY(run_forward(p, L, dev, ws, status, st, weight, bias, pr, loss, lse, entropy, correct, n_valid,
                        entropy_sum, pr.cmp ? pr.c_lse : nullptr));
   const float* lse_use = pr.cmp ? pr.c_lse : lse;
@@ -761,6 +1057,12 @@ int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit) {
   if (chunk_cols < 0 || dh_ksplit < 0 || dh_ksplit > kMaxKSplit) return FLCE_ERR_INVALID_ARG;
   g_force_chunk_cols.store(chunk_cols);
   g_force_dh_ksplit.store(dh_ksplit);
+  return FLCE_OK;
+}
+
+int flce_testing_set_token_chunk(int64_t rows) {
+  if (rows < 0) return FLCE_ERR_INVALID_ARG;
+  g_force_token_rows.store(rows);
   return FLCE_OK;
 }
 

@@ -1,6 +1,7 @@
 // flce_bwd.cu — backward kernels: the recompute GEMM with the logit-gradient
-// epilogue (four variants: bias x soft cap), the dW store GEMM, the dh
-// accumulate GEMM, the ordered dbias reduction and the dh K-split finalize.
+// epilogue (four variants: bias x soft cap), the dW store GEMM, the dh / dW
+// accumulate GEMM, the logit gradient of the token-chunked backward (from kept
+// logits), the ordered dbias reduction and the dh K-split finalize.
 #include <cuda_runtime.h>
 
 #include "flce_gemm_launch.cuh"
@@ -23,6 +24,92 @@ cudaError_t launch_store_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
 cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& sc, const AccumParams& p,
                               int* status, int num_sms, cudaStream_t stream) {
   return launch_gemm<EpiAccum>(pair, maps, sc, p, status, num_sms, stream);
+}
+
+// Token-chunked backward: G from the kept fp32 logits of one token chunk.
+// Thread t of a block handles kZGradVec consecutive columns over the block's
+// kZGradRows rows: per row one 32-byte load of z and one 16-byte store of G,
+// both coalesced across the block (HBM-bound: 6 bytes per logit).  The column
+// sums of G (fp32, before rounding) over the block's rows are the dbias
+// partials, added in row order.
+template <bool kSoftcap>
+__global__ void __launch_bounds__(kZGradThreads) zgrad_kernel(ZGradParams p) {
+  __shared__ float s_lse2[kZGradRows];  // lse * log2(e)
+  __shared__ float s_wd[kZGradRows];    // w_n * s (0 at ignored rows)
+  __shared__ int64_t s_t[kZGradRows];   // target column
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kZGradRows;
+  const int rows = p.rows - r0 < kZGradRows ? static_cast<int>(p.rows - r0) : kZGradRows;
+  for (int i = threadIdx.x; i < kZGradRows; i += kZGradThreads) {
+    float lse2 = 0.f, wd = 0.f;
+    int64_t t = -1;
+    if (i < rows) {
+      const int64_t row = r0 + i;
+      t = __ldg(p.targets + row);
+      lse2 = __ldg(p.lse + row) * kLog2e;
+      const bool valid = t != p.ignore_index && t >= 0 && t < p.vocab;
+      if (valid) wd = token_weight(p.reduction, p.dloss, row, p.n_valid, p.num_items) * p.scale;
+      if (!valid) t = -1;
+    }
+    s_lse2[i] = lse2;
+    s_wd[i] = wd;
+    s_t[i] = t;
+  }
+  __syncthreads();
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * kZGradThreads + threadIdx.x) * kZGradVec;
+  if (c0 >= p.vocab) return;
+  const float* __restrict__ zp = p.z + r0 * p.ldz + c0;  // 32-byte aligned: ldz % 32 == 0, c0 % 8 == 0
+  uint16_t* __restrict__ gp = p.g + r0 * p.ldz + c0;
+  const int valid_cols = p.vocab - c0 < kZGradVec ? static_cast<int>(p.vocab - c0) : kZGradVec;
+  float colsum[kZGradVec];
+#pragma unroll
+  for (int j = 0; j < kZGradVec; ++j) colsum[j] = 0.f;
+#pragma unroll 4
+  for (int r = 0; r < rows; ++r) {
+    const float4 za = __ldcs(reinterpret_cast<const float4*>(zp + r * p.ldz));
+    const float4 zb = __ldcs(reinterpret_cast<const float4*>(zp + r * p.ldz) + 1);
+    const float z[kZGradVec] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+    const float lse2 = s_lse2[r], wd = s_wd[r];
+    const int64_t tj = s_t[r] - c0;
+    float g[kZGradVec];
+#pragma unroll
+    for (int j = 0; j < kZGradVec; ++j) {
+      const float pr = ex2_approx(fmaf(z[j], kLog2e, -lse2));  // e^(z - lse)
+      float d = wd;
+      if (kSoftcap) {
+        const float th = z[j] * p.inv_softcap;                   // z / c
+        d = wd * fmaf(-th, th, 1.f);                             // w s (1 - (z/c)^2)
+      }
+      g[j] = d * (pr - (j == tj ? 1.f : 0.f));
+      if (j >= valid_cols) g[j] = 0.f;
+      colsum[j] += g[j];
+    }
+    uint4 pk;
+    pk.x = pack_bf16x2(g[0], g[1]);
+    pk.y = pack_bf16x2(g[2], g[3]);
+    pk.z = pack_bf16x2(g[4], g[5]);
+    pk.w = pack_bf16x2(g[6], g[7]);
+    *reinterpret_cast<uint4*>(gp + r * p.ldz) = pk;
+  }
+  if (p.dbias_part) {
+    float* dst = p.dbias_part + static_cast<int64_t>(blockIdx.y) * p.ldz + c0;
+#pragma unroll
+    for (int j = 0; j < kZGradVec; ++j)
+      if (j < valid_cols) dst[j] = colsum[j];
+  }
+}
+
+cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream) {
+  const int64_t gx = (p.vocab + kZGradCols - 1) / kZGradCols;
+  const int64_t gy = (p.rows + kZGradRows - 1) / kZGradRows;
+  if (gx == 0 || gy == 0) return cudaSuccess;
+  if (gy > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  if (softcap) {
+    zgrad_kernel<true><<<grid, kZGradThreads, 0, stream>>>(p);
+  } else {
+    zgrad_kernel<false><<<grid, kZGradThreads, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
 }
 
 // dbias[j] = sum over m tiles of the per-tile column sums, in m order.

@@ -129,6 +129,32 @@ cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t str
   return cudaGetLastError();
 }
 
+// Valid-target count ahead of the forward (the token-chunked backward needs the
+// mean's denominator before the last chunk's forward has run).
+__global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* targets, int64_t n, int64_t vocab,
+                                                           int64_t ignore_index, int64_t* n_valid) {
+  long long c = 0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int64_t t = targets[i];
+    c += (t != ignore_index && t >= 0 && t < vocab) ? 1 : 0;
+  }
+  __shared__ long long s_c[32];
+  c = warp_sum(c);
+  if ((threadIdx.x & 31) == 0) s_c[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long total = 0;
+    for (int i = 0; i < 32; ++i) total += s_c[i];
+    n_valid[0] = total;
+  }
+}
+
+cudaError_t launch_count_valid(const int64_t* targets, int64_t n, int64_t vocab, int64_t ignore_index,
+                               int64_t* n_valid, cudaStream_t stream) {
+  count_valid_kernel<<<1, 1024, 0, stream>>>(targets, n, vocab, ignore_index, n_valid);
+  return cudaGetLastError();
+}
+
 // Final scalars from the block partials, in a fixed order (one block).
 __global__ void __launch_bounds__(256) fwd_reduce_kernel(ReduceParams p) {
   double loss_d = 0.0, ent_d = 0.0;

@@ -240,6 +240,14 @@ struct EpiFwd {
         if (kBias) x += bch[j];
         z[j] = kSoftcap ? p.softcap * tanh_from_exp2_arg(x * k_t) : x * p.scale;
       }
+      if (p.z_out && st.row < p.n_tokens) {  // keep the logits for the token-chunked backward
+        float* dst = p.z_out + st.row * p.ldz + vc;  // 128 B, 128-byte aligned (ldz % 32 == 0)
+        const auto u = [&](int j) { return __float_as_uint(z[j]); };
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_global_v8(dst + 8 * q, u(8 * q), u(8 * q + 1), u(8 * q + 2), u(8 * q + 3), u(8 * q + 4), u(8 * q + 5),
+                       u(8 * q + 6), u(8 * q + 7));
+      }
       if (ragged) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -313,6 +321,17 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
   return v[0];
 }
 
+// Upstream weight w_n of a valid token: dloss[n] (none), dloss (sum) or
+// dloss / denominator (mean; num_items when > 0, else the valid count).
+__device__ __forceinline__ float token_weight(int reduction, const float* dloss, int64_t row, const int64_t* n_valid,
+                                              float num_items) {
+  if (reduction == 0) return __ldg(dloss + row);
+  if (reduction == 1) return __ldg(dloss);
+  const float den =
+      num_items > 0.f ? num_items : static_cast<float>(__ldg(reinterpret_cast<const long long*>(n_valid)));
+  return den > 0.f ? __ldg(dloss) / den : 0.f;
+}
+
 template <bool kBias, bool kSoftcap>
 struct EpiGrad {
   using Params = GradParams;
@@ -331,18 +350,7 @@ struct EpiGrad {
       st.target = __ldg(p.targets + st.row);
       st.lse2 = __ldg(p.lse + st.row) * kLog2e;
       const bool valid = st.target != p.ignore_index && st.target >= 0 && st.target < p.vocab;
-      if (valid) {
-        if (p.reduction == 0) {
-          st.w = __ldg(p.dloss + st.row);
-        } else if (p.reduction == 1) {
-          st.w = __ldg(p.dloss);
-        } else {
-          const float den = p.num_items > 0.f
-                                ? p.num_items
-                                : static_cast<float>(__ldg(reinterpret_cast<const long long*>(p.n_valid)));
-          st.w = den > 0.f ? __ldg(p.dloss) / den : 0.f;
-        }
-      }
+      if (valid) st.w = token_weight(p.reduction, p.dloss, st.row, p.n_valid, p.num_items);
     }
   }
 

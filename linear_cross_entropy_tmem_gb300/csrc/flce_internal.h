@@ -100,6 +100,8 @@ struct FwdParams {
   float* part_best;       // largest z
   int32_t* part_idx;      // its lowest vocabulary index
   float* z_target;        // [n_tokens] z at the target, written by the owning split
+  float* z_out;           // token-chunked backward: every z, fp32 [n_tokens][ldz]; nullptr = not kept
+  int64_t ldz;            // multiple of 32 and >= vocab rounded up to 32
 };
 
 // Backward recompute: G = w_n (softmax - onehot) * dz/dacc for one vocabulary
@@ -121,6 +123,29 @@ struct GradParams {
   uint16_t* g;            // bf16 [n_tokens][ldg]
   int64_t ldg;
   float* dbias_part;      // [m_tiles][ldg] or nullptr
+};
+
+// Token-chunked backward: G = w_n (e^(z - lse) - onehot) * dz/dx from the kept
+// fp32 logits of one token chunk, as bf16, with per-128-row column sums for
+// dbias.  Thread blocks cover kZGradRows rows x kZGradCols columns.
+constexpr int kZGradThreads = 256;
+constexpr int kZGradVec = 8;                               // columns per thread
+constexpr int kZGradCols = kZGradThreads * kZGradVec;      // 2048
+constexpr int kZGradRows = kBM;                            // rows per block = dbias partial granularity
+struct ZGradParams {
+  int64_t rows, vocab;    // rows of this chunk
+  const float* z;         // [rows][ldz] fp32
+  int64_t ldz;
+  uint16_t* g;            // [rows][ldz] bf16
+  int32_t reduction;
+  float scale, softcap, inv_softcap;
+  int64_t ignore_index;
+  const int64_t* targets; // [rows]
+  const float* lse;       // [rows]
+  const float* dloss;     // [1] or [rows] (reduction none)
+  const int64_t* n_valid; // [1] over the whole batch
+  float num_items;
+  float* dbias_part;      // [ceil(rows / kZGradRows)][ldz] or nullptr
 };
 
 // Plain store of the accumulator (dW, and the test GEMM).

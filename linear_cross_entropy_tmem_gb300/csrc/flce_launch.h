@@ -62,6 +62,11 @@ cudaError_t launch_store_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
 cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& sc, const AccumParams& p,
                               int* status, int num_sms, cudaStream_t stream);
 
+cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream);
+// n_valid[0] = number of targets in [0, vocab) other than ignore_index (one block).
+cudaError_t launch_count_valid(const int64_t* targets, int64_t n, int64_t vocab, int64_t ignore_index,
+                               int64_t* n_valid, cudaStream_t stream);
+
 cudaError_t launch_split_hidden(const float* h, uint16_t* hi, uint16_t* lo, int64_t n, int grid,
                                 cudaStream_t stream);
 cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream);

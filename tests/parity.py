@@ -37,6 +37,33 @@ def run_gpu(h, W, b, t, dloss, *, logit_scale, softcap, reduction, ignore_index=
     return out
 
 
+def launch_kinds(fn, cap=256):
+    """Run fn() with the library's launch log on; return the kinds (binding.LAUNCH_KINDS names) of the
+    kernels it launched, in order."""
+    import ctypes
+
+    from linear_cross_entropy_tmem_gb300 import binding as B
+    lib = B.load()
+    recs = (B.FlceLaunchRecord * cap)()
+    events = []
+    for i in range(cap):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()  # torch creates the CUDA event on its first record
+        e1.record()
+        events.append((e0, e1))
+        recs[i].begin_event = ctypes.c_void_p(e0.cuda_event)
+        recs[i].end_event = ctypes.c_void_p(e1.cuda_event)
+    count = ctypes.c_int32(0)
+    torch.cuda.synchronize()
+    B.check(lib.flce_testing_set_launch_log(recs, cap, ctypes.byref(count)), "launch log")
+    try:
+        out = fn()
+        torch.cuda.synchronize()
+    finally:
+        B.check(lib.flce_testing_set_launch_log(None, 0, None), "launch log")
+    return out, [B.LAUNCH_KINDS[recs[i].kind] for i in range(count.value)]
+
+
 def correct_bounds(z: np.ndarray, t: np.ndarray, valid: np.ndarray, argmax: np.ndarray):
     """Range of correct counts a kernel may report when near-ties (gap < 1e-3) flip."""
     rows = np.arange(z.shape[0])

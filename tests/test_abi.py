@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.flce_abi_version() == 2
+    assert lib.flce_abi_version() == 3
     for code in range(0, 10):
         assert lib.flce_status_string(code).decode() not in ("", "unknown status")
     assert lib.flce_status_string(12345).decode() == "unknown status"
@@ -87,13 +87,40 @@ def test_workspace_size_needs_no_gpu_and_never_scales_with_n_times_v(lib):
             assert bw < 2 * N * V  # far below a full (tokens x vocab) bf16 buffer
     st, n = _ws(lib, _problem(n_tokens=0), 1)
     assert st == B.FLCE_OK
-    # the fused call's scratch regions overlap: it needs no more than the larger of the two plus
-    # the shared part
-    for kw in (dict(), dict(hidden_dtype=B.FLCE_F32), dict(flags=B.FLCE_FLAG_COMPACT_VALID)):
+    # with the recompute backward the fused call's scratch regions overlap: it needs no more
+    # than the larger of the two plus the shared part
+    rec = B.FLCE_FLAG_BWD_RECOMPUTE
+    for kw in (dict(flags=rec), dict(hidden_dtype=B.FLCE_F32, flags=rec),
+               dict(flags=B.FLCE_FLAG_COMPACT_VALID | rec)):
         pr = _problem(n_tokens=4096, hidden=1024, vocab=50000, **kw)
         fw, bw, fu = (_ws(lib, pr, k)[1] for k in (0, 1, 2))
         assert max(fw, bw) <= fu <= fw + bw
     assert _ws(lib, _problem(), 3)[0] == B.FLCE_ERR_INVALID_ARG
+
+
+def test_keep_logits_workspace(lib):
+    """The token-chunked backward keeps fp32 logits + bf16 G for at most half of the tokens, plus
+    an fp32 dW accumulator; the automatic choice keeps logits from D = 1024 up and for N > 256."""
+    keep, rec = B.FLCE_FLAG_BWD_KEEP_LOGITS, B.FLCE_FLAG_BWD_RECOMPUTE
+    for (N, D, V) in [(16384, 4096, 151936), (16384, 640, 262144), (8192, 2048, 128256), (4096, 1024, 50000),
+                      (300, 200, 1000), (257, 136, 777)]:
+        ldz = (V + 31) // 32 * 32
+        ws = {f: _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=f), 2) for f in (0, keep, rec)}
+        assert all(st == B.FLCE_OK for st, _ in ws.values())
+        k, r, a = ws[keep][1], ws[rec][1], ws[0][1]
+        assert a == (k if D >= 1024 else r)
+        half = ((N + 1) // 2 + 255) // 256 * 256
+        # kept logits + G, dbias partials, fp32 dW, dh K-split slots (at most 16), split records
+        bound = 6 * min(half, N) * ldz + 4 * ((N + 127) // 128) * ldz + 4 * V * D + 16 * 4 * half * D \
+            + (5 * 4 * 64 * 2 + 8) * half + (1 << 20)
+        assert r < k <= bound
+        if N * V >= 1 << 28:  # the chunk's kept logits + G stay within the 4 GiB budget (+ one row group)
+            assert k - 4 * V * D - 16 * 4 * half * D - 4 * ((N + 127) // 128) * ldz <= (4 << 30) + 6 * 256 * ldz \
+                + (5 * 4 * 64 * 2 + 8) * half + (1 << 20)
+    # with N <= 256 there are no two chunks: the recompute runs and sizes its workspace
+    for N in (1, 100, 256):
+        pk, pr = (_problem(n_tokens=N, hidden=2048, vocab=248320, flags=f) for f in (keep, rec))
+        assert _ws(lib, pk, 2) == _ws(lib, pr, 2)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -109,6 +136,8 @@ def test_workspace_size_needs_no_gpu_and_never_scales_with_n_times_v(lib):
     (dict(num_items_in_batch=-1.0), B.FLCE_ERR_INVALID_ARG),
     (dict(num_items_in_batch=float("inf")), B.FLCE_ERR_INVALID_ARG),
     (dict(flags=8), B.FLCE_ERR_INVALID_ARG),
+    (dict(flags=B.FLCE_FLAG_BWD_RECOMPUTE | B.FLCE_FLAG_BWD_KEEP_LOGITS), B.FLCE_ERR_INVALID_ARG),
+    (dict(flags=B.FLCE_FLAG_BWD_KEEP_LOGITS | B.FLCE_FLAG_COMPACT_VALID), B.FLCE_ERR_INVALID_ARG),
     (dict(reserved=1), B.FLCE_ERR_INVALID_ARG),
 ])
 def test_problem_validation(lib, kw, code):

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from linear_cross_entropy_tmem_gb300.synthetic import TINY, Workload, make_inputs
-from tests.parity import TOL_LSE, compare_backward, compare_forward, run_gpu
+from tests.parity import TOL_LSE, compare_backward, compare_forward, launch_kinds, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -38,10 +38,11 @@ CASES = {
 
 @pytest.fixture(autouse=True)
 def _reset_tuning():
-    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_tuning
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_token_chunk, testing_set_tuning
     yield
     testing_set_tuning(0, 0)
     testing_set_gemm_mode(0)
+    testing_set_token_chunk(0)
 
 
 def _run_case(w: Workload, tuning):
@@ -295,7 +296,7 @@ def test_fused_call_equals_separate_calls(name, compact, mode):
     kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction, compact=compact,
               num_items_in_batch=500.0 if w.reduction == "mean" else 0.0)
     sep = run_gpu(h, W, b, t, dloss, **kw)
-    fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, **kw)
+    fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd="recompute", **kw)
     torch.cuda.synchronize()
     assert F.flce_read_device_status(fwd.workspace) == 0
     for x, y in ((fwd.loss, sep["fwd"].loss), (fwd.lse, sep["fwd"].lse), (fwd.entropy, sep["fwd"].entropy),
@@ -309,6 +310,74 @@ def test_fused_call_equals_separate_calls(name, compact, mode):
                                logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction,
                                num_items_in_batch=kw["num_items_in_batch"])
         compare_forward(fwd, ref_f, reduction=w.reduction)
+
+
+# ---------------------------------------------------------------------------
+# Token-chunked backward of the fused call (kept fp32 logits, 6NVD)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("chunk", [256, 0], ids=["chunk256", "auto-chunk"])
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["auto", "single-cta", "cta-pair"])
+@pytest.mark.parametrize("name", [n for n, (w, _) in CASES.items() if w.n_tokens > 256])
+def test_keep_logits_parity(name, mode, chunk):
+    """Every output of the token-chunked fused call against the oracle, element by element, with
+    several token chunks (ragged last chunk) and the dh K split of the case."""
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_token_chunk, testing_set_tuning
+    w, tuning = CASES[name]
+    testing_set_gemm_mode(mode)
+    testing_set_tuning(*tuning)
+    testing_set_token_chunk(chunk)
+    hc, Wc, bc, tc, dc = make_inputs(w, "cpu")
+    h, W, b, t, dloss = [x.cuda() if x is not None else None for x in (hc, Wc, bc, tc, dc)]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    (fwd, grads), kinds = launch_kinds(
+        lambda: F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd="keep_logits", **kw))
+    assert F.flce_read_device_status(fwd.workspace) == 0
+    chunks = kinds.count("bwd_logit_grad")
+    assert chunks >= 2 and "bwd_recompute" not in kinds
+    assert kinds.count("fwd_logits") == kinds.count("bwd_dhidden") == kinds.count("bwd_dweight") == chunks
+    ref_f = oracle.forward(hc, Wc, bc, tc, **kw)
+    ref_b = oracle.backward(hc, Wc, bc, tc, dloss=dc, **kw)
+    z = oracle.logits(hc, Wc, bc, logit_scale=w.logit_scale, softcap=w.softcap)
+    compare_forward(fwd, ref_f, reduction=w.reduction, z=z, t=tc.numpy())
+    compare_backward(grads, ref_b)
+
+
+@pytest.mark.parametrize("reduction,items", [("mean", 0.0), ("mean", 700.0), ("sum", 0.0), ("none", 0.0)])
+def test_keep_logits_reductions_and_all_ignored(reduction, items):
+    """The mean's denominator (counted before the first chunk, or num_items_in_batch), the other
+    reductions, and an all-ignored batch (zero loss, exact zero gradients) on the token path."""
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_token_chunk
+    testing_set_token_chunk(256)
+    w = Workload("kl", 700, 256, 3000, sigma_w=0.1, bias=True, reduction=reduction, ignore_every=5, seed=11)
+    hc, Wc, bc, tc, dc = make_inputs(w, "cpu")
+    for targets in (tc, torch.full_like(tc, -100)):
+        h, W, b, t, dloss = [x.cuda() for x in (hc, Wc, bc, targets, dc)]
+        kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=reduction, num_items_in_batch=items)
+        fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd="keep_logits", **kw)
+        torch.cuda.synchronize()
+        assert F.flce_read_device_status(fwd.workspace) == 0
+        ref_f = oracle.forward(hc, Wc, bc, targets, **kw)
+        ref_b = oracle.backward(hc, Wc, bc, targets, dloss=dc, **kw)
+        compare_forward(fwd, ref_f, reduction=reduction)
+        if int(ref_f["n_valid"]) == 0:
+            assert all(int(torch.count_nonzero(g)) == 0 for g in grads)
+        else:
+            compare_backward(grads, ref_b)
+
+
+def test_keep_logits_is_deterministic():
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_token_chunk
+    testing_set_token_chunk(256)
+    w, _ = CASES["multi-chunk ksplit1 N640 D512 V2560 none"]
+    h, W, b, t, dloss = [x.cuda() if x is not None else None for x in make_inputs(w, "cpu")]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction, bwd="keep_logits")
+    a = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, **kw)
+    c = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, **kw)
+    for x, y in zip((a[0].loss, a[0].lse, a[0].entropy, *a[1][:2]), (c[0].loss, c[0].lse, c[0].entropy, *c[1][:2])):
+        assert torch.equal(x, y)
 
 
 # ---------------------------------------------------------------------------
@@ -369,6 +438,49 @@ def test_no_writes_past_outputs_or_workspace(name, compact, mode):
     assert np.abs(lse[valid] - ref_f["lse"][valid]).max() <= TOL_LSE
     if compact:  # compaction leaves ignored rows out of the matmul and writes lse 0 for them
         assert np.all(lse[~valid] == 0.0)
+    dh = bufs["dh"][:sizes["dh"]].view(h.dtype).view(N, D)
+    dW = bufs["dW"][:sizes["dW"]].view(torch.bfloat16).view(V, D)
+    db = None if b is None else bufs["db"][:sizes["db"]].view(b.dtype)
+    compare_backward((dh, dW, db), ref_b)
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["single-cta", "cta-pair"])
+@pytest.mark.parametrize("name", ["ragged N300 D200 V1000 bias-bf16 s0.7 c5 sum",
+                                  "fp32-h N257 D136 V777 bias s0.0625 c30 none",
+                                  "multi-chunk ksplit3 N384 D256 V3000 bias mean"])
+def test_keep_logits_no_writes_past_outputs_or_workspace(name, mode):
+    """Canary tails after every output and the workspace of the token-chunked fused call."""
+    import ctypes
+
+    import linear_cross_entropy_tmem_gb300.api as api
+    from linear_cross_entropy_tmem_gb300 import binding as B
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_token_chunk, testing_set_tuning
+    w, tuning = CASES[name]
+    testing_set_gemm_mode(mode)
+    testing_set_tuning(*tuning)
+    testing_set_token_chunk(256)
+    hc, Wc, bc, tc, dc = make_inputs(w, "cpu")
+    h, W, b, t, dloss = [x.cuda() if x is not None else None for x in (hc, Wc, bc, tc, dc)]
+    N, D, V = w.n_tokens, w.hidden, w.vocab
+    prob = api.make_problem(N, D, V, hidden_dtype=h.dtype, bias_dtype=b.dtype if b is not None else torch.bfloat16,
+                            logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction, bwd="keep_logits")
+    f32, hb = 4, h.element_size()
+    sizes = {"loss": (N if w.reduction == "none" else 1) * f32, "lse": N * f32, "ent": N * f32, "corr": 8, "nv": 8,
+             "es": f32, "ws": api.flce_workspace_size(prob, 2), "dh": N * D * hb, "dW": V * D * 2,
+             "db": V * b.element_size() if b is not None else 0}
+    bufs = {k: _guarded(v) for k, v in sizes.items()}
+    p = {k: ctypes.c_void_p(v.data_ptr()) for k, v in bufs.items()}
+    ptr = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    B.check(B.load().flce_forward_backward(ctypes.byref(prob), ptr(h), ptr(W), ptr(b), ptr(t), ptr(dloss), p["loss"],
+                                           p["lse"], p["ent"], p["corr"], p["nv"], p["es"], p["dh"], p["dW"],
+                                           p["db"] if b is not None else None, p["ws"], sizes["ws"], s),
+            "forward_backward")
+    torch.cuda.synchronize()
+    for k, buf in bufs.items():
+        assert torch.all(buf[sizes[k]:] == CANARY), f"write past the end of {k}"
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    ref_b = oracle.backward(hc, Wc, bc, tc, dloss=dc, **kw)
     dh = bufs["dh"][:sizes["dh"]].view(h.dtype).view(N, D)
     dW = bufs["dW"][:sizes["dW"]].view(torch.bfloat16).view(V, D)
     db = None if b is None else bufs["db"][:sizes["db"]].view(b.dtype)
