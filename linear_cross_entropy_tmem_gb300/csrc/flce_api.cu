@@ -209,7 +209,7 @@ int token_dh_ksplit_bound(int64_t nc, int64_t hidden) {
   const int forced = g_force_dh_ksplit.load();
   if (forced > 0) return std::min(forced, kMaxKSplit);
   const int64_t tiles = cdiv(nc, kBM) * cdiv(hidden, kBN);
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxKSplit, cdiv(2048, tiles))));
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxKSplit, cdiv(4096, tiles))));
 }
 
 // [status][hi, lo][forward records of one chunk][kept logits][G][dbias
@@ -728,7 +728,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
 }
 
 // K splits of one token chunk's dh product: the fewest that fill the device's
-// CTAs (or clusters) within 2 % of the best wave efficiency.
+// CTAs (or clusters) within 1 % of the best wave efficiency.
 int choose_token_ksplit(int64_t tiles, int ctas, int bound) {
   if (g_force_dh_ksplit.load() > 0) return bound;
   double best = 0.0;
@@ -739,7 +739,7 @@ int choose_token_ksplit(int64_t tiles, int ctas, int bound) {
     best = std::max(best, eff[k]);
   }
   for (int k = 1; k <= bound; ++k)
-    if (eff[k] >= best - 0.02) return k;
+    if (eff[k] >= best - 0.01) return k;
   return 1;
 }
 
@@ -872,7 +872,11 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     s3.b_mn = 1;
     s3.ksplit = ksplit;
     s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
-    s3.group_m = std::max(1, dh_ctas / std::max(1, s3.n_tiles * ksplit));
+    // K = V: the head and the chunk's G (each ~ V * D or rows * V bf16) stream
+    // from HBM; all m tiles run together over one K slice so that each W
+    // slice is read once per chunk and each G slice once per few n tiles.
+    s3.group_m = 16;
+    s3.ks_outer = 1;
     finish_sched(s3);
     uint8_t* dh_out = static_cast<uint8_t*>(dhidden) + size_t(r0) * D * out_elem;
     AccumParams ap{};

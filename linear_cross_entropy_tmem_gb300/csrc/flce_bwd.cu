@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kZGradThreads) zgrad_kernel(ZGradParams p) {
     pk.y = pack_bf16x2(g[2], g[3]);
     pk.z = pack_bf16x2(g[4], g[5]);
     pk.w = pack_bf16x2(g[6], g[7]);
-    *reinterpret_cast<uint4*>(gp + r * p.ldz) = pk;
+    __stcs(reinterpret_cast<uint4*>(gp + r * p.ldz), pk);
   }
   if (p.dbias_part) {
     float* dst = p.dbias_part + static_cast<int64_t>(blockIdx.y) * p.ldz + c0;

@@ -304,6 +304,14 @@ __device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, ui
                "r"(e), "r"(f), "r"(g), "r"(h)
                : "memory");
 }
+// Streaming variant: the lines are allocated evict-first, for data that is
+// not read again before it would leave L2 anyway (kept logits, G, fp32 slots).
+__device__ __forceinline__ void st_global_v8_cs(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                                uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+               "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
 __device__ __forceinline__ void ld_global_v8(const void* p, uint32_t (&r)[8]) {
   asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])

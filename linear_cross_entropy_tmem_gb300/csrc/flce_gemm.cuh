@@ -75,8 +75,13 @@ __device__ __forceinline__ Unit decode_unit(const GemmSched& sc, int u, int rows
   const int rest = r / gm;
   Unit t;
   t.m_blk = m0 + m_local;
-  t.ks = rest % sc.ksplit;
-  t.n_unit = rest / sc.ksplit;
+  if (sc.ks_outer) {  // units running together share one K slice (long K, operands far beyond L2)
+    t.n_unit = rest % sc.n_units;
+    t.ks = rest / sc.n_units;
+  } else {
+    t.ks = rest % sc.ksplit;
+    t.n_unit = rest / sc.ksplit;
+  }
   t.n_first = t.n_unit * sc.n_per_unit;
   t.n_count = min(sc.n_per_unit, sc.n_tiles - t.n_first);
   t.kb_first = t.ks * sc.kb_per_split;
@@ -245,8 +250,8 @@ struct EpiFwd {
         const auto u = [&](int j) { return __float_as_uint(z[j]); };
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          st_global_v8(dst + 8 * q, u(8 * q), u(8 * q + 1), u(8 * q + 2), u(8 * q + 3), u(8 * q + 4), u(8 * q + 5),
-                       u(8 * q + 6), u(8 * q + 7));
+          st_global_v8_cs(dst + 8 * q, u(8 * q), u(8 * q + 1), u(8 * q + 2), u(8 * q + 3), u(8 * q + 4),
+                          u(8 * q + 5), u(8 * q + 6), u(8 * q + 7));
       }
       if (ragged) {
 #pragma unroll
@@ -546,8 +551,13 @@ struct EpiAccum {
         }
       }
       const auto u = [&](int j) { return __float_as_uint(v[j]); };
-      if (!p.write_final || p.out_f32) {
-        float* dst = !p.write_final ? slot : reinterpret_cast<float*>(p.out) + orow * p.cols + col;
+      if (!p.write_final) {  // fp32 slot (32-byte aligned), read back by a later launch
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_global_v8_cs(slot + 8 * q, u(8 * q), u(8 * q + 1), u(8 * q + 2), u(8 * q + 3), u(8 * q + 4),
+                          u(8 * q + 5), u(8 * q + 6), u(8 * q + 7));
+      } else if (p.out_f32) {
+        float* dst = reinterpret_cast<float*>(p.out) + orow * p.cols + col;
         if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {  // the caller's output is only 16-byte aligned
 #pragma unroll
           for (int q = 0; q < 4; ++q)

@@ -68,6 +68,7 @@ struct GemmSched {
   int32_t n_per_unit;
   int32_t n_units;        // ceil(n_tiles / n_per_unit)
   int32_t group_m;
+  int32_t ks_outer;       // 0: within a group of m tiles the K split varies fastest after m; 1: the n unit does
   int32_t total_units;
   int32_t a_mn, b_mn;     // operand majorness: 0 = K-major, 1 = MN-major
   int32_t a_mn_off, a_k_off;   // coordinate offsets into the A tensor map

@@ -1,5 +1,6 @@
 """GPU parity at the five benchmark sizes, in the launch configuration bench.py
-times (same planner, same seeded device draws).
+times (the fused call with its automatic backward, same planner, same seeded
+device draws), plus flce_forward + flce_backward and valid-token compaction.
 
 Per-token outputs are compared on every token against the oracle's forward run
 over groups of tokens; the scalar outputs against its sums.  Gradients are
@@ -20,17 +21,29 @@ from tests.parity import (TOL_ENT, TOL_GRAD, TOL_LOSS, TOL_LSE, near_tie_bounds_
 pytestmark = [pytest.mark.gpu, pytest.mark.fullsize]
 
 
-@pytest.mark.parametrize("name,compact", [("tiny", False), ("chunk", False), ("commandr", False), ("gemma", False),
-                                          ("qwen8b", False), ("commandr", True)],
-                         ids=["tiny", "chunk", "commandr", "gemma", "qwen8b", "commandr-compact"])
-def test_parity_full_size(name, compact):
+def _run(h, W, b, t, dloss, entry, compact, kw):
+    """The fused call (automatic backward: kept logits from D = 1024 up, else the recompute), as
+    bench.py times it, or flce_forward followed by flce_backward."""
+    import linear_cross_entropy_tmem_gb300 as F
+    if entry == "separate":
+        gpu = run_gpu(h, W, b, t, dloss, compact=compact, **kw)
+        return gpu["status"], gpu["fwd"], gpu["bwd"]
+    fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, compact=compact, **kw)
+    torch.cuda.synchronize()
+    return F.flce_read_device_status(fwd.workspace), fwd, grads
+
+
+@pytest.mark.parametrize("name,compact,entry", [
+    ("tiny", False, "fused"), ("chunk", False, "fused"), ("commandr", False, "fused"), ("gemma", False, "fused"),
+    ("qwen8b", False, "fused"), ("qwen8b", False, "separate"), ("commandr", True, "fused")],
+    ids=["tiny", "chunk", "commandr-keep-logits", "gemma", "qwen8b-keep-logits", "qwen8b-separate",
+         "commandr-compact"])
+def test_parity_full_size(name, compact, entry):
     w = WORKLOADS[name]
     h, W, b, t, dloss = make_inputs(w, "cuda")
     kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
-    gpu = run_gpu(h, W, b, t, dloss, compact=compact, **kw)
-    assert gpu["status"] == 0
-    f = gpu["fwd"]
-    dh, dW, db = gpu["bwd"]
+    status, f, (dh, dW, db) = _run(h, W, b, t, dloss, entry, compact, kw)
+    assert status == 0
     g = torch.Generator().manual_seed(1234)
     rows = torch.randperm(w.n_tokens, generator=g)[:64].sort().values
     vrows = torch.randperm(w.vocab, generator=g)[:64].sort().values
@@ -42,7 +55,7 @@ def test_parity_full_size(name, compact):
     db_g = db[vrows.cuda()].cpu() if db is not None else None
     hc, Wc, tc, dlc = h.cpu(), W.cpu(), t.cpu(), dloss.cpu()
     bc = b.cpu() if b is not None else None
-    del h, W, b, t, dloss, dh, dW, db, gpu
+    del h, W, b, t, dloss, dh, dW, db
     torch.cuda.empty_cache()
 
     ref = oracle_forward_rowblocks(hc, Wc, bc, tc, **kw)
