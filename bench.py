@@ -22,6 +22,7 @@ import ctypes
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -296,24 +297,29 @@ class Runner:
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources with comments and whitespace removed, so that documentation edits
+    keep committed counters valid while any code change invalidates them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_cross_entropy_tmem_gb300", "csrc")
+    strip = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode())
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            code = "".join(strip.sub("", fh.read()).split())
+        h.update(f.encode())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kind, workload):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+def committed_traffic(kind, workload, backward):
+    """DRAM bytes per launch from the committed ncu summary (workload -> backward algorithm ->
+    launch kind), if taken on the current kernels."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh)
     except (OSError, ValueError):
         return None
-    e = rec.get(workload, {}).get(kind)
+    e = rec.get(workload, {}).get(backward, {}).get(kind)
     if not e or e.get("kernel_source_hash") != kernel_source_hash():
         return None
     return e.get("dram_bytes_per_launch")
@@ -396,7 +402,9 @@ def flce_arm(args):
         d = per_kind.setdefault(k, [0, 0.0])
         d[0] += 1
         d[1] += events[i][0].elapsed_time(events[i][1])
-    flops_kind = 2.0 * w.n_tokens * w.vocab * w.hidden  # per step, for each GEMM kind
+    # Tokens the products run over: all of them, or the valid ones under compaction.
+    rows_mult = int(run.n_valid.item()) if args.compact else w.n_tokens
+    flops_kind = 2.0 * rows_mult * w.vocab * w.hidden  # per step, for each GEMM kind
     gemm_kinds = [k for k in per_kind if k not in ("other", "bwd_logit_grad")]
     keep = "bwd_logit_grad" in per_kind  # the token-chunked backward ran (6NVD instead of 8NVD)
     zgrad_bytes = 6.0 * w.n_tokens * w.vocab  # per step: fp32 logits read, bf16 G written
@@ -411,7 +419,8 @@ def flce_arm(args):
     tokens = w.n_tokens * world
     value = tokens / (ms_max * 1e-3)
     tflops = w.flops() * world / (ms_max * 1e-3) / 1e12
-    tflops_exec = tflops * (0.75 if keep else 1.0)
+    exec_flops = 8.0 * rows_mult * w.vocab * w.hidden * (0.75 if keep else 1.0)
+    tflops_exec = exec_flops * world / (ms_max * 1e-3) / 1e12
 
     # ---- end to end through host buffers: H2D inputs, step, D2H loss + metrics
     e2e = None
@@ -470,12 +479,13 @@ def flce_arm(args):
             # accounting counts 8NVD per forward + backward whatever the algorithm
             "tflops": tflops_exec,
             "tflops_8nvd_accounting": tflops,
-            "flops_per_step": {"executed": w.flops() * (0.75 if keep else 1.0), "metric_8nvd": w.flops()},
+            "flops_per_step": {"executed": exec_flops, "metric_8nvd": w.flops()},
             "pct_of_peak": {"of_burst": tflops_exec / peak_burst, "of_sustained": tflops_exec / peak,
                             "source": peak_src, "flops": "executed"},
             "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
                          "peak_kind": f"bf16 sustained ({peak_src})", "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": committed_traffic(dominant, args.workload),
+                         "traffic": committed_traffic(dominant, args.workload, "keep_logits" if keep else "recompute")
+                         if not (args.tokens or args.vocab or args.compact) else None,
                          "launches": n_l, "avg_launch_ms": t_ms / n_l},
             "kernels": {k: {"launches": v[0], "ms_per_step": v[1] / args.steps,
                             "tflops": (flops_kind * args.steps / (v[1] * 1e-3) / 1e12) if k in gemm_kinds else None,

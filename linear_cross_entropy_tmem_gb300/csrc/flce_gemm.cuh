@@ -1,24 +1,27 @@
 // flce_gemm.cuh — the persistent, warp-specialised tcgen05 GEMM that every
 // product of the fused linear cross-entropy runs on, and its epilogues.
 //
-//   warp 4      TMA producer: fills a 4-stage shared-memory ring with 128-byte
-//               swizzled bf16 tiles of A (128 x 64) and B (256 x 64).
-//   warp 5      MMA issuer: one elected thread issues tcgen05.mma (M=128,
-//               N=256, K=16) into one of two TMEM accumulators (2 x 256 fp32
-//               columns) and commits stage releases / accumulator-ready
-//               signals to mbarriers.  The whole warp owns the TMEM allocation.
-//   warps 0-3   epilogue: thread i owns TMEM lane i (one output row), reads 32
-//               columns at a time with tcgen05.ld and runs the epilogue policy
-//               while the MMA of the next tile fills the other accumulator.
+//   warp 8      TMA producer: fills a shared-memory ring with 128-byte swizzled
+//               bf16 tiles of A and B (4 stages of 128x64 + 256x64 for one CTA;
+//               6 stages of 128x64 + its 128x64 half of B per CTA of a pair).
+//   warp 9      MMA issuer: one elected thread issues tcgen05.mma (M=128 or,
+//               for a CTA pair, M=256; N=256; K=16) into one of two TMEM
+//               accumulators (2 x 256 fp32 columns) and commits stage releases
+//               and accumulator-ready signals to mbarriers.  The whole warp owns
+//               the TMEM allocation.
+//   warps 0-7   two epilogue groups in ping-pong: group g owns accumulator g
+//               and takes every other tile; thread i of a group owns TMEM lane i
+//               (one output row) and reads 32 columns at a time with tcgen05.ld.
 //
 // Epilogue policies:
 //   EpiFwd    logits -> bias, scale, soft cap -> online (max, sum exp,
 //             sum exp*z, argmax, target logit) per token across a vocabulary
-//             split; one partial record per (split, token).
+//             split, one record per (split, group, token); optionally keeps z.
 //   EpiGrad   recomputed logits -> G = w_n (softmax - onehot) dz/dacc in bf16
 //             for one vocabulary chunk, plus per-tile dbias column sums.
 //   EpiStore  accumulator -> bf16 / fp32 store (dW; the test GEMM).
-//   EpiAccum  accumulator -> fp32 K-split slot (=, +=) or the final dh store.
+//   EpiAccum  accumulator -> fp32 slot (=, +=) or the final store (dh; dW of
+//             the token-chunked backward).
 //
 // Every wait is bounded (see mbar_wait); a role that gives up raises a
 // CTA-wide abort flag, the others stop at their next wait, in-flight copies
