@@ -93,8 +93,8 @@ enum {
    *   (TRL PR #6863, opening section: token chunks whose logits come from a
    *   bf16 tensor-core product and are held in fp32).  6*N*V*D flops, at the
    *   price of about 6 bytes of scratch per logit of a chunk plus a 4*V*D-byte
-   *   fp32 dweight accumulator.  Needs N > 256 (else the recompute runs) and
-   *   cannot be combined with FLCE_FLAG_COMPACT_VALID (FLCE_ERR_INVALID_ARG).
+   *   fp32 dweight accumulator.  Needs N > 256 (else the recompute runs).  With
+   *   FLCE_FLAG_COMPACT_VALID the chunks cut the gathered valid tokens.
    */
   FLCE_FLAG_BWD_RECOMPUTE = 2u,
   FLCE_FLAG_BWD_KEEP_LOGITS = 4u

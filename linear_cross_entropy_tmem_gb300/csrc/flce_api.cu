@@ -30,7 +30,6 @@ constexpr size_t kGChunkBudget = size_t(1) << 30;  // bytes of the bf16 G chunk
 // logit of the extra pass over the kept logits).
 constexpr size_t kLogitChunkBudget = size_t(4) << 30;
 constexpr int64_t kKeepLogitsMinHidden = 1024;
-constexpr int64_t kTokenChunkAlign = 256;          // rows; a multiple of kMergeThreads and kZGradRows
 constexpr int kMaxDevices = 64;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -103,7 +102,6 @@ int validate(const flce_problem* p) {
   constexpr uint32_t kKnownFlags = FLCE_FLAG_COMPACT_VALID | FLCE_FLAG_BWD_RECOMPUTE | FLCE_FLAG_BWD_KEEP_LOGITS;
   if ((p->flags & ~kKnownFlags) != 0 || p->reserved != 0) return FLCE_ERR_INVALID_ARG;
   if ((p->flags & FLCE_FLAG_BWD_RECOMPUTE) && (p->flags & FLCE_FLAG_BWD_KEEP_LOGITS)) return FLCE_ERR_INVALID_ARG;
-  if ((p->flags & FLCE_FLAG_BWD_KEEP_LOGITS) && (p->flags & FLCE_FLAG_COMPACT_VALID)) return FLCE_ERR_INVALID_ARG;
   if (p->hidden % 8 != 0) return FLCE_ERR_MISALIGNED;
   return FLCE_OK;
 }
@@ -138,6 +136,7 @@ struct Layout {
   int64_t n_tchunks = 0;
   int64_t ldz = 0;        // row stride of the kept logits and of G (elements)
   size_t z = 0, zg = 0, dw_acc = 0;
+  size_t c_chunk_rows = 0;  // under compaction: valid rows of each token chunk
 };
 
 // Test/tuning overrides (flce_testing_set_tuning, flce_testing_set_gemm_mode); 0 = automatic.
@@ -185,7 +184,6 @@ bool keep_logits(const flce_problem* p) {
   if (p->flags & FLCE_FLAG_BWD_RECOMPUTE) return false;
   if (p->n_tokens <= kTokenChunkAlign) return false;  // fewer than two chunks
   if (p->flags & FLCE_FLAG_BWD_KEEP_LOGITS) return true;
-  if (compact(p)) return false;
   return p->hidden >= kKeepLogitsMinHidden;
 }
 
@@ -231,6 +229,18 @@ Layout make_token_layout(const flce_problem* p, bool has_bias) {
   L.nc = token_chunk_rows(N, V);
   L.n_tchunks = cdiv(N, L.nc);
   L.ldz = logit_row_stride(V);
+  if (compact(p)) {  // the chunks run over the compacted tokens
+    const size_t blocks = size_t(cdiv(N, kCompactBlock));
+    L.c_count = take(4);
+    L.c_blocks = take(blocks * 4);
+    L.c_offsets = take(blocks * 4);
+    L.c_map = take(size_t(N) * 4);
+    L.c_targets = take(size_t(N) * 8);
+    if (p->hidden_dtype != FLCE_F32) L.c_hidden = take(size_t(N) * D * 2);
+    L.c_lse = take(size_t(N) * 4);
+    L.c_dloss = take(size_t(N) * 4);
+    L.c_chunk_rows = take(size_t(L.n_tchunks) * 4);
+  }
   const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN)) * kEpilogueGroups;
   const size_t part = size_t(splits) * L.nc * 4;
   L.part_m = take(part);
@@ -763,6 +773,16 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
   float* dbias_part = bias ? reinterpret_cast<float*>(ws + L.dbias_part) : nullptr;
   float* dh_part = L.need_dh_part ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
   BlockPartial* blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
+  // Under compaction the chunks cut the compacted tokens: chunk c holds
+  // chunk_rows[c] of them (device-side), its outputs go through the row map,
+  // and ignored tokens keep a zero dhidden row.
+  int32_t* chunk_rows = pr.cmp ? reinterpret_cast<int32_t*>(ws + L.c_chunk_rows) : nullptr;
+  if (pr.cmp) {
+    FLCE_TRY(fail(cudaMemsetAsync(dhidden, 0, size_t(N) * D * out_elem, st)));
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+      return launch_chunk_rows(pr.row_count, L.nc, static_cast<int>(L.n_tchunks), chunk_rows, st);
+    }));
+  }
 
   // The mean's denominator is needed by the first chunk's gradient.
   if (p->reduction == FLCE_RED_MEAN && !(p->num_items_in_batch > 0.0)) {
@@ -785,6 +805,8 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     const uint8_t* a_main = static_cast<const uint8_t*>(pr.a_main) + size_t(r0) * D * 2;
     const uint8_t* a_lo = h32 ? reinterpret_cast<const uint8_t*>(pr.lo) + size_t(r0) * D * 2 : nullptr;
     const int64_t* tgt = pr.tgt + r0;
+    const int32_t* lim = pr.cmp ? chunk_rows + c : nullptr;      // valid rows of the chunk (device)
+    const int32_t* rmap = pr.cmp ? pr.row_map + r0 : nullptr;   // chunk row -> token
 
     // (1) logits of the chunk: online statistics, and z kept in fp32
     const bool pair_f = use_pair(rows, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
@@ -799,6 +821,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     const int splits = choose_splits(sf.m_tiles, sf.n_tiles, pair_f ? dev.num_sms / 2 : dev.num_sms, &per_unit);
     sf.n_per_unit = per_unit;
     sf.group_m = pair_f ? 16 : 32;
+    sf.m_limit = lim;
     finish_sched(sf);
     FwdParams fp{};
     fp.n_tokens = rows;
@@ -836,10 +859,14 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     mp.part_idx = fp.part_idx;
     mp.z_target = fp.z_target;
     mp.targets = tgt;
-    mp.lse = lse + r0;
-    mp.entropy = entropy ? entropy + r0 : nullptr;
-    mp.loss_tok = none ? loss + r0 : nullptr;
+    const int64_t o0 = pr.cmp ? 0 : r0;  // with a row map the merge writes token rows
+    mp.lse = lse + o0;
+    mp.entropy = entropy ? entropy + o0 : nullptr;
+    mp.loss_tok = none ? loss + o0 : nullptr;
     mp.blocks = blocks + r0 / kMergeThreads;  // r0 % kMergeThreads == 0
+    mp.row_map = rmap;
+    mp.row_count = lim;
+    mp.lse_compact = pr.cmp ? pr.c_lse + r0 : nullptr;
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_merge(mp, status, st); }));
 
     // (2) G and the dbias partials from the kept logits
@@ -855,8 +882,9 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     zp.inv_softcap = fp.inv_softcap;
     zp.ignore_index = p->ignore_index;
     zp.targets = tgt;
-    zp.lse = lse + r0;
-    zp.dloss = none ? dloss + r0 : dloss;
+    zp.lse = pr.cmp ? pr.c_lse + r0 : lse + r0;
+    zp.dloss = none ? (pr.c_dloss ? pr.c_dloss : dloss) + r0 : dloss;
+    zp.row_limit = lim;
     zp.n_valid = n_valid;
     zp.num_items = static_cast<float>(p->num_items_in_batch);
     zp.dbias_part = dbias_part ? dbias_part + (r0 / kZGradRows) * L.ldz : nullptr;
@@ -877,8 +905,9 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     // slice is read once per chunk and each G slice once per few n tiles.
     s3.group_m = 16;
     s3.ks_outer = 1;
+    s3.m_limit = lim;
     finish_sched(s3);
-    uint8_t* dh_out = static_cast<uint8_t*>(dhidden) + size_t(r0) * D * out_elem;
+    uint8_t* dh_out = static_cast<uint8_t*>(dhidden) + (pr.cmp ? 0 : size_t(r0) * D * out_elem);
     AccumParams ap{};
     ap.rows = rows;
     ap.cols = D;
@@ -888,11 +917,13 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     ap.write_final = ksplit == 1 ? 1 : 0;
     ap.out = dh_out;
     ap.out_f32 = h32 ? 1 : 0;
+    ap.row_map = rmap;
+    ap.row_count = lim;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_DHIDDEN, st,
                     [&] { return launch_accum_gemm(pair_dh, mh, s3, ap, status, dev.num_sms, st); }));
     if (ksplit > 1) {
       FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-        return launch_dh_finalize(dh_part, rows * D, ksplit, rows, D, dh_out, h32 ? 1 : 0, nullptr, nullptr,
+        return launch_dh_finalize(dh_part, rows * D, ksplit, rows, D, dh_out, h32 ? 1 : 0, rmap, lim,
                                   dev.num_sms * 4, st);
       }));
     }
@@ -908,6 +939,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     s2.a_mn = 1;
     s2.b_mn = 1;
     s2.group_m = std::max(1, dw_ctas / std::max(1, s2.n_tiles));
+    s2.k_limit = lim;
     finish_sched(s2);
     AccumParams aw{};
     aw.rows = V;
@@ -926,7 +958,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
   if (bias) {
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
       return launch_dbias_reduce(dbias_part, L.ldz, static_cast<int>(cdiv(N, kZGradRows)), V, dbias,
-                                 p->bias_dtype == FLCE_F32, nullptr, st);
+                                 p->bias_dtype == FLCE_F32, pr.row_count, st);
     }));
   }
   return FLCE_OK;

@@ -38,7 +38,15 @@ __global__ void __launch_bounds__(kZGradThreads) zgrad_kernel(ZGradParams p) {
   __shared__ float s_wd[kZGradRows];    // w_n * s (0 at ignored rows)
   __shared__ int64_t s_t[kZGradRows];   // target column
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kZGradRows;
-  const int rows = p.rows - r0 < kZGradRows ? static_cast<int>(p.rows - r0) : kZGradRows;
+  int64_t lim = p.rows, lim_pad = p.rows;  // rows with a logit; rows the GEMMs read
+  if (p.row_limit) {
+    lim = *p.row_limit < p.rows ? *p.row_limit : p.rows;
+    lim_pad = (lim + kTokenChunkAlign - 1) / kTokenChunkAlign * kTokenChunkAlign;
+    if (lim_pad > p.rows) lim_pad = p.rows;
+  }
+  if (r0 >= lim_pad) return;
+  const int rows = lim - r0 < kZGradRows ? static_cast<int>(lim - r0 > 0 ? lim - r0 : 0) : kZGradRows;
+  const int zero_rows = lim_pad - r0 < kZGradRows ? static_cast<int>(lim_pad - r0) : kZGradRows;
   for (int i = threadIdx.x; i < kZGradRows; i += kZGradThreads) {
     float lse2 = 0.f, wd = 0.f;
     int64_t t = -1;
@@ -90,6 +98,8 @@ __global__ void __launch_bounds__(kZGradThreads) zgrad_kernel(ZGradParams p) {
     pk.w = pack_bf16x2(g[6], g[7]);
     __stcs(reinterpret_cast<uint4*>(gp + r * p.ldz), pk);
   }
+  for (int r = rows; r < zero_rows; ++r)  // past the valid rows of a compacted chunk: exact zeros
+    __stcs(reinterpret_cast<uint4*>(gp + r * p.ldz), make_uint4(0u, 0u, 0u, 0u));
   if (p.dbias_part) {
     float* dst = p.dbias_part + static_cast<int64_t>(blockIdx.y) * p.ldz + c0;
 #pragma unroll

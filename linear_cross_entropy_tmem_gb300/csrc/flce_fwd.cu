@@ -155,6 +155,20 @@ cudaError_t launch_count_valid(const int64_t* targets, int64_t n, int64_t vocab,
   return cudaGetLastError();
 }
 
+// Rows of each token chunk under compaction: out[c] = clamp(count - c * rows_per_chunk, 0, rows_per_chunk).
+__global__ void chunk_rows_kernel(const int32_t* count, int64_t rows_per_chunk, int n_chunks, int32_t* out) {
+  for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) {
+    const int64_t left = static_cast<int64_t>(*count) - c * rows_per_chunk;
+    out[c] = static_cast<int32_t>(left <= 0 ? 0 : (left < rows_per_chunk ? left : rows_per_chunk));
+  }
+}
+
+cudaError_t launch_chunk_rows(const int32_t* count, int64_t rows_per_chunk, int n_chunks, int32_t* out,
+                              cudaStream_t stream) {
+  chunk_rows_kernel<<<1, 256, 0, stream>>>(count, rows_per_chunk, n_chunks, out);
+  return cudaGetLastError();
+}
+
 // Final scalars from the block partials, in a fixed order (one block).
 __global__ void __launch_bounds__(256) fwd_reduce_kernel(ReduceParams p) {
   double loss_d = 0.0, ent_d = 0.0;

@@ -133,8 +133,12 @@ constexpr int kZGradThreads = 256;
 constexpr int kZGradVec = 8;                               // columns per thread
 constexpr int kZGradCols = kZGradThreads * kZGradVec;      // 2048
 constexpr int kZGradRows = kBM;                            // rows per block = dbias partial granularity
+constexpr int kTokenChunkAlign = 256;  // token chunks start on multiples of this (>= any GEMM tile height)
 struct ZGradParams {
   int64_t rows, vocab;    // rows of this chunk
+  // Under compaction: rows at or past *row_limit get G = 0 up to the next
+  // multiple of kTokenChunkAlign (the GEMMs read that far) and nothing past it.
+  const int32_t* row_limit;
   const float* z;         // [rows][ldz] fp32
   int64_t ldz;
   uint16_t* g;            // [rows][ldz] bf16

@@ -63,6 +63,9 @@ cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
                               int* status, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream);
+// Under compaction, the valid rows of each token chunk of the kept-logits backward.
+cudaError_t launch_chunk_rows(const int32_t* count, int64_t rows_per_chunk, int n_chunks, int32_t* out,
+                              cudaStream_t stream);
 // n_valid[0] = number of targets in [0, vocab) other than ignore_index (one block).
 cudaError_t launch_count_valid(const int64_t* targets, int64_t n, int64_t vocab, int64_t ignore_index,
                                int64_t* n_valid, cudaStream_t stream);

@@ -117,6 +117,12 @@ def test_keep_logits_workspace(lib):
         if N * V >= 1 << 28:  # the chunk's kept logits + G stay within the 4 GiB budget (+ one row group)
             assert k - 4 * V * D - 16 * 4 * half * D - 4 * ((N + 127) // 128) * ldz <= (4 << 30) + 6 * 256 * ldz \
                 + (5 * 4 * 64 * 2 + 8) * half + (1 << 20)
+    # with compaction the layout adds the compaction buffers (row map, targets, hidden copy,
+    # compacted lse / upstream grads, chunk row counts), about (4 + 8 + 2 D + 4 + 4) bytes per token
+    for (N, D, V) in [(16384, 4096, 151936), (8192, 2048, 128256), (700, 256, 3000)]:
+        k = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=keep), 2)[1]
+        st, kc = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=keep | B.FLCE_FLAG_COMPACT_VALID), 2)
+        assert st == B.FLCE_OK and k < kc <= k + N * (20 + 2 * D) + (1 << 16)
     # with N <= 256 there are no two chunks: the recompute runs and sizes its workspace
     for N in (1, 100, 256):
         pk, pr = (_problem(n_tokens=N, hidden=2048, vocab=248320, flags=f) for f in (keep, rec))
@@ -137,7 +143,6 @@ def test_keep_logits_workspace(lib):
     (dict(num_items_in_batch=float("inf")), B.FLCE_ERR_INVALID_ARG),
     (dict(flags=8), B.FLCE_ERR_INVALID_ARG),
     (dict(flags=B.FLCE_FLAG_BWD_RECOMPUTE | B.FLCE_FLAG_BWD_KEEP_LOGITS), B.FLCE_ERR_INVALID_ARG),
-    (dict(flags=B.FLCE_FLAG_BWD_KEEP_LOGITS | B.FLCE_FLAG_COMPACT_VALID), B.FLCE_ERR_INVALID_ARG),
     (dict(reserved=1), B.FLCE_ERR_INVALID_ARG),
 ])
 def test_problem_validation(lib, kw, code):

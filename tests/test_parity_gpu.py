@@ -343,8 +343,33 @@ def test_keep_logits_parity(name, mode, chunk):
     compare_backward(grads, ref_b)
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["auto", "single-cta", "cta-pair"])
+@pytest.mark.parametrize("ignore_every", [17, 3])
+@pytest.mark.parametrize("name", [n for n in COMPACT_CASES if CASES[n][0].n_tokens > 256])
+def test_keep_logits_with_compaction(name, ignore_every, mode):
+    """Kept logits over the compacted tokens: 256-row chunks of the valid tokens (a partial chunk
+    and, with a third of the tokens ignored, chunks with no valid row at all)."""
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_token_chunk, testing_set_tuning
+    w, tuning = CASES[name]
+    w = w.scaled(ignore_every=ignore_every)
+    testing_set_gemm_mode(mode)
+    testing_set_tuning(*tuning)
+    testing_set_token_chunk(256)
+    h, W, b, t, dloss = make_inputs(w, "cpu")
+    dev = [x.cuda() if x is not None else None for x in (h, W, b, t, dloss)]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    (fwd, grads), kinds = launch_kinds(lambda: F.flce_forward_backward(
+        dev[0], dev[1], dev[3], dev[4], dev[2], entropy=True, compact=True, bwd="keep_logits", **kw))
+    assert F.flce_read_device_status(fwd.workspace) == 0
+    assert kinds.count("bwd_logit_grad") >= 2 and "bwd_recompute" not in kinds
+    _compare_compacted({"fwd": fwd, "bwd": grads}, oracle.forward(h, W, b, t, **kw),
+                       oracle.backward(h, W, b, t, dloss=dloss, **kw), t, w.reduction)
+
+
+@pytest.mark.parametrize("compact", [False, True], ids=["all-tokens", "compact"])
 @pytest.mark.parametrize("reduction,items", [("mean", 0.0), ("mean", 700.0), ("sum", 0.0), ("none", 0.0)])
-def test_keep_logits_reductions_and_all_ignored(reduction, items):
+def test_keep_logits_reductions_and_all_ignored(reduction, items, compact):
     """The mean's denominator (counted before the first chunk, or num_items_in_batch), the other
     reductions, and an all-ignored batch (zero loss, exact zero gradients) on the token path."""
     import linear_cross_entropy_tmem_gb300 as F
@@ -355,11 +380,18 @@ def test_keep_logits_reductions_and_all_ignored(reduction, items):
     for targets in (tc, torch.full_like(tc, -100)):
         h, W, b, t, dloss = [x.cuda() for x in (hc, Wc, bc, targets, dc)]
         kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=reduction, num_items_in_batch=items)
-        fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd="keep_logits", **kw)
+        fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd="keep_logits", compact=compact,
+                                             **kw)
         torch.cuda.synchronize()
         assert F.flce_read_device_status(fwd.workspace) == 0
         ref_f = oracle.forward(hc, Wc, bc, targets, **kw)
         ref_b = oracle.backward(hc, Wc, bc, targets, dloss=dc, **kw)
+        if compact:  # compaction writes lse = entropy = 0 at ignored tokens: compare the valid ones
+            v = torch.from_numpy(ref_f["valid"]).cuda()
+            fwd = fwd._replace(lse=torch.where(v, fwd.lse, 0.0), entropy=torch.where(v, fwd.entropy, 0.0))
+            ref_f = dict(ref_f, lse=np.where(ref_f["valid"], ref_f["lse"], 0.0),
+                         entropy=np.where(ref_f["valid"], ref_f["entropy"], 0.0))
+            assert torch.all(fwd.lse[~v] == 0)
         compare_forward(fwd, ref_f, reduction=reduction)
         if int(ref_f["n_valid"]) == 0:
             assert all(int(torch.count_nonzero(g)) == 0 for g in grads)
