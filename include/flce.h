@@ -97,7 +97,22 @@ enum {
    *   FLCE_FLAG_COMPACT_VALID the chunks cut the gathered valid tokens.
    */
   FLCE_FLAG_BWD_RECOMPUTE = 2u,
-  FLCE_FLAG_BWD_KEEP_LOGITS = 4u
+  FLCE_FLAG_BWD_KEEP_LOGITS = 4u,
+  /*
+   * fp32 operands at full single precision: an fp32 hidden state (and an fp32
+   * head) is split into three bf16 terms, t0 = rn(x), t1 = rn(x - t0),
+   * t2 = rn(x - t0 - t1), which sum to x exactly for |x| >= 2^-100 (below,
+   * the lower terms are subnormal and lose bits); the logit product sums the
+   * term products of total order <= 2 (3 products for fp32 hidden with a bf16
+   * head, 6 with an fp32 head), so it carries the fp32 inputs' 24 bits into the
+   * tensor cores' fp32 accumulation, whose own error (about K/16 units in the
+   * last place of the accumulator) then dominates for long K.  Without it fp32
+   * operands take two terms (about 16 bits: 2 products, or 3 with an fp32
+   * head).  No effect on bf16 operands.
+   * (The pages' fp32 path: TRL PR #6859, review "verified" bullet 3, with the
+   * head cast to the activations' dtype.)
+   */
+  FLCE_FLAG_FP32_FULL = 8u
 };
 
 /* Status codes returned by every call (and stored in the device status word). */
@@ -120,10 +135,14 @@ enum {
  *   hidden     D, 8 <= D, D % 8 == 0 (16-byte rows for the tensor-memory copies)
  *   vocab      V >= 1
  *   hidden_dtype  FLCE_BF16 or FLCE_F32.  fp32 hidden is split on the device
- *                 into a bf16 high part and a bf16 low part whose two products
- *                 are summed (about 16 bits of mantissa).
- *   weight_dtype  FLCE_BF16 (the head is cast to the activation dtype by the
- *                 caller; TRL PR #6859 review, "verified" bullet 3).
+ *                 into bf16 terms whose products are summed: two terms (about
+ *                 16 bits of mantissa), or three with FLCE_FLAG_FP32_FULL.
+ *   weight_dtype  FLCE_BF16, or FLCE_F32 with an fp32 hidden state (the head is
+ *                 cast to the activations' dtype by the caller; TRL PR #6859
+ *                 review, "verified" bullet 3).  bf16 hidden with an fp32
+ *                 head is FLCE_ERR_DTYPE_MISMATCH.  An fp32 head is split on
+ *                 the device into bf16 terms like an fp32 hidden state, and
+ *                 dweight is then fp32.
  *   bias_dtype    FLCE_BF16 or FLCE_F32; ignored when bias is NULL.  The bias
  *                 is added in fp32 after the fp32-accumulated product.
  *   logit_scale   s (1.0f = identity)
@@ -202,7 +221,7 @@ FLCE_API int flce_forward(const flce_problem* problem, const void* hidden, const
  *   n_valid  [1] int64 from flce_forward (the mean's denominator)
  *   dloss    fp32 upstream gradient: [1] for mean / sum, [N] for none
  *   dhidden  [N, D] in hidden_dtype (written, not accumulated), 16-byte aligned
- *   dweight  [V, D] bf16 (written, not accumulated), 16-byte aligned
+ *   dweight  [V, D] in weight_dtype (written, not accumulated), 16-byte aligned
  *   dbias    [V] in bias_dtype; must be NULL exactly when bias is NULL
  *   workspace, workspace_bytes: at least flce_workspace_size(problem, 1)
  * All-ignored batches produce exact zero gradients.

@@ -34,9 +34,10 @@ def make_problem(n_tokens: int, hidden: int, vocab: int, *, hidden_dtype=torch.b
                  weight_dtype=torch.bfloat16, bias_dtype=torch.bfloat16, logit_scale: float = 1.0,
                  softcap: float = 0.0, ignore_index: int = -100, reduction: str = "mean",
                  num_items_in_batch: float = 0.0, compact: bool = False,
-                 bwd: str = "auto") -> B.FlceProblem:
+                 bwd: str = "auto", fp32_full: bool = False) -> B.FlceProblem:
     """``bwd`` picks the backward algorithm of the fused call: "auto", "recompute" or
-    "keep_logits" (token-chunked; see FLCE_FLAG_BWD_KEEP_LOGITS in include/flce.h)."""
+    "keep_logits" (token-chunked; see FLCE_FLAG_BWD_KEEP_LOGITS in include/flce.h).
+    ``fp32_full`` splits fp32 operands into three bf16 terms (FLCE_FLAG_FP32_FULL)."""
     if reduction not in B.REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(B.REDUCTIONS)}")
     if bwd not in B.BWD_ALGOS:
@@ -47,7 +48,8 @@ def make_problem(n_tokens: int, hidden: int, vocab: int, *, hidden_dtype=torch.b
         bias_dtype=_dtype_code(bias_dtype, "bias"), reduction=B.REDUCTIONS[reduction],
         logit_scale=float(logit_scale), final_logit_softcapping=float(softcap), ignore_index=int(ignore_index),
         num_items_in_batch=float(num_items_in_batch),
-        flags=(B.FLCE_FLAG_COMPACT_VALID if compact else 0) | B.BWD_ALGOS[bwd],
+        flags=(B.FLCE_FLAG_COMPACT_VALID if compact else 0) | B.BWD_ALGOS[bwd]
+        | (B.FLCE_FLAG_FP32_FULL if fp32_full else 0),
         reserved=0)
 
 
@@ -92,7 +94,7 @@ def flce_forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tens
                  bias: Optional[torch.Tensor] = None, *, logit_scale: float = 1.0, softcap: float = 0.0,
                  ignore_index: int = -100, reduction: str = "mean", entropy: bool = False,
                  num_items_in_batch: float = 0.0, compact: bool = False,
-                 workspace: Optional[torch.Tensor] = None) -> ForwardResult:
+                 fp32_full: bool = False, workspace: Optional[torch.Tensor] = None) -> ForwardResult:
     """Forward of the fused linear cross-entropy (see ``flce_forward`` in include/flce.h)."""
     _require_cuda(hidden, weight, targets, bias)
     for t, n in ((hidden, "hidden"), (weight, "weight"), (targets, "targets"), (bias, "bias")):
@@ -104,7 +106,8 @@ def flce_forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tens
     prob = make_problem(N, D, V, hidden_dtype=hidden.dtype, weight_dtype=weight.dtype,
                         bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
                         logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
-                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact)
+                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact,
+                        fp32_full=fp32_full)
     dev = hidden.device
     ws = _workspace(flce_workspace_size(prob, False), dev, workspace)
     f32 = dict(dtype=torch.float32, device=dev)
@@ -127,7 +130,7 @@ def flce_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Ten
                   n_valid: torch.Tensor, dloss: torch.Tensor, bias: Optional[torch.Tensor] = None, *,
                   logit_scale: float = 1.0, softcap: float = 0.0, ignore_index: int = -100,
                   reduction: str = "mean", num_items_in_batch: float = 0.0, compact: bool = False,
-                  workspace: Optional[torch.Tensor] = None, outputs=None):
+                  fp32_full: bool = False, workspace: Optional[torch.Tensor] = None, outputs=None):
     """Backward (see ``flce_backward`` in include/flce.h); returns (dhidden, dweight, dbias)."""
     _require_cuda(hidden, weight, targets, lse, n_valid, dloss, bias)
     for t, n in ((hidden, "hidden"), (weight, "weight"), (targets, "targets"), (bias, "bias"), (lse, "lse")):
@@ -137,7 +140,8 @@ def flce_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Ten
     prob = make_problem(N, D, V, hidden_dtype=hidden.dtype, weight_dtype=weight.dtype,
                         bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
                         logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
-                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact)
+                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact,
+                        fp32_full=fp32_full)
     dev = hidden.device
     ws = _workspace(flce_workspace_size(prob, True), dev, workspace)
     dloss = dloss.to(dtype=torch.float32).contiguous().reshape(-1)
@@ -159,7 +163,7 @@ def flce_forward_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: t
                           bias: Optional[torch.Tensor] = None, *, logit_scale: float = 1.0, softcap: float = 0.0,
                           ignore_index: int = -100, reduction: str = "mean", entropy: bool = False,
                           num_items_in_batch: float = 0.0, compact: bool = False, bwd: str = "auto",
-                          workspace: Optional[torch.Tensor] = None):
+                          fp32_full: bool = False, workspace: Optional[torch.Tensor] = None):
     """Forward and backward in one call (see ``flce_forward_backward`` in include/flce.h);
     ``bwd`` as in :func:`make_problem`.
 
@@ -174,7 +178,8 @@ def flce_forward_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: t
     prob = make_problem(N, D, V, hidden_dtype=hidden.dtype, weight_dtype=weight.dtype,
                         bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
                         logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
-                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact, bwd=bwd)
+                        reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact, bwd=bwd,
+                        fp32_full=fp32_full)
     dev = hidden.device
     ws = _workspace(flce_workspace_size(prob, 2), dev, workspace)
     f32 = dict(dtype=torch.float32, device=dev)

@@ -94,12 +94,11 @@ int validate(const flce_problem* p) {
   if (p->reduction < FLCE_RED_NONE || p->reduction > FLCE_RED_MEAN) return FLCE_ERR_INVALID_ARG;
   if (!std::isfinite(p->logit_scale) || !std::isfinite(p->final_logit_softcapping)) return FLCE_ERR_INVALID_ARG;
   if (p->hidden_dtype != FLCE_BF16 && p->hidden_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED_DTYPE;
-  if (p->weight_dtype != FLCE_BF16) {
-    if (p->weight_dtype == FLCE_F32 && p->hidden_dtype == FLCE_BF16) return FLCE_ERR_DTYPE_MISMATCH;
-    return FLCE_ERR_UNSUPPORTED_DTYPE;
-  }
+  if (p->weight_dtype != FLCE_BF16 && p->weight_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED_DTYPE;
+  if (p->weight_dtype == FLCE_F32 && p->hidden_dtype == FLCE_BF16) return FLCE_ERR_DTYPE_MISMATCH;
   if (!std::isfinite(p->num_items_in_batch) || p->num_items_in_batch < 0.0) return FLCE_ERR_INVALID_ARG;
-  constexpr uint32_t kKnownFlags = FLCE_FLAG_COMPACT_VALID | FLCE_FLAG_BWD_RECOMPUTE | FLCE_FLAG_BWD_KEEP_LOGITS;
+  constexpr uint32_t kKnownFlags =
+      FLCE_FLAG_COMPACT_VALID | FLCE_FLAG_BWD_RECOMPUTE | FLCE_FLAG_BWD_KEEP_LOGITS | FLCE_FLAG_FP32_FULL;
   if ((p->flags & ~kKnownFlags) != 0 || p->reserved != 0) return FLCE_ERR_INVALID_ARG;
   if ((p->flags & FLCE_FLAG_BWD_RECOMPUTE) && (p->flags & FLCE_FLAG_BWD_KEEP_LOGITS)) return FLCE_ERR_INVALID_ARG;
   if (p->hidden % 8 != 0) return FLCE_ERR_MISALIGNED;
@@ -107,6 +106,52 @@ int validate(const flce_problem* p) {
 }
 
 bool compact(const flce_problem* p) { return (p->flags & FLCE_FLAG_COMPACT_VALID) != 0; }
+
+// bf16 terms the products read of each operand: 1 for bf16, 2 for fp32 (about
+// 16 significant bits), 3 with FLCE_FLAG_FP32_FULL (all 24).
+int term_count(int32_t dtype, const flce_problem* p) {
+  if (dtype != FLCE_F32) return 1;
+  return (p->flags & FLCE_FLAG_FP32_FULL) ? 3 : 2;
+}
+int h_terms(const flce_problem* p) { return term_count(p->hidden_dtype, p); }
+int w_terms(const flce_problem* p) { return term_count(p->weight_dtype, p); }
+size_t weight_elem(const flce_problem* p) { return p->weight_dtype == FLCE_F32 ? 4 : 2; }
+
+// K segments: (A term, B term) pairs packed for GemmSched::seg_maps.
+uint32_t pack_segments(const int (*pairs)[2], int n) {
+  uint32_t m = 0;
+  for (int i = 0; i < n; ++i) m |= static_cast<uint32_t>(pairs[i][0] | (pairs[i][1] << 2)) << (4 * i);
+  return m;
+}
+// Logit products sum_k h[n,k] W[v,k] over the bf16 terms: every h term with a
+// bf16 head; with an fp32 head the term pairs of total order <= 1 (two-term
+// splits: 3 products) or <= 2 (three-term splits: 6 products).  Every segment
+// runs the whole K range into one accumulator, so the smallest products go
+// first: their partial sums stay small, and the tensor cores' accumulation
+// error (about one ulp of the accumulator per MMA step) is then that of the
+// leading product alone.
+int logit_segments(int nh, int nw, uint32_t* maps) {
+  static const int kPairs2[3][2] = {{1, 0}, {0, 1}, {0, 0}};
+  static const int kPairs3[6][2] = {{2, 0}, {1, 1}, {0, 2}, {1, 0}, {0, 1}, {0, 0}};
+  static const int kHOnly[3][3][2] = {{{0, 0}}, {{1, 0}, {0, 0}}, {{2, 0}, {1, 0}, {0, 0}}};
+  if (nw == 1) {
+    *maps = pack_segments(kHOnly[nh - 1], nh);
+    return nh;
+  }
+  if (nw == 2) {
+    *maps = pack_segments(kPairs2, 3);
+    return 3;
+  }
+  *maps = pack_segments(kPairs3, 6);
+  return 6;
+}
+// Gradient products with G (one bf16 term) as A and the n terms of h or W as
+// B, smallest first.
+int b_term_segments(int n, uint32_t* maps) {
+  static const int kBOnly[3][3][2] = {{{0, 0}}, {{0, 1}, {0, 0}}, {{0, 2}, {0, 1}, {0, 0}}};
+  *maps = pack_segments(kBOnly[n - 1], n);
+  return n;
+}
 
 int check_bias_dtype(const flce_problem* p, const void* bias) {
   if (bias && p->bias_dtype != FLCE_BF16 && p->bias_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED_DTYPE;
@@ -119,7 +164,8 @@ int check_bias_dtype(const flce_problem* p, const void* bias) {
 // ---------------------------------------------------------------------------
 struct Layout {
   size_t status = 0;
-  size_t hi = 0, lo = 0;
+  size_t h_term[3] = {0, 0, 0};  // bf16 terms of an fp32 hidden state
+  size_t w_term[3] = {0, 0, 0};  // bf16 terms of an fp32 head
   size_t part_m = 0, part_s = 0, part_a = 0, part_best = 0, part_idx = 0, z_target = 0, blocks = 0;
   size_t g = 0, dbias_part = 0, dh_part = 0;
   // valid-token compaction
@@ -210,6 +256,13 @@ int token_dh_ksplit_bound(int64_t nc, int64_t hidden) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxKSplit, cdiv(4096, tiles))));
 }
 
+template <class Take>
+void take_terms(const flce_problem* p, Layout& L, Take& take) {
+  const int th = h_terms(p), tw = w_terms(p);
+  for (int i = 0; th > 1 && i < th; ++i) L.h_term[i] = take(size_t(p->n_tokens) * p->hidden * 2);
+  for (int i = 0; tw > 1 && i < tw; ++i) L.w_term[i] = take(size_t(p->vocab) * p->hidden * 2);
+}
+
 // [status][hi, lo][forward records of one chunk][kept logits][G][dbias
 // partials of all row tiles][fp32 dW accumulator][dh K-split slots].
 Layout make_token_layout(const flce_problem* p, bool has_bias) {
@@ -222,10 +275,7 @@ Layout make_token_layout(const flce_problem* p, bool has_bias) {
     off = align_up(off + bytes, 256);
     return at;
   };
-  if (p->hidden_dtype == FLCE_F32) {
-    L.hi = take(size_t(N) * D * 2);
-    L.lo = take(size_t(N) * D * 2);
-  }
+  take_terms(p, L, take);
   L.nc = token_chunk_rows(N, V);
   L.n_tchunks = cdiv(N, L.nc);
   L.ldz = logit_row_stride(V);
@@ -274,10 +324,7 @@ Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
     off = align_up(off + bytes, 256);
     return at;
   };
-  if (p->hidden_dtype == FLCE_F32) {
-    L.hi = take(size_t(N) * D * 2);
-    L.lo = take(size_t(N) * D * 2);
-  }
+  take_terms(p, L, take);
   if (compact(p)) {
     const size_t blocks = size_t(cdiv(N, kCompactBlock));
     L.c_count = take(4);
@@ -285,7 +332,7 @@ Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
     L.c_offsets = take(blocks * 4);
     L.c_map = take(size_t(N) * 4);
     L.c_targets = take(size_t(N) * 8);
-    if (p->hidden_dtype != FLCE_F32) L.c_hidden = take(size_t(N) * D * 2);  // fp32 input compacts into hi / lo
+    if (p->hidden_dtype != FLCE_F32) L.c_hidden = take(size_t(N) * D * 2);  // fp32 input compacts into its terms
     if (kind != kForward) {
       L.c_lse = take(size_t(N) * 4);
       L.c_dloss = take(size_t(N) * 4);
@@ -320,13 +367,13 @@ Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
   return L;
 }
 
-GemmSched base_sched(int64_t m_rows, int64_t n_cols, int64_t k, int nseg, int seg_a, bool pair = false) {
+GemmSched base_sched(int64_t m_rows, int64_t n_cols, int64_t k, int nseg, uint32_t seg_maps, bool pair = false) {
   GemmSched s{};
   s.m_tiles = static_cast<int32_t>(cdiv(m_rows, pair ? kPairRows : kBM));
   s.n_tiles = static_cast<int32_t>(cdiv(n_cols, kBN));
   s.k_blocks = static_cast<int32_t>(cdiv(k, kBK));
   s.nseg = nseg;
-  s.seg_a = seg_a;
+  s.seg_maps = seg_maps;
   s.ksplit = 1;
   s.kb_per_split = s.k_blocks;
   s.n_per_unit = 1;
@@ -450,8 +497,9 @@ namespace {
 // and compacted per-token arrays.
 struct Prep {
   bool h32 = false, cmp = false;
-  const void* a_main = nullptr;
-  uint16_t* lo = nullptr;
+  int nh = 1, nw = 1;                          // bf16 terms of h and of W
+  const void* h[3] = {nullptr, nullptr, nullptr};  // [N][D] bf16 (compacted under compaction)
+  const void* w[3] = {nullptr, nullptr, nullptr};  // [V][D] bf16
   const int32_t* row_count = nullptr;
   const int32_t* row_map = nullptr;
   const int64_t* tgt = nullptr;
@@ -460,16 +508,28 @@ struct Prep {
 };
 
 int prepare(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
-            cudaStream_t st, const void* hidden, const int64_t* targets, const float* lse_in, const float* dloss,
-            float* lse_def, float* ent_def, float* loss_def, Prep* out) {
+            cudaStream_t st, const void* hidden, const void* weight, const int64_t* targets, const float* lse_in,
+            const float* dloss, float* lse_def, float* ent_def, float* loss_def, Prep* out) {
   const int64_t N = p->n_tokens, D = p->hidden;
   Prep r;
   r.h32 = p->hidden_dtype == FLCE_F32;
   r.cmp = compact(p);
   r.tgt = targets;
-  r.a_main = hidden;
-  uint16_t* hi = r.h32 ? reinterpret_cast<uint16_t*>(ws + L.hi) : nullptr;
-  r.lo = r.h32 ? reinterpret_cast<uint16_t*>(ws + L.lo) : nullptr;
+  r.nh = h_terms(p);
+  r.nw = w_terms(p);
+  r.h[0] = hidden;
+  r.w[0] = weight;
+  uint16_t* ht[3] = {nullptr, nullptr, nullptr};
+  for (int i = 0; r.nh > 1 && i < r.nh; ++i) ht[i] = reinterpret_cast<uint16_t*>(ws + L.h_term[i]);
+  if (r.nw > 1) {  // fp32 head: its bf16 terms
+    uint16_t* wt[3] = {nullptr, nullptr, nullptr};
+    for (int i = 0; i < r.nw; ++i) wt[i] = reinterpret_cast<uint16_t*>(ws + L.w_term[i]);
+    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+      return launch_split_f32(static_cast<const float*>(weight), wt[0], wt[1], wt[2], p->vocab * D,
+                              dev.num_sms * 4, st);
+    }));
+    for (int i = 0; i < r.nw; ++i) r.w[i] = wt[i];
+  }
   const bool none = p->reduction == FLCE_RED_NONE;
   if (r.cmp) {
     CompactParams cp{};
@@ -485,8 +545,9 @@ int prepare(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8
     cp.count = reinterpret_cast<int32_t*>(ws + L.c_count);
     cp.row_map = reinterpret_cast<int32_t*>(ws + L.c_map);
     cp.targets_out = reinterpret_cast<int64_t*>(ws + L.c_targets);
-    cp.hc = r.h32 ? hi : reinterpret_cast<uint16_t*>(ws + L.c_hidden);
-    cp.lo = r.lo;
+    cp.hc = r.h32 ? ht[0] : reinterpret_cast<uint16_t*>(ws + L.c_hidden);
+    cp.lo = ht[1];
+    cp.lo2 = ht[2];
     if (L.c_lse) {
       cp.lse_in = lse_in;
       cp.lse_out = reinterpret_cast<float*>(ws + L.c_lse);
@@ -504,12 +565,13 @@ int prepare(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8
     r.row_count = cp.count;
     r.row_map = cp.row_map;
     r.tgt = cp.targets_out;
-    r.a_main = cp.hc;
+    r.h[0] = cp.hc;
+    for (int i = 1; i < r.nh; ++i) r.h[i] = ht[i];
   } else if (r.h32) {
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-      return launch_split_hidden(static_cast<const float*>(hidden), hi, r.lo, N * D, dev.num_sms * 4, st);
+      return launch_split_f32(static_cast<const float*>(hidden), ht[0], ht[1], ht[2], N * D, dev.num_sms * 4, st);
     }));
-    r.a_main = hi;
+    for (int i = 0; i < r.nh; ++i) r.h[i] = ht[i];
   }
   *out = r;
   return FLCE_OK;
@@ -529,19 +591,34 @@ ReduceParams reduce_params(const flce_problem* p, const Layout& L, uint8_t* ws, 
   return rp;
 }
 
+// Tensor maps of the n bf16 terms of one operand ([outer][inner] rows of
+// row_bytes, `offset` bytes into each term); unused slots repeat term 0.
+int make_term_maps(CUtensorMap* m0, CUtensorMap* m1, CUtensorMap* m2, const void* const* terms, int n,
+                   size_t offset, uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                   uint32_t box_outer) {
+  CUtensorMap* m[3] = {m0, m1, m2};
+  for (int i = 0; i < 3; ++i) {
+    if (i < n) {
+      FLCE_TRY(make_map(m[i], static_cast<const uint8_t*>(terms[i]) + offset, inner, outer, row_bytes, box_inner,
+                        box_outer));
+    } else {
+      *m[i] = *m[0];
+    }
+  }
+  return FLCE_OK;
+}
+
 int run_forward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
                 cudaStream_t st, const void* weight, const void* bias, const Prep& pr, float* loss, float* lse,
                 float* entropy, int64_t* correct, int64_t* n_valid, float* entropy_sum, float* lse_compact) {
   const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
   const bool pair = use_pair(N, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
   TmaMaps maps;
-  FLCE_TRY(make_map(&maps.a0, pr.a_main, D, N, D * 2, kBK, kBM));
-  maps.a1 = maps.a0;
-  if (pr.h32) FLCE_TRY(make_map(&maps.a1, pr.lo, D, N, D * 2, kBK, kBM));
-  FLCE_TRY(make_map(&maps.b0, weight, D, V, D * 2, kBK, pair ? kBN / 2 : kBN));
-  maps.b1 = maps.b0;
-
-  GemmSched sc = base_sched(N, V, D, pr.h32 ? 2 : 1, 1, pair);
+  FLCE_TRY(make_term_maps(&maps.a0, &maps.a1, &maps.a2, pr.h, pr.nh, 0, D, N, D * 2, kBK, kBM));
+  FLCE_TRY(make_term_maps(&maps.b0, &maps.b1, &maps.b2, pr.w, pr.nw, 0, D, V, D * 2, kBK, pair ? kBN / 2 : kBN));
+  uint32_t seg_maps = 0;
+  const int nseg = logit_segments(pr.nh, pr.nw, &seg_maps);
+  GemmSched sc = base_sched(N, V, D, nseg, seg_maps, pair);
   int per_unit = 1;
   const int splits = choose_splits(sc.m_tiles, sc.n_tiles, pair ? dev.num_sms / 2 : dev.num_sms, &per_unit);
   sc.n_per_unit = per_unit;
@@ -612,17 +689,17 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
 
   // Maps that do not change across chunks.
   const bool pair_rec = use_pair(N, cdiv(L.vc, kBN), dev.num_sms);
-  TmaMaps rec;  // recompute: A = h (K-major), B = W (K-major)
-  FLCE_TRY(make_map(&rec.a0, pr.a_main, D, N, D * 2, kBK, kBM));
-  rec.a1 = rec.a0;
-  if (h32) FLCE_TRY(make_map(&rec.a1, pr.lo, D, N, D * 2, kBK, kBM));
-  FLCE_TRY(make_map(&rec.b0, weight, D, V, D * 2, kBK, pair_rec ? kBN / 2 : kBN));
-  rec.b1 = rec.b0;
-  CUtensorMap h_mn, lo_mn, w_mn;  // MN-major views: h for dW, W for dh
-  FLCE_TRY(make_map(&h_mn, pr.a_main, D, N, D * 2, 64, kBK));
-  lo_mn = h_mn;
-  if (h32) FLCE_TRY(make_map(&lo_mn, pr.lo, D, N, D * 2, 64, kBK));
-  FLCE_TRY(make_map(&w_mn, weight, D, V, D * 2, 64, kBK));
+  TmaMaps rec;  // recompute: A = h terms (K-major), B = W terms (K-major)
+  FLCE_TRY(make_term_maps(&rec.a0, &rec.a1, &rec.a2, pr.h, pr.nh, 0, D, N, D * 2, kBK, kBM));
+  FLCE_TRY(make_term_maps(&rec.b0, &rec.b1, &rec.b2, pr.w, pr.nw, 0, D, V, D * 2, kBK, pair_rec ? kBN / 2 : kBN));
+  uint32_t rec_segs = 0, dw_segs = 0, dh_segs = 0;
+  const int rec_nseg = logit_segments(pr.nh, pr.nw, &rec_segs);
+  const int dw_nseg = b_term_segments(pr.nh, &dw_segs);  // dW = G^T (sum of h terms)
+  const int dh_nseg = b_term_segments(pr.nw, &dh_segs);  // dh = G (sum of W terms)
+  TmaMaps hmn, wmn;  // MN-major views: h terms for dW, W terms for dh
+  FLCE_TRY(make_term_maps(&hmn.b0, &hmn.b1, &hmn.b2, pr.h, pr.nh, 0, D, N, D * 2, 64, kBK));
+  FLCE_TRY(make_term_maps(&wmn.b0, &wmn.b1, &wmn.b2, pr.w, pr.nw, 0, D, V, D * 2, 64, kBK));
+  const size_t w_elem = weight_elem(p);
 
   // dh: CTA pairs or single CTAs, and the K split for this device (bounded by
   // the layout's slot count).
@@ -642,7 +719,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     const bool first = c == 0, last = c == L.n_chunks - 1;
 
     // (1) recompute the logits of the chunk and form G (bf16) + dbias partials
-    GemmSched s1 = base_sched(N, width, D, h32 ? 2 : 1, 1, pair_rec);
+    GemmSched s1 = base_sched(N, width, D, rec_nseg, rec_segs, pair_rec);
     s1.b_mn_off = static_cast<int32_t>(v0);
     s1.group_m = pair_rec ? 16 : 32;
     s1.m_limit = pr.row_count;
@@ -681,11 +758,12 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     // (2) dW[v0 : v0+width] = G^T h    (A = G MN-major, B = h MN-major, K = N)
     TmaMaps mw;
     FLCE_TRY(make_map(&mw.a0, g, width, N, L.vc * 2, 64, kBK));
-    mw.a1 = mw.a0;
-    mw.b0 = h_mn;
-    mw.b1 = lo_mn;
+    mw.a1 = mw.a2 = mw.a0;
+    mw.b0 = hmn.b0;
+    mw.b1 = hmn.b1;
+    mw.b2 = hmn.b2;
     const bool pair_dw = use_pair(width, cdiv(D, kBN), dev.num_sms);
-    GemmSched s2 = base_sched(width, D, N, h32 ? 2 : 1, 0, pair_dw);
+    GemmSched s2 = base_sched(width, D, N, dw_nseg, dw_segs, pair_dw);
     s2.a_mn = 1;
     s2.b_mn = 1;
     s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
@@ -694,19 +772,20 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     StoreParams sp{};
     sp.rows = width;
     sp.cols = D;
-    sp.out = static_cast<uint8_t*>(dweight) + size_t(v0) * D * 2;
+    sp.out = static_cast<uint8_t*>(dweight) + size_t(v0) * D * w_elem;
     sp.ldo = D;
-    sp.out_f32 = 0;
+    sp.out_f32 = w_elem == 4 ? 1 : 0;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
                     [&] { return launch_store_gemm(pair_dw, mw, s2, sp, status, dev.num_sms, st); }));
 
     // (3) dh (+)= G W[v0 : v0+width]   (A = G K-major, B = W MN-major, K = width)
     TmaMaps mh;
     FLCE_TRY(make_map(&mh.a0, g, width, N, L.vc * 2, kBK, kBM));
-    mh.a1 = mh.a0;
-    mh.b0 = w_mn;
-    mh.b1 = w_mn;
-    GemmSched s3 = base_sched(N, D, width, 1, 0, pair_dh);
+    mh.a1 = mh.a2 = mh.a0;
+    mh.b0 = wmn.b0;
+    mh.b1 = wmn.b1;
+    mh.b2 = wmn.b2;
+    GemmSched s3 = base_sched(N, D, width, dh_nseg, dh_segs, pair_dh);
     s3.b_mn = 1;
     s3.b_k_off = static_cast<int32_t>(v0);
     s3.ksplit = ksplit;
@@ -789,8 +868,13 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st,
                     [&] { return launch_count_valid(pr.tgt, N, V, p->ignore_index, n_valid, st); }));
   }
-  CUtensorMap w_mn;  // W as the MN-major B operand of dh
-  FLCE_TRY(make_map(&w_mn, weight, D, V, D * 2, 64, kBK));
+  TmaMaps wmn;  // W terms as the MN-major B operand of dh
+  FLCE_TRY(make_term_maps(&wmn.b0, &wmn.b1, &wmn.b2, pr.w, pr.nw, 0, D, V, D * 2, 64, kBK));
+  uint32_t logit_segs = 0, dw_segs = 0, dh_segs = 0;
+  const int logit_nseg = logit_segments(pr.nh, pr.nw, &logit_segs);
+  const int dw_nseg = b_term_segments(pr.nh, &dw_segs);
+  const int dh_nseg = b_term_segments(pr.nw, &dh_segs);
+  const size_t w_elem = weight_elem(p);
   const bool pair_dh = use_pair(L.nc, cdiv(D, kBN), dev.num_sms);
   const int dh_ctas = pair_dh ? dev.num_sms / 2 : dev.num_sms;
   const int ksplit =
@@ -802,8 +886,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     const int64_t r0 = c * L.nc;
     const int64_t rows = std::min<int64_t>(L.nc, N - r0);
     const bool last = c == L.n_tchunks - 1;
-    const uint8_t* a_main = static_cast<const uint8_t*>(pr.a_main) + size_t(r0) * D * 2;
-    const uint8_t* a_lo = h32 ? reinterpret_cast<const uint8_t*>(pr.lo) + size_t(r0) * D * 2 : nullptr;
+    const size_t h_off = size_t(r0) * D * 2;  // the chunk's rows in every h term
     const int64_t* tgt = pr.tgt + r0;
     const int32_t* lim = pr.cmp ? chunk_rows + c : nullptr;      // valid rows of the chunk (device)
     const int32_t* rmap = pr.cmp ? pr.row_map + r0 : nullptr;   // chunk row -> token
@@ -811,12 +894,9 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     // (1) logits of the chunk: online statistics, and z kept in fp32
     const bool pair_f = use_pair(rows, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
     TmaMaps fm;
-    FLCE_TRY(make_map(&fm.a0, a_main, D, rows, D * 2, kBK, kBM));
-    fm.a1 = fm.a0;
-    if (h32) FLCE_TRY(make_map(&fm.a1, a_lo, D, rows, D * 2, kBK, kBM));
-    FLCE_TRY(make_map(&fm.b0, weight, D, V, D * 2, kBK, pair_f ? kBN / 2 : kBN));
-    fm.b1 = fm.b0;
-    GemmSched sf = base_sched(rows, V, D, h32 ? 2 : 1, 1, pair_f);
+    FLCE_TRY(make_term_maps(&fm.a0, &fm.a1, &fm.a2, pr.h, pr.nh, h_off, D, rows, D * 2, kBK, kBM));
+    FLCE_TRY(make_term_maps(&fm.b0, &fm.b1, &fm.b2, pr.w, pr.nw, 0, D, V, D * 2, kBK, pair_f ? kBN / 2 : kBN));
+    GemmSched sf = base_sched(rows, V, D, logit_nseg, logit_segs, pair_f);
     int per_unit = 1;
     const int splits = choose_splits(sf.m_tiles, sf.n_tiles, pair_f ? dev.num_sms / 2 : dev.num_sms, &per_unit);
     sf.n_per_unit = per_unit;
@@ -893,10 +973,11 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     // (3) dh rows of the chunk = G W   (A = G K-major, B = W MN-major, K = V)
     TmaMaps mh;
     FLCE_TRY(make_map(&mh.a0, g, V, rows, L.ldz * 2, kBK, kBM));
-    mh.a1 = mh.a0;
-    mh.b0 = w_mn;
-    mh.b1 = w_mn;
-    GemmSched s3 = base_sched(rows, D, V, 1, 0, pair_dh);
+    mh.a1 = mh.a2 = mh.a0;
+    mh.b0 = wmn.b0;
+    mh.b1 = wmn.b1;
+    mh.b2 = wmn.b2;
+    GemmSched s3 = base_sched(rows, D, V, dh_nseg, dh_segs, pair_dh);
     s3.b_mn = 1;
     s3.ksplit = ksplit;
     s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
@@ -931,11 +1012,9 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     // (4) dW (+)= G^T h[chunk]   (A = G MN-major, B = h MN-major, K = chunk rows)
     TmaMaps mw;
     FLCE_TRY(make_map(&mw.a0, g, V, rows, L.ldz * 2, 64, kBK));
-    mw.a1 = mw.a0;
-    FLCE_TRY(make_map(&mw.b0, a_main, D, rows, D * 2, 64, kBK));
-    mw.b1 = mw.b0;
-    if (h32) FLCE_TRY(make_map(&mw.b1, a_lo, D, rows, D * 2, 64, kBK));
-    GemmSched s2 = base_sched(V, D, rows, h32 ? 2 : 1, 0, pair_dw);
+    mw.a1 = mw.a2 = mw.a0;
+    FLCE_TRY(make_term_maps(&mw.b0, &mw.b1, &mw.b2, pr.h, pr.nh, h_off, D, rows, D * 2, 64, kBK));
+    GemmSched s2 = base_sched(V, D, rows, dw_nseg, dw_segs, pair_dw);
     s2.a_mn = 1;
     s2.b_mn = 1;
     s2.group_m = std::max(1, dw_ctas / std::max(1, s2.n_tiles));
@@ -949,7 +1028,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     aw.accumulate = c > 0 ? 1 : 0;
     aw.write_final = last ? 1 : 0;
     aw.out = dweight;
-    aw.out_f32 = 0;
+    aw.out_f32 = w_elem == 4 ? 1 : 0;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
                     [&] { return launch_accum_gemm(pair_dw, mw, s2, aw, status, dev.num_sms, st); }));
   }
@@ -991,7 +1070,7 @@ int check_backward_args(const flce_problem* p, const void* hidden, const void* w
 
 int zero_grads_for_empty(const flce_problem* p, void* dweight, void* dbias, cudaStream_t st) {
   const size_t bias_elem = p->bias_dtype == FLCE_F32 ? 4 : 2;
-  FLCE_TRY(fail(cudaMemsetAsync(dweight, 0, size_t(p->vocab) * p->hidden * 2, st)));
+  FLCE_TRY(fail(cudaMemsetAsync(dweight, 0, size_t(p->vocab) * p->hidden * weight_elem(p), st)));
   if (dbias) FLCE_TRY(fail(cudaMemsetAsync(dbias, 0, size_t(p->vocab) * bias_elem, st)));
   return FLCE_OK;
 }
@@ -1021,7 +1100,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
     return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
   }
   Prep pr;
-  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, targets, nullptr, nullptr, lse, entropy,
+  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, weight, targets, nullptr, nullptr, lse, entropy,
                    p->reduction == FLCE_RED_NONE ? loss : nullptr, &pr));
   return run_forward(p, L, dev, ws, status, st, weight, bias, pr, loss, lse, entropy, correct, n_valid, entropy_sum,
                      nullptr);
@@ -1045,7 +1124,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
   if (p->n_tokens == 0) return zero_grads_for_empty(p, dweight, dbias, st);
   Prep pr;
-  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, targets, lse, dloss, nullptr, nullptr, nullptr, &pr));
+  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, weight, targets, lse, dloss, nullptr, nullptr, nullptr, &pr));
   const float* lse_use = pr.cmp ? pr.c_lse : lse;
   const float* dloss_use = pr.c_dloss ? pr.c_dloss : dloss;
   return run_backward(p, L, dev, ws, status, st, weight, bias, pr, lse_use, n_valid, dloss_use, dhidden, dweight,
@@ -1075,7 +1154,7 @@ int flce_forward_backward(const flce_problem* p, const void* hidden, const void*
     return zero_grads_for_empty(p, dweight, dbias, st);
   }
   Prep pr;
-  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, targets, nullptr, dloss, lse, entropy,
+  FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, weight, targets, nullptr, dloss, lse, entropy,
                    p->reduction == FLCE_RED_NONE ? loss : nullptr, &pr));
   if (L.token) {
     return run_fused_tokens(p, L, dev, ws, status, st, weight, bias, pr, dloss, loss, lse, entropy, correct,
@@ -1132,9 +1211,9 @@ int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int6
   else FLCE_TRY(make_map(&m.a0, A, M, K, lda * 2, 64, kBK));
   if (!b_mn_major) FLCE_TRY(make_map(&m.b0, B, K, N, ldb * 2, kBK, pair ? kBN / 2 : kBN));
   else FLCE_TRY(make_map(&m.b0, B, N, K, ldb * 2, 64, kBK));
-  m.a1 = m.a0;
-  m.b1 = m.b0;
-  GemmSched s = base_sched(M, N, K, 1, 0, pair);
+  m.a1 = m.a2 = m.a0;
+  m.b1 = m.b2 = m.b0;
+  GemmSched s = base_sched(M, N, K, 1, 0u, pair);
   s.a_mn = a_mn_major ? 1 : 0;
   s.b_mn = b_mn_major ? 1 : 0;
   finish_sched(s);

@@ -19,27 +19,47 @@ cudaError_t launch_fwd_gemm(bool bias, bool softcap, bool pair, const TmaMaps& m
 // fp32 hidden -> bf16 hi + bf16 lo, hi = rn(h), lo = rn(h - hi).  hi + lo
 // carries about 16 bits of the 24-bit mantissa.
 // ---------------------------------------------------------------------------
-__global__ void split_hidden_kernel(const float4* __restrict__ h, uint2* __restrict__ hi, uint2* __restrict__ lo,
-                                    int64_t n4) {
+// x = t0 + t1 (+ t2) in bf16 terms: t0 = rn(x), t1 = rn(x - t0), t2 = rn(x - t0 - t1).
+// Each difference is exact in fp32 (the term shares x's exponent range), so two
+// terms carry about 16 significant bits of x and three all 24.
+__device__ __forceinline__ void split_terms(float4 x, uint2& t0, uint2& t1, uint2& t2) {
+  const float v[4] = {x.x, x.y, x.z, x.w};
+  uint32_t a[2], b[2], c[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t p0 = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    const float r0 = v[2 * i] - __uint_as_float(p0 << 16);
+    const float r1 = v[2 * i + 1] - __uint_as_float(p0 & 0xFFFF0000u);
+    const uint32_t p1 = pack_bf16x2(r0, r1);
+    const float s0 = r0 - __uint_as_float(p1 << 16);
+    const float s1 = r1 - __uint_as_float(p1 & 0xFFFF0000u);
+    a[i] = p0;
+    b[i] = p1;
+    c[i] = pack_bf16x2(s0, s1);
+  }
+  t0 = make_uint2(a[0], a[1]);
+  t1 = make_uint2(b[0], b[1]);
+  t2 = make_uint2(c[0], c[1]);
+}
+
+__global__ void split_f32_kernel(const float4* __restrict__ x, uint2* __restrict__ t0, uint2* __restrict__ t1,
+                                 uint2* __restrict__ t2, int64_t n4) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float4 x = h[i];
-    const uint32_t h01 = pack_bf16x2(x.x, x.y);
-    const uint32_t h23 = pack_bf16x2(x.z, x.w);
-    const float r0 = x.x - __uint_as_float(h01 << 16);
-    const float r1 = x.y - __uint_as_float(h01 & 0xFFFF0000u);
-    const float r2 = x.z - __uint_as_float(h23 << 16);
-    const float r3 = x.w - __uint_as_float(h23 & 0xFFFF0000u);
-    hi[i] = make_uint2(h01, h23);
-    lo[i] = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
+    uint2 a, b, c;
+    split_terms(x[i], a, b, c);
+    t0[i] = a;
+    t1[i] = b;
+    if (t2) t2[i] = c;
   }
 }
 
-cudaError_t launch_split_hidden(const float* h, uint16_t* hi, uint16_t* lo, int64_t n, int grid,
-                                cudaStream_t stream) {
+cudaError_t launch_split_f32(const float* x, uint16_t* t0, uint16_t* t1, uint16_t* t2, int64_t n, int grid,
+                             cudaStream_t stream) {
   const int64_t n4 = n / 4;
-  split_hidden_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(h), reinterpret_cast<uint2*>(hi),
-                                                reinterpret_cast<uint2*>(lo), n4);
+  if (n4 == 0) return cudaSuccess;
+  split_f32_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(x), reinterpret_cast<uint2*>(t0),
+                                             reinterpret_cast<uint2*>(t1), reinterpret_cast<uint2*>(t2), n4);
   return cudaGetLastError();
 }
 
@@ -259,15 +279,15 @@ __device__ __forceinline__ void copy_hidden_row(const CompactParams& p, int64_t 
     for (int64_t i = lane; i < D / 8; i += 32) out[i] = in[i];
   } else {
     const float4* in = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.hidden_in) + src * D);
-    uint2* hi = reinterpret_cast<uint2*>(p.hc + dst * D);
-    uint2* lo = reinterpret_cast<uint2*>(p.lo + dst * D);
+    uint2* t0 = reinterpret_cast<uint2*>(p.hc + dst * D);
+    uint2* t1 = reinterpret_cast<uint2*>(p.lo + dst * D);
+    uint2* t2 = p.lo2 ? reinterpret_cast<uint2*>(p.lo2 + dst * D) : nullptr;
     for (int64_t i = lane; i < D / 4; i += 32) {
-      const float4 x = in[i];
-      const uint32_t h01 = pack_bf16x2(x.x, x.y);
-      const uint32_t h23 = pack_bf16x2(x.z, x.w);
-      hi[i] = make_uint2(h01, h23);
-      lo[i] = make_uint2(pack_bf16x2(x.x - __uint_as_float(h01 << 16), x.y - __uint_as_float(h01 & 0xFFFF0000u)),
-                         pack_bf16x2(x.z - __uint_as_float(h23 << 16), x.w - __uint_as_float(h23 & 0xFFFF0000u)));
+      uint2 a, b, c;
+      split_terms(in[i], a, b, c);
+      t0[i] = a;
+      t1[i] = b;
+      if (t2) t2[i] = c;
     }
   }
 }
@@ -279,6 +299,10 @@ __device__ __forceinline__ void zero_hidden_row(const CompactParams& p, int64_t 
   if (p.hidden_f32) {
     uint4* out2 = reinterpret_cast<uint4*>(p.lo + dst * D);
     for (int64_t i = lane; i < D / 8; i += 32) out2[i] = make_uint4(0, 0, 0, 0);
+    if (p.lo2) {
+      uint4* out3 = reinterpret_cast<uint4*>(p.lo2 + dst * D);
+      for (int64_t i = lane; i < D / 8; i += 32) out3[i] = make_uint4(0, 0, 0, 0);
+    }
   }
 }
 

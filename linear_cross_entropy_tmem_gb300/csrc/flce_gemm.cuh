@@ -668,10 +668,26 @@ __device__ __forceinline__ void mbar_wait_teardown(uint64_t* bar, uint32_t parit
   }
 }
 
+// Prefetches the descriptors of the further terms that some K segment uses.
+__device__ __forceinline__ void prefetch_segment_maps(const GemmSched& sc, const CUtensorMap* a1,
+                                                      const CUtensorMap* a2, const CUtensorMap* b1,
+                                                      const CUtensorMap* b2) {
+  uint32_t used = 0;
+  for (int s = 0; s < sc.nseg; ++s) {
+    used |= 1u << ((sc.seg_maps >> (4 * s)) & 3u);
+    used |= 16u << ((sc.seg_maps >> (4 * s + 2)) & 3u);
+  }
+  if (used & 2u) tma_prefetch_map(a1);
+  if (used & 4u) tma_prefetch_map(a2);
+  if (used & 32u) tma_prefetch_map(b1);
+  if (used & 64u) tma_prefetch_map(b2);
+}
+
 template <class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-                const __grid_constant__ CUtensorMap map_b0, const __grid_constant__ CUtensorMap map_b1,
+                const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_b0,
+                const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_b2,
                 const GemmSched sc, const typename Epi::Params ep, int* status) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem sm = carve_smem(smem_raw);
@@ -691,9 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_map(&map_a0);
     tma_prefetch_map(&map_b0);
-    if (sc.nseg > 1) {
-      tma_prefetch_map(sc.seg_a ? &map_a1 : &map_b1);
-    }
+    if (sc.nseg > 1) prefetch_segment_maps(sc, &map_a1, &map_a2, &map_b1, &map_b2);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(sm.tmem_slot, kTmemCols);
@@ -722,8 +736,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
           for (int seg = 0; ok && seg < sc.nseg; ++seg) {
-            const CUtensorMap* ma = (seg && sc.seg_a) ? &map_a1 : &map_a0;
-            const CUtensorMap* mb = (seg && !sc.seg_a) ? &map_b1 : &map_b0;
+            const uint32_t ai = (sc.seg_maps >> (4 * seg)) & 3u, bi = (sc.seg_maps >> (4 * seg + 2)) & 3u;
+            const CUtensorMap* ma = ai == 0 ? &map_a0 : (ai == 1 ? &map_a1 : &map_a2);
+            const CUtensorMap* mb = bi == 0 ? &map_b0 : (bi == 1 ? &map_b1 : &map_b2);
             for (int kb = u.kb_first; kb < u.kb_first + u.kb_count; ++kb) {
               if (!mbar_wait(&sm.empty[stage], phase ^ 1u, sm.ctl, status)) {
                 ok = false;
@@ -897,7 +912,8 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 template <class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-                     const __grid_constant__ CUtensorMap map_b0, const __grid_constant__ CUtensorMap map_b1,
+                     const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_b0,
+                     const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_b2,
                      const GemmSched sc, const typename Epi::Params ep, int* status) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem sm = carve_smem_pair(smem_raw);
@@ -919,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_map(&map_a0);
     tma_prefetch_map(&map_b0);
-    if (sc.nseg > 1) tma_prefetch_map(sc.seg_a ? &map_a1 : &map_b1);
+    if (sc.nseg > 1) prefetch_segment_maps(sc, &map_a1, &map_a2, &map_b1, &map_b2);
   }
   if (warp == kMmaWarp) {
     tmem_alloc_pair(sm.tmem_slot, kTmemCols);
@@ -953,8 +969,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
           const int b_col = sc.b_mn_off + n * kBN + static_cast<int>(rank) * (kBN / 2);
           for (int seg = 0; ok && seg < sc.nseg; ++seg) {
-            const CUtensorMap* ma = (seg && sc.seg_a) ? &map_a1 : &map_a0;
-            const CUtensorMap* mb = (seg && !sc.seg_a) ? &map_b1 : &map_b0;
+            const uint32_t ai = (sc.seg_maps >> (4 * seg)) & 3u, bi = (sc.seg_maps >> (4 * seg + 2)) & 3u;
+            const CUtensorMap* ma = ai == 0 ? &map_a0 : (ai == 1 ? &map_a1 : &map_a2);
+            const CUtensorMap* mb = bi == 0 ? &map_b0 : (bi == 1 ? &map_b1 : &map_b2);
             for (int kb = u.kb_first; kb < u.kb_first + u.kb_count; ++kb) {
               if (!mbar_wait(&sm.empty[stage], phase ^ 1u, sm.ctl, status)) {
                 ok = false;

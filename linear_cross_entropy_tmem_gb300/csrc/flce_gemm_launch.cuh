@@ -18,7 +18,7 @@ static cudaError_t launch_gemm_single(const TmaMaps& m, const GemmSched& sc, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(sc.total_units, num_sms));
-  kern<<<grid, kThreads, kGemmSmemBytes, stream>>>(m.a0, m.a1, m.b0, m.b1, sc, p, status);
+  kern<<<grid, kThreads, kGemmSmemBytes, stream>>>(m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
   return cudaGetLastError();
 }
 
@@ -52,7 +52,7 @@ static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const
   }
   const int clusters = std::max(1, std::min(std::min(sc.total_units, num_sms / 2), resident[dev]));
   cfg.gridDim = dim3(2 * clusters);
-  return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.b0, m.b1, sc, p, status);
+  return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
 }
 
 template <class Epi>

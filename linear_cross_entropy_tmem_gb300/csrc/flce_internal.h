@@ -44,6 +44,8 @@ constexpr int kGemmSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes 
 constexpr int kGemmPairSmemBytes =
     1024 /*alignment slack*/ + kStagesPair * kStagePairBytes + kBarrierBytes + kEpiSmemBytes;
 
+constexpr int kMaxSegments = 6;   // fp32 x fp32 with three-term splits: 6 products
+
 // A bounded wait inside a kernel gives up after this much wall time.
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
@@ -61,8 +63,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct GemmSched {
   int32_t m_tiles, n_tiles;
   int32_t k_blocks;       // 64-wide K blocks over the whole K range
-  int32_t nseg;           // 1, or 2 when the fp32 hidden state is split into hi + lo
-  int32_t seg_a;          // 1: segment 1 switches the A map; 0: it switches the B map
+  // K segments: products of bf16 terms of fp32 operands summed into one
+  // accumulator.  Segment s (< nseg <= kMaxSegments) multiplies A map
+  // (seg_maps >> 4s) & 3 by B map (seg_maps >> (4s + 2)) & 3.
+  int32_t nseg;
+  uint32_t seg_maps;
   int32_t ksplit;         // K splits per output tile
   int32_t kb_per_split;
   int32_t n_per_unit;
@@ -186,8 +191,9 @@ struct CompactParams {
   int32_t* count;          // [1] number of valid tokens
   int32_t* row_map;        // [N] compacted position -> original row
   int64_t* targets_out;    // [N] compacted targets (ignore_index past the count)
-  uint16_t* hc;            // [N][D] bf16 compacted hidden (bf16 input), or hi part (fp32 input)
-  uint16_t* lo;            // [N][D] lo part (fp32 input), else nullptr
+  uint16_t* hc;            // [N][D] bf16 compacted hidden (bf16 input), or first bf16 term (fp32 input)
+  uint16_t* lo;            // [N][D] second bf16 term (fp32 input), else nullptr
+  uint16_t* lo2;           // [N][D] third bf16 term (fp32 input split in three), else nullptr
   const float* lse_in;     // backward: [N] lse to compact, or nullptr
   float* lse_out;
   const float* dloss_in;   // backward, reduction none: [N] upstream grads to compact, or nullptr

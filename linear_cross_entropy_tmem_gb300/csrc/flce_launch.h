@@ -8,8 +8,10 @@
 
 namespace flce {
 
+// A and B operand maps; a1, a2, b1, b2 are the further bf16 terms of split
+// fp32 operands (GemmSched::seg_maps picks the pair of each K segment).
 struct TmaMaps {
-  CUtensorMap a0, a1, b0, b1;
+  CUtensorMap a0, a1, a2, b0, b1, b2;
 };
 
 // Per-token merge of the split partials, with per-block partial sums.
@@ -70,8 +72,9 @@ cudaError_t launch_chunk_rows(const int32_t* count, int64_t rows_per_chunk, int 
 cudaError_t launch_count_valid(const int64_t* targets, int64_t n, int64_t vocab, int64_t ignore_index,
                                int64_t* n_valid, cudaStream_t stream);
 
-cudaError_t launch_split_hidden(const float* h, uint16_t* hi, uint16_t* lo, int64_t n, int grid,
-                                cudaStream_t stream);
+// x (fp32, n % 4 == 0) -> bf16 terms t0 = rn(x), t1 = rn(x - t0) [, t2 = rn(x - t0 - t1)].
+cudaError_t launch_split_f32(const float* x, uint16_t* t0, uint16_t* t1, uint16_t* t2, int64_t n, int grid,
+                             cudaStream_t stream);
 cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream);
 cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream);
 cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int64_t cols, void* dbias,

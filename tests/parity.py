@@ -24,10 +24,10 @@ NEAR_TIE = 1e-3
 
 
 def run_gpu(h, W, b, t, dloss, *, logit_scale, softcap, reduction, ignore_index=-100, backward=True,
-            num_items_in_batch=0.0, compact=False):
+            num_items_in_batch=0.0, compact=False, fp32_full=False):
     import linear_cross_entropy_tmem_gb300 as F
     kw = dict(logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index, reduction=reduction,
-              num_items_in_batch=num_items_in_batch, compact=compact)
+              num_items_in_batch=num_items_in_batch, compact=compact, fp32_full=fp32_full)
     f = F.flce_forward(h, W, t, b, entropy=True, **kw)
     out = {"fwd": f}
     if backward:

@@ -98,6 +98,27 @@ def test_workspace_size_needs_no_gpu_and_never_scales_with_n_times_v(lib):
     assert _ws(lib, _problem(), 3)[0] == B.FLCE_ERR_INVALID_ARG
 
 
+def test_fp32_terms_workspace(lib):
+    """fp32 operands add their bf16 terms: 2 (default) or 3 (FLCE_FLAG_FP32_FULL) copies of N x D for
+    the hidden state and of V x D for an fp32 head; bf16 operands are unaffected by the flag."""
+    N, D, V = 1024, 512, 8000
+    full = B.FLCE_FLAG_FP32_FULL
+    for bwd in (0, 1, 2):
+        for rec in (B.FLCE_FLAG_BWD_RECOMPUTE, B.FLCE_FLAG_BWD_KEEP_LOGITS):
+            base = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=rec), bwd)[1]
+            assert _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=rec | full), bwd)[1] == base
+            h2 = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, hidden_dtype=B.FLCE_F32, flags=rec), bwd)[1]
+            h3 = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, hidden_dtype=B.FLCE_F32, flags=rec | full), bwd)[1]
+            w2 = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, hidden_dtype=B.FLCE_F32, weight_dtype=B.FLCE_F32,
+                                   flags=rec), bwd)[1]
+            w3 = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, hidden_dtype=B.FLCE_F32, weight_dtype=B.FLCE_F32,
+                                   flags=rec | full), bwd)[1]
+            assert abs((h2 - base) - 2 * N * D * 2) <= 1024
+            assert abs((h3 - h2) - N * D * 2) <= 1024
+            assert abs((w2 - h2) - 2 * V * D * 2) <= 1024
+            assert abs((w3 - h3) - 3 * V * D * 2) <= 1024
+
+
 def test_keep_logits_workspace(lib):
     """The token-chunked backward keeps fp32 logits + bf16 G for at most half of the tokens, plus
     an fp32 dW accumulator; the automatic choice keeps logits from D = 1024 up and for N > 256."""
@@ -136,12 +157,12 @@ def test_keep_logits_workspace(lib):
     (dict(hidden=130), B.FLCE_ERR_MISALIGNED),
     (dict(reduction=7), B.FLCE_ERR_INVALID_ARG),
     (dict(weight_dtype=B.FLCE_F32), B.FLCE_ERR_DTYPE_MISMATCH),
-    (dict(weight_dtype=B.FLCE_F32, hidden_dtype=B.FLCE_F32), B.FLCE_ERR_UNSUPPORTED_DTYPE),
+    (dict(weight_dtype=5, hidden_dtype=B.FLCE_F32), B.FLCE_ERR_UNSUPPORTED_DTYPE),
     (dict(hidden_dtype=5), B.FLCE_ERR_UNSUPPORTED_DTYPE),
     (dict(logit_scale=float("nan")), B.FLCE_ERR_INVALID_ARG),
     (dict(num_items_in_batch=-1.0), B.FLCE_ERR_INVALID_ARG),
     (dict(num_items_in_batch=float("inf")), B.FLCE_ERR_INVALID_ARG),
-    (dict(flags=8), B.FLCE_ERR_INVALID_ARG),
+    (dict(flags=16), B.FLCE_ERR_INVALID_ARG),
     (dict(flags=B.FLCE_FLAG_BWD_RECOMPUTE | B.FLCE_FLAG_BWD_KEEP_LOGITS), B.FLCE_ERR_INVALID_ARG),
     (dict(reserved=1), B.FLCE_ERR_INVALID_ARG),
 ])

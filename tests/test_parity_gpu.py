@@ -517,3 +517,86 @@ def test_keep_logits_no_writes_past_outputs_or_workspace(name, mode):
     dW = bufs["dW"][:sizes["dW"]].view(torch.bfloat16).view(V, D)
     db = None if b is None else bufs["db"][:sizes["db"]].view(b.dtype)
     compare_backward((dh, dW, db), ref_b)
+
+
+# ---------------------------------------------------------------------------
+# fp32 operands: an fp32 head (with fp32 hidden states); two- and three-term splits
+# ---------------------------------------------------------------------------
+def _fp32_head(W_bf16: torch.Tensor, seed: int) -> torch.Tensor:
+    """An fp32 head close to the bf16 one whose values use all 24 significand bits."""
+    g = torch.Generator().manual_seed(seed)
+    return (W_bf16.float() * (1.0 + 0.01 * torch.randn(W_bf16.shape, generator=g))).contiguous()
+
+
+FP32_CASES = {
+    "fp32-h N257 D136 V777 bias s0.0625 c30 none": CASES["fp32-h N257 D136 V777 bias s0.0625 c30 none"][0],
+    "fp32-h multi-chunk N200 D64 V1500 softcap sum": CASES["fp32-h multi-chunk N200 D64 V1500 softcap sum"][0],
+    "fp32-h N700 D256 V3000 bias mean": Workload("h32w32", 700, 256, 3000, sigma_w=0.1, hidden_dtype=torch.float32,
+                                                 bias=True, seed=13),
+}
+
+
+@pytest.mark.parametrize("full", [False, True], ids=["two-term", "three-term"])
+@pytest.mark.parametrize("entry", ["separate", "fused-recompute", "fused-keep", "fused-keep-compact"])
+@pytest.mark.parametrize("name", list(FP32_CASES))
+def test_fp32_head_parity(name, entry, full):
+    """fp32 hidden states with an fp32 head (FLCE_F32 weight, fp32 dweight) on every entry point."""
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_token_chunk
+    testing_set_token_chunk(256)
+    w = FP32_CASES[name]
+    h, Wb, b, t, dloss = make_inputs(w, "cpu")
+    W = _fp32_head(Wb, w.seed)
+    dev = [x.cuda() if x is not None else None for x in (h, W, b, t, dloss)]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    ref_f = oracle.forward(h, W, b, t, **kw)
+    ref_b = oracle.backward(h, W, b, t, dloss=dloss, **kw)
+    if entry == "separate":
+        gpu = run_gpu(*dev, fp32_full=full, **kw)
+        assert gpu["status"] == 0
+        fwd, grads = gpu["fwd"], gpu["bwd"]
+    else:
+        bwd = "recompute" if entry == "fused-recompute" else "keep_logits"
+        fwd, grads = F.flce_forward_backward(dev[0], dev[1], dev[3], dev[4], dev[2], entropy=True, bwd=bwd,
+                                             compact=entry.endswith("compact"), fp32_full=full, **kw)
+        torch.cuda.synchronize()
+        assert F.flce_read_device_status(fwd.workspace) == 0
+    assert grads[1].dtype == torch.float32
+    if entry.endswith("compact"):
+        _compare_compacted({"fwd": fwd, "bwd": grads}, ref_f, ref_b, t, w.reduction)
+        return
+    z = oracle.logits(h, W, b, logit_scale=w.logit_scale, softcap=w.softcap)
+    compare_forward(fwd, ref_f, reduction=w.reduction, z=z, t=t.numpy())
+    compare_backward(grads, ref_b)
+
+
+@pytest.mark.parametrize("fp32_head", [False, True], ids=["bf16-head", "fp32-head"])
+def test_fp32_full_removes_operand_rounding(fp32_head):
+    """Three-term splits carry all 24 bits of fp32 operands.  With one MMA step (K = 16) the
+    operands' rounding dominates the two-term error, and the three-term lse error against the exact
+    fp64 logits drops to the level of fp32 arithmetic.  At K = 512 the tensor core's fp32
+    accumulation (about K/16 ulps of the accumulator) dominates both, so the split must only not
+    make it worse."""
+    import linear_cross_entropy_tmem_gb300 as F
+    for D, check in ((16, "operand"), (512, "accumulation")):
+        N, V = 512, 4096
+        g = torch.Generator().manual_seed(21 + D)
+        h = torch.randn(N, D, generator=g)                    # fp32 with all 24 bits used
+        W = torch.randn(V, D, generator=g) * (10.0 / D ** 0.5)  # logits of order 10
+        if not fp32_head:
+            W = W.to(torch.bfloat16)
+        t = torch.randint(0, V, (N,), generator=g)
+        ref = oracle.forward(h, W, None, t)
+        err = {}
+        for full in (False, True):
+            f = F.flce_forward(h.cuda(), W.cuda(), t.cuda(), None, fp32_full=full)
+            torch.cuda.synchronize()
+            err[full] = float(np.abs(f.lse.double().cpu().numpy() - ref["lse"]).max())
+        if check == "operand":
+            # each of the (3 or 6) term products is one accumulation step of at most ~1 ulp of the
+            # accumulator (|logit| <= ~48 here, ulp 3.8e-6), plus the lse's own fp32 arithmetic
+            nseg = 6 if fp32_head else 3
+            assert err[True] <= (nseg + 4) * 3.8e-6, (D, err)
+            assert 4 * err[True] <= err[False], (D, err)
+        else:
+            assert err[True] <= 1.2 * err[False] and err[True] <= 5e-4, (D, err)
