@@ -609,7 +609,7 @@ int make_term_maps(CUtensorMap* m0, CUtensorMap* m1, CUtensorMap* m2, const void
 }
 
 int run_forward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
-                cudaStream_t st, const void* weight, const void* bias, const Prep& pr, float* loss, float* lse,
+                cudaStream_t st, const void* bias, const Prep& pr, float* loss, float* lse,
                 float* entropy, int64_t* correct, int64_t* n_valid, float* entropy_sum, float* lse_compact) {
   const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
   const bool pair = use_pair(N, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
@@ -674,7 +674,7 @@ int run_forward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, u
 }
 
 int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
-                 cudaStream_t st, const void* weight, const void* bias, const Prep& pr, const float* lse_use,
+                 cudaStream_t st, const void* bias, const Prep& pr, const float* lse_use,
                  const int64_t* n_valid, const float* dloss_use, void* dhidden, void* dweight, void* dbias) {
   const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
   const bool h32 = pr.h32;
@@ -838,7 +838,7 @@ int choose_token_ksplit(int64_t tiles, int ctas, int bound) {
 // chunk's dh rows come from one product over the whole vocabulary, and dW
 // accumulates in fp32 across chunks (the last chunk writes the bf16 result).
 int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
-                     cudaStream_t st, const void* weight, const void* bias, const Prep& pr, const float* dloss,
+                     cudaStream_t st, const void* bias, const Prep& pr, const float* dloss,
                      float* loss, float* lse, float* entropy, int64_t* correct, int64_t* n_valid,
                      float* entropy_sum, void* dhidden, void* dweight, void* dbias) {
   const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
@@ -1102,7 +1102,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   Prep pr;
   FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, weight, targets, nullptr, nullptr, lse, entropy,
                    p->reduction == FLCE_RED_NONE ? loss : nullptr, &pr));
-  return run_forward(p, L, dev, ws, status, st, weight, bias, pr, loss, lse, entropy, correct, n_valid, entropy_sum,
+  return run_forward(p, L, dev, ws, status, st, bias, pr, loss, lse, entropy, correct, n_valid, entropy_sum,
                      nullptr);
 }
 
@@ -1127,7 +1127,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, weight, targets, lse, dloss, nullptr, nullptr, nullptr, &pr));
   const float* lse_use = pr.cmp ? pr.c_lse : lse;
   const float* dloss_use = pr.c_dloss ? pr.c_dloss : dloss;
-  return run_backward(p, L, dev, ws, status, st, weight, bias, pr, lse_use, n_valid, dloss_use, dhidden, dweight,
+  return run_backward(p, L, dev, ws, status, st, bias, pr, lse_use, n_valid, dloss_use, dhidden, dweight,
                       dbias);
 }
 
@@ -1157,14 +1157,14 @@ int flce_forward_backward(const flce_problem* p, const void* hidden, const void*
   FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, weight, targets, nullptr, dloss, lse, entropy,
                    p->reduction == FLCE_RED_NONE ? loss : nullptr, &pr));
   if (L.token) {
-    return run_fused_tokens(p, L, dev, ws, status, st, weight, bias, pr, dloss, loss, lse, entropy, correct,
+    return run_fused_tokens(p, L, dev, ws, status, st, bias, pr, dloss, loss, lse, entropy, correct,
                             n_valid, entropy_sum, dhidden, dweight, dbias);
   }
-  FLCE_TRY(run_forward(p, L, dev, ws, status, st, weight, bias, pr, loss, lse, entropy, correct, n_valid,
+  FLCE_TRY(run_forward(p, L, dev, ws, status, st, bias, pr, loss, lse, entropy, correct, n_valid,
                        entropy_sum, pr.cmp ? pr.c_lse : nullptr));
   const float* lse_use = pr.cmp ? pr.c_lse : lse;
   const float* dloss_use = pr.c_dloss ? pr.c_dloss : dloss;
-  return run_backward(p, L, dev, ws, status, st, weight, bias, pr, lse_use, n_valid, dloss_use, dhidden, dweight,
+  return run_backward(p, L, dev, ws, status, st, bias, pr, lse_use, n_valid, dloss_use, dhidden, dweight,
                       dbias);
 }
 
