@@ -749,7 +749,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     }));
     if (bias) {
       FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-        return launch_dbias_reduce(dbias_part, L.vc, static_cast<int>(cdiv(N, kBM)), width,
+        return launch_dbias_reduce(dbias_part, L.vc, static_cast<int>(cdiv(N, kBM)), kBM, width,
                                    static_cast<uint8_t*>(dbias) + v0 * bias_elem,
                                    p->bias_dtype == FLCE_F32, pr.row_count, st);
       }));
@@ -1036,7 +1036,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
   FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); }));
   if (bias) {
     FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-      return launch_dbias_reduce(dbias_part, L.ldz, static_cast<int>(cdiv(N, kZGradRows)), V, dbias,
+      return launch_dbias_reduce(dbias_part, L.ldz, static_cast<int>(cdiv(N, kZGradRows)), kZGradRows, V, dbias,
                                  p->bias_dtype == FLCE_F32, pr.row_count, st);
     }));
   }

@@ -27,93 +27,99 @@ cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
 }
 
 // Token-chunked backward: G from the kept fp32 logits of one token chunk.
-// Thread t of a block handles kZGradVec consecutive columns over the block's
-// kZGradRows rows: per row one 32-byte load of z and one 16-byte store of G,
-// both coalesced across the block (HBM-bound: 6 bytes per logit).  The column
-// sums of G (fp32, before rounding) over the block's rows are the dbias
-// partials, added in row order.
+// Thread t of a block handles kZGradVec consecutive columns over one tile of
+// kZGradRows rows at a time (row tiles grid-strided over blockIdx.y): per row
+// one 32-byte load of z and one 16-byte store of G, both coalesced across the
+// block (HBM-bound: 6 bytes per logit).  The column sums of G (fp32, before
+// rounding) over a tile's rows are that tile's dbias partials, added in row
+// order.  Short tiles (32 rows) keep the last wave of blocks small.
 template <bool kSoftcap>
 __global__ void __launch_bounds__(kZGradThreads) zgrad_kernel(ZGradParams p) {
   __shared__ float s_lse2[kZGradRows];  // lse * log2(e)
   __shared__ float s_wd[kZGradRows];    // w_n * s (0 at ignored rows)
   __shared__ int64_t s_t[kZGradRows];   // target column
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kZGradRows;
   int64_t lim = p.rows, lim_pad = p.rows;  // rows with a logit; rows the GEMMs read
   if (p.row_limit) {
     lim = *p.row_limit < p.rows ? *p.row_limit : p.rows;
     lim_pad = (lim + kTokenChunkAlign - 1) / kTokenChunkAlign * kTokenChunkAlign;
     if (lim_pad > p.rows) lim_pad = p.rows;
   }
-  if (r0 >= lim_pad) return;
-  const int rows = lim - r0 < kZGradRows ? static_cast<int>(lim - r0 > 0 ? lim - r0 : 0) : kZGradRows;
-  const int zero_rows = lim_pad - r0 < kZGradRows ? static_cast<int>(lim_pad - r0) : kZGradRows;
-  for (int i = threadIdx.x; i < kZGradRows; i += kZGradThreads) {
-    float lse2 = 0.f, wd = 0.f;
-    int64_t t = -1;
-    if (i < rows) {
-      const int64_t row = r0 + i;
-      t = __ldg(p.targets + row);
-      lse2 = __ldg(p.lse + row) * kLog2e;
-      const bool valid = t != p.ignore_index && t >= 0 && t < p.vocab;
-      if (valid) wd = token_weight(p.reduction, p.dloss, row, p.n_valid, p.num_items) * p.scale;
-      if (!valid) t = -1;
-    }
-    s_lse2[i] = lse2;
-    s_wd[i] = wd;
-    s_t[i] = t;
-  }
-  __syncthreads();
+  const int64_t row_tiles = (p.rows + kZGradRows - 1) / kZGradRows;
   const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * kZGradThreads + threadIdx.x) * kZGradVec;
-  if (c0 >= p.vocab) return;
-  const float* __restrict__ zp = p.z + r0 * p.ldz + c0;  // 32-byte aligned: ldz % 32 == 0, c0 % 8 == 0
-  uint16_t* __restrict__ gp = p.g + r0 * p.ldz + c0;
-  const int valid_cols = p.vocab - c0 < kZGradVec ? static_cast<int>(p.vocab - c0) : kZGradVec;
-  float colsum[kZGradVec];
-#pragma unroll
-  for (int j = 0; j < kZGradVec; ++j) colsum[j] = 0.f;
-#pragma unroll 4
-  for (int r = 0; r < rows; ++r) {
-    const float4 za = __ldcs(reinterpret_cast<const float4*>(zp + r * p.ldz));
-    const float4 zb = __ldcs(reinterpret_cast<const float4*>(zp + r * p.ldz) + 1);
-    const float z[kZGradVec] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
-    const float lse2 = s_lse2[r], wd = s_wd[r];
-    const int64_t tj = s_t[r] - c0;
-    float g[kZGradVec];
-#pragma unroll
-    for (int j = 0; j < kZGradVec; ++j) {
-      const float pr = ex2_approx(fmaf(z[j], kLog2e, -lse2));  // e^(z - lse)
-      float d = wd;
-      if (kSoftcap) {
-        const float th = z[j] * p.inv_softcap;                   // z / c
-        d = wd * fmaf(-th, th, 1.f);                             // w s (1 - (z/c)^2)
+  const bool active = c0 < p.vocab;  // threads past the vocabulary still take the barriers
+  const int valid_cols = !active ? 0 : (p.vocab - c0 < kZGradVec ? static_cast<int>(p.vocab - c0) : kZGradVec);
+  for (int64_t rt = blockIdx.y; rt < row_tiles; rt += gridDim.y) {
+    const int64_t r0 = rt * kZGradRows;
+    if (r0 >= lim_pad) break;  // uniform over the block; later tiles are further out
+    const int rows = lim - r0 < kZGradRows ? static_cast<int>(lim - r0 > 0 ? lim - r0 : 0) : kZGradRows;
+    const int zero_rows = lim_pad - r0 < kZGradRows ? static_cast<int>(lim_pad - r0) : kZGradRows;
+    __syncthreads();  // the previous tile's readers of the row data are done
+    for (int i = threadIdx.x; i < kZGradRows; i += kZGradThreads) {
+      float lse2 = 0.f, wd = 0.f;
+      int64_t t = -1;
+      if (i < rows) {
+        const int64_t row = r0 + i;
+        t = __ldg(p.targets + row);
+        lse2 = __ldg(p.lse + row) * kLog2e;
+        const bool valid = t != p.ignore_index && t >= 0 && t < p.vocab;
+        if (valid) wd = token_weight(p.reduction, p.dloss, row, p.n_valid, p.num_items) * p.scale;
+        if (!valid) t = -1;
       }
-      g[j] = d * (pr - (j == tj ? 1.f : 0.f));
-      if (j >= valid_cols) g[j] = 0.f;
-      colsum[j] += g[j];
+      s_lse2[i] = lse2;
+      s_wd[i] = wd;
+      s_t[i] = t;
     }
-    uint4 pk;
-    pk.x = pack_bf16x2(g[0], g[1]);
-    pk.y = pack_bf16x2(g[2], g[3]);
-    pk.z = pack_bf16x2(g[4], g[5]);
-    pk.w = pack_bf16x2(g[6], g[7]);
-    __stcs(reinterpret_cast<uint4*>(gp + r * p.ldz), pk);
-  }
-  for (int r = rows; r < zero_rows; ++r)  // past the valid rows of a compacted chunk: exact zeros
-    __stcs(reinterpret_cast<uint4*>(gp + r * p.ldz), make_uint4(0u, 0u, 0u, 0u));
-  if (p.dbias_part) {
-    float* dst = p.dbias_part + static_cast<int64_t>(blockIdx.y) * p.ldz + c0;
+    __syncthreads();
+    if (!active) continue;
+    const float* __restrict__ zp = p.z + r0 * p.ldz + c0;  // 32-byte aligned: ldz % 32 == 0, c0 % 8 == 0
+    uint16_t* __restrict__ gp = p.g + r0 * p.ldz + c0;
+    float colsum[kZGradVec];
 #pragma unroll
-    for (int j = 0; j < kZGradVec; ++j)
-      if (j < valid_cols) dst[j] = colsum[j];
+    for (int j = 0; j < kZGradVec; ++j) colsum[j] = 0.f;
+#pragma unroll 4
+    for (int r = 0; r < rows; ++r) {
+      const float4 za = __ldcs(reinterpret_cast<const float4*>(zp + r * p.ldz));
+      const float4 zb = __ldcs(reinterpret_cast<const float4*>(zp + r * p.ldz) + 1);
+      const float z[kZGradVec] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+      const float lse2 = s_lse2[r], wd = s_wd[r];
+      const int64_t tj = s_t[r] - c0;
+      float g[kZGradVec];
+#pragma unroll
+      for (int j = 0; j < kZGradVec; ++j) {
+        const float pr = ex2_approx(fmaf(z[j], kLog2e, -lse2));  // e^(z - lse)
+        float d = wd;
+        if (kSoftcap) {
+          const float th = z[j] * p.inv_softcap;                   // z / c
+          d = wd * fmaf(-th, th, 1.f);                             // w s (1 - (z/c)^2)
+        }
+        g[j] = d * (pr - (j == tj ? 1.f : 0.f));
+        if (j >= valid_cols) g[j] = 0.f;
+        colsum[j] += g[j];
+      }
+      uint4 pk;
+      pk.x = pack_bf16x2(g[0], g[1]);
+      pk.y = pack_bf16x2(g[2], g[3]);
+      pk.z = pack_bf16x2(g[4], g[5]);
+      pk.w = pack_bf16x2(g[6], g[7]);
+      __stcs(reinterpret_cast<uint4*>(gp + r * p.ldz), pk);
+    }
+    for (int r = rows; r < zero_rows; ++r)  // past the valid rows of a compacted chunk: exact zeros
+      __stcs(reinterpret_cast<uint4*>(gp + r * p.ldz), make_uint4(0u, 0u, 0u, 0u));
+    if (p.dbias_part) {
+      float* dst = p.dbias_part + rt * p.ldz + c0;
+#pragma unroll
+      for (int j = 0; j < kZGradVec; ++j)
+        if (j < valid_cols) dst[j] = colsum[j];
+    }
   }
 }
 
 cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream) {
   const int64_t gx = (p.vocab + kZGradCols - 1) / kZGradCols;
-  const int64_t gy = (p.rows + kZGradRows - 1) / kZGradRows;
-  if (gx == 0 || gy == 0) return cudaSuccess;
-  if (gy > 65535) return cudaErrorInvalidConfiguration;
-  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  const int64_t row_tiles = (p.rows + kZGradRows - 1) / kZGradRows;
+  if (gx == 0 || row_tiles == 0) return cudaSuccess;
+  if (gx > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(row_tiles < 65535 ? row_tiles : 65535));
   if (softcap) {
     zgrad_kernel<true><<<grid, kZGradThreads, 0, stream>>>(p);
   } else {
@@ -123,12 +129,12 @@ cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream
 }
 
 // dbias[j] = sum over m tiles of the per-tile column sums, in m order.
-__global__ void dbias_reduce_kernel(const float* __restrict__ part, int64_t ldg, int m_tiles, int64_t cols,
-                                    void* dbias, int bias_f32, const int32_t* row_count) {
+__global__ void dbias_reduce_kernel(const float* __restrict__ part, int64_t ldg, int m_tiles, int rows_per_tile,
+                                    int64_t cols, void* dbias, int bias_f32, const int32_t* row_count) {
   const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (j >= cols) return;
   // Under compaction only the tiles that hold a valid token were computed.
-  const int tiles = row_count ? min(m_tiles, (*row_count + kBM - 1) / kBM) : m_tiles;
+  const int tiles = row_count ? min(m_tiles, (*row_count + rows_per_tile - 1) / rows_per_tile) : m_tiles;
   float s = 0.f;
   for (int m = 0; m < tiles; ++m) s += part[static_cast<int64_t>(m) * ldg + j];
   if (bias_f32) {
@@ -138,12 +144,12 @@ __global__ void dbias_reduce_kernel(const float* __restrict__ part, int64_t ldg,
   }
 }
 
-cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int64_t cols, void* dbias,
-                                int bias_f32, const int32_t* row_count, cudaStream_t stream) {
+cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int rows_per_tile, int64_t cols,
+                                void* dbias, int bias_f32, const int32_t* row_count, cudaStream_t stream) {
   const int64_t blocks = (cols + 255) / 256;
   if (blocks == 0) return cudaSuccess;
-  dbias_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, ldg, m_tiles, cols, dbias, bias_f32,
-                                                                          row_count);
+  dbias_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, ldg, m_tiles, rows_per_tile, cols,
+                                                                          dbias, bias_f32, row_count);
   return cudaGetLastError();
 }
 

@@ -137,7 +137,7 @@ struct GradParams {
 constexpr int kZGradThreads = 256;
 constexpr int kZGradVec = 8;                               // columns per thread
 constexpr int kZGradCols = kZGradThreads * kZGradVec;      // 2048
-constexpr int kZGradRows = kBM;                            // rows per block = dbias partial granularity
+constexpr int kZGradRows = 32;     // rows per tile of a block = dbias partial granularity
 constexpr int kTokenChunkAlign = 256;  // token chunks start on multiples of this (>= any GEMM tile height)
 struct ZGradParams {
   int64_t rows, vocab;    // rows of this chunk

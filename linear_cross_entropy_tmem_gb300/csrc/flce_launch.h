@@ -77,8 +77,9 @@ cudaError_t launch_split_f32(const float* x, uint16_t* t0, uint16_t* t1, uint16_
                              cudaStream_t stream);
 cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream);
 cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream);
-cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int64_t cols, void* dbias,
-                                int bias_f32, const int32_t* row_count, cudaStream_t stream);
+// dbias[j] = sum over the m_tiles per-tile partials (tiles of rows_per_tile rows), in tile order.
+cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int rows_per_tile, int64_t cols,
+                                void* dbias, int bias_f32, const int32_t* row_count, cudaStream_t stream);
 cudaError_t launch_dh_finalize(const float* part, int64_t stride, int ksplit, int64_t rows, int64_t cols, void* out,
                                int out_f32, const int32_t* row_map, const int32_t* row_count, int grid,
                                cudaStream_t stream);

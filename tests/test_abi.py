@@ -132,11 +132,11 @@ def test_keep_logits_workspace(lib):
         assert a == (k if D >= 1024 else r)
         half = ((N + 1) // 2 + 255) // 256 * 256
         # kept logits + G, dbias partials, fp32 dW, dh K-split slots (at most 16), split records
-        bound = 6 * min(half, N) * ldz + 4 * ((N + 127) // 128) * ldz + 4 * V * D + 16 * 4 * half * D \
+        bound = 6 * min(half, N) * ldz + 4 * ((N + 31) // 32) * ldz + 4 * V * D + 16 * 4 * half * D \
             + (5 * 4 * 64 * 2 + 8) * half + (1 << 20)
         assert r < k <= bound
         if N * V >= 1 << 28:  # the chunk's kept logits + G stay within the 4 GiB budget (+ one row group)
-            assert k - 4 * V * D - 16 * 4 * half * D - 4 * ((N + 127) // 128) * ldz <= (4 << 30) + 6 * 256 * ldz \
+            assert k - 4 * V * D - 16 * 4 * half * D - 4 * ((N + 31) // 32) * ldz <= (4 << 30) + 6 * 256 * ldz \
                 + (5 * 4 * 64 * 2 + 8) * half + (1 << 20)
     # with compaction the layout adds the compaction buffers (row map, targets, hidden copy,
     # compacted lse / upstream grads, chunk row counts), about (4 + 8 + 2 D + 4 + 4) bytes per token
