@@ -53,6 +53,11 @@ def parse_args(argv=None):
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures of a small case)")
     ap.add_argument("--separate", action="store_true",
                     help="flce_forward + flce_backward per step instead of one flce_forward_backward call")
+    ap.add_argument("--autograd", action="store_true",
+                    help="time the torch autograd wrapper: linear_cross_entropy(...) + loss.backward() per step "
+                         "(gradients computed in the forward for mean / sum); no e2e leg")
+    ap.add_argument("--grad-in-backward", action="store_true",
+                    help="with --autograd: the separate backward instead of gradients in the forward")
     ap.add_argument("--bwd", default="auto", choices=["auto", "recompute", "keep_logits"],
                     help="backward algorithm of the fused call (FLCE_FLAG_BWD_*); auto keeps the logits of "
                          "token chunks from D = 1024 up")
@@ -242,7 +247,8 @@ def reference_arm(args):
 class Runner:
     """Preallocated buffers and raw C-ABI calls for one forward + backward step."""
 
-    def __init__(self, w, device, seed_offset=0, compact=False, fused=False, bwd="auto"):
+    def __init__(self, w, device, seed_offset=0, compact=False, fused=False, bwd="auto", autograd=False,
+                 grad_in_forward=True):
         import torch
 
         import linear_cross_entropy_tmem_gb300.api as api
@@ -281,11 +287,26 @@ class Runner:
                          p(self.n_valid), p(self.dloss), p(self.dh), p(self.dW), p(self.db), p(self.ws_b),
                          self.ws_b.numel(), s)
 
+        self.autograd = autograd
+        self.grad_in_forward = grad_in_forward
+        if autograd:
+            self.leaves = [x.detach().requires_grad_(True) if x is not None else None for x in (self.h, self.W, self.b)]
         self.fb_args = (ctypes.byref(self.prob), p(self.h), p(self.W), p(self.b), p(self.t), p(self.dloss),
                         p(self.loss), p(self.lse), None, p(self.correct), p(self.n_valid), p(self.ent_sum),
                         p(self.dh), p(self.dW), p(self.db), p(self.ws_fb), self.ws_fb.numel(), s)
 
     def step(self):
+        if self.autograd:  # the torch API a training loop calls
+            import linear_cross_entropy_tmem_gb300 as F
+            h, W, b = self.leaves
+            for x in self.leaves:
+                if x is not None:
+                    x.grad = None
+            w = self.w
+            loss = F.linear_cross_entropy(h, W, self.t, b, logit_scale=w.logit_scale, softcap=w.softcap,
+                                          reduction=w.reduction, grad_in_forward=self.grad_in_forward)[0]
+            loss.backward(self.dloss if w.reduction == "none" else None)
+            return
         if self.fused:
             self.B.check(self.lib.flce_forward_backward(*self.fb_args), "flce_forward_backward")
             return
@@ -353,7 +374,12 @@ def flce_arm(args):
     lib = B.load()
     B.check(lib.flce_testing_set_gemm_mode(args.gemm_mode), "gemm mode")
     B.check(lib.flce_testing_set_token_chunk(args.token_chunk), "token chunk")  # before sizing the workspace
-    run = Runner(w, device, seed_offset=rank, compact=args.compact, fused=not args.separate, bwd=args.bwd)
+    run = Runner(w, device, seed_offset=rank, compact=args.compact, fused=not args.separate, bwd=args.bwd,
+                 autograd=args.autograd, grad_in_forward=not args.grad_in_backward)
+    if args.autograd:
+        if args.compact:
+            raise SystemExit("--autograd does not combine with --compact")
+        args.no_e2e = True
 
     for _ in range(args.warmup):
         run.step()
@@ -390,11 +416,12 @@ def flce_arm(args):
     clock = clocks.stop()
     ms = start.elapsed_time(end) / args.steps
     status = ctypes.c_int(0)
-    ws_status = run.ws_fb if run.fused else run.ws_b
-    B.check(lib.flce_read_device_status(ctypes.c_void_p(ws_status.data_ptr()), None, ctypes.byref(status)),
-            "status")
-    if status.value != 0:
-        raise RuntimeError(f"device status {status.value} during the timed region")
+    if not args.autograd:  # (the autograd API allocates its workspace per call)
+        ws_status = run.ws_fb if run.fused else run.ws_b
+        B.check(lib.flce_read_device_status(ctypes.c_void_p(ws_status.data_ptr()), None, ctypes.byref(status)),
+                "status")
+        if status.value != 0:
+            raise RuntimeError(f"device status {status.value} during the timed region")
 
     per_kind = {}
     for i in range(count.value):
@@ -492,7 +519,10 @@ def flce_arm(args):
                        "reduction": w.reduction, "parallelism": f"replicas x{world}" if world > 1 else "none",
                        "gemm_mode": ["auto", "single-cta", "cta-pair"][args.gemm_mode],
                        "compact_valid_tokens": bool(args.compact),
-                       "entry": "flce_forward + flce_backward" if args.separate else "flce_forward_backward",
+                       "entry": ("linear_cross_entropy + backward (autograd, gradients "
+                                 + ("in the backward)" if args.grad_in_backward else "in the forward)"))
+                       if args.autograd else
+                       "flce_forward + flce_backward" if args.separate else "flce_forward_backward",
                        "backward": "keep_logits (token chunks, 6NVD)" if keep else "recompute (8NVD)",
                        "l2": "inputs larger than L2 (1.25 GB head), no flush"},
             # executed flops: 6NVD with kept logits, 8NVD with the recompute; the metric's own

@@ -255,6 +255,22 @@ FLCE_API int flce_forward_backward(const flce_problem* problem, const void* hidd
                                    size_t workspace_bytes, flce_stream_t stream);
 
 /*
+ * Gradients computed before the upstream gradient is known, scaled once it is:
+ * x[i] = rn(x[i] * *scale) in place, with an fp32 multiply and one rounding
+ * (Liger-Kernel PR #1574, Summary item 2: the saved gradient scaled by the
+ * upstream gradient in the backward).  A caller that runs
+ * flce_forward_backward with dloss = 1 for a mean / sum loss (whose
+ * gradients are linear in the scalar upstream gradient) scales dhidden,
+ * dweight and dbias with it when the upstream gradient arrives.
+ *   scale   device pointer to one fp32; when it holds exactly 1 the buffer is
+ *           neither read nor written
+ *   x, n    device buffer of n elements of `dtype` (FLCE_BF16 or FLCE_F32)
+ * Asynchronous on `stream`.  Returns FLCE_OK, FLCE_ERR_INVALID_ARG,
+ * FLCE_ERR_UNSUPPORTED_DTYPE or FLCE_ERR_CUDA.
+ */
+FLCE_API int flce_scale_gradient(const float* scale, void* x, int64_t n, int32_t dtype, flce_stream_t stream);
+
+/*
  * Synchronises `stream`, then copies the device status word at the start of
  * `workspace` into *status (FLCE_OK or one of the FLCE_ERR_* device codes).
  * Returns FLCE_OK, FLCE_ERR_INVALID_ARG or FLCE_ERR_CUDA.

@@ -6,5 +6,5 @@ materialising the (tokens x vocab) logits.  See ``include/flce.h``.
 """
 from .api import (  # noqa: F401
     ForwardResult, LinearCrossEntropy, flce_backward, flce_forward, flce_forward_backward, flce_read_device_status,
-    flce_status_string, flce_workspace_size, linear_cross_entropy, make_problem,
+    flce_status_string, flce_workspace_size, linear_cross_entropy, make_problem, scale_gradient,
 )

@@ -215,35 +215,68 @@ def flce_status_string(status: int) -> str:
     return B.load().flce_status_string(int(status)).decode()
 
 
+def scale_gradient(x: torch.Tensor, scale: torch.Tensor) -> torch.Tensor:
+    """``x *= scale`` in place on the device (see ``flce_scale_gradient``); ``scale`` is a one-element
+    fp32 device tensor, and nothing is read or written when it holds exactly 1."""
+    _require_cuda(x, scale)
+    _contig(x, "x")
+    scale = scale.to(dtype=torch.float32).contiguous().reshape(-1)[:1]
+    B.check(B.load().flce_scale_gradient(_ptr(scale), _ptr(x), x.numel(), _dtype_code(x.dtype, "x"),
+                                         _stream(x.device)), "flce_scale_gradient")
+    return x
+
+
 class LinearCrossEntropy(torch.autograd.Function):
-    """Autograd wrapper: loss of ``hidden @ weight.T (+ bias)`` against ``targets``."""
+    """Autograd wrapper: loss of ``hidden @ weight.T (+ bias)`` against ``targets``.
+
+    With ``grad_in_forward`` (the default) and a mean or sum loss, the forward already computes the
+    gradients for an upstream gradient of 1 in one fused call (``flce_forward_backward``, which keeps
+    the logits of token chunks from D = 1024 up), and the backward scales them by the upstream
+    gradient in place (``flce_scale_gradient``; nothing happens for the usual 1).  Gradients are linear
+    in a scalar upstream gradient, so this is the same result up to one rounding.  A second backward
+    through the same graph recomputes them (``flce_backward``) instead of rescaling."""
 
     @staticmethod
     def forward(ctx, hidden, weight, bias, targets, logit_scale, softcap, ignore_index, reduction,
-                num_items_in_batch=0.0, compact=False):
-        r = flce_forward(hidden, weight, targets, bias, logit_scale=logit_scale, softcap=softcap,
-                         ignore_index=ignore_index, reduction=reduction, num_items_in_batch=num_items_in_batch,
-                         compact=compact)
+                num_items_in_batch=0.0, compact=False, grad_in_forward=True, fp32_full=False):
+        kw = dict(logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index, reduction=reduction,
+                  num_items_in_batch=num_items_in_batch, compact=compact, fp32_full=fp32_full)
+        need = any(ctx.needs_input_grad[:3])
+        ctx.grads = None
+        if grad_in_forward and need and reduction != "none":
+            ones = torch.ones(1, dtype=torch.float32, device=hidden.device)
+            r, grads = flce_forward_backward(hidden, weight, targets, ones, bias, **kw)
+            ctx.grads = grads
+        else:
+            r = flce_forward(hidden, weight, targets, bias, **kw)
         ctx.save_for_backward(hidden, weight, bias, targets, r.lse, r.n_valid)
-        ctx.cfg = (logit_scale, softcap, ignore_index, reduction, num_items_in_batch, compact)
+        ctx.cfg = kw
         ctx.mark_non_differentiable(r.correct, r.n_valid, r.entropy_sum)
         return r.loss, r.correct, r.n_valid, r.entropy_sum
 
     @staticmethod
     def backward(ctx, dloss, _dc, _dn, _de):
-        hidden, weight, bias, targets, lse, n_valid = ctx.saved_tensors
-        s, c, ig, red, items, cmp = ctx.cfg
-        dh, dW, db = flce_backward(hidden, weight, targets, lse, n_valid, dloss.contiguous(), bias,
-                                   logit_scale=s, softcap=c, ignore_index=ig, reduction=red,
-                                   num_items_in_batch=items, compact=cmp)
-        return dh, dW, db, None, None, None, None, None, None, None
+        if ctx.grads is not None:
+            dh, dW, db = ctx.grads
+            ctx.grads = None  # scaled in place once; another backward recomputes
+            g = dloss.reshape(-1)[:1]
+            for x in (dh, dW, db):
+                if x is not None:
+                    scale_gradient(x, g)
+        else:
+            hidden, weight, bias, targets, lse, n_valid = ctx.saved_tensors
+            dh, dW, db = flce_backward(hidden, weight, targets, lse, n_valid, dloss.contiguous(), bias, **ctx.cfg)
+        return dh, dW, db, None, None, None, None, None, None, None, None, None
 
 
 def linear_cross_entropy(hidden, weight, targets, bias=None, *, logit_scale=1.0, softcap=0.0,
-                         ignore_index=-100, reduction="mean", num_items_in_batch=0.0, compact=False):
-    """Returns (loss, correct, n_valid, entropy_sum); only ``loss`` carries gradients."""
+                         ignore_index=-100, reduction="mean", num_items_in_batch=0.0, compact=False,
+                         grad_in_forward=True, fp32_full=False):
+    """Returns (loss, correct, n_valid, entropy_sum); only ``loss`` carries gradients.
+    ``grad_in_forward``: see :class:`LinearCrossEntropy`."""
     return LinearCrossEntropy.apply(hidden, weight, bias, targets, float(logit_scale), float(softcap),
-                                    int(ignore_index), reduction, float(num_items_in_batch), bool(compact))
+                                    int(ignore_index), reduction, float(num_items_in_batch), bool(compact),
+                                    bool(grad_in_forward), bool(fp32_full))
 
 
 def testing_gemm(A: torch.Tensor, B_: torch.Tensor, *, a_mn_major: bool, b_mn_major: bool, M: int, N: int,

@@ -1168,6 +1168,18 @@ int flce_forward_backward(const flce_problem* p, const void* hidden, const void*
                       dbias);
 }
 
+int flce_scale_gradient(const float* scale, void* x, int64_t n, int32_t dtype, flce_stream_t stream) {
+  if (!scale || n < 0 || (n > 0 && !x)) return FLCE_ERR_INVALID_ARG;
+  if (dtype != FLCE_BF16 && dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED_DTYPE;
+  if (n == 0) return FLCE_OK;
+  DeviceInfo dev;
+  FLCE_TRY(get_device(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return logged(FLCE_LAUNCH_OTHER, st, [&] {
+    return launch_scale(scale, x, n, dtype == FLCE_F32 ? 1 : 0, dev.num_sms * 8, st);
+  });
+}
+
 int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit) {
   if (chunk_cols < 0 || dh_ksplit < 0 || dh_ksplit > kMaxKSplit) return FLCE_ERR_INVALID_ARG;
   g_force_chunk_cols.store(chunk_cols);

@@ -128,6 +128,29 @@ cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream
   return cudaGetLastError();
 }
 
+// x[i] = rn(x[i] * s) in place (fp32 multiply, one rounding), s = *scale read
+// on the device; nothing is read or written when s == 1.
+__global__ void scale_kernel(const float* __restrict__ scale, void* x, int64_t n, int x_f32) {
+  const float s = __ldg(scale);
+  if (s == 1.0f) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (x_f32) {
+    float* v = static_cast<float*>(x);
+    for (int64_t i = i0; i < n; i += stride) v[i] *= s;
+  } else {
+    uint16_t* v = static_cast<uint16_t*>(x);
+    for (int64_t i = i0; i < n; i += stride)
+      v[i] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(static_cast<uint32_t>(v[i]) << 16) * s, 0.f) & 0xFFFFu);
+  }
+}
+
+cudaError_t launch_scale(const float* scale, void* x, int64_t n, int x_f32, int grid, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  scale_kernel<<<grid, 256, 0, stream>>>(scale, x, n, x_f32);
+  return cudaGetLastError();
+}
+
 // dbias[j] = sum over m tiles of the per-tile column sums, in m order.
 __global__ void dbias_reduce_kernel(const float* __restrict__ part, int64_t ldg, int m_tiles, int rows_per_tile,
                                     int64_t cols, void* dbias, int bias_f32, const int32_t* row_count) {

@@ -77,6 +77,8 @@ cudaError_t launch_split_f32(const float* x, uint16_t* t0, uint16_t* t1, uint16_
                              cudaStream_t stream);
 cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream);
 cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream);
+// x *= *scale in place (bf16 or fp32), skipped on the device when *scale == 1.
+cudaError_t launch_scale(const float* scale, void* x, int64_t n, int x_f32, int grid, cudaStream_t stream);
 // dbias[j] = sum over the m_tiles per-tile partials (tiles of rows_per_tile rows), in tile order.
 cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int rows_per_tile, int64_t cols,
                                 void* dbias, int bias_f32, const int32_t* row_count, cudaStream_t stream);

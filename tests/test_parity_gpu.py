@@ -183,6 +183,53 @@ def test_autograd_wrapper_matches_direct_calls():
     assert torch.equal(hh.grad, dh) and torch.equal(WW.grad, dW) and torch.equal(bb.grad, db)
 
 
+def test_scale_gradient_is_one_fp32_multiply_and_rounding():
+    """flce_scale_gradient: x = rn(x * s) in place, bit for bit what an fp32 multiply followed by one
+    rounding to the buffer's dtype gives; s == 1 leaves the buffer untouched."""
+    import linear_cross_entropy_tmem_gb300 as F
+    g = torch.Generator().manual_seed(31)
+    for dt in (torch.bfloat16, torch.float32):
+        x0 = (torch.randn(100003, generator=g) * 3).to(dt).cuda()
+        for s in (2.5, -0.37, 1.0, 0.0):
+            x = x0.clone()
+            F.scale_gradient(x, torch.full((1,), s, device="cuda"))
+            torch.cuda.synchronize()
+            assert torch.equal(x, (x0.float() * s).to(dt)), (dt, s)
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+@pytest.mark.parametrize("D", [200, 1024], ids=["recompute", "keep-logits"])
+def test_autograd_gradients_in_forward(D, reduction):
+    """The autograd wrapper computes mean / sum gradients in the forward (fused call with an upstream
+    gradient of 1) and scales them by the upstream gradient in the backward; 'none' keeps the
+    separate backward.  Checked against the oracle with a non-power-of-two upstream gradient, and a
+    second backward through the same graph (retain_graph) accumulates the same gradient again."""
+    import linear_cross_entropy_tmem_gb300 as F
+    w = Workload("ag", 700, D, 3000, sigma_w=0.1, bias=True, softcap=10.0, reduction=reduction, seed=15)
+    hc, Wc, bc, tc, dc = make_inputs(w, "cpu")
+    h, W, b, t = (x.cuda() for x in (hc, Wc, bc, tc))
+    up = dc.cuda() if reduction == "none" else torch.full((), 2.5, device="cuda")
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=reduction)
+    ref_b = oracle.backward(hc, Wc, bc, tc, dloss=up.cpu().reshape(-1), **kw)
+    hh, WW, bb = (x.clone().requires_grad_(True) for x in (h, W, b))
+    loss, correct, n_valid, ent = F.linear_cross_entropy(hh, WW, t, bb, **kw)
+    loss.backward(up, retain_graph=True)
+    torch.cuda.synchronize()
+    compare_backward((hh.grad, WW.grad, bb.grad), ref_b)
+    first = [x.grad.clone() for x in (hh, WW, bb)]
+    loss.backward(up)  # recomputed: the saved gradients were scaled in place by the first backward
+    torch.cuda.synchronize()
+    for x, g1 in zip((hh, WW, bb), first):
+        assert oracle.relative_frobenius(x.grad.float().cpu(), 2 * g1.float().cpu()) <= 1e-2
+    hh2, WW2, bb2 = (x.clone().requires_grad_(True) for x in (h, W, b))
+    loss2, *_ = F.linear_cross_entropy(hh2, WW2, t, bb2, grad_in_forward=False, **kw)
+    assert torch.equal(loss, loss2)
+    loss2.backward(up)
+    torch.cuda.synchronize()
+    for g1, x in zip(first, (hh2, WW2, bb2)):
+        assert oracle.relative_frobenius(g1.float().cpu(), x.grad.float().cpu()) <= 1e-2
+
+
 # ---------------------------------------------------------------------------
 # num_items_in_batch and valid-token compaction
 # ---------------------------------------------------------------------------
