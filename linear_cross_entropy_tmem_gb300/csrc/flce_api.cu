@@ -84,6 +84,20 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS ? FLCE_OK : FLCE_ERR_CUDA;
 }
 
+// Output map of the TMA-store epilogue: [rows][cols] bf16 or fp32, 32 x 32
+// boxes whose 64-byte (bf16) or 128-byte (fp32) rows use the matching swizzle.
+int make_store_map(CUtensorMap* m, void* base, bool f32, uint64_t cols, uint64_t rows, uint64_t row_bytes) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FLCE_OK : FLCE_ERR_CUDA;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int validate(const flce_problem* p) {
@@ -772,9 +786,9 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     StoreParams sp{};
     sp.rows = width;
     sp.cols = D;
-    sp.out = static_cast<uint8_t*>(dweight) + size_t(v0) * D * w_elem;
-    sp.ldo = D;
     sp.out_f32 = w_elem == 4 ? 1 : 0;
+    FLCE_TRY(make_store_map(&sp.out_map, static_cast<uint8_t*>(dweight) + size_t(v0) * D * w_elem, w_elem == 4, D,
+                            width, D * w_elem));
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
                     [&] { return launch_store_gemm(pair_dw, mw, s2, sp, status, dev.num_sms, st); }));
 
@@ -1232,9 +1246,8 @@ int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int6
   StoreParams sp{};
   sp.rows = M;
   sp.cols = N;
-  sp.out = C;
-  sp.ldo = ldc;
   sp.out_f32 = 1;
+  FLCE_TRY(make_store_map(&sp.out_map, C, true, N, M, ldc * 4));
   return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_store_gemm(pair, m, s, sp, nullptr, dev.num_sms, st); });
 }
 

@@ -212,6 +212,8 @@ __device__ __forceinline__ float max32(const float (&z)[32]) {
 template <bool kBias, bool kSoftcap>
 struct EpiFwd {
   using Params = FwdParams;
+  static constexpr int kTailBytes = 0;  // epilogue shared memory
+  __device__ static void finish(const Params&) {}
   struct State {
     int64_t row, target;
     float m, s, a, best, zt;
@@ -343,6 +345,8 @@ __device__ __forceinline__ float token_weight(int reduction, const float* dloss,
 template <bool kBias, bool kSoftcap>
 struct EpiGrad {
   using Params = GradParams;
+  static constexpr int kTailBytes = kEpiSmemBytes;  // dbias column-sum staging
+  __device__ static void finish(const Params&) {}
   struct State {
     int64_t row, target;
     float lse2;  // lse * log2(e)
@@ -454,76 +458,70 @@ struct EpiGrad {
 // ============================================================================
 struct EpiStore {
   using Params = StoreParams;
+  // One staging buffer per epilogue warp.
+  static constexpr int kTailBytes = kEpilogueGroups * kEpilogueWarps * kStoreStageBytes;
   struct State {
     int64_t row;
   };
   __device__ static void begin_unit(const Params&, const Unit& u, State& st, int) { st.row = u.row0 + epi_tid(); }
-  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st, float*,
-                              int) {
+
+  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State&, float* epi_smem,
+                              int grp) {
     const int64_t col_tile = static_cast<int64_t>(n_tile) * kBN;
+    const int nch = chunks_below(col_tile, p.cols);
+    const int warp = threadIdx.x >> 5;  // 0-7: the CTA's epilogue warps
+    const int64_t row_base = u.row0 + (warp % kEpilogueWarps) * 32;
+    if (row_base >= p.rows) return;  // this warp's 32 rows are past the output
+    uint8_t* buf = reinterpret_cast<uint8_t*>(epi_smem - grp * kEpiSmemGroupFloats) + warp * kStoreStageBytes;
     if (u.kb_count == 0) {  // no K blocks (all tokens ignored under compaction): the product is zero
       uint32_t zero[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) zero[j] = 0u;
-      const int nch = chunks_below(col_tile, p.cols);
 #pragma unroll 1
-      for (int c = 0; c < nch; ++c) store(p, st, col_tile + c * 32, zero);
+      for (int c = 0; c < nch; ++c) put(p, buf, col_tile + c * 32, row_base, zero);
       return;
     }
-    for_each_tmem_chunk(taddr, chunks_below(col_tile, p.cols),
-                        [&](const uint32_t (&r)[32], int c) { store(p, st, col_tile + c * 32, r); });
+    for_each_tmem_chunk(taddr, nch, [&](const uint32_t (&r)[32], int c) { put(p, buf, col_tile + c * 32, row_base, r); });
   }
 
-  __device__ static void store(const Params& p, const State& st, int64_t col, const uint32_t (&r)[32]) {
-    {
-      if (st.row >= p.rows) return;
-      const int64_t n = p.cols - col;
-      if (p.out_f32) {
-        float* dst = reinterpret_cast<float*>(p.out) + st.row * p.ldo + col;
-        if (n >= 32 && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+  // Stages this warp's 32 x 32 box (lane = row) in its buffer with the tensor
+  // map's swizzle, then lane 0 stores it with TMA.  Swizzle: 16-byte chunk j
+  // of row r lands at chunk j ^ (bits 7-8 of the row offset) for 64-byte rows
+  // (bf16) and j ^ (bits 7-9) for 128-byte rows (fp32).
+  __device__ static void put(const Params& p, uint8_t* buf, int64_t col, int64_t row_base,
+                             const uint32_t (&r)[32]) {
+    const uint32_t lane = lane_id();
+    if (lane == 0) bulk_wait_read_all();  // the previous box has left this buffer
+    __syncwarp();
+    if (p.out_f32) {
+      uint8_t* row = buf + lane * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st_global_v8(dst + 8 * q, r[8 * q], r[8 * q + 1], r[8 * q + 2], r[8 * q + 3], r[8 * q + 4], r[8 * q + 5],
-                         r[8 * q + 6], r[8 * q + 7]);
-        } else if (n >= 32) {
+      for (int j = 0; j < 8; ++j)
+        st_shared_v4(row + ((j ^ (lane & 7)) * 16), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    } else {
+      uint8_t* row = buf + lane * 64;
+      const auto f = [&](int j) { return __uint_as_float(r[j]); };
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<uint4*>(dst)[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < n) dst[j] = __uint_as_float(r[j]);
-        }
-      } else {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + st.row * p.ldo + col;
-        const auto f = [&](int j) { return __uint_as_float(r[j]); };
-        if (n >= 32 && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            st_global_v8(dst + 16 * q, pack_bf16x2(f(16 * q + 0), f(16 * q + 1)),
-                         pack_bf16x2(f(16 * q + 2), f(16 * q + 3)), pack_bf16x2(f(16 * q + 4), f(16 * q + 5)),
-                         pack_bf16x2(f(16 * q + 6), f(16 * q + 7)), pack_bf16x2(f(16 * q + 8), f(16 * q + 9)),
-                         pack_bf16x2(f(16 * q + 10), f(16 * q + 11)), pack_bf16x2(f(16 * q + 12), f(16 * q + 13)),
-                         pack_bf16x2(f(16 * q + 14), f(16 * q + 15)));
-        } else if (n >= 32) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 pk;
-            pk.x = pack_bf16x2(f(8 * q + 0), f(8 * q + 1));
-            pk.y = pack_bf16x2(f(8 * q + 2), f(8 * q + 3));
-            pk.z = pack_bf16x2(f(8 * q + 4), f(8 * q + 5));
-            pk.w = pack_bf16x2(f(8 * q + 6), f(8 * q + 7));
-            reinterpret_cast<uint4*>(dst)[q] = pk;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < n) dst[j] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]), 0.f) & 0xFFFFu);
-        }
-      }
+      for (int j = 0; j < 4; ++j)
+        st_shared_v4(row + ((j ^ ((lane >> 1) & 3)) * 16), pack_bf16x2(f(8 * j), f(8 * j + 1)),
+                     pack_bf16x2(f(8 * j + 2), f(8 * j + 3)), pack_bf16x2(f(8 * j + 4), f(8 * j + 5)),
+                     pack_bf16x2(f(8 * j + 6), f(8 * j + 7)));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&p.out_map, buf, static_cast<int32_t>(col), static_cast<int32_t>(row_base));
+      bulk_commit_group();
     }
   }
+
   __device__ static void end_unit(const Params&, const Unit&, State&, int) {}
+
+  // Every box this warp stored is complete before the kernel ends.
+  __device__ static void finish(const Params&) {
+    if (lane_id() == 0) bulk_wait_all();
+    __syncwarp();
+  }
 };
 
 // ============================================================================
@@ -531,6 +529,8 @@ struct EpiStore {
 // ============================================================================
 struct EpiAccum {
   using Params = AccumParams;
+  static constexpr int kTailBytes = 0;
+  __device__ static void finish(const Params&) {}
   struct State {
     int64_t row;
   };
@@ -654,7 +654,7 @@ __device__ __forceinline__ GemmSmem carve_smem(uint8_t* raw) {
   s.drain = s.tempty + kAccBufs;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
   s.ctl = reinterpret_cast<CtaControl*>(s.tmem_slot + 2);
-  s.epi = reinterpret_cast<float*>(bar + kBarrierBytes);
+  s.epi = reinterpret_cast<float*>(bar + 1024);  // 1024-aligned epilogue region
   return s;
 }
 
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                 const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_b0,
                 const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_b2,
-                const GemmSched sc, const typename Epi::Params ep, int* status) {
+                const GemmSched sc, const __grid_constant__ typename Epi::Params ep, int* status) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem sm = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5;
@@ -865,6 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) Epi::end_unit(ep, u, st, grp);
     }
+    Epi::finish(ep);
   }
 
   tc_fence_before();
@@ -899,7 +900,7 @@ __device__ __forceinline__ GemmSmem carve_smem_pair(uint8_t* raw) {
   s.drain = s.tempty + kAccBufs;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
   s.ctl = reinterpret_cast<CtaControl*>(s.tmem_slot + 2);
-  s.epi = reinterpret_cast<float*>(bar + kBarrierBytes);
+  s.epi = reinterpret_cast<float*>(bar + 1024);  // 1024-aligned epilogue region
   return s;
 }
 
@@ -914,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                      const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_b0,
                      const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_b2,
-                     const GemmSched sc, const typename Epi::Params ep, int* status) {
+                     const GemmSched sc, const __grid_constant__ typename Epi::Params ep, int* status) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem sm = carve_smem_pair(smem_raw);
   const int warp = threadIdx.x >> 5;
@@ -1100,6 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) Epi::end_unit(ep, u, st, grp);
     }
+    Epi::finish(ep);
     if (!ok) aborted = true;
   }
 

@@ -15,10 +15,11 @@ template <class Epi>
 static cudaError_t launch_gemm_single(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
                                       int* status, int num_sms, cudaStream_t stream) {
   auto kern = gemm_kernel<Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  constexpr int smem = kGemmSmemBase + Epi::kTailBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(sc.total_units, num_sms));
-  kern<<<grid, kThreads, kGemmSmemBytes, stream>>>(m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
+  kern<<<grid, kThreads, smem, stream>>>(m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
   return cudaGetLastError();
 }
 
@@ -26,7 +27,8 @@ template <class Epi>
 static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
                                     int* status, int num_sms, cudaStream_t stream) {
   auto kern = gemm_pair_kernel<Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmPairSmemBytes);
+  constexpr int smem = kGemmPairSmemBase + Epi::kTailBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -35,7 +37,7 @@ static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kGemmPairSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;

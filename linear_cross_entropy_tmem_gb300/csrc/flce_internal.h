@@ -2,6 +2,8 @@
 // and the sm_103a kernels.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstdint>
 
 namespace flce {
@@ -40,9 +42,10 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;               // 320
 constexpr int kEpiSmemGroupFloats = kEpilogueWarps * kBN;   // dbias column-sum staging per group
 constexpr int kEpiSmemBytes = kEpilogueGroups * kEpiSmemGroupFloats * 4;
 constexpr int kBarrierBytes = 256;
-constexpr int kGemmSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarrierBytes + kEpiSmemBytes;
-constexpr int kGemmPairSmemBytes =
-    1024 /*alignment slack*/ + kStagesPair * kStagePairBytes + kBarrierBytes + kEpiSmemBytes;
+// Dynamic shared memory: alignment slack, the stage ring, the barriers padded
+// to 1024 bytes, then the epilogue's own region (its 1024-aligned tail).
+constexpr int kGemmSmemBase = 1024 + kStages * kStageBytes + 1024;
+constexpr int kGemmPairSmemBase = 1024 + kStagesPair * kStagePairBytes + 1024;
 
 constexpr int kMaxSegments = 6;   // fp32 x fp32 with three-term splits: 6 products
 
@@ -158,11 +161,13 @@ struct ZGradParams {
   float* dbias_part;      // [ceil(rows / kZGradRows)][ldz] or nullptr
 };
 
-// Plain store of the accumulator (dW, and the test GEMM).
+// Plain store of the accumulator (dW, and the test GEMM), through TMA stores:
+// each epilogue warp stages its 32 rows x 32 columns in shared memory
+// (kStoreStageBytes per warp) and one lane copies the box out.
+constexpr int kStoreStageBytes = 32 * 32 * 4;
 struct StoreParams {
+  CUtensorMap out_map;    // [rows][cols] in the output dtype, box 32 x 32, 64-byte (bf16) / 128-byte (fp32) swizzle
   int64_t rows, cols;     // valid extent of the output
-  void* out;
-  int64_t ldo;
   int32_t out_f32;
 };
 
