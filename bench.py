@@ -405,9 +405,11 @@ def flce_arm(args):
     torch.cuda.synchronize()
     launches0 = lib.flce_testing_launch_count()
     B.check(lib.flce_testing_set_launch_log(recs, cap, ctypes.byref(count)), "launch log")
+    step_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     start.record()
-    for _ in range(args.steps):
+    for k in range(args.steps):
         run.step()
+        step_ends[k].record()
     end.record()
     torch.cuda.synchronize()
     B.check(lib.flce_testing_set_launch_log(None, 0, None), "launch log")
@@ -415,6 +417,11 @@ def flce_arm(args):
     barrier(dist, device)
     clock = clocks.stop()
     ms = start.elapsed_time(end) / args.steps
+    per_step = [start.elapsed_time(step_ends[0])] + [step_ends[k - 1].elapsed_time(step_ends[k])
+                                                      for k in range(1, args.steps)]
+    qs = statistics.quantiles(per_step, n=10, method="inclusive") if len(per_step) > 1 else per_step * 9
+    step_quantiles = {"p20": qs[1], "p50": statistics.median(per_step), "p80": qs[7], "min": min(per_step),
+                      "max": max(per_step)}
     status = ctypes.c_int(0)
     if not args.autograd:  # (the autograd API allocates its workspace per call)
         ws_status = run.ws_fb if run.fused else run.ws_b
@@ -513,6 +520,7 @@ def flce_arm(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step_quantiles": step_quantiles,
             "vs_baseline": None, "dtype": "bf16" if w.hidden_dtype == torch.bfloat16 else "f32+bf16",
             "data": "synthetic",
             "config": {"workload": w.name, "n_tokens": w.n_tokens, "hidden": w.hidden, "vocab": w.vocab,
