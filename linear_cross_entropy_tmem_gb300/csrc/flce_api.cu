@@ -1089,6 +1089,15 @@ int zero_grads_for_empty(const flce_problem* p, void* dweight, void* dbias, cuda
   return FLCE_OK;
 }
 
+// A one-word vocabulary: the softmax is exactly 1, so (softmax - onehot) and
+// every gradient are exactly 0 (the kernels would leave rounding noise of
+// e^(z - lse) - 1 instead).
+int zero_grads_single_class(const flce_problem* p, void* dhidden, void* dweight, void* dbias, cudaStream_t st) {
+  const size_t h_elem = p->hidden_dtype == FLCE_F32 ? 4 : 2;
+  FLCE_TRY(fail(cudaMemsetAsync(dhidden, 0, size_t(p->n_tokens) * p->hidden * h_elem, st)));
+  return zero_grads_for_empty(p, dweight, dbias, st);
+}
+
 }  // namespace
 }  // namespace flce
 
@@ -1137,6 +1146,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   int* status = reinterpret_cast<int*>(ws + L.status);
   FLCE_TRY(fail(cudaMemsetAsync(status, 0, sizeof(int), st)));
   if (p->n_tokens == 0) return zero_grads_for_empty(p, dweight, dbias, st);
+  if (p->vocab == 1) return zero_grads_single_class(p, dhidden, dweight, dbias, st);
   Prep pr;
   FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, weight, targets, lse, dloss, nullptr, nullptr, nullptr, &pr));
   const float* lse_use = pr.cmp ? pr.c_lse : lse;
@@ -1171,11 +1181,13 @@ int flce_forward_backward(const flce_problem* p, const void* hidden, const void*
   FLCE_TRY(prepare(p, L, dev, ws, status, st, hidden, weight, targets, nullptr, dloss, lse, entropy,
                    p->reduction == FLCE_RED_NONE ? loss : nullptr, &pr));
   if (L.token) {
-    return run_fused_tokens(p, L, dev, ws, status, st, bias, pr, dloss, loss, lse, entropy, correct,
-                            n_valid, entropy_sum, dhidden, dweight, dbias);
+    FLCE_TRY(run_fused_tokens(p, L, dev, ws, status, st, bias, pr, dloss, loss, lse, entropy, correct, n_valid,
+                              entropy_sum, dhidden, dweight, dbias));
+    return p->vocab == 1 ? zero_grads_single_class(p, dhidden, dweight, dbias, st) : FLCE_OK;
   }
   FLCE_TRY(run_forward(p, L, dev, ws, status, st, bias, pr, loss, lse, entropy, correct, n_valid,
                        entropy_sum, pr.cmp ? pr.c_lse : nullptr));
+  if (p->vocab == 1) return zero_grads_single_class(p, dhidden, dweight, dbias, st);
   const float* lse_use = pr.cmp ? pr.c_lse : lse;
   const float* dloss_use = pr.c_dloss ? pr.c_dloss : dloss;
   return run_backward(p, L, dev, ws, status, st, bias, pr, lse_use, n_valid, dloss_use, dhidden, dweight,
