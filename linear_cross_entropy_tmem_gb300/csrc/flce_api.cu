@@ -937,6 +937,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     fp.z_target = reinterpret_cast<float*>(ws + L.z_target);
     fp.z_out = z;
     fp.ldz = L.ldz;
+    FLCE_TRY(make_store_map(&fp.z_map, z, true, L.ldz, rows, L.ldz * 4));
     FLCE_TRY(logged(FLCE_LAUNCH_FWD_LOGITS, st, [&] {
       return launch_fwd_gemm(bias != nullptr, softcap, pair_f, fm, sf, fp, status, dev.num_sms, st);
     }));

@@ -209,11 +209,58 @@ __device__ __forceinline__ float max32(const float (&z)[32]) {
 // ============================================================================
 // Epilogue: forward statistics over one vocabulary split
 // ============================================================================
+// Stages this warp's 32 x 32 box (lane = row; r = the row's 32 values as
+// bits) in `buf` with the tensor map's swizzle, then lane 0 stores it with TMA
+// at (col, row_base).  Swizzle: 16-byte chunk j of row r lands at chunk
+// j ^ (bits 7-8 of the row offset) for 64-byte rows (bf16) and j ^ (bits 7-9)
+// for 128-byte rows (fp32).  buf: kStoreStageBytes, 1024-byte aligned.
+__device__ __forceinline__ void store_box_tma(const CUtensorMap* map, uint8_t* buf, bool f32, int64_t col,
+                                              int64_t row_base, const uint32_t (&r)[32]) {
+  const uint32_t lane = lane_id();
+  if (lane == 0) bulk_wait_read_all();  // the previous box has left this buffer
+  __syncwarp();
+  if (f32) {
+    uint8_t* row = buf + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(row + ((j ^ (lane & 7)) * 16), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+  } else {
+    uint8_t* row = buf + lane * 64;
+    const auto f = [&](int j) { return __uint_as_float(r[j]); };
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_shared_v4(row + ((j ^ ((lane >> 1) & 3)) * 16), pack_bf16x2(f(8 * j), f(8 * j + 1)),
+                   pack_bf16x2(f(8 * j + 2), f(8 * j + 3)), pack_bf16x2(f(8 * j + 4), f(8 * j + 5)),
+                   pack_bf16x2(f(8 * j + 6), f(8 * j + 7)));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, buf, static_cast<int32_t>(col), static_cast<int32_t>(row_base));
+    bulk_commit_group();
+  }
+}
+
+// This warp's staging buffer (one per epilogue warp, in the epilogue region
+// whose group slice is epi_smem).
+__device__ __forceinline__ uint8_t* warp_stage_buffer(float* epi_smem, int grp) {
+  return reinterpret_cast<uint8_t*>(epi_smem - grp * kEpiSmemGroupFloats) + (threadIdx.x >> 5) * kStoreStageBytes;
+}
+
+// Every box this warp stored is complete.
+__device__ __forceinline__ void finish_box_stores() {
+  if (lane_id() == 0) bulk_wait_all();
+  __syncwarp();
+}
+
 template <bool kBias, bool kSoftcap>
 struct EpiFwd {
   using Params = FwdParams;
-  static constexpr int kTailBytes = 0;  // epilogue shared memory
-  __device__ static void finish(const Params&) {}
+  // Staging of the kept logits (TMA stores), one buffer per epilogue warp.
+  static constexpr int kTailBytes = kEpilogueGroups * kEpilogueWarps * kStoreStageBytes;
+  __device__ static void finish(const Params& p) {
+    if (p.z_out) finish_box_stores();
+  }
   struct State {
     int64_t row, target;
     float m, s, a, best, zt;
@@ -233,9 +280,13 @@ struct EpiFwd {
     st.has_zt = false;
   }
 
-  __device__ static void tile(const Params& p, const Unit& /*u*/, int n_tile, uint32_t taddr, State& st,
-                              float* /*epi_smem*/, int /*grp*/) {
+  __device__ static void tile(const Params& p, const Unit& u, int n_tile, uint32_t taddr, State& st,
+                              float* epi_smem, int grp) {
     const int64_t v_tile = static_cast<int64_t>(n_tile) * kBN;
+    // Kept logits: this warp's 32 rows go out as 32 x 32 boxes (the map clips rows past the chunk).
+    const int64_t row_base = u.row0 + ((threadIdx.x >> 5) % kEpilogueWarps) * 32;
+    const bool keep_z = p.z_out != nullptr && row_base < p.n_tokens;
+    uint8_t* zbuf = warp_stage_buffer(epi_smem, grp);
     // z = c tanh(s x / c): tanh takes t = 2 (s x / c) log2 e = x k_t
     const float k_t = p.scale * p.inv_softcap * 2.0f * kLog2e;
     for_each_tmem_chunk<false>(taddr, chunks_below(v_tile, p.vocab), [&](const uint32_t (&r)[32], int c) {
@@ -250,13 +301,11 @@ struct EpiFwd {
         if (kBias) x += bch[j];
         z[j] = kSoftcap ? p.softcap * tanh_from_exp2_arg(x * k_t) : x * p.scale;
       }
-      if (p.z_out && st.row < p.n_tokens) {  // keep the logits for the token-chunked backward
-        float* dst = p.z_out + st.row * p.ldz + vc;  // 128 B, 128-byte aligned (ldz % 32 == 0)
-        const auto u = [&](int j) { return __float_as_uint(z[j]); };
+      if (keep_z) {  // keep the logits for the token-chunked backward
+        uint32_t zb[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_global_v8_cs(dst + 8 * q, u(8 * q), u(8 * q + 1), u(8 * q + 2), u(8 * q + 3), u(8 * q + 4),
-                          u(8 * q + 5), u(8 * q + 6), u(8 * q + 7));
+        for (int j = 0; j < 32; ++j) zb[j] = __float_as_uint(z[j]);
+        store_box_tma(&p.z_map, zbuf, true, vc, row_base, zb);
       }
       if (ragged) {
 #pragma unroll
@@ -472,56 +521,23 @@ struct EpiStore {
     const int warp = threadIdx.x >> 5;  // 0-7: the CTA's epilogue warps
     const int64_t row_base = u.row0 + (warp % kEpilogueWarps) * 32;
     if (row_base >= p.rows) return;  // this warp's 32 rows are past the output
-    uint8_t* buf = reinterpret_cast<uint8_t*>(epi_smem - grp * kEpiSmemGroupFloats) + warp * kStoreStageBytes;
+    uint8_t* buf = warp_stage_buffer(epi_smem, grp);
     if (u.kb_count == 0) {  // no K blocks (all tokens ignored under compaction): the product is zero
       uint32_t zero[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) zero[j] = 0u;
 #pragma unroll 1
-      for (int c = 0; c < nch; ++c) put(p, buf, col_tile + c * 32, row_base, zero);
+      for (int c = 0; c < nch; ++c) store_box_tma(&p.out_map, buf, p.out_f32, col_tile + c * 32, row_base, zero);
       return;
     }
-    for_each_tmem_chunk(taddr, nch, [&](const uint32_t (&r)[32], int c) { put(p, buf, col_tile + c * 32, row_base, r); });
-  }
-
-  // Stages this warp's 32 x 32 box (lane = row) in its buffer with the tensor
-  // map's swizzle, then lane 0 stores it with TMA.  Swizzle: 16-byte chunk j
-  // of row r lands at chunk j ^ (bits 7-8 of the row offset) for 64-byte rows
-  // (bf16) and j ^ (bits 7-9) for 128-byte rows (fp32).
-  __device__ static void put(const Params& p, uint8_t* buf, int64_t col, int64_t row_base,
-                             const uint32_t (&r)[32]) {
-    const uint32_t lane = lane_id();
-    if (lane == 0) bulk_wait_read_all();  // the previous box has left this buffer
-    __syncwarp();
-    if (p.out_f32) {
-      uint8_t* row = buf + lane * 128;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        st_shared_v4(row + ((j ^ (lane & 7)) * 16), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-    } else {
-      uint8_t* row = buf + lane * 64;
-      const auto f = [&](int j) { return __uint_as_float(r[j]); };
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        st_shared_v4(row + ((j ^ ((lane >> 1) & 3)) * 16), pack_bf16x2(f(8 * j), f(8 * j + 1)),
-                     pack_bf16x2(f(8 * j + 2), f(8 * j + 3)), pack_bf16x2(f(8 * j + 4), f(8 * j + 5)),
-                     pack_bf16x2(f(8 * j + 6), f(8 * j + 7)));
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(&p.out_map, buf, static_cast<int32_t>(col), static_cast<int32_t>(row_base));
-      bulk_commit_group();
-    }
+    for_each_tmem_chunk(taddr, nch, [&](const uint32_t (&r)[32], int c) {
+      store_box_tma(&p.out_map, buf, p.out_f32, col_tile + c * 32, row_base, r);
+    });
   }
 
   __device__ static void end_unit(const Params&, const Unit&, State&, int) {}
 
-  // Every box this warp stored is complete before the kernel ends.
-  __device__ static void finish(const Params&) {
-    if (lane_id() == 0) bulk_wait_all();
-    __syncwarp();
-  }
+  __device__ static void finish(const Params&) { finish_box_stores(); }
 };
 
 // ============================================================================

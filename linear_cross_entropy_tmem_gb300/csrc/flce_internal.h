@@ -89,11 +89,14 @@ struct GemmSched {
 };
 
 // ---- Epilogue parameter blocks --------------------------------------------
+// Epilogue TMA stores: each warp stages a 32 x 32 box (fp32 at most).
+constexpr int kStoreStageBytes = 32 * 32 * 4;
 // Forward: online per-token statistics over each unit's vocabulary range
 // (one unit = one vocabulary split of one m tile).  Each epilogue group keeps
 // its own statistics over the unit's tiles it processed and writes its own
 // record: record r = split * kEpilogueGroups + group.
 struct FwdParams {
+  CUtensorMap z_map;      // kept logits [n_tokens][ldz] fp32, 32 x 32 boxes, 128-byte swizzle (with z_out)
   int64_t n_tokens, vocab;
   const void* bias;       // nullptr, bf16 or fp32 [V]
   int32_t bias_f32;
@@ -164,7 +167,6 @@ struct ZGradParams {
 // Plain store of the accumulator (dW, and the test GEMM), through TMA stores:
 // each epilogue warp stages its 32 rows x 32 columns in shared memory
 // (kStoreStageBytes per warp) and one lane copies the box out.
-constexpr int kStoreStageBytes = 32 * 32 * 4;
 struct StoreParams {
   CUtensorMap out_map;    // [rows][cols] in the output dtype, box 32 x 32, 64-byte (bf16) / 128-byte (fp32) swizzle
   int64_t rows, cols;     // valid extent of the output
