@@ -51,6 +51,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = automatic)")
     ap.add_argument("--tokens", type=int, default=0, help="override N (profiling captures of a small case)")
     ap.add_argument("--vocab", type=int, default=0, help="override V (profiling captures of a small case)")
+    ap.add_argument("--hidden", type=int, default=0, help="override D (calibration sweeps)")
     ap.add_argument("--separate", action="store_true",
                     help="flce_forward + flce_backward per step instead of one flce_forward_backward call")
     ap.add_argument("--autograd", action="store_true",
@@ -60,7 +61,7 @@ def parse_args(argv=None):
                     help="with --autograd: the separate backward instead of gradients in the forward")
     ap.add_argument("--bwd", default="auto", choices=["auto", "recompute", "keep_logits"],
                     help="backward algorithm of the fused call (FLCE_FLAG_BWD_*); auto keeps the logits of "
-                         "token chunks from D = 1024 up")
+                         "token chunks from D = 1280 up")
     ap.add_argument("--compact", action="store_true",
                     help="gather the valid tokens first (FLCE_FLAG_COMPACT_VALID)")
     ap.add_argument("--token-chunk", type=int, default=0,
@@ -354,8 +355,11 @@ def pick_workload(args):
         kw["n_tokens"] = args.tokens
     if args.vocab:
         kw["vocab"] = args.vocab
+    if args.hidden:
+        kw["hidden"] = args.hidden
     if kw:
-        w = w.scaled(name=f"{w.name} (N={kw.get('n_tokens', w.n_tokens)}, V={kw.get('vocab', w.vocab)})", **kw)
+        w = w.scaled(name=f"{w.name} (N={kw.get('n_tokens', w.n_tokens)}, D={kw.get('hidden', w.hidden)}, "
+                          f"V={kw.get('vocab', w.vocab)})", **kw)
     return w
 
 
@@ -543,7 +547,7 @@ def flce_arm(args):
             "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
                          "peak_kind": f"bf16 sustained ({peak_src})", "unit": "TFLOP/s", "frac": achieved / peak,
                          "traffic": committed_traffic(dominant, args.workload, "keep_logits" if keep else "recompute")
-                         if not (args.tokens or args.vocab or args.compact) else None,
+                         if not (args.tokens or args.vocab or args.hidden or args.compact) else None,
                          "launches": n_l, "avg_launch_ms": t_ms / n_l},
             "kernels": {k: {"launches": v[0], "ms_per_step": v[1] / args.steps,
                             "tflops": (flops_kind * args.steps / (v[1] * 1e-3) / 1e12) if k in gemm_kinds else None,

@@ -25,11 +25,13 @@ constexpr int kMaxSplits = 64;                     // forward vocabulary splits
 constexpr int kMaxKSplit = 16;                     // dh K splits
 constexpr size_t kGChunkBudget = size_t(1) << 30;  // bytes of the bf16 G chunk
 // Token-chunked backward: bytes of the kept fp32 logits + bf16 G of one chunk,
-// and the smallest hidden size for which the automatic choice keeps logits
-// (below it the recompute's 2*D flops per logit cost less than the 6 bytes per
-// logit of the extra pass over the kept logits).
+// and the smallest hidden size for which the automatic choice keeps logits:
+// below it the recompute's 2*D flops per logit cost less than the 6 bytes per
+// logit of the extra pass over the kept logits (measured on GB300 at
+// N = 16384, V = 151936: the recompute is faster at D = 1152, kept logits at
+// D = 1280).
 constexpr size_t kLogitChunkBudget = size_t(4) << 30;
-constexpr int64_t kKeepLogitsMinHidden = 1024;
+constexpr int64_t kKeepLogitsMinHidden = 1280;
 constexpr int kMaxDevices = 64;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }

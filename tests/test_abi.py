@@ -121,7 +121,7 @@ def test_fp32_terms_workspace(lib):
 
 def test_keep_logits_workspace(lib):
     """The token-chunked backward keeps fp32 logits + bf16 G for at most half of the tokens, plus
-    an fp32 dW accumulator; the automatic choice keeps logits from D = 1024 up and for N > 256."""
+    an fp32 dW accumulator; the automatic choice keeps logits from D = 1280 up and for N > 256."""
     keep, rec = B.FLCE_FLAG_BWD_KEEP_LOGITS, B.FLCE_FLAG_BWD_RECOMPUTE
     for (N, D, V) in [(16384, 4096, 151936), (16384, 640, 262144), (8192, 2048, 128256), (4096, 1024, 50000),
                       (300, 200, 1000), (257, 136, 777)]:
@@ -129,7 +129,7 @@ def test_keep_logits_workspace(lib):
         ws = {f: _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=f), 2) for f in (0, keep, rec)}
         assert all(st == B.FLCE_OK for st, _ in ws.values())
         k, r, a = ws[keep][1], ws[rec][1], ws[0][1]
-        assert a == (k if D >= 1024 else r)
+        assert a == (k if D >= 1280 else r)
         half = ((N + 1) // 2 + 255) // 256 * 256
         # kept logits + G, dbias partials, fp32 dW, dh K-split slots (at most 16), split records
         bound = 6 * min(half, N) * ldz + 4 * ((N + 31) // 32) * ldz + 4 * V * D + 16 * 4 * half * D \

@@ -198,7 +198,7 @@ def test_scale_gradient_is_one_fp32_multiply_and_rounding():
 
 
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
-@pytest.mark.parametrize("D", [200, 1024], ids=["recompute", "keep-logits"])
+@pytest.mark.parametrize("D", [200, 1280], ids=["recompute", "keep-logits"])
 def test_autograd_gradients_in_forward(D, reduction):
     """The autograd wrapper computes mean / sum gradients in the forward (fused call with an upstream
     gradient of 1) and scales them by the upstream gradient in the backward; 'none' keeps the
