@@ -39,6 +39,11 @@
  *     flce_read_device_status.
  *   - Results are deterministic: no floating-point atomics; every reduction
  *     runs in a fixed order.
+ *   - flce_forward, flce_backward and flce_forward_backward enqueue only
+ *     kernels and asynchronous memsets, so a step built from them can be
+ *     captured into a CUDA graph once the device's one-time set-up has run
+ *     (any earlier call on that device with the same problem), and replayed
+ *     with the same pointers; replays give the eager results bit for bit.
  */
 #ifndef FLCE_H_
 #define FLCE_H_

@@ -647,3 +647,72 @@ def test_fp32_full_removes_operand_rounding(fp32_head):
             assert 4 * err[True] <= err[False], (D, err)
         else:
             assert err[True] <= 1.2 * err[False] and err[True] <= 5e-4, (D, err)
+
+
+@pytest.mark.parametrize("entry", ["fused-keep", "fused-recompute", "separate"])
+def test_cuda_graph_capture_replays_bitwise(entry):
+    """The entry points enqueue only kernels and async memsets on the caller's stream, with no host
+    synchronisation and no allocation, so a step can be captured into a CUDA graph once and replayed;
+    each replay gives the eager results bit for bit (after one eager call, which also does the
+    library's one-time per-device set-up)."""
+    import linear_cross_entropy_tmem_gb300 as F
+    import linear_cross_entropy_tmem_gb300.api as api
+    from linear_cross_entropy_tmem_gb300.api import testing_set_token_chunk
+    testing_set_token_chunk(256)
+    w = Workload("graph", 700, 256, 3000, sigma_w=0.1, bias=True, softcap=20.0, reduction="mean", seed=16)
+    h, W, b, t, dloss = [x.cuda() for x in make_inputs(w, "cpu")]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction)
+    bwd = {"fused-keep": "keep_logits", "fused-recompute": "recompute", "separate": "auto"}[entry]
+    prob = api.make_problem(700, 256, 3000, bias_dtype=b.dtype, bwd=bwd, **kw)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    outs = dict(loss=torch.empty(1, **f32), lse=torch.empty(700, **f32), ent=torch.empty(700, **f32),
+                corr=torch.empty(1, dtype=torch.int64, device="cuda"), nv=torch.empty(1, dtype=torch.int64, device="cuda"),
+                es=torch.empty(1, **f32), dh=torch.empty_like(h), dW=torch.empty_like(W), db=torch.empty_like(b))
+    if entry == "separate":
+        ws_f = torch.empty(api.flce_workspace_size(prob, 0), dtype=torch.uint8, device="cuda")
+        ws_b = torch.empty(api.flce_workspace_size(prob, 1), dtype=torch.uint8, device="cuda")
+    else:
+        ws = torch.empty(api.flce_workspace_size(prob, 2), dtype=torch.uint8, device="cuda")
+    import ctypes
+
+    from linear_cross_entropy_tmem_gb300 import binding as B
+    lib = B.load()
+    ptr = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+
+    def step():
+        s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        o = outs
+        if entry == "separate":
+            B.check(lib.flce_forward(ctypes.byref(prob), ptr(h), ptr(W), ptr(b), ptr(t), ptr(o["loss"]), ptr(o["lse"]),
+                                     ptr(o["ent"]), ptr(o["corr"]), ptr(o["nv"]), ptr(o["es"]), ptr(ws_f),
+                                     ws_f.numel(), s), "forward")
+            B.check(lib.flce_backward(ctypes.byref(prob), ptr(h), ptr(W), ptr(b), ptr(t), ptr(o["lse"]), ptr(o["nv"]),
+                                      ptr(dloss), ptr(o["dh"]), ptr(o["dW"]), ptr(o["db"]), ptr(ws_b), ws_b.numel(), s),
+                    "backward")
+        else:
+            B.check(lib.flce_forward_backward(ctypes.byref(prob), ptr(h), ptr(W), ptr(b), ptr(t), ptr(dloss),
+                                              ptr(o["loss"]), ptr(o["lse"]), ptr(o["ent"]), ptr(o["corr"]),
+                                              ptr(o["nv"]), ptr(o["es"]), ptr(o["dh"]), ptr(o["dW"]), ptr(o["db"]),
+                                              ptr(ws), ws.numel(), s), "forward_backward")
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # eager: the reference results, and the library's one-time set-up
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in outs.items()}
+    for v in outs.values():
+        v.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        for v in outs.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for k in ref:
+            assert torch.equal(outs[k], ref[k]), k
+    ref_f = oracle.forward(h.cpu(), W.cpu(), b.cpu(), t.cpu(), **kw)
+    assert abs(float(outs["loss"]) - ref_f["loss"]) <= 2e-3
