@@ -60,6 +60,43 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ float tanh_from_exp2_arg(float t) {
   return fmaf(-2.0f, rcp_approx(ex2_approx(t) + 1.0f), 1.0f);
 }
+// max(a, b, c) in one instruction (three-input max of the sm_100 family).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs.  The sm_100 family issues add, mul and fma on two fp32
+// lanes held in one 64-bit register as a single instruction, each lane rounded
+// to nearest exactly as the scalar instruction would; the epilogues use them to
+// halve their issue slots.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t y;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(a), "l"(b));
+  return y;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t y;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(a), "l"(b));
+  return y;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t y;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(a), "l"(b), "l"(c));
+  return y;
+}
+__device__ __forceinline__ uint64_t f2_splat(float x) { return f2_pack(x, x); }
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

@@ -195,15 +195,13 @@ __device__ __forceinline__ bool epilogue_all(bool ok, int id) {
 // Thread index within its epilogue group (its TMEM lane, i.e. its tile row).
 __device__ __forceinline__ int epi_tid() { return static_cast<int>(threadIdx.x) & (kEpilogueThreads - 1); }
 
-__device__ __forceinline__ float max32(const float (&z)[32]) {
-  float t[16];
+__device__ __forceinline__ float max32(const float (&z)[32]) {  // 16 three-input maxima
+  float t[10];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = fmaxf(z[i], z[i + 16]);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) t[i] = fmaxf(t[i], t[i + 8]);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) t[i] = fmaxf(t[i], t[i + 4]);
-  return fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
+  for (int i = 0; i < 10; ++i) t[i] = max3f(z[3 * i], z[3 * i + 1], z[3 * i + 2]);
+  const float u = max3f(z[30], z[31], t[0]);
+  const float a = max3f(t[1], t[2], t[3]), b = max3f(t[4], t[5], t[6]), c = max3f(t[7], t[8], t[9]);
+  return fmaxf(max3f(a, b, c), u);
 }
 
 // ============================================================================
@@ -287,8 +285,11 @@ struct EpiFwd {
     const int64_t row_base = u.row0 + ((threadIdx.x >> 5) % kEpilogueWarps) * 32;
     const bool keep_z = p.z_out != nullptr && row_base < p.n_tokens;
     uint8_t* zbuf = warp_stage_buffer(epi_smem, grp);
-    // z = c tanh(s x / c): tanh takes t = 2 (s x / c) log2 e = x k_t
-    const float k_t = p.scale * p.inv_softcap * 2.0f * kLog2e;
+    // z = c tanh(s x / c) = c - 2c / (2^t + 1) with t = 2 (s x / c) log2 e = x k_t.  The
+    // arithmetic runs on packed fp32 pairs (columns j, j + 1).
+    const uint64_t k_t2 = f2_splat(p.scale * p.inv_softcap * 2.0f * kLog2e);
+    const uint64_t scale2 = f2_splat(p.scale), one2 = f2_splat(1.0f);
+    const uint64_t cap2 = f2_splat(p.softcap), m2cap2 = f2_splat(-2.0f * p.softcap);
     for_each_tmem_chunk<false>(taddr, chunks_below(v_tile, p.vocab), [&](const uint32_t (&r)[32], int c) {
       const int64_t vc = v_tile + c * 32;
       const bool ragged = vc + 32 > p.vocab;
@@ -296,10 +297,17 @@ struct EpiFwd {
       if (kBias) load_bias_chunk(p.bias, p.bias_f32, p.bias_vec, vc, p.vocab, bch);
       float z[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float x = __uint_as_float(r[j]);
-        if (kBias) x += bch[j];
-        z[j] = kSoftcap ? p.softcap * tanh_from_exp2_arg(x * k_t) : x * p.scale;
+      for (int j = 0; j < 32; j += 2) {
+        uint64_t x = f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+        if (kBias) x = f2_add(x, f2_pack(bch[j], bch[j + 1]));
+        if (kSoftcap) {
+          float t0, t1, e0, e1;
+          f2_unpack(f2_mul(x, k_t2), t0, t1);
+          f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), one2), e0, e1);
+          f2_unpack(f2_fma(f2_pack(rcp_approx(e0), rcp_approx(e1)), m2cap2, cap2), z[j], z[j + 1]);
+        } else {
+          f2_unpack(f2_mul(x, scale2), z[j], z[j + 1]);
+        }
       }
       if (keep_z) {  // keep the logits for the token-chunked backward
         uint32_t zb[32];
@@ -327,14 +335,23 @@ struct EpiFwd {
         st.a *= f;
         st.m = cmax;
       }
-      const float mb = st.m * kLog2e;
-      float s4[4] = {0.f, 0.f, 0.f, 0.f}, a4[4] = {0.f, 0.f, 0.f, 0.f};
+      // Four partial sums per chunk (columns j mod 4), two packed pairs each.
+      const uint64_t l2e2 = f2_splat(kLog2e), nmb2 = f2_splat(-st.m * kLog2e);
+      uint64_t s2[2] = {0ull, 0ull}, a2[2] = {0ull, 0ull};
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float e = ex2_approx(fmaf(z[j], kLog2e, -mb));
-        s4[j & 3] += e;
-        a4[j & 3] = fmaf(e, z[j], a4[j & 3]);
+      for (int j = 0; j < 32; j += 2) {
+        const uint64_t zz = f2_pack(z[j], z[j + 1]);
+        float u0, u1;
+        f2_unpack(f2_fma(zz, l2e2, nmb2), u0, u1);
+        const uint64_t e = f2_pack(ex2_approx(u0), ex2_approx(u1));
+        s2[(j >> 1) & 1] = f2_add(s2[(j >> 1) & 1], e);
+        a2[(j >> 1) & 1] = f2_fma(e, zz, a2[(j >> 1) & 1]);
       }
+      float s4[4], a4[4];
+      f2_unpack(s2[0], s4[0], s4[1]);
+      f2_unpack(s2[1], s4[2], s4[3]);
+      f2_unpack(a2[0], a4[0], a4[1]);
+      f2_unpack(a2[1], a4[2], a4[3]);
       st.s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
       st.a += (a4[0] + a4[1]) + (a4[2] + a4[3]);
       const int64_t tl = st.target - vc;
@@ -437,20 +454,34 @@ struct EpiGrad {
     const float wd = st.w * p.scale;
     const float k_t = p.scale * p.inv_softcap * 2.0f * kLog2e;
     const float k_p = kSoftcap ? p.softcap * kLog2e : p.scale * kLog2e;
+    const uint64_t k_t2 = f2_splat(k_t), k_p2 = f2_splat(k_p), nlse2 = f2_splat(-st.lse2);
+    const uint64_t wd2 = f2_splat(wd), nwd2 = f2_splat(-wd);
+    const uint64_t one2 = f2_splat(1.0f), mone2 = f2_splat(-1.0f), m2two2 = f2_splat(-2.0f);
     const int nch = chunks_below(v_tile, p.vocab);
     for_each_tmem_chunk<false>(taddr, nch, [&](const uint32_t (&r)[32], int c) {
       const int64_t vc = v_tile + c * 32;
       const bool ragged = vc + 32 > p.vocab;
       float bch[32];
       if (kBias) load_bias_chunk(p.bias, p.bias_f32, p.bias_vec, vc, p.vocab, bch);
+      // The grad_terms arithmetic on packed fp32 pairs (columns j, j + 1), rounded alike.
       float g[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float x = __uint_as_float(r[j]);
-        if (kBias) x += bch[j];
-        float d, pr;
-        grad_terms(p, x, wd, k_t, k_p, st, d, pr);
-        g[j] = d * pr;
+      for (int j = 0; j < 32; j += 2) {
+        uint64_t x = f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+        if (kBias) x = f2_add(x, f2_pack(bch[j], bch[j + 1]));
+        float q0, q1;
+        if (kSoftcap) {
+          float t0, t1, e0, e1;
+          f2_unpack(f2_mul(x, k_t2), t0, t1);
+          f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), one2), e0, e1);
+          const uint64_t th = f2_fma(f2_pack(rcp_approx(e0), rcp_approx(e1)), m2two2, one2);  // tanh
+          f2_unpack(f2_fma(th, k_p2, nlse2), q0, q1);
+          const uint64_t d = f2_mul(f2_fma(th, th, mone2), nwd2);  // w s (1 - th^2)
+          f2_unpack(f2_mul(d, f2_pack(ex2_approx(q0), ex2_approx(q1))), g[j], g[j + 1]);
+        } else {
+          f2_unpack(f2_fma(x, k_p2, nlse2), q0, q1);
+          f2_unpack(f2_mul(wd2, f2_pack(ex2_approx(q0), ex2_approx(q1))), g[j], g[j + 1]);
+        }
       }
       const int64_t tl = st.target - vc;
       if (tl >= 0 && tl < 32) {  // the target column: subtract the one-hot term
