@@ -97,6 +97,25 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   return y;
 }
 __device__ __forceinline__ uint64_t f2_splat(float x) { return f2_pack(x, x); }
+
+// min(x, c) that keeps a NaN x (fminf would return c).
+__device__ __forceinline__ float min_nan(float x, float c) {
+  float y;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(x), "f"(c));
+  return y;
+}
+
+// 1 / (2^t + 1) for two arguments with ONE hardware reciprocal, which costs twice the
+// MUFU time of an exp2: with a = 2^t0 + 1 and b = 2^t1 + 1, 1/a = b / (ab) and
+// 1/b = a / (ab).  t is clamped to 63 first (there 1/(2^t + 1) < 2^-63, and tanh
+// built from it is 1 in fp32), so that ab <= 2^127 stays finite.  Relative error about
+// 3 ulp (product, reciprocal, final product).  The pair comes back SWAPPED:
+// lo = 1/(2^t1 + 1), hi = 1/(2^t0 + 1), so that no register move is needed.
+__device__ __forceinline__ uint64_t f2_inv_exp2p1_swapped(float t0, float t1) {
+  float a, b;
+  f2_unpack(f2_add(f2_pack(ex2_approx(min_nan(t0, 63.f)), ex2_approx(min_nan(t1, 63.f))), f2_splat(1.0f)), a, b);
+  return f2_mul(f2_pack(a, b), f2_splat(rcp_approx(a * b)));
+}
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

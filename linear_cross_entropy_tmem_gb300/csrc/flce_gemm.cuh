@@ -288,7 +288,7 @@ struct EpiFwd {
     // z = c tanh(s x / c) = c - 2c / (2^t + 1) with t = 2 (s x / c) log2 e = x k_t.  The
     // arithmetic runs on packed fp32 pairs (columns j, j + 1).
     const uint64_t k_t2 = f2_splat(p.scale * p.inv_softcap * 2.0f * kLog2e);
-    const uint64_t scale2 = f2_splat(p.scale), one2 = f2_splat(1.0f);
+    const uint64_t scale2 = f2_splat(p.scale);
     const uint64_t cap2 = f2_splat(p.softcap), m2cap2 = f2_splat(-2.0f * p.softcap);
     for_each_tmem_chunk<false>(taddr, chunks_below(v_tile, p.vocab), [&](const uint32_t (&r)[32], int c) {
       const int64_t vc = v_tile + c * 32;
@@ -300,11 +300,10 @@ struct EpiFwd {
       for (int j = 0; j < 32; j += 2) {
         uint64_t x = f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
         if (kBias) x = f2_add(x, f2_pack(bch[j], bch[j + 1]));
-        if (kSoftcap) {
-          float t0, t1, e0, e1;
+        if (kSoftcap) {  // the reciprocal pair comes back swapped: low lane = column j + 1
+          float t0, t1;
           f2_unpack(f2_mul(x, k_t2), t0, t1);
-          f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), one2), e0, e1);
-          f2_unpack(f2_fma(f2_pack(rcp_approx(e0), rcp_approx(e1)), m2cap2, cap2), z[j], z[j + 1]);
+          f2_unpack(f2_fma(f2_inv_exp2p1_swapped(t0, t1), m2cap2, cap2), z[j + 1], z[j]);
         } else {
           f2_unpack(f2_mul(x, scale2), z[j], z[j + 1]);
         }
@@ -335,12 +334,14 @@ struct EpiFwd {
         st.a *= f;
         st.m = cmax;
       }
-      // Four partial sums per chunk (columns j mod 4), two packed pairs each.
+      // Four partial sums per chunk (columns j mod 4), two packed pairs each.  The pairs keep the
+      // lane order the z arithmetic left them in (low lane = column j + kLo).
+      constexpr int kLo = kSoftcap ? 1 : 0;
       const uint64_t l2e2 = f2_splat(kLog2e), nmb2 = f2_splat(-st.m * kLog2e);
       uint64_t s2[2] = {0ull, 0ull}, a2[2] = {0ull, 0ull};
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const uint64_t zz = f2_pack(z[j], z[j + 1]);
+        const uint64_t zz = f2_pack(z[j + kLo], z[j + 1 - kLo]);
         float u0, u1;
         f2_unpack(f2_fma(zz, l2e2, nmb2), u0, u1);
         const uint64_t e = f2_pack(ex2_approx(u0), ex2_approx(u1));
@@ -348,10 +349,10 @@ struct EpiFwd {
         a2[(j >> 1) & 1] = f2_fma(e, zz, a2[(j >> 1) & 1]);
       }
       float s4[4], a4[4];
-      f2_unpack(s2[0], s4[0], s4[1]);
-      f2_unpack(s2[1], s4[2], s4[3]);
-      f2_unpack(a2[0], a4[0], a4[1]);
-      f2_unpack(a2[1], a4[2], a4[3]);
+      f2_unpack(s2[0], s4[kLo], s4[1 - kLo]);
+      f2_unpack(s2[1], s4[2 + kLo], s4[3 - kLo]);
+      f2_unpack(a2[0], a4[kLo], a4[1 - kLo]);
+      f2_unpack(a2[1], a4[2 + kLo], a4[3 - kLo]);
       st.s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
       st.a += (a4[0] + a4[1]) + (a4[2] + a4[3]);
       const int64_t tl = st.target - vc;
@@ -470,14 +471,13 @@ struct EpiGrad {
         uint64_t x = f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
         if (kBias) x = f2_add(x, f2_pack(bch[j], bch[j + 1]));
         float q0, q1;
-        if (kSoftcap) {
-          float t0, t1, e0, e1;
+        if (kSoftcap) {  // from the swapped reciprocal pair on, the low lane is column j + 1
+          float t0, t1;
           f2_unpack(f2_mul(x, k_t2), t0, t1);
-          f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), one2), e0, e1);
-          const uint64_t th = f2_fma(f2_pack(rcp_approx(e0), rcp_approx(e1)), m2two2, one2);  // tanh
+          const uint64_t th = f2_fma(f2_inv_exp2p1_swapped(t0, t1), m2two2, one2);  // tanh
           f2_unpack(f2_fma(th, k_p2, nlse2), q0, q1);
           const uint64_t d = f2_mul(f2_fma(th, th, mone2), nwd2);  // w s (1 - th^2)
-          f2_unpack(f2_mul(d, f2_pack(ex2_approx(q0), ex2_approx(q1))), g[j], g[j + 1]);
+          f2_unpack(f2_mul(d, f2_pack(ex2_approx(q0), ex2_approx(q1))), g[j + 1], g[j]);
         } else {
           f2_unpack(f2_fma(x, k_p2, nlse2), q0, q1);
           f2_unpack(f2_mul(wd2, f2_pack(ex2_approx(q0), ex2_approx(q1))), g[j], g[j + 1]);

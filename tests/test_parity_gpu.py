@@ -716,3 +716,31 @@ def test_cuda_graph_capture_replays_bitwise(entry):
             assert torch.equal(outs[k], ref[k]), k
     ref_f = oracle.forward(h.cpu(), W.cpu(), b.cpu(), t.cpu(), **kw)
     assert abs(float(outs["loss"]) - ref_f["loss"]) <= 2e-3
+
+
+@pytest.mark.parametrize("softcap", [0.0, 30.0], ids=["plain", "softcap"])
+def test_nan_hidden_row_stays_in_its_row(softcap):
+    """A NaN in one hidden row makes every logit of that row NaN, so its loss, lse and dh row are
+    NaN (no clamp or maximum may turn it into a finite value), while every other row keeps the
+    oracle's values: rows are independent until dW and the reductions sum over them."""
+    import linear_cross_entropy_tmem_gb300 as F
+    w = Workload("nan", 300, 200, 1000, sigma_w=0.15, softcap=softcap, reduction="none", seed=21)
+    h, W, b, t, dloss = make_inputs(w, "cpu")
+    bad = int(np.flatnonzero(t.numpy() != -100)[20])  # a valid token
+    h_nan = h.clone()
+    h_nan[bad, 5] = float("nan")
+    kw = dict(softcap=softcap, reduction="none")
+    f = F.flce_forward(h_nan.cuda(), W.cuda(), t.cuda(), entropy=True, **kw)
+    g = F.flce_backward(h_nan.cuda(), W.cuda(), t.cuda(), f.lse, f.n_valid, dloss.cuda(), **kw)
+    torch.cuda.synchronize()
+    assert F.flce_read_device_status(f.workspace) == 0
+    ref = oracle.forward(h, W, None, t, **kw)
+    ref_b = oracle.backward(h, W, None, t, dloss=dloss, **kw)
+    keep = np.arange(w.n_tokens) != bad
+    lse, loss, dh = f.lse.cpu().numpy(), f.loss.cpu().numpy(), g[0].float().cpu().numpy()
+    assert np.isnan(lse[bad]) and np.isnan(dh[bad]).all()
+    assert np.isnan(loss[bad])
+    assert np.abs(lse[keep] - ref["lse"][keep]).max() < TOL_LSE
+    assert np.abs(loss[keep] - ref["loss_tok"][keep]).max() < TOL_LSE
+    ref_dh = ref_b["dh"][keep]
+    assert np.linalg.norm(dh[keep] - ref_dh) <= 1e-2 * np.linalg.norm(ref_dh)
