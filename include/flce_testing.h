@@ -43,6 +43,16 @@ FLCE_API int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit);
 FLCE_API int flce_testing_set_gemm_mode(int mode);
 
 /*
+ * Process-wide switch of the operand multicast, for tests and tuning.  1: a
+ * CTA-pair product whose B operand is MN-major (dh, dW), and the test GEMM,
+ * run as clusters of two CTA pairs over a 512-row m tile; both pairs need the
+ * same B tile and each CTA loads half of its share, multicast by TMA to itself
+ * and its counterpart in the other pair.  0 (the default): plain CTA pairs.
+ * Results are bitwise the same either way.  Not thread-safe.
+ */
+FLCE_API int flce_testing_set_multicast(int on);
+
+/*
  * Process-wide override of the token-chunk size of the token-chunked backward
  * (FLCE_FLAG_BWD_KEEP_LOGITS), for tests and tuning: rows per chunk, rounded up
  * to 256 and capped at half of N rounded up to 256; 0 restores the automatic

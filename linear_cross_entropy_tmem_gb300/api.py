@@ -301,3 +301,9 @@ def testing_set_token_chunk(rows: int = 0) -> None:
 def testing_set_gemm_mode(mode: int = 0) -> None:
     """0 automatic, 1 single-CTA GEMM kernel only, 2 CTA-pair kernel only (tests, A/B timing)."""
     B.check(B.load().flce_testing_set_gemm_mode(int(mode)), "flce_testing_set_gemm_mode")
+
+
+def testing_set_multicast(on: bool = False) -> None:
+    """1: CTA-pair products with an MN-major B operand run as clusters of two pairs sharing B by TMA
+    multicast; 0 (default): plain CTA pairs (tests, A/B timing)."""
+    B.check(B.load().flce_testing_set_multicast(1 if on else 0), "flce_testing_set_multicast")

@@ -81,6 +81,7 @@ SIGNATURES = {
     "flce_testing_set_tuning": (c_int, [c_int64, c_int]),
     "flce_scale_gradient": (c_int, [c_void_p, c_void_p, c_int64, c_int32, c_void_p]),
     "flce_testing_set_gemm_mode": (c_int, [c_int]),
+    "flce_testing_set_multicast": (c_int, [c_int]),
     "flce_testing_set_token_chunk": (c_int, [c_int64]),
     "flce_testing_set_launch_log": (c_int, [c_void_p, c_int32, POINTER(c_int32)]),
     "flce_testing_launch_count": (c_int64, []),

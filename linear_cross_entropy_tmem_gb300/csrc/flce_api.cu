@@ -206,6 +206,7 @@ std::atomic<int64_t> g_force_chunk_cols{0};
 std::atomic<int> g_force_dh_ksplit{0};
 std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel
 std::atomic<int64_t> g_force_token_rows{0};
+std::atomic<int> g_multicast{0};  // flce_testing_set_multicast
 
 // CTA pairs (256-row tiles) when there are at least 256 rows and enough units
 // to give every cluster work; otherwise single CTAs (128-row tiles).
@@ -214,6 +215,20 @@ bool use_pair(int64_t m_rows, int64_t units_per_pair_row, int num_sms) {
   if (mode == 1) return false;
   if (mode == 2) return true;
   return m_rows >= kPairRows && cdiv(m_rows, kPairRows) * units_per_pair_row >= num_sms / 2;
+}
+
+// Run a CTA-pair product as clusters of two pairs that share the B tile by TMA
+// multicast (GemmSched::quad, 512-row m tiles), which cuts the operand bytes
+// each pair pulls from L2 by a quarter.  Needs at least two 256-row m tiles.
+// Called on a pair schedule before finish_sched.  Off unless switched on for
+// testing: fewer clusters of four than pairs are resident on a GB300, and the
+// lost SMs cost more than the L2 bytes save (dh and dW 2-4 % slower per clock
+// at the Qwen3-8B-like head, dW 10 % slower at the Gemma-like one).
+void use_quad(GemmSched& s, bool pair, int64_t m_rows) {
+  if (!pair || g_multicast.load() == 0 || cdiv(m_rows, kPairRows) < 2) return;
+  s.quad = 1;
+  s.m_tiles = static_cast<int32_t>(cdiv(m_rows, 2 * kPairRows));
+  s.group_m = std::max(1, s.group_m / 2);
 }
 
 int64_t chunk_width(int64_t n_tokens, int64_t vocab) {
@@ -228,13 +243,17 @@ int64_t chunk_width(int64_t n_tokens, int64_t vocab) {
   return cdiv(cdiv(vocab, n_chunks), kBN) * kBN;
 }
 
+// fp32 dh slots of the recompute backward (K splits of each chunk's dh
+// product).  Small products split K to fill the GPU (at least 8 K blocks per
+// split); mid-sized ones (up to 2048 128-row tiles) get up to 8 slots so that
+// the run can even out the last wave of tiles (choose_token_ksplit).
 int dh_ksplit_bound(int64_t n_tokens, int64_t hidden, int64_t vc) {
   const int forced = g_force_dh_ksplit.load();
   if (forced > 0) return std::min(forced, kMaxKSplit);
   const int64_t tiles = cdiv(n_tokens, kBM) * cdiv(hidden, kBN);
-  if (tiles >= 128) return 1;
   const int64_t kb = cdiv(vc, kBK);
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxKSplit, kb / 8)));
+  const int64_t cap = tiles >= 128 ? std::min<int64_t>(8, cdiv(2048, tiles)) : kMaxKSplit;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cap, kb / 8)));
 }
 
 enum LayoutKind { kForward = 0, kBackward = 1, kFused = 2 };
@@ -689,6 +708,71 @@ int run_forward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, u
   return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
 }
 
+// K splits of one token chunk's dh product: the fewest that fill the device's
+// CTAs (or clusters) within 1 % of the best wave efficiency.
+int choose_token_ksplit(int64_t tiles, int ctas, int bound) {
+  if (g_force_dh_ksplit.load() > 0) return bound;
+  double best = 0.0;
+  std::vector<double> eff(bound + 1, 0.0);
+  for (int k = 1; k <= bound; ++k) {
+    const int64_t units = tiles * k;
+    eff[k] = double(units) / double(cdiv(units, ctas) * ctas);
+    best = std::max(best, eff[k]);
+  }
+  for (int k = 1; k <= bound; ++k)
+    if (eff[k] >= best - 0.01) return k;
+  return 1;
+}
+
+// K splits of the recompute backward's dh product.  Every split adds an fp32
+// slot that each chunk reads and writes back in the epilogue, so the wave
+// efficiency is weighed against 2 % per split (measured on the Gemma-like
+// head: 3 splits 3.74 ms, 5 splits 4.3 ms, 1 split 3.9 ms per step).
+int choose_recompute_ksplit(int64_t tiles, int ctas, int bound) {
+  if (g_force_dh_ksplit.load() > 0) return bound;
+  double best = -1.0;
+  int best_k = 1;
+  for (int k = 1; k <= bound; ++k) {
+    const int64_t units = tiles * k;
+    const double score = double(units) / double(cdiv(units, ctas) * ctas) * (1.0 - 0.02 * k);
+    if (score > best + 1e-9) {
+      best = score;
+      best_k = k;
+    }
+  }
+  return best_k;
+}
+
+// Column width of the recompute backward's vocabulary chunks, at most L.vc:
+// the width with the least dW time plus per-chunk overhead.  A dW unit is one
+// output tile over K = N, so a wave of units (one per CTA or CTA pair) takes
+// cdiv(N, 64) k-blocks of MMA time either way; each chunk adds launches and
+// tails worth about kChunkOverheadKBlocks k-blocks (~15 us; one 64-deep
+// k-block of a pair's 256 x 256 tile is ~0.27 us at 1.9 GHz).  Widths down to
+// half of L.vc are considered.
+constexpr double kChunkOverheadKBlocks = 56.0;
+int64_t recompute_chunk_cols(const Layout& L, int64_t N, int64_t D, int64_t V, int num_sms) {
+  if (g_force_chunk_cols.load() > 0 || !L.need_dh_part) return L.vc;
+  const int64_t max_t = L.vc / kBN, n_t = cdiv(D, kBN);
+  const double wave = double(cdiv(N, kBK));
+  double best = 0.0;
+  int64_t best_t = max_t;
+  for (int64_t t = max_t; t >= std::max<int64_t>(1, max_t / 2); --t) {
+    double cost = 0.0;
+    for (int64_t v0 = 0; v0 < V; v0 += t * kBN) {
+      const int64_t width = std::min<int64_t>(t * kBN, V - v0);
+      const bool pair = use_pair(width, n_t, num_sms);
+      cost += wave * double(cdiv(cdiv(width, pair ? kPairRows : kBM) * n_t, pair ? num_sms / 2 : num_sms)) +
+              kChunkOverheadKBlocks;
+    }
+    if (t == max_t || cost < best - 1e-9) {
+      best = cost;
+      best_t = t;
+    }
+  }
+  return best_t * kBN;
+}
+
 int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
                  cudaStream_t st, const void* bias, const Prep& pr, const float* lse_use,
                  const int64_t* n_valid, const float* dloss_use, void* dhidden, void* dweight, void* dbias) {
@@ -722,17 +806,16 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
   const bool pair_dh = use_pair(N, cdiv(D, kBN), dev.num_sms);
   const int dh_ctas = pair_dh ? dev.num_sms / 2 : dev.num_sms;
   const int64_t dh_tiles = cdiv(N, pair_dh ? kPairRows : kBM) * cdiv(D, kBN);
-  int ksplit = 1;
-  if (g_force_dh_ksplit.load() > 0) {
-    ksplit = L.ksplit_max;
-  } else if (L.ksplit_max > 1) {
-    ksplit = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(L.ksplit_max, dh_ctas / dh_tiles)));
-  }
+  const int ksplit = L.ksplit_max > 1 ? choose_recompute_ksplit(dh_tiles, dh_ctas, L.ksplit_max) : 1;
 
-  for (int64_t c = 0; c < L.n_chunks; ++c) {
-    const int64_t v0 = c * L.vc;
-    const int64_t width = std::min<int64_t>(L.vc, V - v0);
-    const bool first = c == 0, last = c == L.n_chunks - 1;
+  // Vocabulary chunks of at most L.vc columns (the G scratch keeps L.vc as its
+  // row stride).
+  const int64_t vcw = recompute_chunk_cols(L, N, D, V, dev.num_sms);
+  const int64_t n_chunks = cdiv(V, vcw);
+  for (int64_t c = 0; c < n_chunks; ++c) {
+    const int64_t v0 = c * vcw;
+    const int64_t width = std::min<int64_t>(vcw, V - v0);
+    const bool first = c == 0, last = c == n_chunks - 1;
 
     // (1) recompute the logits of the chunk and form G (bf16) + dbias partials
     GemmSched s1 = base_sched(N, width, D, rec_nseg, rec_segs, pair_rec);
@@ -784,6 +867,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     s2.b_mn = 1;
     s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
     s2.k_limit = pr.row_count;
+    use_quad(s2, pair_dw, width);
     finish_sched(s2);
     StoreParams sp{};
     sp.rows = width;
@@ -808,6 +892,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
     s3.group_m = std::max(1, dh_ctas / std::max(1, s3.n_tiles * ksplit));
     s3.m_limit = pr.row_count;
+    use_quad(s3, pair_dh, N);
     finish_sched(s3);
     AccumParams ap{};
     ap.rows = N;
@@ -830,22 +915,6 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     }));
   }
   return FLCE_OK;
-}
-
-// K splits of one token chunk's dh product: the fewest that fill the device's
-// CTAs (or clusters) within 1 % of the best wave efficiency.
-int choose_token_ksplit(int64_t tiles, int ctas, int bound) {
-  if (g_force_dh_ksplit.load() > 0) return bound;
-  double best = 0.0;
-  std::vector<double> eff(bound + 1, 0.0);
-  for (int k = 1; k <= bound; ++k) {
-    const int64_t units = tiles * k;
-    eff[k] = double(units) / double(cdiv(units, ctas) * ctas);
-    best = std::max(best, eff[k]);
-  }
-  for (int k = 1; k <= bound; ++k)
-    if (eff[k] >= best - 0.01) return k;
-  return 1;
 }
 
 // Token-chunked forward + backward (FLCE_FLAG_BWD_KEEP_LOGITS).  Per chunk of
@@ -1004,6 +1073,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     s3.group_m = 16;
     s3.ks_outer = 1;
     s3.m_limit = lim;
+    use_quad(s3, pair_dh, rows);
     finish_sched(s3);
     uint8_t* dh_out = static_cast<uint8_t*>(dhidden) + (pr.cmp ? 0 : size_t(r0) * D * out_elem);
     AccumParams ap{};
@@ -1036,6 +1106,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     s2.b_mn = 1;
     s2.group_m = std::max(1, dw_ctas / std::max(1, s2.n_tiles));
     s2.k_limit = lim;
+    use_quad(s2, pair_dw, V);
     finish_sched(s2);
     AccumParams aw{};
     aw.rows = V;
@@ -1228,6 +1299,12 @@ int flce_testing_set_gemm_mode(int mode) {
   return FLCE_OK;
 }
 
+int flce_testing_set_multicast(int on) {
+  if (on != 0 && on != 1) return FLCE_ERR_INVALID_ARG;
+  g_multicast.store(on);
+  return FLCE_OK;
+}
+
 int flce_testing_set_launch_log(flce_launch_record* records, int32_t capacity, int32_t* count) {
   if (records && (capacity < 0 || !count)) return FLCE_ERR_INVALID_ARG;
   g_log = records;
@@ -1247,17 +1324,20 @@ int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int6
   FLCE_TRY(get_device(&dev));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool pair = use_pair(M, cdiv(N, kBN), dev.num_sms);
-  TmaMaps m;
-  if (!a_mn_major) FLCE_TRY(make_map(&m.a0, A, K, M, lda * 2, kBK, kBM));
-  else FLCE_TRY(make_map(&m.a0, A, M, K, lda * 2, 64, kBK));
-  if (!b_mn_major) FLCE_TRY(make_map(&m.b0, B, K, N, ldb * 2, kBK, pair ? kBN / 2 : kBN));
-  else FLCE_TRY(make_map(&m.b0, B, N, K, ldb * 2, 64, kBK));
-  m.a1 = m.a2 = m.a0;
-  m.b1 = m.b2 = m.b0;
   GemmSched s = base_sched(M, N, K, 1, 0u, pair);
   s.a_mn = a_mn_major ? 1 : 0;
   s.b_mn = b_mn_major ? 1 : 0;
+  use_quad(s, pair, M);
   finish_sched(s);
+  // K-major B: a CTA pair loads 128-row halves; under multicast each CTA loads 64 rows.
+  const uint32_t b_rows = !pair ? kBN : (s.quad ? kBN / 4 : kBN / 2);
+  TmaMaps m;
+  if (!a_mn_major) FLCE_TRY(make_map(&m.a0, A, K, M, lda * 2, kBK, kBM));
+  else FLCE_TRY(make_map(&m.a0, A, M, K, lda * 2, 64, kBK));
+  if (!b_mn_major) FLCE_TRY(make_map(&m.b0, B, K, N, ldb * 2, kBK, b_rows));
+  else FLCE_TRY(make_map(&m.b0, B, N, K, ldb * 2, 64, kBK));
+  m.a1 = m.a2 = m.a0;
+  m.b1 = m.b2 = m.b0;
   StoreParams sp{};
   sp.rows = M;
   sp.cols = N;

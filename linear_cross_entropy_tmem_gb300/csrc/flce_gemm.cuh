@@ -254,6 +254,7 @@ __device__ __forceinline__ void finish_box_stores() {
 template <bool kBias, bool kSoftcap>
 struct EpiFwd {
   using Params = FwdParams;
+  static constexpr bool kQuadOk = false;  // no multicast variant built for the logit products
   // Staging of the kept logits (TMA stores), one buffer per epilogue warp.
   static constexpr int kTailBytes = kEpilogueGroups * kEpilogueWarps * kStoreStageBytes;
   __device__ static void finish(const Params& p) {
@@ -412,6 +413,7 @@ __device__ __forceinline__ float token_weight(int reduction, const float* dloss,
 template <bool kBias, bool kSoftcap>
 struct EpiGrad {
   using Params = GradParams;
+  static constexpr bool kQuadOk = false;
   static constexpr int kTailBytes = kEpiSmemBytes;  // dbias column-sum staging
   __device__ static void finish(const Params&) {}
   struct State {
@@ -538,6 +540,7 @@ struct EpiGrad {
 // ============================================================================
 struct EpiStore {
   using Params = StoreParams;
+  static constexpr bool kQuadOk = true;
   // One staging buffer per epilogue warp.
   static constexpr int kTailBytes = kEpilogueGroups * kEpilogueWarps * kStoreStageBytes;
   struct State {
@@ -576,6 +579,7 @@ struct EpiStore {
 // ============================================================================
 struct EpiAccum {
   using Params = AccumParams;
+  static constexpr bool kQuadOk = true;
   static constexpr int kTailBytes = 0;
   __device__ static void finish(const Params&) {}
   struct State {
@@ -925,14 +929,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 // ============================================================================
-// The CTA-pair kernel (cta_group::2): a cluster of two CTAs computes a 256 x 256
-// tile.  Each CTA loads its own 128 rows of A and its own half of B (no TMA
-// multicast); the leader CTA's MMA thread issues M=256 MMAs that read both
+// The CTA-pair kernel (cta_group::2): a pair of CTAs (cluster ranks 2p, 2p+1)
+// computes a 256 x 256 tile.  Each CTA loads its own 128 rows of A and its own
+// half of B; the pair leader's MMA thread issues M=256 MMAs that read both
 // CTAs' shared memory and write 128 x 256 fp32 into each CTA's TMEM.
 //   full[s]    in the leader: both CTAs' copies of stage s complete on it
 //   empty[s]   in each CTA: multicast commit from the leader's MMA thread
 //   tfull[b]   in each CTA: multicast commit, accumulator b ready
 //   tempty[b]  in the leader: 4 epilogue warps of each CTA arrive (8 total)
+// kQuad: a cluster of two pairs takes the two 256-row m tiles of a 512-row
+// super tile with the same n tile and K range, so both pairs need the same B
+// tile.  Each CTA loads one half of its B half and multicasts it to itself and
+// the CTA of the same pair rank in the other pair: every pair pulls 3/4 of the
+// operand bytes from L2 that it would alone.  A stage is free only when both
+// pairs have consumed it, so empty[s] takes one commit from each pair leader.
 // ============================================================================
 __device__ __forceinline__ GemmSmem carve_smem_pair(uint8_t* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -957,7 +967,7 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   }
 }
 
-template <class Epi>
+template <class Epi, bool kQuad>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                      const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_b0,
@@ -966,13 +976,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   GemmSmem sm = carve_smem_pair(smem_raw);
   const int warp = threadIdx.x >> 5;
+  constexpr uint32_t kCtas = kQuad ? 4u : 2u;
+  constexpr int kTileRows = kQuad ? 2 * kPairRows : kPairRows;  // rows per unit of the cluster
   const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
+  const uint32_t pair_rank = rank & 1u, leader_rank = rank & ~1u, pair_id = rank >> 1;
+  const bool leader = pair_rank == 0;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << leader_rank);
+  // B copies go to this CTA and the same pair rank of the other pair.
+  const uint16_t b_mask = static_cast<uint16_t>(0x5u << pair_rank);
+  static_assert(kBN / 128 == 2, "the multicast B split takes one 64-column atom per pair");
 
   if (threadIdx.x == kTmaWarp * 32) {
     for (int s = 0; s < kStagesPair; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], kQuad ? 2 : 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&sm.tfull[b], 1);
@@ -993,9 +1010,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot;
-  const Limits lim = read_limits(sc, kPairRows);
-  const int cid = blockIdx.x >> 1;
-  const int ncl = gridDim.x >> 1;
+  const Limits lim = read_limits(sc, kTileRows);
+  const int cid = static_cast<int>(blockIdx.x / kCtas);
+  const int ncl = static_cast<int>(gridDim.x / kCtas);
   bool aborted = false;
 
   if (warp == kTmaWarp) {
@@ -1011,11 +1028,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       for (int uu = cid; ok && uu < lim.total_units; uu += ncl) {
-        const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
+        const Unit u = decode_unit(sc, uu, kTileRows, rank, lim);
         if (u.skip) continue;
         const int a_row = sc.a_mn_off + static_cast<int>(u.row0);
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
-          const int b_col = sc.b_mn_off + n * kBN + static_cast<int>(rank) * (kBN / 2);
+          const int b_col = sc.b_mn_off + n * kBN + static_cast<int>(pair_rank) * (kBN / 2);
           for (int seg = 0; ok && seg < sc.nseg; ++seg) {
             const uint32_t ai = (sc.seg_maps >> (4 * seg)) & 3u, bi = (sc.seg_maps >> (4 * seg + 2)) & 3u;
             const CUtensorMap* ma = ai == 0 ? &map_a0 : (ai == 1 ? &map_a1 : &map_a2);
@@ -1025,7 +1042,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-              const uint32_t fb = map_to_cta(smem_u32(&sm.full[stage]), 0);
+              const uint32_t fb = map_to_cta(smem_u32(&sm.full[stage]), leader_rank);
               if (leader) mbar_arrive_expect_tx(&sm.full[stage], 2 * kStagePairBytes);
               uint8_t* sa = sm.a + stage * kATileBytes;
               uint8_t* sb = sm.b + stage * kBHalfBytes;
@@ -1037,7 +1054,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < kBM / 64; ++j)
                   tma_load_2d_pair(sa + j * kMnAtomBytes, ma, fb, a_row + 64 * j, sc.a_k_off + k);
               }
-              if (!sc.b_mn) {
+              if (kQuad) {  // rows (K-major; the map's box is 64 rows) or atom pair_id of the half
+                if (!sc.b_mn)
+                  tma_load_2d_pair_mc(sb + pair_id * (kBHalfBytes / 2), mb, fb, sc.b_k_off + k,
+                                      b_col + static_cast<int>(pair_id) * (kBN / 4), b_mask);
+                else
+                  tma_load_2d_pair_mc(sb + pair_id * kMnAtomBytes, mb, fb, b_col + 64 * static_cast<int>(pair_id),
+                                      sc.b_k_off + k, b_mask);
+              } else if (!sc.b_mn) {
                 tma_load_2d_pair(sb, mb, fb, sc.b_k_off + k, b_col);
               } else {
 #pragma unroll
@@ -1069,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int uu = cid; ok && uu < lim.total_units; uu += ncl) {
-        const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
+        const Unit u = decode_unit(sc, uu, kTileRows, rank, lim);
         if (u.skip) continue;
         for (int n = u.n_first; ok && n < u.n_first + u.n_count; ++n) {
           if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, sm.ctl, status)) {
@@ -1097,7 +1121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
                 accumulate = 1;
               }
-              umma_commit_pair(&sm.empty[stage], 0x3);  // stage free in both CTAs
+              // stage free in both CTAs (in all four: the other pair's B copies land here too)
+              umma_commit_pair(&sm.empty[stage], kQuad ? static_cast<uint16_t>(0xF) : pair_mask);
               if (++stage == kStagesPair) {
                 stage = 0;
                 phase ^= 1u;
@@ -1105,7 +1130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          umma_commit_pair(&sm.tfull[acc], 0x3);  // accumulator ready in both CTAs
+          umma_commit_pair(&sm.tfull[acc], pair_mask);  // accumulator ready in both CTAs
           if (++acc == kAccBufs) {
             acc = 0;
             acc_phase ^= 1u;
@@ -1113,7 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) aborted = true;
-      umma_commit_pair(sm.drain, 0x1);
+      umma_commit_pair(sm.drain, static_cast<uint16_t>(1u << rank));
       mbar_wait_teardown(sm.drain, 0);
     }
     __syncwarp();
@@ -1125,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t seq = 0, phase = 0;
     bool ok = true;
     for (int uu = cid; ok && uu < lim.total_units; uu += ncl) {
-      const Unit u = decode_unit(sc, uu, kPairRows, rank, lim);
+      const Unit u = decode_unit(sc, uu, kTileRows, rank, lim);
         if (u.skip) continue;
       typename Epi::State st;
       Epi::begin_unit(ep, u, st, grp);
@@ -1143,7 +1168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Epi::tile(ep, u, n, tmem_base + lane_base + grp * kBN, st, epi, grp);
         tc_fence_before();
         __syncwarp();
-        if (lane_id() == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&sm.tempty[grp]), 0));
+        if (lane_id() == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&sm.tempty[grp]), leader_rank));
         phase ^= 1u;
       }
       if (ok) Epi::end_unit(ep, u, st, grp);

@@ -23,16 +23,17 @@ static cudaError_t launch_gemm_single(const TmaMaps& m, const GemmSched& sc, con
   return cudaGetLastError();
 }
 
-template <class Epi>
-static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
-                                    int* status, int num_sms, cudaStream_t stream) {
-  auto kern = gemm_pair_kernel<Epi>;
+template <class Epi, bool kQuad>
+static cudaError_t launch_gemm_cluster(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
+                                       int* status, int num_sms, cudaStream_t stream) {
+  auto kern = gemm_pair_kernel<Epi, kQuad>;
+  constexpr int kCtas = kQuad ? 4 : 2;
   constexpr int smem = kGemmPairSmemBase + Epi::kTailBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kCtas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
@@ -47,14 +48,24 @@ static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (resident[dev] == 0) {
-    cfg.gridDim = dim3(2 * std::max(1, num_sms / 2));
+    cfg.gridDim = dim3(kCtas * std::max(1, num_sms / kCtas));
     int n = 0;
     if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
     resident[dev] = std::max(1, n);
   }
-  const int clusters = std::max(1, std::min(std::min(sc.total_units, num_sms / 2), resident[dev]));
-  cfg.gridDim = dim3(2 * clusters);
+  const int clusters = std::max(1, std::min(std::min(sc.total_units, num_sms / kCtas), resident[dev]));
+  cfg.gridDim = dim3(kCtas * clusters);
   return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
+}
+
+template <class Epi>
+static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
+                                    int* status, int num_sms, cudaStream_t stream) {
+  if (sc.quad) {
+    if constexpr (Epi::kQuadOk) return launch_gemm_cluster<Epi, true>(m, sc, p, status, num_sms, stream);
+    else return cudaErrorInvalidValue;
+  }
+  return launch_gemm_cluster<Epi, false>(m, sc, p, status, num_sms, stream);
 }
 
 template <class Epi>

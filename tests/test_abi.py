@@ -77,10 +77,12 @@ def test_workspace_size_needs_no_gpu_and_never_scales_with_n_times_v(lib):
         st, bw = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, hidden_dtype=B.FLCE_F32), 1)
         # forward: O(N * splits); backward: one bf16 G chunk of at most 1 GiB,
         # its per-tile dbias sums (1/64 of it in fp32 per 128 rows), the fp32 hi/lo
-        # split and the fp32 dh accumulator (4 N D bytes each at most)
+        # split (4 N D bytes at most) and the fp32 dh slots (4 N D bytes each: one per
+        # K split, at most 8 once the dh product has 128 tiles of 128 x 256)
         # five 4-byte split records per token, up to 64 splits x 2 epilogue groups, + z[target]
         assert fw <= (5 * 4 * 64 * 2 + 4) * N + (1 << 20)
-        assert bw <= (1 << 30) + (1 << 30) // 64 + 3 * 4 * N * D + (1 << 20)
+        slots = 8 if -(-N // 128) * -(-D // 256) >= 128 else 16
+        assert bw <= (1 << 30) + (1 << 30) // 64 + (1 + slots) * 4 * N * D + (1 << 20)
         # the G chunk covers at most about half of the vocabulary
         assert bw <= N * (V // 2 + 256) * 2 * (1 + 1 / 32) + 16 * 4 * N * D + 4 * N * D + (1 << 20)
         if N * V >= 1 << 28:

@@ -744,3 +744,28 @@ def test_nan_hidden_row_stays_in_its_row(softcap):
     assert np.abs(loss[keep] - ref["loss_tok"][keep]).max() < TOL_LSE
     ref_dh = ref_b["dh"][keep]
     assert np.linalg.norm(dh[keep] - ref_dh) <= 1e-2 * np.linalg.norm(ref_dh)
+
+
+@pytest.mark.parametrize("bwd", ["recompute", "keep_logits"])
+def test_multicast_products_equal_plain_pairs_bitwise(bwd):
+    """dh and dW from clusters of two CTA pairs that share the B operand by TMA multicast equal those
+    of plain CTA pairs bit for bit (same MMAs, same order), with a ragged last 512-row tile on both
+    the token (dh) and the vocabulary (dW) side; the forward outputs are untouched."""
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_multicast
+    w = Workload("mc", 1300, 512, 3000, sigma_w=0.08, bias=True, seed=31)
+    h, W, b, t, dloss = (x.cuda() for x in make_inputs(w, "cpu"))
+    out = {}
+    try:
+        testing_set_gemm_mode(2)
+        for on in (False, True):
+            testing_set_multicast(on)
+            fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd=bwd)
+            torch.cuda.synchronize()
+            assert F.flce_read_device_status(fwd.workspace) == 0
+            out[on] = (fwd.loss.clone(), fwd.lse.clone()) + tuple(g.clone() for g in grads)
+    finally:
+        testing_set_multicast(False)
+        testing_set_gemm_mode(0)
+    for a, c in zip(out[False], out[True]):
+        assert torch.equal(a, c)
