@@ -43,14 +43,16 @@ FLCE_API int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit);
 FLCE_API int flce_testing_set_gemm_mode(int mode);
 
 /*
- * Process-wide switch of the operand multicast, for tests and tuning.  1: a
+ * Process-wide switch of the operand multicast, for tests and tuning.  A
  * CTA-pair product whose B operand is MN-major (dh, dW), and the test GEMM,
- * run as clusters of two CTA pairs over a 512-row m tile; both pairs need the
- * same B tile and each CTA loads half of its share, multicast by TMA to itself
- * and its counterpart in the other pair.  0 (the default): plain CTA pairs.
- * Results are bitwise the same either way.  Not thread-safe.
+ * can run as clusters of two CTA pairs over a 512-row m tile: both pairs need
+ * the same B tile, and each CTA loads half of its share and multicasts it by
+ * TMA to itself and its counterpart in the other pair.  mode 1 (the default):
+ * where the device fits as many waves of units into the resident clusters of
+ * four as into the resident pairs; 2: wherever there are two m tiles; 0: never.
+ * Results are bitwise the same in every mode.  Not thread-safe.
  */
-FLCE_API int flce_testing_set_multicast(int on);
+FLCE_API int flce_testing_set_multicast(int mode);
 
 /*
  * Process-wide override of the token-chunk size of the token-chunked backward

@@ -303,7 +303,7 @@ def testing_set_gemm_mode(mode: int = 0) -> None:
     B.check(B.load().flce_testing_set_gemm_mode(int(mode)), "flce_testing_set_gemm_mode")
 
 
-def testing_set_multicast(on: bool = False) -> None:
-    """1: CTA-pair products with an MN-major B operand run as clusters of two pairs sharing B by TMA
-    multicast; 0 (default): plain CTA pairs (tests, A/B timing)."""
-    B.check(B.load().flce_testing_set_multicast(1 if on else 0), "flce_testing_set_multicast")
+def testing_set_multicast(mode: int = 1) -> None:
+    """Operand multicast of the dh / dW products (clusters of two CTA pairs sharing B): 1 automatic
+    (default), 2 always, 0 never (tests, A/B timing)."""
+    B.check(B.load().flce_testing_set_multicast(int(mode)), "flce_testing_set_multicast")

@@ -206,7 +206,7 @@ std::atomic<int64_t> g_force_chunk_cols{0};
 std::atomic<int> g_force_dh_ksplit{0};
 std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel
 std::atomic<int64_t> g_force_token_rows{0};
-std::atomic<int> g_multicast{0};  // flce_testing_set_multicast
+std::atomic<int> g_multicast{1};  // flce_testing_set_multicast: 0 off, 1 automatic, 2 always
 
 // CTA pairs (256-row tiles) when there are at least 256 rows and enough units
 // to give every cluster work; otherwise single CTAs (128-row tiles).
@@ -220,15 +220,29 @@ bool use_pair(int64_t m_rows, int64_t units_per_pair_row, int num_sms) {
 // Run a CTA-pair product as clusters of two pairs that share the B tile by TMA
 // multicast (GemmSched::quad, 512-row m tiles), which cuts the operand bytes
 // each pair pulls from L2 by a quarter.  Needs at least two 256-row m tiles.
-// Called on a pair schedule before finish_sched.  Off unless switched on for
-// testing: fewer clusters of four than pairs are resident on a GB300, and the
-// lost SMs cost more than the L2 bytes save (dh and dW 2-4 % slower per clock
-// at the Qwen3-8B-like head, dW 10 % slower at the Gemma-like one).
-void use_quad(GemmSched& s, bool pair, int64_t m_rows) {
-  if (!pair || g_multicast.load() == 0 || cdiv(m_rows, kPairRows) < 2) return;
+// Called on a pair schedule (n_tiles, n_per_unit and ksplit set) before
+// finish_sched.  A cluster of four must fit in one GPC, so fewer of them than
+// pairs are resident on a GB300: only where that costs no extra wave of units
+// does the multicast pay (measured: Gemma-like dh 3.93 -> 3.74 ms at equal
+// waves; one extra wave made dW 10 % slower there, and dh and dW of the
+// Qwen3-8B-like head 2-4 % slower per clock).
+int use_quad(GemmSched& s, bool pair, int64_t m_rows, int num_sms) {
+  const int mode = g_multicast.load();
+  if (!pair || mode == 0 || cdiv(m_rows, kPairRows) < 2) return FLCE_OK;
+  if (mode == 1) {
+    int pairs = 0, quads = 0;
+    if (gradient_gemm_clusters(false, num_sms, &pairs) != cudaSuccess ||
+        gradient_gemm_clusters(true, num_sms, &quads) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    const int64_t per_m = cdiv(s.n_tiles, s.n_per_unit) * s.ksplit;
+    const int64_t waves_pair = cdiv(cdiv(m_rows, kPairRows) * per_m, pairs);
+    const int64_t waves_quad = cdiv(cdiv(m_rows, 2 * kPairRows) * per_m, quads);
+    if (waves_quad > waves_pair) return FLCE_OK;
+  }
   s.quad = 1;
   s.m_tiles = static_cast<int32_t>(cdiv(m_rows, 2 * kPairRows));
   s.group_m = std::max(1, s.group_m / 2);
+  return FLCE_OK;
 }
 
 int64_t chunk_width(int64_t n_tokens, int64_t vocab) {
@@ -867,7 +881,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     s2.b_mn = 1;
     s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
     s2.k_limit = pr.row_count;
-    use_quad(s2, pair_dw, width);
+    FLCE_TRY(use_quad(s2, pair_dw, width, dev.num_sms));
     finish_sched(s2);
     StoreParams sp{};
     sp.rows = width;
@@ -892,7 +906,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
     s3.group_m = std::max(1, dh_ctas / std::max(1, s3.n_tiles * ksplit));
     s3.m_limit = pr.row_count;
-    use_quad(s3, pair_dh, N);
+    FLCE_TRY(use_quad(s3, pair_dh, N, dev.num_sms));
     finish_sched(s3);
     AccumParams ap{};
     ap.rows = N;
@@ -1073,7 +1087,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     s3.group_m = 16;
     s3.ks_outer = 1;
     s3.m_limit = lim;
-    use_quad(s3, pair_dh, rows);
+    FLCE_TRY(use_quad(s3, pair_dh, rows, dev.num_sms));
     finish_sched(s3);
     uint8_t* dh_out = static_cast<uint8_t*>(dhidden) + (pr.cmp ? 0 : size_t(r0) * D * out_elem);
     AccumParams ap{};
@@ -1106,7 +1120,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     s2.b_mn = 1;
     s2.group_m = std::max(1, dw_ctas / std::max(1, s2.n_tiles));
     s2.k_limit = lim;
-    use_quad(s2, pair_dw, V);
+    FLCE_TRY(use_quad(s2, pair_dw, V, dev.num_sms));
     finish_sched(s2);
     AccumParams aw{};
     aw.rows = V;
@@ -1299,9 +1313,9 @@ int flce_testing_set_gemm_mode(int mode) {
   return FLCE_OK;
 }
 
-int flce_testing_set_multicast(int on) {
-  if (on != 0 && on != 1) return FLCE_ERR_INVALID_ARG;
-  g_multicast.store(on);
+int flce_testing_set_multicast(int mode) {
+  if (mode < 0 || mode > 2) return FLCE_ERR_INVALID_ARG;
+  g_multicast.store(mode);
   return FLCE_OK;
 }
 
@@ -1327,7 +1341,7 @@ int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int6
   GemmSched s = base_sched(M, N, K, 1, 0u, pair);
   s.a_mn = a_mn_major ? 1 : 0;
   s.b_mn = b_mn_major ? 1 : 0;
-  use_quad(s, pair, M);
+  FLCE_TRY(use_quad(s, pair, M, dev.num_sms));
   finish_sched(s);
   // K-major B: a CTA pair loads 128-row halves; under multicast each CTA loads 64 rows.
   const uint32_t b_rows = !pair ? kBN : (s.quad ? kBN / 4 : kBN / 2);

@@ -26,6 +26,11 @@ cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
   return launch_gemm<EpiAccum>(pair, maps, sc, p, status, num_sms, stream);
 }
 
+cudaError_t gradient_gemm_clusters(bool quad, int num_sms, int* clusters) {
+  return quad ? resident_clusters<EpiAccum, true>(num_sms, clusters)
+              : resident_clusters<EpiAccum, false>(num_sms, clusters);
+}
+
 // Token-chunked backward: G from the kept fp32 logits of one token chunk.
 // Thread t of a block handles kZGradVec consecutive columns over one tile of
 // kZGradRows rows at a time (row tiles grid-strided over blockIdx.y): per row

@@ -24,36 +24,59 @@ static cudaError_t launch_gemm_single(const TmaMaps& m, const GemmSched& sc, con
 }
 
 template <class Epi, bool kQuad>
-static cudaError_t launch_gemm_cluster(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
-                                       int* status, int num_sms, cudaStream_t stream) {
-  auto kern = gemm_pair_kernel<Epi, kQuad>;
-  constexpr int kCtas = kQuad ? 4 : 2;
-  constexpr int smem = kGemmPairSmemBase + Epi::kTailBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+static cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCtas;
+  attr[0].val.clusterDim.x = kQuad ? 4 : 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = kGemmPairSmemBase + Epi::kTailBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Clusters that can be resident at once (one CTA per SM), cached per device.
+  return cfg;
+}
+
+// Clusters of the CTA-pair kernel (two CTAs, or four with kQuad) that can be
+// resident at once on the current device, one CTA per SM; cached per device.
+// A cluster must fit in one GPC, so the count of four-CTA clusters can be
+// below num_sms / 4.
+template <class Epi, bool kQuad>
+static cudaError_t resident_clusters(int num_sms, int* out) {
+  auto kern = gemm_pair_kernel<Epi, kQuad>;
+  constexpr int kCtas = kQuad ? 4 : 2;
   static int resident[64] = {0};
   int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (resident[dev] == 0) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kGemmPairSmemBase + Epi::kTailBytes)) != cudaSuccess)
+      return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster_config<Epi, kQuad>(attr, nullptr);
     cfg.gridDim = dim3(kCtas * std::max(1, num_sms / kCtas));
     int n = 0;
     if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
     resident[dev] = std::max(1, n);
   }
-  const int clusters = std::max(1, std::min(std::min(sc.total_units, num_sms / kCtas), resident[dev]));
+  *out = std::min(resident[dev], std::max(1, num_sms / kCtas));
+  return cudaSuccess;
+}
+
+template <class Epi, bool kQuad>
+static cudaError_t launch_gemm_cluster(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
+                                       int* status, int num_sms, cudaStream_t stream) {
+  auto kern = gemm_pair_kernel<Epi, kQuad>;
+  constexpr int kCtas = kQuad ? 4 : 2;
+  int resident = 0;
+  cudaError_t e = resident_clusters<Epi, kQuad>(num_sms, &resident);  // also sets the smem attribute
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config<Epi, kQuad>(attr, stream);
+  const int clusters = std::max(1, std::min(sc.total_units, resident));
   cfg.gridDim = dim3(kCtas * clusters);
   return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
 }

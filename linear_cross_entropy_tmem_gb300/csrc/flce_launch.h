@@ -63,6 +63,9 @@ cudaError_t launch_store_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
                               int* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& sc, const AccumParams& p,
                               int* status, int num_sms, cudaStream_t stream);
+// Clusters of the dh / dW kernels (CTA pairs, or two pairs with quad) that
+// can be resident at once on the current device.
+cudaError_t gradient_gemm_clusters(bool quad, int num_sms, int* clusters);
 
 cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream);
 // Under compaction, the valid rows of each token chunk of the kept-logits backward.

@@ -232,3 +232,19 @@ def test_oracle_is_not_imported_by_the_product_path():
     for f in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True):
         src = open(f).read()
         assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), f
+
+
+def test_testing_switches_validate_their_arguments(lib):
+    """The process-wide test/tuning switches reject out-of-range values and accept every
+    documented one (they only store a setting, so no GPU is needed)."""
+    assert lib.flce_testing_set_gemm_mode(3) == B.FLCE_ERR_INVALID_ARG
+    assert lib.flce_testing_set_multicast(3) == B.FLCE_ERR_INVALID_ARG
+    assert lib.flce_testing_set_multicast(-1) == B.FLCE_ERR_INVALID_ARG
+    try:
+        for mode in (0, 2, 1):
+            assert lib.flce_testing_set_multicast(mode) == B.FLCE_OK
+        for mode in (1, 2, 0):
+            assert lib.flce_testing_set_gemm_mode(mode) == B.FLCE_OK
+    finally:
+        lib.flce_testing_set_multicast(1)
+        lib.flce_testing_set_gemm_mode(0)

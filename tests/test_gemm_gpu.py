@@ -31,9 +31,9 @@ def gemm_mode(request):
 @pytest.fixture
 def multicast(request):
     from linear_cross_entropy_tmem_gb300.api import testing_set_multicast
-    testing_set_multicast(request.param)
+    testing_set_multicast(2 if request.param else 0)
     yield request.param
-    testing_set_multicast(False)
+    testing_set_multicast(1)
 
 
 @pytest.mark.parametrize("gemm_mode,multicast", [(1, True), (2, False), (2, True)], indirect=True,
@@ -70,11 +70,11 @@ def test_multicast_clusters_are_bitwise_plain_pairs(lib, b_mn, M, N, K):
     try:
         testing_set_gemm_mode(2)
         for on in (False, True):
-            testing_set_multicast(on)
+            testing_set_multicast(2 if on else 0)
             out[on] = testing_gemm(A, Bm, a_mn_major=False, b_mn_major=bool(b_mn), M=M, N=N, K=K)
             torch.cuda.synchronize()
     finally:
-        testing_set_multicast(False)
+        testing_set_multicast(1)
         testing_set_gemm_mode(0)
     assert torch.equal(out[False], out[True])
     B_nk = Bm.cpu().double() if not b_mn else Bm.cpu().double()[:, :N].T  # logical [N][K]

@@ -759,13 +759,13 @@ def test_multicast_products_equal_plain_pairs_bitwise(bwd):
     try:
         testing_set_gemm_mode(2)
         for on in (False, True):
-            testing_set_multicast(on)
+            testing_set_multicast(2 if on else 0)
             fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd=bwd)
             torch.cuda.synchronize()
             assert F.flce_read_device_status(fwd.workspace) == 0
             out[on] = (fwd.loss.clone(), fwd.lse.clone()) + tuple(g.clone() for g in grads)
     finally:
-        testing_set_multicast(False)
+        testing_set_multicast(1)
         testing_set_gemm_mode(0)
     for a, c in zip(out[False], out[True]):
         assert torch.equal(a, c)
