@@ -769,3 +769,32 @@ def test_multicast_products_equal_plain_pairs_bitwise(bwd):
         testing_set_gemm_mode(0)
     for a, c in zip(out[False], out[True]):
         assert torch.equal(a, c)
+
+
+@pytest.mark.parametrize("bwd", ["recompute", "keep_logits"])
+def test_multicast_with_compaction_matches_oracle_and_plain_pairs(bwd):
+    """Under FLCE_FLAG_COMPACT_VALID the dh / dW units are enumerated over the m tiles that hold a
+    valid row (a device-side count); with the B multicast clusters those tiles are 512 rows and the
+    count cuts the last one anywhere. The results match the oracle and the plain CTA pairs bitwise."""
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_multicast
+    w = Workload("mcc", 1300, 256, 2600, sigma_w=0.1, bias=True, ignore_every=3, seed=33)
+    h, W, b, t, dloss = make_inputs(w, "cpu")
+    dev = [x.cuda() for x in (h, W, b, t, dloss)]
+    out = {}
+    try:
+        testing_set_gemm_mode(2)
+        for mode in (0, 2):
+            testing_set_multicast(mode)
+            fwd, grads = F.flce_forward_backward(dev[0], dev[1], dev[3], dev[4], dev[2], entropy=True,
+                                                 compact=True, bwd=bwd)
+            torch.cuda.synchronize()
+            assert F.flce_read_device_status(fwd.workspace) == 0
+            out[mode] = (fwd, grads)
+    finally:
+        testing_set_multicast(1)
+        testing_set_gemm_mode(0)
+    for a, c in zip(out[0][1], out[2][1]):
+        assert torch.equal(a, c)
+    _compare_compacted({"fwd": out[2][0], "bwd": out[2][1]}, oracle.forward(h, W, b, t),
+                       oracle.backward(h, W, b, t, dloss=dloss), t, "mean")
