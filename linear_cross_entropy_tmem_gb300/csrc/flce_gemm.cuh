@@ -3,7 +3,8 @@
 //
 //   warp 8      TMA producer: fills a shared-memory ring with 128-byte swizzled
 //               bf16 tiles of A and B (4 stages of 128x64 + 256x64 for one CTA;
-//               6 stages of 128x64 + its 128x64 half of B per CTA of a pair).
+//               6 stages of 128x64 + its 128x64 half of B per CTA of a pair;
+//               with two pairs per cluster the B halves are TMA-multicast).
 //   warp 9      MMA issuer: one elected thread issues tcgen05.mma (M=128 or,
 //               for a CTA pair, M=256; N=256; K=16) into one of two TMEM
 //               accumulators (2 x 256 fp32 columns) and commits stage releases
