@@ -55,6 +55,27 @@ FLCE_API int flce_testing_set_gemm_mode(int mode);
 FLCE_API int flce_testing_set_multicast(int mode);
 
 /*
+ * The backward plan the library makes for `problem` on a device with `num_sms`
+ * SMs, for tests of the host-side planning; it needs no GPU.  for_backward as
+ * in flce_workspace_size: 1 for flce_backward, 2 for flce_forward_backward.
+ * The multicast choice, which needs the device's resident cluster counts, is
+ * not part of it.  The testing overrides above apply.  Returns FLCE_OK, the
+ * validation error of `problem`, or FLCE_ERR_INVALID_ARG.
+ */
+typedef struct {
+  int32_t keep_logits;       /* 1: token-chunked backward (6NVD); 0: recompute (8NVD) */
+  int32_t dh_pair;           /* 1: the dh product runs on CTA pairs (256-row tiles) */
+  int64_t token_chunk_rows;  /* keep_logits: tokens per chunk */
+  int64_t vocab_chunk_cols;  /* recompute: columns of the G scratch (its row stride) */
+  int64_t run_chunk_cols;    /* recompute: columns per chunk as run, at most vocab_chunk_cols */
+  int64_t n_chunks;          /* chunks as run: token chunks, or vocabulary chunks */
+  int32_t dh_ksplit_max;     /* fp32 dh slots in the workspace */
+  int32_t dh_ksplit;         /* K splits of the dh product as run */
+} flce_testing_plan_info;
+FLCE_API int flce_testing_plan(const flce_problem* problem, int for_backward, int num_sms,
+                               flce_testing_plan_info* out);
+
+/*
  * Process-wide override of the token-chunk size of the token-chunked backward
  * (FLCE_FLAG_BWD_KEEP_LOGITS), for tests and tuning: rows per chunk, rounded up
  * to 256 and capped at half of N rounded up to 256; 0 restores the automatic

@@ -64,6 +64,20 @@ class FlceProblem(ctypes.Structure):
 _LIB = None
 
 # name -> (restype, argtypes); every function ``include/*.h`` declares.
+class FlceTestingPlanInfo(ctypes.Structure):
+    """Mirror of ``flce_testing_plan_info``."""
+    _fields_ = [
+        ("keep_logits", c_int32),
+        ("dh_pair", c_int32),
+        ("token_chunk_rows", c_int64),
+        ("vocab_chunk_cols", c_int64),
+        ("run_chunk_cols", c_int64),
+        ("n_chunks", c_int64),
+        ("dh_ksplit_max", c_int32),
+        ("dh_ksplit", c_int32),
+    ]
+
+
 SIGNATURES = {
     "flce_workspace_size": (c_int, [POINTER(FlceProblem), c_int, POINTER(c_size_t)]),
     "flce_forward": (c_int, [POINTER(FlceProblem), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -82,6 +96,7 @@ SIGNATURES = {
     "flce_scale_gradient": (c_int, [c_void_p, c_void_p, c_int64, c_int32, c_void_p]),
     "flce_testing_set_gemm_mode": (c_int, [c_int]),
     "flce_testing_set_multicast": (c_int, [c_int]),
+    "flce_testing_plan": (c_int, [POINTER(FlceProblem), c_int, c_int, POINTER(FlceTestingPlanInfo)]),
     "flce_testing_set_token_chunk": (c_int, [c_int64]),
     "flce_testing_set_launch_log": (c_int, [c_void_p, c_int32, POINTER(c_int32)]),
     "flce_testing_launch_count": (c_int64, []),

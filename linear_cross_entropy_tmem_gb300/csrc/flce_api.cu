@@ -787,6 +787,29 @@ int64_t recompute_chunk_cols(const Layout& L, int64_t N, int64_t D, int64_t V, i
   return best_t * kBN;
 }
 
+// The dh product's kernel (CTA pairs or single CTAs), its CTA (or pair) count
+// and its K split, for each backward algorithm.
+struct DhPlan {
+  bool pair;
+  int ctas;
+  int ksplit;
+};
+DhPlan plan_recompute_dh(const Layout& L, int64_t N, int64_t D, int num_sms) {
+  DhPlan d;
+  d.pair = use_pair(N, cdiv(D, kBN), num_sms);
+  d.ctas = d.pair ? num_sms / 2 : num_sms;
+  const int64_t tiles = cdiv(N, d.pair ? kPairRows : kBM) * cdiv(D, kBN);
+  d.ksplit = L.ksplit_max > 1 ? choose_recompute_ksplit(tiles, d.ctas, L.ksplit_max) : 1;
+  return d;
+}
+DhPlan plan_token_dh(const Layout& L, int64_t D, int num_sms) {
+  DhPlan d;
+  d.pair = use_pair(L.nc, cdiv(D, kBN), num_sms);
+  d.ctas = d.pair ? num_sms / 2 : num_sms;
+  d.ksplit = choose_token_ksplit(cdiv(L.nc, d.pair ? kPairRows : kBM) * cdiv(D, kBN), d.ctas, L.ksplit_max);
+  return d;
+}
+
 int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
                  cudaStream_t st, const void* bias, const Prep& pr, const float* lse_use,
                  const int64_t* n_valid, const float* dloss_use, void* dhidden, void* dweight, void* dbias) {
@@ -817,10 +840,10 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
 
   // dh: CTA pairs or single CTAs, and the K split for this device (bounded by
   // the layout's slot count).
-  const bool pair_dh = use_pair(N, cdiv(D, kBN), dev.num_sms);
-  const int dh_ctas = pair_dh ? dev.num_sms / 2 : dev.num_sms;
-  const int64_t dh_tiles = cdiv(N, pair_dh ? kPairRows : kBM) * cdiv(D, kBN);
-  const int ksplit = L.ksplit_max > 1 ? choose_recompute_ksplit(dh_tiles, dh_ctas, L.ksplit_max) : 1;
+  const DhPlan dhp = plan_recompute_dh(L, N, D, dev.num_sms);
+  const bool pair_dh = dhp.pair;
+  const int dh_ctas = dhp.ctas;
+  const int ksplit = dhp.ksplit;
 
   // Vocabulary chunks of at most L.vc columns (the G scratch keeps L.vc as its
   // row stride).
@@ -974,10 +997,10 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
   const int dw_nseg = b_term_segments(pr.nh, &dw_segs);
   const int dh_nseg = b_term_segments(pr.nw, &dh_segs);
   const size_t w_elem = weight_elem(p);
-  const bool pair_dh = use_pair(L.nc, cdiv(D, kBN), dev.num_sms);
-  const int dh_ctas = pair_dh ? dev.num_sms / 2 : dev.num_sms;
-  const int ksplit =
-      choose_token_ksplit(cdiv(L.nc, pair_dh ? kPairRows : kBM) * cdiv(D, kBN), dh_ctas, L.ksplit_max);
+  const DhPlan dhp = plan_token_dh(L, D, dev.num_sms);
+  const bool pair_dh = dhp.pair;
+  const int dh_ctas = dhp.ctas;
+  const int ksplit = dhp.ksplit;
   const bool pair_dw = use_pair(V, cdiv(D, kBN), dev.num_sms);
   const int dw_ctas = pair_dw ? dev.num_sms / 2 : dev.num_sms;
 
@@ -1310,6 +1333,31 @@ int flce_testing_set_token_chunk(int64_t rows) {
 int flce_testing_set_gemm_mode(int mode) {
   if (mode < 0 || mode > 2) return FLCE_ERR_INVALID_ARG;
   g_gemm_mode.store(mode);
+  return FLCE_OK;
+}
+
+int flce_testing_plan(const flce_problem* problem, int for_backward, int num_sms, flce_testing_plan_info* out) {
+  if (!out || num_sms < 2 || num_sms > 4096 || (for_backward != 1 && for_backward != 2)) return FLCE_ERR_INVALID_ARG;
+  FLCE_TRY(validate(problem));
+  const Layout L = make_layout(problem, for_backward == 2 ? kFused : kBackward, true);
+  const int64_t N = problem->n_tokens, D = problem->hidden, V = problem->vocab;
+  flce_testing_plan_info info{};
+  DhPlan d;
+  if (L.token) {
+    info.keep_logits = 1;
+    info.token_chunk_rows = L.nc;
+    info.n_chunks = L.n_tchunks;
+    d = plan_token_dh(L, D, num_sms);
+  } else {
+    info.vocab_chunk_cols = L.vc;
+    info.run_chunk_cols = recompute_chunk_cols(L, N, D, V, num_sms);
+    info.n_chunks = cdiv(V, info.run_chunk_cols);
+    d = plan_recompute_dh(L, N, D, num_sms);
+  }
+  info.dh_ksplit_max = L.ksplit_max;
+  info.dh_ksplit = d.ksplit;
+  info.dh_pair = d.pair ? 1 : 0;
+  *out = info;
   return FLCE_OK;
 }
 
