@@ -260,7 +260,7 @@ int64_t chunk_width(int64_t n_tokens, int64_t vocab) {
 // fp32 dh slots of the recompute backward (K splits of each chunk's dh
 // product).  Small products split K to fill the GPU (at least 8 K blocks per
 // split); mid-sized ones (up to 2048 128-row tiles) get up to 8 slots so that
-// the run can even out the last wave of tiles (choose_token_ksplit).
+// the run can even out the last wave of tiles (choose_recompute_ksplit).
 int dh_ksplit_bound(int64_t n_tokens, int64_t hidden, int64_t vc) {
   const int forced = g_force_dh_ksplit.load();
   if (forced > 0) return std::min(forced, kMaxKSplit);

@@ -467,7 +467,8 @@ struct EpiGrad {
       const bool ragged = vc + 32 > p.vocab;
       float bch[32];
       if (kBias) load_bias_chunk(p.bias, p.bias_f32, p.bias_vec, vc, p.vocab, bch);
-      // The grad_terms arithmetic on packed fp32 pairs (columns j, j + 1), rounded alike.
+      // The grad_terms arithmetic on packed fp32 pairs (columns j, j + 1); with the soft cap the
+      // two columns share one reciprocal (f2_inv_exp2p1_swapped).
       float g[32];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
