@@ -55,12 +55,15 @@ FLCE_API int flce_testing_set_gemm_mode(int mode);
 FLCE_API int flce_testing_set_multicast(int mode);
 
 /*
- * The backward plan the library makes for `problem` on a device with `num_sms`
- * SMs, for tests of the host-side planning; it needs no GPU.  for_backward as
- * in flce_workspace_size: 1 for flce_backward, 2 for flce_forward_backward.
- * The multicast choice, which needs the device's resident cluster counts, is
- * not part of it.  The testing overrides above apply.  Returns FLCE_OK, the
- * validation error of `problem`, or FLCE_ERR_INVALID_ARG.
+ * The plan the library makes for `problem` on a device with `num_sms` SMs, for
+ * tests of the host-side planning; it needs no GPU.  for_backward as in
+ * flce_workspace_size: 0 for flce_forward (only the fwd_* fields are set), 1
+ * for flce_backward (the fwd_* fields describe flce_forward), 2 for
+ * flce_forward_backward (with kept logits the forward runs per token chunk:
+ * the fwd_* fields describe the first chunk).  The multicast choice, which
+ * needs the device's resident cluster counts, is not part of it.  The testing
+ * overrides above apply.  Returns FLCE_OK, the validation error of `problem`,
+ * or FLCE_ERR_INVALID_ARG.
  */
 typedef struct {
   int32_t keep_logits;       /* 1: token-chunked backward (6NVD); 0: recompute (8NVD) */
@@ -71,6 +74,10 @@ typedef struct {
   int64_t n_chunks;          /* chunks as run: token chunks, or vocabulary chunks */
   int32_t dh_ksplit_max;     /* fp32 dh slots in the workspace */
   int32_t dh_ksplit;         /* K splits of the dh product as run */
+  int32_t fwd_pair;          /* 1: the forward logit product runs on CTA pairs */
+  int32_t fwd_splits;        /* vocabulary splits of the forward (records per token) */
+  int32_t fwd_tiles_per_split;  /* 256-column vocabulary tiles per split */
+  int32_t reserved;          /* 0 */
 } flce_testing_plan_info;
 FLCE_API int flce_testing_plan(const flce_problem* problem, int for_backward, int num_sms,
                                flce_testing_plan_info* out);

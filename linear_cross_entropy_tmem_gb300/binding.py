@@ -75,6 +75,10 @@ class FlceTestingPlanInfo(ctypes.Structure):
         ("n_chunks", c_int64),
         ("dh_ksplit_max", c_int32),
         ("dh_ksplit", c_int32),
+        ("fwd_pair", c_int32),
+        ("fwd_splits", c_int32),
+        ("fwd_tiles_per_split", c_int32),
+        ("reserved", c_int32),
     ]
 
 

@@ -460,6 +460,22 @@ int choose_splits(int64_t m_tiles, int64_t n_tiles, int num_sms, int* per_unit) 
   return best_s;
 }
 
+// The forward logit product over `rows` tokens: its kernel (CTA pairs or
+// single CTAs) and its vocabulary splits.
+struct FwdPlan {
+  bool pair;
+  int splits;
+  int per_unit;  // vocabulary tiles per split
+};
+FwdPlan plan_forward(int64_t rows, int64_t V, int num_sms) {
+  FwdPlan f;
+  f.pair = use_pair(rows, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), num_sms);
+  f.per_unit = 1;
+  f.splits = choose_splits(cdiv(rows, f.pair ? kPairRows : kBM), cdiv(V, kBN), f.pair ? num_sms / 2 : num_sms,
+                           &f.per_unit);
+  return f;
+}
+
 int fail(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
 
 // Launch log (flce_testing_set_launch_log) and launch counter.
@@ -661,16 +677,16 @@ int run_forward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, u
                 cudaStream_t st, const void* bias, const Prep& pr, float* loss, float* lse,
                 float* entropy, int64_t* correct, int64_t* n_valid, float* entropy_sum, float* lse_compact) {
   const int64_t N = p->n_tokens, D = p->hidden, V = p->vocab;
-  const bool pair = use_pair(N, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
+  const FwdPlan fpl = plan_forward(N, V, dev.num_sms);
+  const bool pair = fpl.pair;
   TmaMaps maps;
   FLCE_TRY(make_term_maps(&maps.a0, &maps.a1, &maps.a2, pr.h, pr.nh, 0, D, N, D * 2, kBK, kBM));
   FLCE_TRY(make_term_maps(&maps.b0, &maps.b1, &maps.b2, pr.w, pr.nw, 0, D, V, D * 2, kBK, pair ? kBN / 2 : kBN));
   uint32_t seg_maps = 0;
   const int nseg = logit_segments(pr.nh, pr.nw, &seg_maps);
   GemmSched sc = base_sched(N, V, D, nseg, seg_maps, pair);
-  int per_unit = 1;
-  const int splits = choose_splits(sc.m_tiles, sc.n_tiles, pair ? dev.num_sms / 2 : dev.num_sms, &per_unit);
-  sc.n_per_unit = per_unit;
+  const int splits = fpl.splits;
+  sc.n_per_unit = fpl.per_unit;
   sc.group_m = pair ? 16 : 32;
   sc.m_limit = pr.row_count;
   finish_sched(sc);
@@ -1014,14 +1030,14 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     const int32_t* rmap = pr.cmp ? pr.row_map + r0 : nullptr;   // chunk row -> token
 
     // (1) logits of the chunk: online statistics, and z kept in fp32
-    const bool pair_f = use_pair(rows, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), dev.num_sms);
+    const FwdPlan fpl = plan_forward(rows, V, dev.num_sms);
+    const bool pair_f = fpl.pair;
     TmaMaps fm;
     FLCE_TRY(make_term_maps(&fm.a0, &fm.a1, &fm.a2, pr.h, pr.nh, h_off, D, rows, D * 2, kBK, kBM));
     FLCE_TRY(make_term_maps(&fm.b0, &fm.b1, &fm.b2, pr.w, pr.nw, 0, D, V, D * 2, kBK, pair_f ? kBN / 2 : kBN));
     GemmSched sf = base_sched(rows, V, D, logit_nseg, logit_segs, pair_f);
-    int per_unit = 1;
-    const int splits = choose_splits(sf.m_tiles, sf.n_tiles, pair_f ? dev.num_sms / 2 : dev.num_sms, &per_unit);
-    sf.n_per_unit = per_unit;
+    const int splits = fpl.splits;
+    sf.n_per_unit = fpl.per_unit;
     sf.group_m = pair_f ? 16 : 32;
     sf.m_limit = lim;
     finish_sched(sf);
@@ -1337,11 +1353,24 @@ int flce_testing_set_gemm_mode(int mode) {
 }
 
 int flce_testing_plan(const flce_problem* problem, int for_backward, int num_sms, flce_testing_plan_info* out) {
-  if (!out || num_sms < 2 || num_sms > 4096 || (for_backward != 1 && for_backward != 2)) return FLCE_ERR_INVALID_ARG;
+  if (!out || num_sms < 2 || num_sms > 4096 || for_backward < 0 || for_backward > 2) return FLCE_ERR_INVALID_ARG;
   FLCE_TRY(validate(problem));
-  const Layout L = make_layout(problem, for_backward == 2 ? kFused : kBackward, true);
   const int64_t N = problem->n_tokens, D = problem->hidden, V = problem->vocab;
   flce_testing_plan_info info{};
+  if (for_backward == 0) {
+    const FwdPlan f = plan_forward(N, V, num_sms);
+    info.fwd_pair = f.pair ? 1 : 0;
+    info.fwd_splits = f.splits;
+    info.fwd_tiles_per_split = f.per_unit;
+    *out = info;
+    return FLCE_OK;
+  }
+  const Layout L = make_layout(problem, for_backward == 2 ? kFused : kBackward, true);
+  // The forward of the fused call with kept logits runs per token chunk.
+  const FwdPlan f = plan_forward(L.token ? L.nc : N, V, num_sms);
+  info.fwd_pair = f.pair ? 1 : 0;
+  info.fwd_splits = f.splits;
+  info.fwd_tiles_per_split = f.per_unit;
   DhPlan d;
   if (L.token) {
     info.keep_logits = 1;

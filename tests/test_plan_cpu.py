@@ -75,6 +75,27 @@ def test_one_chunk_plan(lib):
     assert info.dh_ksplit == 9
 
 
+def test_forward_split_plans(lib):
+    """The forward splits the vocabulary so that (m tiles x splits) units fill whole waves of 76
+    pairs.  Gemma-like: 64 m tiles x 19 splits of 54 tiles = 1216 units = 16 waves (99.8 % of the
+    slots do work); 38 or 57 splits tie and the fewer win.  Qwen3-8B-like, kept logits: each
+    4096-token chunk has 16 m tiles, and 33 splits of 18 of its 594 tiles give 528 units in 7 waves
+    (99.25 %), ahead of 19 splits of 32 (4 full waves but 97.7 %: the last split is short) and
+    46 splits of 13 (96.2 %).  The forward alone (flce_forward) plans the whole batch: 64 m tiles,
+    and 33 splits of 18 give 2112 units in 28 waves (99.25 %)."""
+    gemma = _problem(16384, 640, 262144, final_logit_softcapping=30.0)
+    for fb in (0, 1, 2):
+        info = _plan(lib, gemma, fb)
+        assert (info.fwd_pair, info.fwd_splits, info.fwd_tiles_per_split) == (1, 19, 54)
+    qwen = _problem(16384, 4096, 151936)
+    fused = _plan(lib, qwen, 2)
+    assert fused.keep_logits == 1
+    assert (fused.fwd_pair, fused.fwd_splits, fused.fwd_tiles_per_split) == (1, 33, 18)
+    fwd = _plan(lib, qwen, 0)
+    assert (fwd.fwd_pair, fwd.fwd_splits, fwd.fwd_tiles_per_split) == (1, 33, 18)
+    assert fwd.n_chunks == 0 and fwd.dh_ksplit == 0  # the forward plan only
+
+
 def test_overrides_apply_to_the_plan(lib):
     try:
         assert lib.flce_testing_set_tuning(1000, 3) == B.FLCE_OK
@@ -89,7 +110,8 @@ def test_overrides_apply_to_the_plan(lib):
 def test_plan_rejects_bad_arguments(lib):
     info = B.FlceTestingPlanInfo()
     p = _problem(512, 128, 4096)
-    assert lib.flce_testing_plan(ctypes.byref(p), 0, 152, ctypes.byref(info)) == B.FLCE_ERR_INVALID_ARG
+    assert lib.flce_testing_plan(ctypes.byref(p), 3, 152, ctypes.byref(info)) == B.FLCE_ERR_INVALID_ARG
+    assert lib.flce_testing_plan(ctypes.byref(p), -1, 152, ctypes.byref(info)) == B.FLCE_ERR_INVALID_ARG
     assert lib.flce_testing_plan(ctypes.byref(p), 1, 1, ctypes.byref(info)) == B.FLCE_ERR_INVALID_ARG
     assert lib.flce_testing_plan(ctypes.byref(p), 1, 152, None) == B.FLCE_ERR_INVALID_ARG
     bad = _problem(512, 128, 0)
@@ -105,6 +127,9 @@ def test_plan_invariants(lib, sms):
         for fb in (1, 2):
             info = _plan(lib, _problem(N, D, V), fb, sms)
             assert 1 <= info.dh_ksplit <= info.dh_ksplit_max <= 16
+            n_t = cdiv(V, 256)
+            assert 1 <= info.fwd_splits <= min(64, n_t)
+            assert info.fwd_splits == cdiv(n_t, info.fwd_tiles_per_split)  # no empty split
             if info.keep_logits:
                 assert fb == 2 and D >= 1280 and N > 256
                 assert info.token_chunk_rows % 256 == 0
