@@ -344,10 +344,32 @@ def check_num_items_in_batch(o):
     assert abs(a - total / 3) <= 1e-15 * max(1.0, abs(total))
 
 
+def check_rows_independent(o):
+    """Tokens are independent until the sums over them: a NaN in one hidden row makes exactly that
+    row's lse, loss and dh row NaN and leaves every other row's lse, loss, entropy and dh as they
+    were (the GPU NaN test compares the other rows with the oracle on the clean input)."""
+    h, W, b, t = _rand_case(91, n=6, d=5, v=13, bias=True)
+    dl = np.linspace(0.5, 1.5, 6)
+    keep = np.arange(6) != 3
+    assert t[3] != IGN
+    for softcap in (0.0, 4.0):
+        kw = dict(logit_scale=0.8, softcap=softcap, reduction="none")
+        ref_f = o.forward(h, W, b, t, **kw)
+        ref_b = o.backward(h, W, b, t, dloss=dl, **kw)
+        hn = h.copy()
+        hn[3, 1] = np.nan
+        f = o.forward(hn, W, b, t, **kw)
+        g = o.backward(hn, W, b, t, dloss=dl, **kw)
+        assert np.isnan(f["lse"][3]) and np.isnan(f["loss_tok"][3]) and np.isnan(g["dh"][3]).all()
+        for key in ("lse", "loss_tok", "entropy"):
+            np.testing.assert_allclose(f[key][keep], ref_f[key][keep], rtol=1e-13, atol=0)
+        np.testing.assert_allclose(g["dh"][keep], ref_b["dh"][keep], rtol=1e-12, atol=1e-300)
+
+
 ALL_CHECKS = [
     check_forward_matches_torch, check_entropy_matches_scipy, check_softcap_limits,
     check_gradients_finite_difference, check_zero_head_closed_form, check_invariants,
     check_all_ignored, check_vocab_one, check_argmax_targets_exact_accuracy,
     check_ties_lowest_index, check_brute_force_python, check_sympy_exact,
-    check_subset_helpers, check_out_of_range_target, check_num_items_in_batch,
+    check_subset_helpers, check_out_of_range_target, check_num_items_in_batch, check_rows_independent,
 ]
