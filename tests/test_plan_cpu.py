@@ -142,3 +142,20 @@ def test_plan_invariants(lib, sms):
                 assert run <= vc and run >= max(1, vc // 256 // 2) * 256  # widths down to half the tiles
                 assert info.n_chunks == cdiv(V, run)
                 assert N * vc * 2 <= max(1 << 30, N * 256 * 2)  # the G chunk stays within 1 GiB
+
+
+def test_backward_algorithm_follows_flags(lib):
+    """The fused call keeps logits from D = 1280 up when there are at least two 256-token chunks;
+    FLCE_FLAG_BWD_RECOMPUTE and FLCE_FLAG_BWD_KEEP_LOGITS force either algorithm (keeping logits
+    still needs N > 256), with and without valid-token compaction and fp32 hidden states.
+    flce_backward always recomputes."""
+    rec, keep, cmp_ = B.FLCE_FLAG_BWD_RECOMPUTE, B.FLCE_FLAG_BWD_KEEP_LOGITS, B.FLCE_FLAG_COMPACT_VALID
+    for extra in (0, cmp_):
+        for dt in (B.FLCE_BF16, B.FLCE_F32):
+            kw = dict(hidden_dtype=dt)
+            assert _plan(lib, _problem(4096, 1280, 50000, flags=extra, **kw), 2).keep_logits == 1
+            assert _plan(lib, _problem(4096, 1152, 50000, flags=extra, **kw), 2).keep_logits == 0
+            assert _plan(lib, _problem(4096, 1280, 50000, flags=extra | rec, **kw), 2).keep_logits == 0
+            assert _plan(lib, _problem(4096, 640, 50000, flags=extra | keep, **kw), 2).keep_logits == 1
+            assert _plan(lib, _problem(256, 4096, 50000, flags=extra | keep, **kw), 2).keep_logits == 0
+            assert _plan(lib, _problem(4096, 4096, 50000, flags=extra | keep, **kw), 1).keep_logits == 0
