@@ -366,10 +366,49 @@ def check_rows_independent(o):
         np.testing.assert_allclose(g["dh"][keep], ref_b["dh"][keep], rtol=1e-12, atol=1e-300)
 
 
+def check_relative_frobenius(o):
+    """The gradient tolerance's measure against values worked out by hand: ``||a - ref||_F /
+    ||ref||_F`` with a difference (3, 4) (norm 5) over a reference (6, 8) (norm 10) is exactly 0.5;
+    it is scale-invariant (a relative, not an absolute, error), not symmetric in its arguments, 0 for
+    two zero arrays and infinite for a nonzero array against a zero reference.  It widens bf16, fp32
+    and fp64 torch tensors as well as NumPy arrays."""
+    ref = np.array([[0.0, 0.0], [6.0, 8.0]])
+    a = ref + np.array([[3.0, 4.0], [0.0, 0.0]])
+    assert o.relative_frobenius(a, ref) == 0.5
+    assert o.relative_frobenius(ref, a) == 5.0 / math.sqrt(9.0 + 16.0 + 36.0 + 64.0)
+    for k in (1e-3, 3.7, -2.0, 1e6):
+        assert abs(o.relative_frobenius(k * a, k * ref) - 0.5) < 1e-15
+    assert o.relative_frobenius(np.zeros((2, 3)), np.zeros((2, 3))) == 0.0
+    assert o.relative_frobenius(np.ones(3), np.zeros(3)) == math.inf
+    # every entry here is a small integer, exact in bf16 and fp32
+    for dt in (torch.bfloat16, torch.float32, torch.float64):
+        assert o.relative_frobenius(torch.tensor(a, dtype=dt), torch.tensor(ref, dtype=dt)) == 0.5
+    # one entry off by 1 in a 4 x 4 reference of twos: sqrt(1) / sqrt(16 * 4) = 1/8
+    r = np.full((4, 4), 2.0)
+    x = r.copy()
+    x[1, 2] = 3.0
+    assert o.relative_frobenius(torch.tensor(x, dtype=torch.bfloat16), r) == 0.125
+
+
+def check_widen_exact(o):
+    """Widening is exact: bf16 1/3 is 0.333984375 (8 significant bits, rounded to nearest), fp32
+    1/3 is 11184811 / 2^25, and an fp64 tensor keeps every bit; bf16 / fp32 NumPy-side inputs
+    widen to the same values."""
+    third = torch.tensor([1.0 / 3.0], dtype=torch.float64)
+    assert o.widen(third.to(torch.bfloat16))[0] == 0.333984375
+    assert o.widen(third.to(torch.float32))[0] == 11184811.0 / 2.0 ** 25
+    assert o.widen(third)[0] == 1.0 / 3.0
+    assert o.widen(np.float32(1.0 / 3.0)) == 11184811.0 / 2.0 ** 25
+    tiny = torch.tensor([2.0 ** -133, -(2.0 ** 100) * 1.5], dtype=torch.float64)
+    assert o.widen(tiny.to(torch.bfloat16)).tolist() == [2.0 ** -133, -(2.0 ** 100) * 1.5]
+    assert o.widen(tiny.to(torch.float32)).dtype == np.float64
+
+
 ALL_CHECKS = [
     check_forward_matches_torch, check_entropy_matches_scipy, check_softcap_limits,
     check_gradients_finite_difference, check_zero_head_closed_form, check_invariants,
     check_all_ignored, check_vocab_one, check_argmax_targets_exact_accuracy,
     check_ties_lowest_index, check_brute_force_python, check_sympy_exact,
     check_subset_helpers, check_out_of_range_target, check_num_items_in_batch, check_rows_independent,
+    check_relative_frobenius, check_widen_exact,
 ]

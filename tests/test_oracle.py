@@ -54,6 +54,17 @@ MUTANTS = {
     "num_items ignored in the forward": [("denom = float(num_items_in_batch) if num_items_in_batch > 0 else n_valid",
                                           "denom = n_valid")],
     "num_items ignored in the backward": [("        n_valid = float(num_items_in_batch)", "        pass")],
+    "frobenius sqrt dropped": [("den = math.sqrt(float((ref * ref).sum()))", "den = float((ref * ref).sum())"),
+                               ("num = math.sqrt(float(((a - ref) ** 2).sum()))",
+                                "num = float(((a - ref) ** 2).sum())")],
+    "frobenius ratio inverted": [("    return num / den", "    return den / num")],
+    "frobenius absolute error": [("    return num / den", "    return num")],
+    "frobenius max-abs instead": [("num = math.sqrt(float(((a - ref) ** 2).sum()))",
+                                   "num = float(np.abs(a - ref).max()) * math.sqrt(a.size)")],
+    "widen through fp32": [('x = x.detach().to("cpu").double().numpy()',
+                            'x = x.detach().to("cpu").float().double().numpy()')],
+    "widen through bf16": [('x = x.detach().to("cpu").double().numpy()',
+                            'x = x.detach().to("cpu").bfloat16().double().numpy()')],
 }
 
 
