@@ -15,6 +15,8 @@
 // zero (the status word) and writes every other scratch byte before reading
 // it.  Calls whose GPU work overlaps in time (different streams, threads or
 // processes sharing the context) race on the array.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -24,26 +26,68 @@
 namespace {
 
 constexpr size_t kScratchBytes = FLCE_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
+constexpr int kCacheSlots = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+struct Slot {
+  unsigned long long ctx_id;  // 0 = empty
+  void* addr;
+};
+Slot g_slots[kCacheSlots] = {};
+int g_next_slot = 0;
 
-// Device address of g_scratch on the current device.  In host code the name
-// g_scratch is only a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+// Process-unique id of the current CUDA context (0 when none is current yet).
+int current_context_id(unsigned long long* id) {
+  if (!g_ctx_current || !g_ctx_id) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return FLCE_ERR_CUDA;
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return FLCE_ERR_CUDA;
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return FLCE_ERR_CUDA;
+  *id = 0;
+  if (ctx && g_ctx_id(ctx, id) != CUDA_SUCCESS) return FLCE_ERR_CUDA;
+  return FLCE_OK;
+}
+
+// Device address of g_scratch in the current context.  In host code the name
+// g_scratch is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress (with the caller's device current) the first time a
+// context calls, and cached under the context's process-unique id: another
+// context on the same device, or the new one after cudaDeviceReset, looks it
+// up again instead of reusing an address that is not valid there.
 int scratch_address(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FLCE_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return FLCE_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return FLCE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  unsigned long long id = 0;
+  if (current_context_id(&id) != FLCE_OK) return FLCE_ERR_CUDA;
+  for (int i = 0; id != 0 && i < kCacheSlots; ++i) {
+    if (g_slots[i].ctx_id == id) {
+      *out = g_slots[i].addr;
+      return FLCE_OK;
+    }
   }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;  // makes the device's primary context current when none was
+  if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return FLCE_ERR_CUDA;
+  if (id == 0 && current_context_id(&id) != FLCE_OK) return FLCE_ERR_CUDA;
+  if (id != 0) {
+    g_slots[g_next_slot] = Slot{id, p};
+    g_next_slot = (g_next_slot + 1) % kCacheSlots;
+  }
+  *out = p;
   return FLCE_OK;
 }
 
