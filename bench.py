@@ -68,9 +68,6 @@ def parse_args(argv=None):
                     help="rows per token chunk of the keep-logits backward (0 = automatic; tuning)")
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM kernel: 0 automatic, 1 single CTA, 2 CTA pair (A/B timing)")
-    ap.add_argument("--multicast", type=int, default=1, choices=[0, 1, 2],
-                    help="dh and dW as clusters of two CTA pairs sharing B by TMA multicast: 1 where it costs "
-                         "no extra wave (default), 2 always, 0 never (A/B timing)")
     ap.add_argument("--dh-ksplit", type=int, default=0,
                     help="force the K splits of the recompute backward's dh product (0 = automatic; tuning)")
     return ap.parse_args(argv)
@@ -382,7 +379,6 @@ def flce_arm(args):
     w = pick_workload(args)
     lib = B.load()
     B.check(lib.flce_testing_set_gemm_mode(args.gemm_mode), "gemm mode")
-    B.check(lib.flce_testing_set_multicast(args.multicast), "multicast")
     B.check(lib.flce_testing_set_tuning(0, args.dh_ksplit), "dh K splits")
     B.check(lib.flce_testing_set_token_chunk(args.token_chunk), "token chunk")  # before sizing the workspace
     run = Runner(w, device, seed_offset=rank, compact=args.compact, fused=not args.separate, bwd=args.bwd,
@@ -537,7 +533,6 @@ def flce_arm(args):
             "config": {"workload": w.name, "n_tokens": w.n_tokens, "hidden": w.hidden, "vocab": w.vocab,
                        "reduction": w.reduction, "parallelism": f"replicas x{world}" if world > 1 else "none",
                        "gemm_mode": ["auto", "single-cta", "cta-pair"][args.gemm_mode],
-                       "multicast": ["never", "auto", "always"][args.multicast],
                        "compact_valid_tokens": bool(args.compact),
                        "entry": ("linear_cross_entropy + backward (autograd, gradients "
                                  + ("in the backward)" if args.grad_in_backward else "in the forward)"))

@@ -25,6 +25,11 @@
  *     owned by the caller.  The library allocates no device or host memory and
  *     keeps no state between calls other than a per-device cache of the SM
  *     count and kernel attributes.
+ *   - hidden, weight, dhidden, dweight and the workspace must be memory of
+ *     the current device (its device memory, or managed memory): the tensor
+ *     maps and the kernels address this GPU's memory only.  Host memory
+ *     (pageable, pinned or registered) and another GPU's memory are refused
+ *     with FLCE_ERR_INVALID_ARG before anything is enqueued.
  *   - Tensors are dense and row-major: hidden [N, D], weight [V, D], bias [V],
  *     targets [N] (int64), lse [N], dloss [1] or [N].
  *   - Every launch is enqueued on `stream` (0 = the legacy default stream) and
@@ -92,13 +97,16 @@ enum {
    *   vocabulary again per row).  8*N*V*D flops; the scratch is bounded (a
    *   bf16 gradient chunk of at most 1 GiB).
    * FLCE_FLAG_BWD_KEEP_LOGITS: token-chunked.  The tokens are cut into chunks
-   *   of at most half of N; the forward product of a chunk keeps its fp32
-   *   logits in the workspace, and the chunk's logit gradient, dhidden rows and
-   *   dweight contribution are formed from them before the next chunk starts
-   *   (TRL PR #6863, opening section: token chunks whose logits come from a
-   *   bf16 tensor-core product and are held in fp32).  6*N*V*D flops, at the
-   *   price of about 6 bytes of scratch per logit of a chunk plus a 4*V*D-byte
-   *   fp32 dweight accumulator.  Needs N > 256 (else the recompute runs).  With
+   *   of at most half of N (rounded up to 256 rows), whose kept logits stay
+   *   within a 4 GiB budget; a batch of at most 256 tokens is one chunk, whose
+   *   kept logits are at most 256 x V.  The forward product of a chunk keeps
+   *   its fp32 logits in the workspace, and the chunk's logit gradient,
+   *   dhidden rows and dweight / dbias contributions are formed from them
+   *   before the next chunk starts (TRL PR #6863, opening section: token
+   *   chunks whose logits come from a bf16 tensor-core product and are held
+   *   in fp32).  6*N*V*D flops, at the price of about 6 bytes of scratch per
+   *   logit of a chunk plus 4*V*(D + 1) bytes of fp32 dweight / dbias
+   *   accumulators (not needed with one chunk).  With
    *   FLCE_FLAG_COMPACT_VALID the chunks cut the gathered valid tokens.
    */
   FLCE_FLAG_BWD_RECOMPUTE = 2u,
@@ -113,7 +121,10 @@ enum {
    * tensor cores' fp32 accumulation, whose own error (about K/16 units in the
    * last place of the accumulator) then dominates for long K.  Without it fp32
    * operands take two terms (about 16 bits: 2 products, or 3 with an fp32
-   * head).  No effect on bf16 operands.
+   * head) in the logit products, and their leading term alone in the
+   * gradient products dweight = G^T hidden and dhidden = G weight, whose
+   * other operand G is rounded to bf16 (with this flag those take all three
+   * terms).  No effect on bf16 operands.
    * (The pages' fp32 path: TRL PR #6859, review "verified" bullet 3, with the
    * head cast to the activations' dtype.)
    */
@@ -123,7 +134,7 @@ enum {
 /* Status codes returned by every call (and stored in the device status word). */
 enum {
   FLCE_OK = 0,
-  FLCE_ERR_INVALID_ARG = 1,         /* null pointer, size out of range, bad enum      */
+  FLCE_ERR_INVALID_ARG = 1,         /* null or non-local pointer, bad size or enum    */
   FLCE_ERR_UNSUPPORTED_DTYPE = 2,   /* e.g. fp32 weight                               */
   FLCE_ERR_DTYPE_MISMATCH = 3,      /* bf16 hidden with a non-bf16 weight              */
   FLCE_ERR_MISALIGNED = 4,          /* pointer not 16-byte aligned, D % 8 != 0         */
@@ -185,7 +196,10 @@ typedef struct {
  * (for_backward = 1) or flce_forward_backward (for_backward = 2) needs for
  * `problem`, written to *bytes.  The size grows
  * with N * (number of vocabulary splits) for the forward and with
- * N * (vocabulary chunk) + N * D for the backward; it never grows with N * V.
+ * N * (vocabulary chunk) + N * D for the recompute backward, whose bf16
+ * gradient chunk is at most 1 GiB; the token-chunked backward holds one token
+ * chunk's logits (at most 4 GiB, or 256 x V for a batch of at most 256
+ * tokens) and O(V * D + N * D) more.  It never grows with N * V.
  * The size is an upper bound that does not depend on the device, so the call
  * needs no GPU.  Returns FLCE_OK or the validation error of `problem`.
  */
@@ -297,8 +311,11 @@ FLCE_API int flce_read_device_status(const void* workspace, flce_stream_t stream
  *     hidden states and a vocabulary of 16K or more that admits about 13K
  *     tokens (2.6 KB of split records per token); fp32 hidden states need
  *     4*N*D more bytes.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     there (with the caller's device current) and caches it under the
+ *     context's process-unique id, so a second context on the device, or the
+ *     new one after cudaDeviceReset, looks it up again; make the first call
+ *     before any stream capture.
  *   - It calls no cudaMalloc, cudaFree or allocating library routine.
  *   - All calls share the one array, which keeps the last call's contents; the
  *     call clears what must start at zero.  Calls whose GPU work overlaps in

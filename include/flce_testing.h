@@ -43,26 +43,13 @@ FLCE_API int flce_testing_set_tuning(int64_t chunk_cols, int dh_ksplit);
 FLCE_API int flce_testing_set_gemm_mode(int mode);
 
 /*
- * Process-wide switch of the operand multicast, for tests and tuning.  A
- * CTA-pair product whose B operand is MN-major (dh, dW), and the test GEMM,
- * can run as clusters of two CTA pairs over a 512-row m tile: both pairs need
- * the same B tile, and each CTA loads half of its share and multicasts it by
- * TMA to itself and its counterpart in the other pair.  mode 1 (the default):
- * where the device fits as many waves of units into the resident clusters of
- * four as into the resident pairs; 2: wherever there are two m tiles; 0: never.
- * Results are bitwise the same in every mode.  Not thread-safe.
- */
-FLCE_API int flce_testing_set_multicast(int mode);
-
-/*
  * The plan the library makes for `problem` on a device with `num_sms` SMs, for
  * tests of the host-side planning; it needs no GPU.  for_backward as in
  * flce_workspace_size: 0 for flce_forward (only the fwd_* fields are set), 1
  * for flce_backward (the fwd_* fields describe flce_forward), 2 for
  * flce_forward_backward (with kept logits the forward runs per token chunk:
- * the fwd_* fields describe the first chunk).  The multicast choice, which
- * needs the device's resident cluster counts, is not part of it.  The testing
- * overrides above apply.  Returns FLCE_OK, the validation error of `problem`,
+ * the fwd_* fields describe the first chunk).  The testing overrides above
+ * apply.  Returns FLCE_OK, the validation error of `problem`,
  * or FLCE_ERR_INVALID_ARG.
  */
 typedef struct {

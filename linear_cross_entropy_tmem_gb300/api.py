@@ -302,8 +302,3 @@ def testing_set_gemm_mode(mode: int = 0) -> None:
     """0 automatic, 1 single-CTA GEMM kernel only, 2 CTA-pair kernel only (tests, A/B timing)."""
     B.check(B.load().flce_testing_set_gemm_mode(int(mode)), "flce_testing_set_gemm_mode")
 
-
-def testing_set_multicast(mode: int = 1) -> None:
-    """Operand multicast of the dh / dW products (clusters of two CTA pairs sharing B): 1 automatic
-    (default), 2 always, 0 never (tests, A/B timing)."""
-    B.check(B.load().flce_testing_set_multicast(int(mode)), "flce_testing_set_multicast")

@@ -99,7 +99,6 @@ SIGNATURES = {
     "flce_testing_set_tuning": (c_int, [c_int64, c_int]),
     "flce_scale_gradient": (c_int, [c_void_p, c_void_p, c_int64, c_int32, c_void_p]),
     "flce_testing_set_gemm_mode": (c_int, [c_int]),
-    "flce_testing_set_multicast": (c_int, [c_int]),
     "flce_testing_plan": (c_int, [POINTER(FlceProblem), c_int, c_int, POINTER(FlceTestingPlanInfo)]),
     "flce_testing_set_token_chunk": (c_int, [c_int64]),
     "flce_testing_set_launch_log": (c_int, [c_void_p, c_int32, POINTER(c_int32)]),

@@ -17,6 +17,12 @@
 #include "flce_launch.h"
 #include "flce_testing.h"
 
+#define FLCE_TRY(expr)               \
+  do {                               \
+    const int rc_ = (expr);          \
+    if (rc_ != FLCE_OK) return rc_;  \
+  } while (0)
+
 namespace flce {
 namespace {
 
@@ -39,6 +45,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct DeviceInfo {
   bool init = false;
+  int index = 0;
   int num_sms = 0;
   int major = 0, minor = 0;
 };
@@ -57,6 +64,7 @@ int get_device(DeviceInfo* out) {
         cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FLCE_ERR_CUDA;
+    d.index = dev;
     d.init = true;
   }
   if (!g_encode) {
@@ -102,6 +110,28 @@ int make_store_map(CUtensorMap* m, void* base, bool f32, uint64_t cols, uint64_t
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The operands the tensor maps and the products address (hidden, weight, the
+// gradients, the workspace) must be memory of the current device: device
+// memory of this GPU or managed memory.  Host memory (pageable, pinned or
+// registered) and another GPU's memory are refused with FLCE_ERR_INVALID_ARG
+// before anything is enqueued.  nullptr passes (the callers check presence).
+int check_local(const DeviceInfo& dev, const void* p) {
+  if (!p) return FLCE_OK;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeManaged) return FLCE_OK;
+  if (a.type == cudaMemoryTypeDevice && a.device == dev.index) return FLCE_OK;
+  return FLCE_ERR_INVALID_ARG;
+}
+template <class... P>
+int check_local(const DeviceInfo& dev, const void* p, P... rest) {
+  FLCE_TRY(check_local(dev, p));
+  return check_local(dev, rest...);
+}
+
 int validate(const flce_problem* p) {
   if (!p) return FLCE_ERR_INVALID_ARG;
   if (p->n_tokens < 0 || p->n_tokens > INT32_MAX - 256) return FLCE_ERR_INVALID_ARG;
@@ -131,6 +161,12 @@ int term_count(int32_t dtype, const flce_problem* p) {
 }
 int h_terms(const flce_problem* p) { return term_count(p->hidden_dtype, p); }
 int w_terms(const flce_problem* p) { return term_count(p->weight_dtype, p); }
+// Terms of h (dW) or W (dh) the gradient products read.  G, their other
+// operand, is rounded to bf16 (8 significant bits), so a second term of the
+// fp32 operand (bits 9 to 16) buys no precision there: by default the
+// gradient products take the leading term only, and all three terms only with
+// FLCE_FLAG_FP32_FULL.
+int grad_terms(int terms, const flce_problem* p) { return (p->flags & FLCE_FLAG_FP32_FULL) ? terms : 1; }
 size_t weight_elem(const flce_problem* p) { return p->weight_dtype == FLCE_F32 ? 4 : 2; }
 
 // K segments: (A term, B term) pairs packed for GemmSched::seg_maps.
@@ -164,6 +200,7 @@ int logit_segments(int nh, int nw, uint32_t* maps) {
 // Gradient products with G (one bf16 term) as A and the n terms of h or W as
 // B, smallest first.
 int b_term_segments(int n, uint32_t* maps) {
+  n = std::max(1, std::min(n, 3));
   static const int kBOnly[3][3][2] = {{{0, 0}}, {{0, 1}, {0, 0}}, {{0, 2}, {0, 1}, {0, 0}}};
   *maps = pack_segments(kBOnly[n - 1], n);
   return n;
@@ -197,7 +234,7 @@ struct Layout {
   int64_t nc = 0;         // rows per token chunk (multiple of kTokenChunkAlign)
   int64_t n_tchunks = 0;
   int64_t ldz = 0;        // row stride of the kept logits and of G (elements)
-  size_t z = 0, zg = 0, dw_acc = 0;
+  size_t z = 0, zg = 0, dw_acc = 0, dbias_acc = 0;
   size_t c_chunk_rows = 0;  // under compaction: valid rows of each token chunk
 };
 
@@ -206,7 +243,6 @@ std::atomic<int64_t> g_force_chunk_cols{0};
 std::atomic<int> g_force_dh_ksplit{0};
 std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel
 std::atomic<int64_t> g_force_token_rows{0};
-std::atomic<int> g_multicast{1};  // flce_testing_set_multicast: 0 off, 1 automatic, 2 always
 
 // CTA pairs (256-row tiles) when there are at least 256 rows and enough units
 // to give every cluster work; otherwise single CTAs (128-row tiles).
@@ -215,34 +251,6 @@ bool use_pair(int64_t m_rows, int64_t units_per_pair_row, int num_sms) {
   if (mode == 1) return false;
   if (mode == 2) return true;
   return m_rows >= kPairRows && cdiv(m_rows, kPairRows) * units_per_pair_row >= num_sms / 2;
-}
-
-// Run a CTA-pair product as clusters of two pairs that share the B tile by TMA
-// multicast (GemmSched::quad, 512-row m tiles), which cuts the operand bytes
-// each pair pulls from L2 by a quarter.  Needs at least two 256-row m tiles.
-// Called on a pair schedule (n_tiles, n_per_unit and ksplit set) before
-// finish_sched.  A cluster of four must fit in one GPC, so fewer of them than
-// pairs are resident on a GB300: only where that costs no extra wave of units
-// does the multicast pay (measured: Gemma-like dh 3.93 -> 3.74 ms at equal
-// waves; one extra wave made dW 10 % slower there, and dh and dW of the
-// Qwen3-8B-like head 2-4 % slower per clock).
-int use_quad(GemmSched& s, bool pair, int64_t m_rows, int num_sms) {
-  const int mode = g_multicast.load();
-  if (!pair || mode == 0 || cdiv(m_rows, kPairRows) < 2) return FLCE_OK;
-  if (mode == 1) {
-    int pairs = 0, quads = 0;
-    if (gradient_gemm_clusters(false, num_sms, &pairs) != cudaSuccess ||
-        gradient_gemm_clusters(true, num_sms, &quads) != cudaSuccess)
-      return FLCE_ERR_CUDA;
-    const int64_t per_m = cdiv(s.n_tiles, s.n_per_unit) * s.ksplit;
-    const int64_t waves_pair = cdiv(cdiv(m_rows, kPairRows) * per_m, pairs);
-    const int64_t waves_quad = cdiv(cdiv(m_rows, 2 * kPairRows) * per_m, quads);
-    if (waves_quad > waves_pair) return FLCE_OK;
-  }
-  s.quad = 1;
-  s.m_tiles = static_cast<int32_t>(cdiv(m_rows, 2 * kPairRows));
-  s.group_m = std::max(1, s.group_m / 2);
-  return FLCE_OK;
 }
 
 int64_t chunk_width(int64_t n_tokens, int64_t vocab) {
@@ -274,10 +282,12 @@ enum LayoutKind { kForward = 0, kBackward = 1, kFused = 2 };
 
 // Backward algorithm of the fused call: keep the logits of token chunks
 // (6NVD) or recompute them (8NVD).  Depends on the problem only, so that
-// flce_workspace_size agrees with the call.
+// flce_workspace_size agrees with the call.  Keeping costs 6 bytes per logit
+// where the recompute costs 2*D flops and another pass over the head, so the
+// threshold on D holds for small batches too (at N <= 256 the recompute also
+// re-reads the whole head for few tokens).
 bool keep_logits(const flce_problem* p) {
   if (p->flags & FLCE_FLAG_BWD_RECOMPUTE) return false;
-  if (p->n_tokens <= kTokenChunkAlign) return false;  // fewer than two chunks
   if (p->flags & FLCE_FLAG_BWD_KEEP_LOGITS) return true;
   return p->hidden >= kKeepLogitsMinHidden;
 }
@@ -285,8 +295,12 @@ bool keep_logits(const flce_problem* p) {
 int64_t logit_row_stride(int64_t vocab) { return cdiv(vocab, 32) * 32; }
 
 // Rows per token chunk: as many as the logit budget allows, balanced over the
-// chunks, at most half of N (so that the kept logits never cover all tokens).
+// chunks, at most half of N rounded up to kTokenChunkAlign (so that the kept
+// logits never cover all tokens of a batch of more than kTokenChunkAlign).  A
+// batch of at most kTokenChunkAlign tokens is one chunk of its own rows: its
+// kept logits are bounded by kTokenChunkAlign * V, whatever N.
 int64_t token_chunk_rows(int64_t n_tokens, int64_t vocab) {
+  if (n_tokens <= kTokenChunkAlign) return std::max<int64_t>(kZGradRows, cdiv(n_tokens, kZGradRows) * kZGradRows);
   const int64_t cap = cdiv(cdiv(n_tokens, 2), kTokenChunkAlign) * kTokenChunkAlign;
   const int64_t forced = g_force_token_rows.load();
   if (forced > 0) return std::min(cap, cdiv(forced, kTokenChunkAlign) * kTokenChunkAlign);
@@ -313,7 +327,9 @@ void take_terms(const flce_problem* p, Layout& L, Take& take) {
 }
 
 // [status][hi, lo][forward records of one chunk][kept logits][G][dbias
-// partials of all row tiles][fp32 dW accumulator][dh K-split slots].
+// partials of one chunk's row tiles][fp32 dbias accumulator][fp32 dW
+// accumulator][dh K-split slots].  With one chunk the two accumulators are
+// not needed: dW and dbias are written straight from that chunk.
 Layout make_token_layout(const flce_problem* p, bool has_bias) {
   Layout L;
   L.token = true;
@@ -351,8 +367,9 @@ Layout make_token_layout(const flce_problem* p, bool has_bias) {
   L.blocks = take(size_t(cdiv(N, kMergeThreads)) * sizeof(BlockPartial));
   L.z = take(size_t(L.nc) * L.ldz * 4);
   L.zg = take(size_t(L.nc) * L.ldz * 2);
-  if (has_bias) L.dbias_part = take(size_t(cdiv(N, kZGradRows)) * L.ldz * 4);
-  L.dw_acc = take(size_t(V) * D * 4);
+  if (has_bias) L.dbias_part = take(size_t(cdiv(L.nc, kZGradRows)) * L.ldz * 4);
+  if (has_bias && L.n_tchunks > 1) L.dbias_acc = take(size_t(L.ldz) * 4);
+  if (L.n_tchunks > 1) L.dw_acc = take(size_t(V) * D * 4);
   L.ksplit_max = token_dh_ksplit_bound(L.nc, D);
   L.need_dh_part = L.ksplit_max > 1;
   if (L.need_dh_part) L.dh_part = take(size_t(L.ksplit_max) * L.nc * D * 4);
@@ -501,12 +518,6 @@ int logged(int kind, cudaStream_t st, F&& launch) {
   }
   return FLCE_OK;
 }
-
-#define FLCE_TRY(expr)               \
-  do {                               \
-    const int rc_ = (expr);          \
-    if (rc_ != FLCE_OK) return rc_;  \
-  } while (0)
 
 }  // namespace
 }  // namespace flce
@@ -847,8 +858,8 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
   FLCE_TRY(make_term_maps(&rec.b0, &rec.b1, &rec.b2, pr.w, pr.nw, 0, D, V, D * 2, kBK, pair_rec ? kBN / 2 : kBN));
   uint32_t rec_segs = 0, dw_segs = 0, dh_segs = 0;
   const int rec_nseg = logit_segments(pr.nh, pr.nw, &rec_segs);
-  const int dw_nseg = b_term_segments(pr.nh, &dw_segs);  // dW = G^T (sum of h terms)
-  const int dh_nseg = b_term_segments(pr.nw, &dh_segs);  // dh = G (sum of W terms)
+  const int dw_nseg = b_term_segments(grad_terms(pr.nh, p), &dw_segs);  // dW = G^T (sum of h terms)
+  const int dh_nseg = b_term_segments(grad_terms(pr.nw, p), &dh_segs);  // dh = G (sum of W terms)
   TmaMaps hmn, wmn;  // MN-major views: h terms for dW, W terms for dh
   FLCE_TRY(make_term_maps(&hmn.b0, &hmn.b1, &hmn.b2, pr.h, pr.nh, 0, D, N, D * 2, 64, kBK));
   FLCE_TRY(make_term_maps(&wmn.b0, &wmn.b1, &wmn.b2, pr.w, pr.nw, 0, D, V, D * 2, 64, kBK));
@@ -903,7 +914,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
       FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
         return launch_dbias_reduce(dbias_part, L.vc, static_cast<int>(cdiv(N, kBM)), kBM, width,
                                    static_cast<uint8_t*>(dbias) + v0 * bias_elem,
-                                   p->bias_dtype == FLCE_F32, pr.row_count, st);
+                                   p->bias_dtype == FLCE_F32, pr.row_count, nullptr, 0, 1, st);
       }));
     }
 
@@ -920,7 +931,6 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     s2.b_mn = 1;
     s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
     s2.k_limit = pr.row_count;
-    FLCE_TRY(use_quad(s2, pair_dw, width, dev.num_sms));
     finish_sched(s2);
     StoreParams sp{};
     sp.rows = width;
@@ -945,7 +955,6 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     s3.kb_per_split = static_cast<int32_t>(cdiv(s3.k_blocks, ksplit));
     s3.group_m = std::max(1, dh_ctas / std::max(1, s3.n_tiles * ksplit));
     s3.m_limit = pr.row_count;
-    FLCE_TRY(use_quad(s3, pair_dh, N, dev.num_sms));
     finish_sched(s3);
     AccumParams ap{};
     ap.rows = N;
@@ -974,7 +983,8 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
 // L.nc tokens: the forward product keeps z (fp32), the merge gives lse and the
 // per-token outputs, zgrad forms G and the dbias partials from the kept z, the
 // chunk's dh rows come from one product over the whole vocabulary, and dW
-// accumulates in fp32 across chunks (the last chunk writes the bf16 result).
+// and dbias accumulate in fp32 across chunks (the last chunk writes the
+// results in their dtypes; a single chunk writes them directly).
 int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& dev, uint8_t* ws, int* status,
                      cudaStream_t st, const void* bias, const Prep& pr, const float* dloss,
                      float* loss, float* lse, float* entropy, int64_t* correct, int64_t* n_valid,
@@ -986,8 +996,9 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
   const size_t out_elem = h32 ? 4 : 2;
   float* z = reinterpret_cast<float*>(ws + L.z);
   uint16_t* g = reinterpret_cast<uint16_t*>(ws + L.zg);
-  float* dw_acc = reinterpret_cast<float*>(ws + L.dw_acc);
+  float* dw_acc = L.dw_acc ? reinterpret_cast<float*>(ws + L.dw_acc) : nullptr;
   float* dbias_part = bias ? reinterpret_cast<float*>(ws + L.dbias_part) : nullptr;
+  float* dbias_acc = bias && L.dbias_acc ? reinterpret_cast<float*>(ws + L.dbias_acc) : nullptr;
   float* dh_part = L.need_dh_part ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
   BlockPartial* blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
   // Under compaction the chunks cut the compacted tokens: chunk c holds
@@ -1010,8 +1021,8 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
   FLCE_TRY(make_term_maps(&wmn.b0, &wmn.b1, &wmn.b2, pr.w, pr.nw, 0, D, V, D * 2, 64, kBK));
   uint32_t logit_segs = 0, dw_segs = 0, dh_segs = 0;
   const int logit_nseg = logit_segments(pr.nh, pr.nw, &logit_segs);
-  const int dw_nseg = b_term_segments(pr.nh, &dw_segs);
-  const int dh_nseg = b_term_segments(pr.nw, &dh_segs);
+  const int dw_nseg = b_term_segments(grad_terms(pr.nh, p), &dw_segs);
+  const int dh_nseg = b_term_segments(grad_terms(pr.nw, p), &dh_segs);
   const size_t w_elem = weight_elem(p);
   const DhPlan dhp = plan_token_dh(L, D, dev.num_sms);
   const bool pair_dh = dhp.pair;
@@ -1106,8 +1117,15 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     zp.row_limit = lim;
     zp.n_valid = n_valid;
     zp.num_items = static_cast<float>(p->num_items_in_batch);
-    zp.dbias_part = dbias_part ? dbias_part + (r0 / kZGradRows) * L.ldz : nullptr;
+    zp.dbias_part = dbias_part;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_LOGIT_GRAD, st, [&] { return launch_zgrad(zp, softcap, st); }));
+    if (bias) {  // the chunk's dbias partials, in row-tile order, into the fp32 accumulator (or dbias)
+      FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
+        return launch_dbias_reduce(dbias_part, L.ldz, static_cast<int>(cdiv(rows, kZGradRows)), kZGradRows, V,
+                                   dbias, p->bias_dtype == FLCE_F32, lim, dbias_acc, c > 0 ? 1 : 0,
+                                   last ? 1 : 0, st);
+      }));
+    }
 
     // (3) dh rows of the chunk = G W   (A = G K-major, B = W MN-major, K = V)
     TmaMaps mh;
@@ -1126,7 +1144,6 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     s3.group_m = 16;
     s3.ks_outer = 1;
     s3.m_limit = lim;
-    FLCE_TRY(use_quad(s3, pair_dh, rows, dev.num_sms));
     finish_sched(s3);
     uint8_t* dh_out = static_cast<uint8_t*>(dhidden) + (pr.cmp ? 0 : size_t(r0) * D * out_elem);
     AccumParams ap{};
@@ -1159,8 +1176,17 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     s2.b_mn = 1;
     s2.group_m = std::max(1, dw_ctas / std::max(1, s2.n_tiles));
     s2.k_limit = lim;
-    FLCE_TRY(use_quad(s2, pair_dw, V, dev.num_sms));
     finish_sched(s2);
+    if (L.n_tchunks == 1) {  // nothing to accumulate: dW goes out through TMA stores
+      StoreParams sp{};
+      sp.rows = V;
+      sp.cols = D;
+      sp.out_f32 = w_elem == 4 ? 1 : 0;
+      FLCE_TRY(make_store_map(&sp.out_map, dweight, w_elem == 4, D, V, D * w_elem));
+      FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
+                      [&] { return launch_store_gemm(pair_dw, mw, s2, sp, status, dev.num_sms, st); }));
+      continue;
+    }
     AccumParams aw{};
     aw.rows = V;
     aw.cols = D;
@@ -1174,14 +1200,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
                     [&] { return launch_accum_gemm(pair_dw, mw, s2, aw, status, dev.num_sms, st); }));
   }
   const ReduceParams rp = reduce_params(p, L, ws, loss, correct, n_valid, entropy_sum);
-  FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); }));
-  if (bias) {
-    FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
-      return launch_dbias_reduce(dbias_part, L.ldz, static_cast<int>(cdiv(N, kZGradRows)), kZGradRows, V, dbias,
-                                 p->bias_dtype == FLCE_F32, pr.row_count, st);
-    }));
-  }
-  return FLCE_OK;
+  return logged(FLCE_LAUNCH_OTHER, st, [&] { return launch_fwd_reduce(rp, st); });
 }
 
 int check_forward_args(const flce_problem* p, const void* hidden, const void* weight, const int64_t* targets,
@@ -1241,6 +1260,7 @@ int flce_forward(const flce_problem* p, const void* hidden, const void* weight, 
   if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   DeviceInfo dev;
   FLCE_TRY(get_device(&dev));
+  FLCE_TRY(check_local(dev, hidden, weight, workspace));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.status);
@@ -1268,6 +1288,7 @@ int flce_backward(const flce_problem* p, const void* hidden, const void* weight,
   if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   DeviceInfo dev;
   FLCE_TRY(get_device(&dev));
+  FLCE_TRY(check_local(dev, hidden, weight, dhidden, dweight, workspace));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.status);
@@ -1295,6 +1316,7 @@ int flce_forward_backward(const flce_problem* p, const void* hidden, const void*
   if (workspace_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   DeviceInfo dev;
   FLCE_TRY(get_device(&dev));
+  FLCE_TRY(check_local(dev, hidden, weight, dhidden, dweight, workspace));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws + L.status);
@@ -1390,12 +1412,6 @@ int flce_testing_plan(const flce_problem* problem, int for_backward, int num_sms
   return FLCE_OK;
 }
 
-int flce_testing_set_multicast(int mode) {
-  if (mode < 0 || mode > 2) return FLCE_ERR_INVALID_ARG;
-  g_multicast.store(mode);
-  return FLCE_OK;
-}
-
 int flce_testing_set_launch_log(flce_launch_record* records, int32_t capacity, int32_t* count) {
   if (records && (capacity < 0 || !count)) return FLCE_ERR_INVALID_ARG;
   g_log = records;
@@ -1418,10 +1434,9 @@ int flce_testing_gemm(int a_mn_major, int b_mn_major, int64_t M, int64_t N, int6
   GemmSched s = base_sched(M, N, K, 1, 0u, pair);
   s.a_mn = a_mn_major ? 1 : 0;
   s.b_mn = b_mn_major ? 1 : 0;
-  FLCE_TRY(use_quad(s, pair, M, dev.num_sms));
   finish_sched(s);
-  // K-major B: a CTA pair loads 128-row halves; under multicast each CTA loads 64 rows.
-  const uint32_t b_rows = !pair ? kBN : (s.quad ? kBN / 4 : kBN / 2);
+  // K-major B: each CTA of a pair loads a 128-row half.
+  const uint32_t b_rows = pair ? kBN / 2 : kBN;
   TmaMaps m;
   if (!a_mn_major) FLCE_TRY(make_map(&m.a0, A, K, M, lda * 2, kBK, kBM));
   else FLCE_TRY(make_map(&m.a0, A, M, K, lda * 2, 64, kBK));

@@ -26,11 +26,6 @@ cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
   return launch_gemm<EpiAccum>(pair, maps, sc, p, status, num_sms, stream);
 }
 
-cudaError_t gradient_gemm_clusters(bool quad, int num_sms, int* clusters) {
-  return quad ? resident_clusters<EpiAccum, true>(num_sms, clusters)
-              : resident_clusters<EpiAccum, false>(num_sms, clusters);
-}
-
 // Token-chunked backward: G from the kept fp32 logits of one token chunk.
 // Thread t of a block handles kZGradVec consecutive columns over one tile of
 // kZGradRows rows at a time (row tiles grid-strided over blockIdx.y): per row
@@ -156,15 +151,25 @@ cudaError_t launch_scale(const float* scale, void* x, int64_t n, int x_f32, int 
   return cudaGetLastError();
 }
 
-// dbias[j] = sum over m tiles of the per-tile column sums, in m order.
+// dbias[j] = sum over m tiles of the per-tile column sums, in m order; with an
+// fp32 accumulator the sum is added to acc[j] (when `accumulate`) and kept
+// there until the call that writes the result (`write_final`).
 __global__ void dbias_reduce_kernel(const float* __restrict__ part, int64_t ldg, int m_tiles, int rows_per_tile,
-                                    int64_t cols, void* dbias, int bias_f32, const int32_t* row_count) {
+                                    int64_t cols, void* dbias, int bias_f32, const int32_t* row_count, float* acc,
+                                    int accumulate, int write_final) {
   const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (j >= cols) return;
   // Under compaction only the tiles that hold a valid token were computed.
   const int tiles = row_count ? min(m_tiles, (*row_count + rows_per_tile - 1) / rows_per_tile) : m_tiles;
   float s = 0.f;
   for (int m = 0; m < tiles; ++m) s += part[static_cast<int64_t>(m) * ldg + j];
+  if (acc) {
+    if (accumulate) s = acc[j] + s;
+    if (!write_final) {
+      acc[j] = s;
+      return;
+    }
+  }
   if (bias_f32) {
     reinterpret_cast<float*>(dbias)[j] = s;
   } else {
@@ -173,11 +178,12 @@ __global__ void dbias_reduce_kernel(const float* __restrict__ part, int64_t ldg,
 }
 
 cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int rows_per_tile, int64_t cols,
-                                void* dbias, int bias_f32, const int32_t* row_count, cudaStream_t stream) {
+                                void* dbias, int bias_f32, const int32_t* row_count, float* acc, int accumulate,
+                                int write_final, cudaStream_t stream) {
   const int64_t blocks = (cols + 255) / 256;
   if (blocks == 0) return cudaSuccess;
-  dbias_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, ldg, m_tiles, rows_per_tile, cols,
-                                                                          dbias, bias_f32, row_count);
+  dbias_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      part, ldg, m_tiles, rows_per_tile, cols, dbias, bias_f32, row_count, acc, accumulate, write_final);
   return cudaGetLastError();
 }
 

@@ -342,18 +342,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c_inner), "r"(c_outer)
       : "memory");
 }
-// The same, multicast: the box lands at the same offset in every CTA of
-// `cta_mask`, and each destination's bytes complete on the barrier at the same
-// offset in the even CTA of the destination's pair (the barrier address names
-// an even CTA).
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
-                                                    int32_t c_inner, int32_t c_outer, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c_inner), "r"(c_outer), "h"(cta_mask)
-      : "memory");
-}
 // Whole-warp calls, executed by one warp in each CTA of the pair.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -378,14 +366,14 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive once on the mbarrier at this shared offset in every CTA of `cta_mask`
-// when all prior tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
+// Arrive once on the mbarrier at shared::cluster address `bar_cluster_addr`
+// (this CTA's or the peer CTA's, from map_to_cta) when all prior tcgen05
+// operations of this thread have completed.  A barrier in each CTA of the
+// pair takes one commit each.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar_cluster_addr) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar_cluster_addr)
+               : "memory");
 }
 
 // 256-bit global accesses (32-byte aligned addresses): one full sector per lane.

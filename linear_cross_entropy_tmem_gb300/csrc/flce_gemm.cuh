@@ -3,8 +3,7 @@
 //
 //   warp 8      TMA producer: fills a shared-memory ring with 128-byte swizzled
 //               bf16 tiles of A and B (4 stages of 128x64 + 256x64 for one CTA;
-//               6 stages of 128x64 + its 128x64 half of B per CTA of a pair;
-//               with two pairs per cluster the B halves are TMA-multicast).
+//               6 stages of 128x64 + its 128x64 half of B per CTA of a pair).
 //   warp 9      MMA issuer: one elected thread issues tcgen05.mma (M=128 or,
 //               for a CTA pair, M=256; N=256; K=16) into one of two TMEM
 //               accumulators (2 x 256 fp32 columns) and commits stage releases
@@ -255,7 +254,6 @@ __device__ __forceinline__ void finish_box_stores() {
 template <bool kBias, bool kSoftcap>
 struct EpiFwd {
   using Params = FwdParams;
-  static constexpr bool kQuadOk = false;  // no multicast variant built for the logit products
   // Staging of the kept logits (TMA stores), one buffer per epilogue warp.
   static constexpr int kTailBytes = kEpilogueGroups * kEpilogueWarps * kStoreStageBytes;
   __device__ static void finish(const Params& p) {
@@ -414,7 +412,6 @@ __device__ __forceinline__ float token_weight(int reduction, const float* dloss,
 template <bool kBias, bool kSoftcap>
 struct EpiGrad {
   using Params = GradParams;
-  static constexpr bool kQuadOk = false;
   static constexpr int kTailBytes = kEpiSmemBytes;  // dbias column-sum staging
   __device__ static void finish(const Params&) {}
   struct State {
@@ -542,7 +539,6 @@ struct EpiGrad {
 // ============================================================================
 struct EpiStore {
   using Params = StoreParams;
-  static constexpr bool kQuadOk = true;
   // One staging buffer per epilogue warp.
   static constexpr int kTailBytes = kEpilogueGroups * kEpilogueWarps * kStoreStageBytes;
   struct State {
@@ -581,7 +577,6 @@ struct EpiStore {
 // ============================================================================
 struct EpiAccum {
   using Params = AccumParams;
-  static constexpr bool kQuadOk = true;
   static constexpr int kTailBytes = 0;
   __device__ static void finish(const Params&) {}
   struct State {
@@ -936,15 +931,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // half of B; the pair leader's MMA thread issues M=256 MMAs that read both
 // CTAs' shared memory and write 128 x 256 fp32 into each CTA's TMEM.
 //   full[s]    in the leader: both CTAs' copies of stage s complete on it
-//   empty[s]   in each CTA: multicast commit from the leader's MMA thread
-//   tfull[b]   in each CTA: multicast commit, accumulator b ready
+//   empty[s]   in each CTA: a commit from the leader's MMA thread to each CTA
+//   tfull[b]   in each CTA: a commit to each CTA, accumulator b ready
 //   tempty[b]  in the leader: 4 epilogue warps of each CTA arrive (8 total)
-// kQuad: a cluster of two pairs takes the two 256-row m tiles of a 512-row
-// super tile with the same n tile and K range, so both pairs need the same B
-// tile.  Each CTA loads one half of its B half and multicasts it to itself and
-// the CTA of the same pair rank in the other pair: every pair pulls 3/4 of the
-// operand bytes from L2 that it would alone.  A stage is free only when both
-// pairs have consumed it, so empty[s] takes one commit from each pair leader.
 // ============================================================================
 __device__ __forceinline__ GemmSmem carve_smem_pair(uint8_t* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -969,7 +958,7 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   }
 }
 
-template <class Epi, bool kQuad>
+template <class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                      const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_b0,
@@ -978,20 +967,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   GemmSmem sm = carve_smem_pair(smem_raw);
   const int warp = threadIdx.x >> 5;
-  constexpr uint32_t kCtas = kQuad ? 4u : 2u;
-  constexpr int kTileRows = kQuad ? 2 * kPairRows : kPairRows;  // rows per unit of the cluster
+  constexpr uint32_t kCtas = 2u;
+  constexpr int kTileRows = kPairRows;  // rows per unit of the pair
   const uint32_t rank = cluster_ctarank();
-  const uint32_t pair_rank = rank & 1u, leader_rank = rank & ~1u, pair_id = rank >> 1;
+  const uint32_t pair_rank = rank & 1u, leader_rank = 0u;
   const bool leader = pair_rank == 0;
-  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << leader_rank);
-  // B copies go to this CTA and the same pair rank of the other pair.
-  const uint16_t b_mask = static_cast<uint16_t>(0x5u << pair_rank);
-  static_assert(kBN / 128 == 2, "the multicast B split takes one 64-column atom per pair");
 
   if (threadIdx.x == kTmaWarp * 32) {
     for (int s = 0; s < kStagesPair; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kQuad ? 2 : 1);
+      mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&sm.tfull[b], 1);
@@ -1056,14 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < kBM / 64; ++j)
                   tma_load_2d_pair(sa + j * kMnAtomBytes, ma, fb, a_row + 64 * j, sc.a_k_off + k);
               }
-              if (kQuad) {  // rows (K-major; the map's box is 64 rows) or atom pair_id of the half
-                if (!sc.b_mn)
-                  tma_load_2d_pair_mc(sb + pair_id * (kBHalfBytes / 2), mb, fb, sc.b_k_off + k,
-                                      b_col + static_cast<int>(pair_id) * (kBN / 4), b_mask);
-                else
-                  tma_load_2d_pair_mc(sb + pair_id * kMnAtomBytes, mb, fb, b_col + 64 * static_cast<int>(pair_id),
-                                      sc.b_k_off + k, b_mask);
-              } else if (!sc.b_mn) {
+              if (!sc.b_mn) {
                 tma_load_2d_pair(sb, mb, fb, sc.b_k_off + k, b_col);
               } else {
 #pragma unroll
@@ -1123,8 +1101,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
                 accumulate = 1;
               }
-              // stage free in both CTAs (in all four: the other pair's B copies land here too)
-              umma_commit_pair(&sm.empty[stage], kQuad ? static_cast<uint16_t>(0xF) : pair_mask);
+              // stage free in both CTAs once these MMAs have read it
+              const uint32_t e = smem_u32(&sm.empty[stage]);
+              umma_commit_pair(e);
+              umma_commit_pair(map_to_cta(e, 1u));
               if (++stage == kStagesPair) {
                 stage = 0;
                 phase ^= 1u;
@@ -1132,7 +1112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          umma_commit_pair(&sm.tfull[acc], pair_mask);  // accumulator ready in both CTAs
+          const uint32_t tf = smem_u32(&sm.tfull[acc]);  // accumulator ready in both CTAs
+          umma_commit_pair(tf);
+          umma_commit_pair(map_to_cta(tf, 1u));
           if (++acc == kAccBufs) {
             acc = 0;
             acc_phase ^= 1u;
@@ -1140,7 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) aborted = true;
-      umma_commit_pair(sm.drain, static_cast<uint16_t>(1u << rank));
+      umma_commit_pair(smem_u32(sm.drain));
       mbar_wait_teardown(sm.drain, 0);
     }
     __syncwarp();

@@ -23,10 +23,10 @@ static cudaError_t launch_gemm_single(const TmaMaps& m, const GemmSched& sc, con
   return cudaGetLastError();
 }
 
-template <class Epi, bool kQuad>
+template <class Epi>
 static cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kQuad ? 4 : 2;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
@@ -38,14 +38,11 @@ static cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, cudaStream_t
   return cfg;
 }
 
-// Clusters of the CTA-pair kernel (two CTAs, or four with kQuad) that can be
-// resident at once on the current device, one CTA per SM; cached per device.
-// A cluster must fit in one GPC, so the count of four-CTA clusters can be
-// below num_sms / 4.
-template <class Epi, bool kQuad>
-static cudaError_t resident_clusters(int num_sms, int* out) {
-  auto kern = gemm_pair_kernel<Epi, kQuad>;
-  constexpr int kCtas = kQuad ? 4 : 2;
+// CTA pairs of the pair kernel that can be resident at once on the current
+// device, one CTA per SM; cached per device.
+template <class Epi>
+static cudaError_t resident_pairs(int num_sms, int* out) {
+  auto kern = gemm_pair_kernel<Epi>;
   static int resident[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -56,39 +53,28 @@ static cudaError_t resident_clusters(int num_sms, int* out) {
                                   kGemmPairSmemBase + Epi::kTailBytes)) != cudaSuccess)
       return e;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster_config<Epi, kQuad>(attr, nullptr);
-    cfg.gridDim = dim3(kCtas * std::max(1, num_sms / kCtas));
+    cudaLaunchConfig_t cfg = cluster_config<Epi>(attr, nullptr);
+    cfg.gridDim = dim3(2 * std::max(1, num_sms / 2));
     int n = 0;
     if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
     resident[dev] = std::max(1, n);
   }
-  *out = std::min(resident[dev], std::max(1, num_sms / kCtas));
+  *out = std::min(resident[dev], std::max(1, num_sms / 2));
   return cudaSuccess;
-}
-
-template <class Epi, bool kQuad>
-static cudaError_t launch_gemm_cluster(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
-                                       int* status, int num_sms, cudaStream_t stream) {
-  auto kern = gemm_pair_kernel<Epi, kQuad>;
-  constexpr int kCtas = kQuad ? 4 : 2;
-  int resident = 0;
-  cudaError_t e = resident_clusters<Epi, kQuad>(num_sms, &resident);  // also sets the smem attribute
-  if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config<Epi, kQuad>(attr, stream);
-  const int clusters = std::max(1, std::min(sc.total_units, resident));
-  cfg.gridDim = dim3(kCtas * clusters);
-  return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
 }
 
 template <class Epi>
 static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
                                     int* status, int num_sms, cudaStream_t stream) {
-  if (sc.quad) {
-    if constexpr (Epi::kQuadOk) return launch_gemm_cluster<Epi, true>(m, sc, p, status, num_sms, stream);
-    else return cudaErrorInvalidValue;
-  }
-  return launch_gemm_cluster<Epi, false>(m, sc, p, status, num_sms, stream);
+  auto kern = gemm_pair_kernel<Epi>;
+  int resident = 0;
+  cudaError_t e = resident_pairs<Epi>(num_sms, &resident);  // also sets the smem attribute
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config<Epi>(attr, stream);
+  const int clusters = std::max(1, std::min(sc.total_units, resident));
+  cfg.gridDim = dim3(2 * clusters);
+  return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
 }
 
 template <class Epi>

@@ -81,10 +81,6 @@ struct GemmSched {
   int32_t a_mn, b_mn;     // operand majorness: 0 = K-major, 1 = MN-major
   int32_t a_mn_off, a_k_off;   // coordinate offsets into the A tensor map
   int32_t b_mn_off, b_k_off;   // coordinate offsets into the B tensor map
-  // CTA-pair kernel only: 1 = clusters of two pairs sharing B by TMA multicast,
-  // m tiles of 512 rows (two pairs x 256).  MN-major B, or K-major B whose map
-  // box is 64 rows.
-  int32_t quad;
   // Optional device-side limits (valid-token compaction): units whose first
   // row is at or past *m_limit are skipped, and the K range stops at *k_limit
   // elements.  nullptr = no limit.

@@ -63,9 +63,6 @@ cudaError_t launch_store_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
                               int* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& sc, const AccumParams& p,
                               int* status, int num_sms, cudaStream_t stream);
-// Clusters of the dh / dW kernels (CTA pairs, or two pairs with quad) that
-// can be resident at once on the current device.
-cudaError_t gradient_gemm_clusters(bool quad, int num_sms, int* clusters);
 
 cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream);
 // Under compaction, the valid rows of each token chunk of the kept-logits backward.
@@ -82,9 +79,13 @@ cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t str
 cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream);
 // x *= *scale in place (bf16 or fp32), skipped on the device when *scale == 1.
 cudaError_t launch_scale(const float* scale, void* x, int64_t n, int x_f32, int grid, cudaStream_t stream);
-// dbias[j] = sum over the m_tiles per-tile partials (tiles of rows_per_tile rows), in tile order.
+// s[j] = sum over the m_tiles per-tile partials (tiles of rows_per_tile rows), in tile order; with
+// an fp32 accumulator `acc` (else nullptr) s[j] is added to acc[j] when `accumulate`.  s goes to
+// dbias in its dtype when `write_final` (or there is no accumulator), else to acc.  Under
+// compaction only the tiles below *row_count rows were computed.
 cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int rows_per_tile, int64_t cols,
-                                void* dbias, int bias_f32, const int32_t* row_count, cudaStream_t stream);
+                                void* dbias, int bias_f32, const int32_t* row_count, float* acc, int accumulate,
+                                int write_final, cudaStream_t stream);
 cudaError_t launch_dh_finalize(const float* part, int64_t stride, int ksplit, int64_t rows, int64_t cols, void* out,
                                int out_f32, const int32_t* row_map, const int32_t* row_count, int grid,
                                cudaStream_t stream);

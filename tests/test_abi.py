@@ -122,8 +122,9 @@ def test_fp32_terms_workspace(lib):
 
 
 def test_keep_logits_workspace(lib):
-    """The token-chunked backward keeps fp32 logits + bf16 G for at most half of the tokens, plus
-    an fp32 dW accumulator; the automatic choice keeps logits from D = 1280 up and for N > 256."""
+    """The token-chunked backward keeps fp32 logits + bf16 G for at most half of the tokens (a batch
+    of at most 256 tokens is one chunk), the dbias partials of one chunk and an fp32 dbias and dW
+    accumulator; the automatic choice keeps logits from D = 1280 up."""
     keep, rec = B.FLCE_FLAG_BWD_KEEP_LOGITS, B.FLCE_FLAG_BWD_RECOMPUTE
     for (N, D, V) in [(16384, 4096, 151936), (16384, 640, 262144), (8192, 2048, 128256), (4096, 1024, 50000),
                       (300, 200, 1000), (257, 136, 777)]:
@@ -133,12 +134,13 @@ def test_keep_logits_workspace(lib):
         k, r, a = ws[keep][1], ws[rec][1], ws[0][1]
         assert a == (k if D >= 1280 else r)
         half = ((N + 1) // 2 + 255) // 256 * 256
-        # kept logits + G, dbias partials, fp32 dW, dh K-split slots (at most 16), split records
-        bound = 6 * min(half, N) * ldz + 4 * ((N + 31) // 32) * ldz + 4 * V * D + 16 * 4 * half * D \
+        # kept logits + G and the dbias partials of one chunk, fp32 dbias and dW accumulators, dh
+        # K-split slots (at most 16), split records of one chunk
+        bound = 6 * min(half, N) * ldz + 4 * ((half + 31) // 32) * ldz + 4 * ldz + 4 * V * D + 16 * 4 * half * D \
             + (5 * 4 * 64 * 2 + 8) * half + (1 << 20)
         assert r < k <= bound
         if N * V >= 1 << 28:  # the chunk's kept logits + G stay within the 4 GiB budget (+ one row group)
-            assert k - 4 * V * D - 16 * 4 * half * D - 4 * ((N + 31) // 32) * ldz <= (4 << 30) + 6 * 256 * ldz \
+            assert k - 4 * V * D - 16 * 4 * half * D - 4 * ((half + 31) // 32) * ldz <= (4 << 30) + 6 * 256 * ldz \
                 + (5 * 4 * 64 * 2 + 8) * half + (1 << 20)
     # with compaction the layout adds the compaction buffers (row map, targets, hidden copy,
     # compacted lse / upstream grads, chunk row counts), about (4 + 8 + 2 D + 4 + 4) bytes per token
@@ -146,10 +148,42 @@ def test_keep_logits_workspace(lib):
         k = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=keep), 2)[1]
         st, kc = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=keep | B.FLCE_FLAG_COMPACT_VALID), 2)
         assert st == B.FLCE_OK and k < kc <= k + N * (20 + 2 * D) + (1 << 16)
-    # with N <= 256 there are no two chunks: the recompute runs and sizes its workspace
+    # a batch of at most 256 tokens is one chunk of its own rows (rounded up to 32): its kept logits
+    # and G, no dW accumulator, dh slots and the split records
     for N in (1, 100, 256):
-        pk, pr = (_problem(n_tokens=N, hidden=2048, vocab=248320, flags=f) for f in (keep, rec))
-        assert _ws(lib, pk, 2) == _ws(lib, pr, 2)
+        D, V = 2048, 248320
+        ldz = (V + 31) // 32 * 32
+        rows = (N + 31) // 32 * 32
+        st, k = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=keep), 2)
+        assert st == B.FLCE_OK
+        assert 6 * rows * ldz < k <= 6 * rows * ldz + 4 * rows * ldz // 32 + 16 * 4 * 256 * D + (1 << 20)
+        assert k < 4 * V * D  # in particular no fp32 dW accumulator
+
+
+def test_keep_logits_workspace_has_no_tokens_times_vocab_term(lib):
+    """With a bias (its partial column sums are the one per-row-tile scratch), N swept from 512 to
+    131072 at V = 262144: the kept-logits workspace stays within the 4 GiB logit budget, the fp32 dW
+    and dbias accumulators, the scratch of one token chunk (whose rows the budget bounds) and terms
+    linear in N (compaction buffers, block sums), with no N * V term."""
+    keep = B.FLCE_FLAG_BWD_KEEP_LOGITS
+    V, D = 262144, 2048
+    ldz = V
+    nc_max = max(256, (4 << 30) // (6 * ldz) // 256 * 256)  # rows of a chunk at the logit budget
+    sizes = {}
+    for N in (512, 2048, 8192, 32768, 131072):
+        nc = min(nc_max, ((N + 1) // 2 + 255) // 256 * 256)
+        for flags in (keep, keep | B.FLCE_FLAG_COMPACT_VALID):
+            st, k = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=flags), 2)
+            assert st == B.FLCE_OK
+            chunk = 6 * nc * ldz + 4 * ldz * ((nc + 31) // 32) + 16 * 4 * nc * D + (5 * 4 * 64 * 2 + 8) * nc
+            linear = N * (20 + 2 * D) + 32 * (N // 256 + 1)
+            assert k <= chunk + 4 * V * D + 4 * ldz + linear + (1 << 20), (N, flags, k)
+            sizes[(N, flags)] = k
+    assert 6 * nc_max * ldz <= 4 << 30
+    # from 32768 to 131072 tokens (chunks at the budget) only the per-token block sums grow
+    assert sizes[(131072, keep)] - sizes[(32768, keep)] < 1 << 20
+    assert sizes[(131072, keep | B.FLCE_FLAG_COMPACT_VALID)] - sizes[(32768, keep | B.FLCE_FLAG_COMPACT_VALID)] \
+        < 98304 * (20 + 2 * D) + (1 << 20)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -238,13 +272,9 @@ def test_testing_switches_validate_their_arguments(lib):
     """The process-wide test/tuning switches reject out-of-range values and accept every
     documented one (they only store a setting, so no GPU is needed)."""
     assert lib.flce_testing_set_gemm_mode(3) == B.FLCE_ERR_INVALID_ARG
-    assert lib.flce_testing_set_multicast(3) == B.FLCE_ERR_INVALID_ARG
-    assert lib.flce_testing_set_multicast(-1) == B.FLCE_ERR_INVALID_ARG
+    assert lib.flce_testing_set_gemm_mode(-1) == B.FLCE_ERR_INVALID_ARG
     try:
-        for mode in (0, 2, 1):
-            assert lib.flce_testing_set_multicast(mode) == B.FLCE_OK
         for mode in (1, 2, 0):
             assert lib.flce_testing_set_gemm_mode(mode) == B.FLCE_OK
     finally:
-        lib.flce_testing_set_multicast(1)
         lib.flce_testing_set_gemm_mode(0)

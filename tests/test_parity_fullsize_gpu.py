@@ -78,11 +78,17 @@ def test_parity_full_size(name, compact, entry):
         assert lo <= c <= hi, (c, lo, hi)
 
     dh_ref = oracle.dhidden_rows(hc, Wc, bc, tc, rows.numpy(), n_valid=nv, dloss=dlc, **kw)
-    assert oracle.relative_frobenius(dh_g, dh_ref) <= TOL_GRAD
     dW_ref, db_ref = oracle.dweight_rows(hc, Wc, bc, tc, vrows.numpy(), ref["lse"], dloss=dlc, **kw)
-    assert oracle.relative_frobenius(dW_g, dW_ref) <= TOL_GRAD
+    err = {"dhidden": oracle.relative_frobenius(dh_g, dh_ref), "dweight": oracle.relative_frobenius(dW_g, dW_ref)}
     if db_g is not None:
-        assert oracle.relative_frobenius(db_g, db_ref) <= TOL_GRAD
+        err["dbias"] = oracle.relative_frobenius(db_g, db_ref)
+    print(f"{name} {entry}{' compact' if compact else ''}: relative Frobenius errors "
+          + ", ".join(f"{k} {v:.2e}" for k, v in err.items()))
+    assert all(v <= TOL_GRAD for v in err.values()), err
+    if w.hidden_dtype == torch.float32:
+        # dweight = G^T h reads h's leading bf16 term only: G itself is rounded to bf16, so the
+        # error is that of two bf16 roundings (RMS about 2^-9 / sqrt(3) each), far inside 1e-2
+        assert err["dweight"] <= 5e-3, err
 
 
 def test_long_context_131k_tokens():

@@ -364,10 +364,11 @@ def test_fused_call_equals_separate_calls(name, compact, mode):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("chunk", [256, 0], ids=["chunk256", "auto-chunk"])
 @pytest.mark.parametrize("mode", [0, 1, 2], ids=["auto", "single-cta", "cta-pair"])
-@pytest.mark.parametrize("name", [n for n, (w, _) in CASES.items() if w.n_tokens > 256])
+@pytest.mark.parametrize("name", list(CASES))
 def test_keep_logits_parity(name, mode, chunk):
     """Every output of the token-chunked fused call against the oracle, element by element, with
-    several token chunks (ragged last chunk) and the dh K split of the case."""
+    several token chunks (ragged last chunk) and the dh K split of the case; a batch of at most 256
+    tokens is one chunk (dW and dbias written straight from it)."""
     import linear_cross_entropy_tmem_gb300 as F
     from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_token_chunk, testing_set_tuning
     w, tuning = CASES[name]
@@ -381,7 +382,7 @@ def test_keep_logits_parity(name, mode, chunk):
         lambda: F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd="keep_logits", **kw))
     assert F.flce_read_device_status(fwd.workspace) == 0
     chunks = kinds.count("bwd_logit_grad")
-    assert chunks >= 2 and "bwd_recompute" not in kinds
+    assert (chunks == 1 if w.n_tokens <= 256 else chunks >= 2) and "bwd_recompute" not in kinds
     assert kinds.count("fwd_logits") == kinds.count("bwd_dhidden") == kinds.count("bwd_dweight") == chunks
     ref_f = oracle.forward(hc, Wc, bc, tc, **kw)
     ref_b = oracle.backward(hc, Wc, bc, tc, dloss=dc, **kw)
@@ -392,10 +393,11 @@ def test_keep_logits_parity(name, mode, chunk):
 
 @pytest.mark.parametrize("mode", [0, 1, 2], ids=["auto", "single-cta", "cta-pair"])
 @pytest.mark.parametrize("ignore_every", [17, 3])
-@pytest.mark.parametrize("name", [n for n in COMPACT_CASES if CASES[n][0].n_tokens > 256])
+@pytest.mark.parametrize("name", list(COMPACT_CASES))
 def test_keep_logits_with_compaction(name, ignore_every, mode):
     """Kept logits over the compacted tokens: 256-row chunks of the valid tokens (a partial chunk
-    and, with a third of the tokens ignored, chunks with no valid row at all)."""
+    and, with a third of the tokens ignored, chunks with no valid row at all), or one chunk for a
+    batch of at most 256 tokens."""
     import linear_cross_entropy_tmem_gb300 as F
     from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_token_chunk, testing_set_tuning
     w, tuning = CASES[name]
@@ -409,7 +411,8 @@ def test_keep_logits_with_compaction(name, ignore_every, mode):
     (fwd, grads), kinds = launch_kinds(lambda: F.flce_forward_backward(
         dev[0], dev[1], dev[3], dev[4], dev[2], entropy=True, compact=True, bwd="keep_logits", **kw))
     assert F.flce_read_device_status(fwd.workspace) == 0
-    assert kinds.count("bwd_logit_grad") >= 2 and "bwd_recompute" not in kinds
+    chunks = kinds.count("bwd_logit_grad")
+    assert (chunks == 1 if w.n_tokens <= 256 else chunks >= 2) and "bwd_recompute" not in kinds
     _compare_compacted({"fwd": fwd, "bwd": grads}, oracle.forward(h, W, b, t, **kw),
                        oracle.backward(h, W, b, t, dloss=dloss, **kw), t, w.reduction)
 
@@ -526,7 +529,8 @@ def test_no_writes_past_outputs_or_workspace(name, compact, mode):
 @pytest.mark.parametrize("mode", [1, 2], ids=["single-cta", "cta-pair"])
 @pytest.mark.parametrize("name", ["ragged N300 D200 V1000 bias-bf16 s0.7 c5 sum",
                                   "fp32-h N257 D136 V777 bias s0.0625 c30 none",
-                                  "multi-chunk ksplit3 N384 D256 V3000 bias mean"])
+                                  "multi-chunk ksplit3 N384 D256 V3000 bias mean",
+                                  "single tile vocab N130 D64 V200 softcap", "D8 V300 mean"])
 def test_keep_logits_no_writes_past_outputs_or_workspace(name, mode):
     """Canary tails after every output and the workspace of the token-chunked fused call."""
     import ctypes
@@ -746,55 +750,51 @@ def test_nan_hidden_row_stays_in_its_row(softcap):
     assert np.linalg.norm(dh[keep] - ref_dh) <= 1e-2 * np.linalg.norm(ref_dh)
 
 
-@pytest.mark.parametrize("bwd", ["recompute", "keep_logits"])
-def test_multicast_products_equal_plain_pairs_bitwise(bwd):
-    """dh and dW from clusters of two CTA pairs that share the B operand by TMA multicast equal those
-    of plain CTA pairs bit for bit (same MMAs, same order), with a ragged last 512-row tile on both
-    the token (dh) and the vocabulary (dW) side; the forward outputs are untouched."""
-    import linear_cross_entropy_tmem_gb300 as F
-    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_multicast
-    w = Workload("mc", 1300, 512, 3000, sigma_w=0.08, bias=True, seed=31)
-    h, W, b, t, dloss = (x.cuda() for x in make_inputs(w, "cpu"))
-    out = {}
-    try:
-        testing_set_gemm_mode(2)
-        for on in (False, True):
-            testing_set_multicast(2 if on else 0)
-            fwd, grads = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd=bwd)
-            torch.cuda.synchronize()
-            assert F.flce_read_device_status(fwd.workspace) == 0
-            out[on] = (fwd.loss.clone(), fwd.lse.clone()) + tuple(g.clone() for g in grads)
-    finally:
-        testing_set_multicast(1)
-        testing_set_gemm_mode(0)
-    for a, c in zip(out[False], out[True]):
-        assert torch.equal(a, c)
+@pytest.mark.parametrize("where", ["hidden", "weight", "dhidden", "dweight", "workspace"])
+@pytest.mark.parametrize("host", ["pinned", "pageable"])
+def test_host_pointers_are_refused_before_any_launch(where, host):
+    """The tensor maps and the products address this GPU's memory only: a host pointer (pinned or
+    pageable) for an operand, a gradient or the workspace is refused with FLCE_ERR_INVALID_ARG before
+    anything is enqueued, so the outputs keep their fill and the status word is untouched."""
+    import ctypes
 
-
-@pytest.mark.parametrize("bwd", ["recompute", "keep_logits"])
-def test_multicast_with_compaction_matches_oracle_and_plain_pairs(bwd):
-    """Under FLCE_FLAG_COMPACT_VALID the dh / dW units are enumerated over the m tiles that hold a
-    valid row (a device-side count); with the B multicast clusters those tiles are 512 rows and the
-    count cuts the last one anywhere. The results match the oracle and the plain CTA pairs bitwise."""
-    import linear_cross_entropy_tmem_gb300 as F
-    from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_multicast
-    w = Workload("mcc", 1300, 256, 2600, sigma_w=0.1, bias=True, ignore_every=3, seed=33)
-    h, W, b, t, dloss = make_inputs(w, "cpu")
-    dev = [x.cuda() for x in (h, W, b, t, dloss)]
-    out = {}
-    try:
-        testing_set_gemm_mode(2)
-        for mode in (0, 2):
-            testing_set_multicast(mode)
-            fwd, grads = F.flce_forward_backward(dev[0], dev[1], dev[3], dev[4], dev[2], entropy=True,
-                                                 compact=True, bwd=bwd)
-            torch.cuda.synchronize()
-            assert F.flce_read_device_status(fwd.workspace) == 0
-            out[mode] = (fwd, grads)
-    finally:
-        testing_set_multicast(1)
-        testing_set_gemm_mode(0)
-    for a, c in zip(out[0][1], out[2][1]):
-        assert torch.equal(a, c)
-    _compare_compacted({"fwd": out[2][0], "bwd": out[2][1]}, oracle.forward(h, W, b, t),
-                       oracle.backward(h, W, b, t, dloss=dloss), t, "mean")
+    import linear_cross_entropy_tmem_gb300.api as api
+    from linear_cross_entropy_tmem_gb300 import binding as B
+    lib = B.load()
+    w = Workload("host-ptr", 300, 64, 1000, sigma_w=0.2, seed=41)
+    h, W, _, t, dloss = (x.cuda() if x is not None else None for x in make_inputs(w, "cpu"))
+    prob = api.make_problem(300, 64, 1000)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    loss = torch.full((1,), float("nan"), **f32)
+    lse = torch.full((300,), float("nan"), **f32)
+    correct = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    n_valid = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    ent = torch.full((1,), float("nan"), **f32)
+    dh = torch.full_like(h, float("nan"))
+    dW = torch.full_like(W, float("nan"))
+    ws = torch.full((api.flce_workspace_size(prob, 2),), 0x5A, dtype=torch.uint8, device="cuda")
+    args = {"hidden": h, "weight": W, "dhidden": dh, "dweight": dW, "workspace": ws}
+    src = args[where]
+    raw = torch.empty(src.numel() * src.element_size() + 256, dtype=torch.uint8,
+                      pin_memory=(host == "pinned"))
+    off = (-raw.data_ptr()) % 256  # 256-byte aligned like the device buffers, so only the location differs
+    args[where] = raw[off:off + src.numel() * src.element_size()].view(src.dtype).view(src.shape)
+    args[where].copy_(src.cpu())
+    p = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.flce_forward_backward(ctypes.byref(prob), p(args["hidden"]), p(args["weight"]), None, p(t), p(dloss),
+                                   p(loss), p(lse), None, p(correct), p(n_valid), p(ent), p(args["dhidden"]),
+                                   p(args["dweight"]), None, p(args["workspace"]), args["workspace"].numel(), s)
+    assert rc == B.FLCE_ERR_INVALID_ARG
+    if where in ("hidden", "weight", "workspace"):
+        rws = torch.full((api.flce_workspace_size(prob, 0),), 0x5A, dtype=torch.uint8, device="cuda")
+        if where == "workspace":
+            rws = args["workspace"]
+        rc = lib.flce_forward(ctypes.byref(prob), p(args["hidden"]), p(args["weight"]), None, p(t), p(loss),
+                              p(lse), None, p(correct), p(n_valid), p(ent), p(rws), rws.numel(), s)
+        assert rc == B.FLCE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.isnan(loss).all() and torch.isnan(lse).all() and int(correct) == -1 and int(n_valid) == -1
+    assert torch.isnan(dh).all() and torch.isnan(dW).all()
+    if where != "workspace":
+        assert bool((ws == 0x5A).all())

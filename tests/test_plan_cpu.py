@@ -75,6 +75,16 @@ def test_one_chunk_plan(lib):
     assert info.dh_ksplit == 9
 
 
+def test_one_chunk_fused_plan_keeps_logits(lib):
+    """The fused call on the same shape keeps the logits of its one 256-token chunk (D = 2048 >= 1280):
+    the dh product over K = V has the same 16 single-CTA tiles and 9 K splits."""
+    info = _plan(lib, _problem(256, 2048, 248320, reduction=B.FLCE_RED_SUM), 2)
+    assert info.keep_logits == 1 and info.n_chunks == 1 and info.token_chunk_rows == 256
+    assert info.dh_pair == 0 and info.dh_ksplit == 9
+    small = _plan(lib, _problem(70, 2048, 248320), 2)
+    assert small.keep_logits == 1 and small.n_chunks == 1 and small.token_chunk_rows == 96
+
+
 def test_forward_split_plans(lib):
     """The forward splits the vocabulary so that (m tiles x splits) units fill whole waves of 76
     pairs.  Gemma-like: 64 m tiles x 19 splits of 54 tiles = 1216 units = 16 waves (99.8 % of the
@@ -131,12 +141,15 @@ def test_plan_invariants(lib, sms):
             assert 1 <= info.fwd_splits <= min(64, n_t)
             assert info.fwd_splits == cdiv(n_t, info.fwd_tiles_per_split)  # no empty split
             if info.keep_logits:
-                assert fb == 2 and D >= 1280 and N > 256
-                assert info.token_chunk_rows % 256 == 0
-                assert info.token_chunk_rows <= cdiv(cdiv(N, 2), 256) * 256
-                assert info.n_chunks == cdiv(N, info.token_chunk_rows) >= 2
+                assert fb == 2 and D >= 1280
+                if N > 256:  # at least two chunks: the kept logits never cover the whole batch
+                    assert info.token_chunk_rows % 256 == 0
+                    assert info.token_chunk_rows <= cdiv(cdiv(N, 2), 256) * 256
+                    assert info.n_chunks == cdiv(N, info.token_chunk_rows) >= 2
+                else:  # one chunk of the batch's rows, rounded up to 32
+                    assert info.token_chunk_rows == cdiv(N, 32) * 32 and info.n_chunks == 1
             else:
-                assert fb == 1 or D < 1280 or N <= 256
+                assert fb == 1 or D < 1280
                 vc, run = info.vocab_chunk_cols, info.run_chunk_cols
                 assert vc % 256 == 0 and run % 256 == 0
                 assert run <= vc and run >= max(1, vc // 256 // 2) * 256  # widths down to half the tiles
@@ -145,10 +158,9 @@ def test_plan_invariants(lib, sms):
 
 
 def test_backward_algorithm_follows_flags(lib):
-    """The fused call keeps logits from D = 1280 up when there are at least two 256-token chunks;
-    FLCE_FLAG_BWD_RECOMPUTE and FLCE_FLAG_BWD_KEEP_LOGITS force either algorithm (keeping logits
-    still needs N > 256), with and without valid-token compaction and fp32 hidden states.
-    flce_backward always recomputes."""
+    """The fused call keeps logits from D = 1280 up (a batch of at most 256 tokens as one chunk);
+    FLCE_FLAG_BWD_RECOMPUTE and FLCE_FLAG_BWD_KEEP_LOGITS force either algorithm, with and without
+    valid-token compaction and fp32 hidden states.  flce_backward always recomputes."""
     rec, keep, cmp_ = B.FLCE_FLAG_BWD_RECOMPUTE, B.FLCE_FLAG_BWD_KEEP_LOGITS, B.FLCE_FLAG_COMPACT_VALID
     for extra in (0, cmp_):
         for dt in (B.FLCE_BF16, B.FLCE_F32):
@@ -157,5 +169,7 @@ def test_backward_algorithm_follows_flags(lib):
             assert _plan(lib, _problem(4096, 1152, 50000, flags=extra, **kw), 2).keep_logits == 0
             assert _plan(lib, _problem(4096, 1280, 50000, flags=extra | rec, **kw), 2).keep_logits == 0
             assert _plan(lib, _problem(4096, 640, 50000, flags=extra | keep, **kw), 2).keep_logits == 1
-            assert _plan(lib, _problem(256, 4096, 50000, flags=extra | keep, **kw), 2).keep_logits == 0
+            assert _plan(lib, _problem(256, 4096, 50000, flags=extra | keep, **kw), 2).keep_logits == 1
+            assert _plan(lib, _problem(256, 4096, 50000, flags=extra | rec, **kw), 2).keep_logits == 0
+            assert _plan(lib, _problem(100, 640, 50000, flags=extra, **kw), 2).keep_logits == 0
             assert _plan(lib, _problem(4096, 4096, 50000, flags=extra | keep, **kw), 1).keep_logits == 0
