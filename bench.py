@@ -10,10 +10,12 @@ headline metric is quoted on.  Prints ONE JSON line (rank 0).
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream,
-max over ranks.  The inputs are larger than L2 (the 1.25 GB head alone is ten
-times the 129 MB L2), so no flush is needed between steps.  For N > 1 every
-rank runs its own replica of the workload (independent batches; the loss needs
-no exchange), so scaling is weak.
+max over ranks.  The inputs of every benchmark head but the tiny one are larger
+than L2 (the Qwen3-8B-like head alone is ten times the 129 MB L2), so no flush
+is needed between their steps; smaller inputs get a 256 MB buffer written
+between steps, outside the steps' events.  For N > 1 every rank runs its own
+replica of the workload (independent batches; the loss needs no exchange), so
+scaling is weak.
 """
 from __future__ import annotations
 
@@ -68,6 +70,9 @@ def parse_args(argv=None):
                     help="rows per token chunk of the keep-logits backward (0 = automatic; tuning)")
     ap.add_argument("--gemm-mode", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM kernel: 0 automatic, 1 single CTA, 2 CTA pair (A/B timing)")
+    ap.add_argument("--e2e-grads", action="store_true",
+                    help="the e2e leg also reads dhidden, dweight and dbias back to pinned host memory every step "
+                         "(by default only the loss and the metrics return; the gradients stay on the device)")
     ap.add_argument("--dh-ksplit", type=int, default=0,
                     help="force the K splits of the recompute backward's dh product (0 = automatic; tuning)")
     return ap.parse_args(argv)
@@ -349,6 +354,35 @@ def committed_traffic(kind, workload, backward):
     return e.get("dram_bytes_per_launch")
 
 
+def kernel_model(w, keep, rows, launches, h_terms, grad_h_terms):
+    """Algorithmic work of each launch kind over one step: flops (2 per multiply-add of the
+    product) and the bytes the kind must move to do its part (operands read, results written),
+    counting the re-reads and accumulator traffic that the chosen algorithm itself implies.
+
+    rows: tokens the products run over; launches: {kind: launches per step}; h_terms: bf16 terms the
+    logit products read of the hidden state (1 for bf16, 2 or 3 for fp32); grad_h_terms: those the
+    dW product reads.  Kept logits run per token chunk (W read once per chunk; dW accumulated in
+    fp32 across chunks); the recompute runs per vocabulary chunk (h read once per chunk)."""
+    R, V, D = float(rows), float(w.vocab), float(w.hidden)
+    eh = 4.0 if w.hidden_dtype.itemsize == 4 else 2.0
+    out = {}
+    prod = 2.0 * R * V * D
+    if keep:
+        nc = max(1, launches.get("bwd_logit_grad", 1))
+        out["fwd_logits"] = (prod, 2 * h_terms * R * D + 2 * nc * V * D + 4 * R * V)
+        out["bwd_logit_grad"] = (0.0, 6 * R * V)
+        out["bwd_dhidden"] = (prod, 2 * R * V + 2 * nc * V * D + eh * R * D)
+        acc = 2 * V * D if nc == 1 else 8 * V * D * (nc - 1) + 2 * V * D
+        out["bwd_dweight"] = (prod, 2 * R * V + 2 * grad_h_terms * R * D + acc)
+    else:
+        nv = max(1, launches.get("bwd_recompute", 1))
+        out["fwd_logits"] = (prod, 2 * h_terms * R * D + 2 * V * D)
+        out["bwd_recompute"] = (prod, 2 * nv * h_terms * R * D + 2 * V * D + 2 * R * V)
+        out["bwd_dweight"] = (prod, 2 * R * V + 2 * nv * grad_h_terms * R * D + 2 * V * D)
+        out["bwd_dhidden"] = (prod, 2 * R * V + 2 * V * D + 4 * R * D * (2 * nv - 1) + eh * R * D)
+    return out
+
+
 def pick_workload(args):
     from linear_cross_entropy_tmem_gb300.synthetic import WORKLOADS
     w = WORKLOADS[args.workload]
@@ -405,6 +439,10 @@ def flce_arm(args):
         recs[i].begin_event = ctypes.c_void_p(e0.cuda_event)
         recs[i].end_event = ctypes.c_void_p(e1.cuda_event)
     count = ctypes.c_int32(0)
+    # Operands that fit in L2 (129 MB) would stay there from one step to the next: write a 256 MB
+    # buffer between steps instead, outside the steps' events.
+    l2_bytes = 129 << 20
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) if run.input_bytes() < 2 * l2_bytes else None
     clocks = ClockSampler(local)
     time.sleep(0.3)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -412,9 +450,13 @@ def flce_arm(args):
     torch.cuda.synchronize()
     launches0 = lib.flce_testing_launch_count()
     B.check(lib.flce_testing_set_launch_log(recs, cap, ctypes.byref(count)), "launch log")
+    step_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     step_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     start.record()
     for k in range(args.steps):
+        if flush is not None:
+            flush.fill_(k & 0xFF)  # evict the previous step's operands from L2 (outside the step's events)
+        step_starts[k].record()
         run.step()
         step_ends[k].record()
     end.record()
@@ -423,9 +465,9 @@ def flce_arm(args):
     launches = lib.flce_testing_launch_count() - launches0
     barrier(dist, device)
     clock = clocks.stop()
-    ms = start.elapsed_time(end) / args.steps
-    per_step = [start.elapsed_time(step_ends[0])] + [step_ends[k - 1].elapsed_time(step_ends[k])
-                                                      for k in range(1, args.steps)]
+    per_step = [step_starts[k].elapsed_time(step_ends[k]) for k in range(args.steps)]
+    # back to back: the whole region; with an L2 flush between steps: the steps alone
+    ms = start.elapsed_time(end) / args.steps if flush is None else sum(per_step) / args.steps
     qs = statistics.quantiles(per_step, n=10, method="inclusive") if len(per_step) > 1 else per_step * 9
     step_quantiles = {"p20": qs[1], "p50": statistics.median(per_step), "p80": qs[7], "min": min(per_step),
                       "max": max(per_step)}
@@ -445,16 +487,40 @@ def flce_arm(args):
         d[1] += events[i][0].elapsed_time(events[i][1])
     # Tokens the products run over: all of them, or the valid ones under compaction.
     rows_mult = int(run.n_valid.item()) if args.compact else w.n_tokens
-    flops_kind = 2.0 * rows_mult * w.vocab * w.hidden  # per step, for each GEMM kind
-    gemm_kinds = [k for k in per_kind if k not in ("other", "bwd_logit_grad")]
     keep = "bwd_logit_grad" in per_kind  # the token-chunked backward ran (6NVD instead of 8NVD)
-    zgrad_bytes = 6.0 * w.n_tokens * w.vocab  # per step: fp32 logits read, bf16 G written
-    dominant = max(gemm_kinds, key=lambda k: per_kind[k][1])
-    n_l, t_ms = per_kind[dominant]
-    achieved = flops_kind * args.steps / (t_ms * 1e-3) / 1e12
+    h_terms = 1 if w.hidden_dtype == torch.bfloat16 else 2
+    model = kernel_model(w, keep, rows_mult, {k: v[0] // args.steps for k, v in per_kind.items()}, h_terms, 1)
     peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # a kernel inside a timed region of half a second or more runs under the sustained power cap
+    timed_s = ms * args.steps * 1e-3
+    peak_f, peak_f_kind = (peak_sus, "sustained") if timed_s >= 0.5 else (peak_burst, "burst")
+    kernels = {}
+    for k, (n_l, t_ms) in sorted(per_kind.items()):
+        e = {"launches": n_l, "ms_per_step": t_ms / args.steps}
+        if k in model:
+            fl, by = model[k]
+            t_s = t_ms * 1e-3 / args.steps
+            tensor = fl / (peak_f * 1e12) >= by / (peak_bw * 1e9)
+            e.update({"flops_per_step": fl, "bytes_per_step": by, "tflops": fl / t_s / 1e12 if fl else None,
+                      "gbs": by / t_s / 1e9, "bound": "tensor" if tensor else "hbm",
+                      "frac": (fl / t_s / 1e12 / peak_f) if tensor else (by / t_s / 1e9 / peak_bw)})
+        kernels[k] = e
+    dominant = max(model, key=lambda k: per_kind.get(k, [0, 0.0])[1])
+    dk = kernels[dominant]
+    n_l, t_ms = per_kind[dominant]
+    if dk["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": dk["tflops"], "peak": peak_f, "unit": "TFLOP/s",
+                "peak_kind": f"bf16 {peak_f_kind} ({peak_src})"}
+    else:
+        roof = {"bound": "hbm", "achieved": dk["gbs"], "peak": peak_bw, "unit": "GB/s",
+                "peak_kind": f"HBM copy bandwidth ({peak_src})"}
+    roof.update({"kernel": dominant, "frac": roof["achieved"] / roof["peak"],
+                 "flops_per_launch": model[dominant][0] / max(1, n_l // args.steps),
+                 "bytes_per_launch": model[dominant][1] / max(1, n_l // args.steps),
+                 "launches": n_l, "avg_launch_ms": t_ms / n_l})
 
     ms_max = max_over_ranks(dist, ms, device)
     tokens = w.n_tokens * world
@@ -482,6 +548,11 @@ def flce_arm(args):
         copy_stream = torch.cuda.Stream(device)
         copied = [torch.cuda.Event() for _ in range(2)]
         released = [torch.cuda.Event() for _ in range(2)]  # the step that last used buffer set i is done
+        grads = [n for n in ("dh", "dW", "db") if getattr(run, n) is not None] if args.e2e_grads else []
+        grads_host = [{n: torch.empty(getattr(run, n).shape, dtype=getattr(run, n).dtype).pin_memory()
+                       for n in grads} for _ in range(2)]
+        d2h_stream = torch.cuda.Stream(device) if grads else None
+        d2h_done = [torch.cuda.Event() for _ in range(2)]  # buffer set i's gradients have reached the host
 
         def e2e_step(k):
             i = k % 2
@@ -492,6 +563,8 @@ def flce_arm(args):
                     getattr(r, name).copy_(v, non_blocking=True)
                 copied[i].record(copy_stream)
             main.wait_event(copied[i])
+            if grads:
+                main.wait_event(d2h_done[i])  # step k-2's gradients have left this buffer set
             r.step()
             res[i][0] = r.loss[0]
             res[i][1] = r.correct[0]
@@ -499,6 +572,12 @@ def flce_arm(args):
             res[i][3] = r.ent_sum[0]
             out_host[i].copy_(res[i], non_blocking=True)
             released[i].record(main)
+            if grads:  # read the gradients back on a third stream, during the next step
+                with torch.cuda.stream(d2h_stream):
+                    d2h_stream.wait_event(released[i])
+                    for n in grads:
+                        grads_host[i][n].copy_(getattr(r, n), non_blocking=True)
+                    d2h_done[i].record(d2h_stream)
 
         for k in range(2):
             e2e_step(k)
@@ -509,14 +588,24 @@ def flce_arm(args):
         copy_stream.wait_stream(main)  # the first copy starts inside the timed region
         for k in range(args.steps):
             e2e_step(k)
+        for ev in d2h_done if grads else ():
+            main.wait_event(ev)  # the last gradients are on the host
         s1.record()  # after the last step, which waited for its copies, and its result copy
         torch.cuda.synchronize()
         e_ms = max_over_ranks(dist, s0.elapsed_time(s1) / args.steps, device)
+        d2h = out_host[0].numel() * out_host[0].element_size() + sum(
+            v.numel() * v.element_size() for v in grads_host[0].values())
         e2e = {"value": tokens / (e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in host.values())),
-               "d2h_bytes_per_step": int(out_host[0].numel() * out_host[0].element_size()),
+               "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms,
-               "overlap": "step k+1's inputs are copied on a second stream during step k (two device buffer sets)"}
+               "returns": ("loss, correct, n_valid, entropy_sum and the gradients dhidden, dweight"
+                           + (", dbias" if "db" in grads else "") if grads else
+                           "loss, correct, n_valid and entropy_sum (32 bytes); dhidden and dweight stay on the "
+                           "device, where an optimizer step would use them"),
+               "overlap": "step k+1's inputs are copied on a second stream during step k (two device buffer sets)"
+                          + ("; step k's gradients are read back on a third stream during step k+1" if grads
+                             else "")}
         del runs
 
     cpu = None
@@ -539,24 +628,19 @@ def flce_arm(args):
                        if args.autograd else
                        "flce_forward + flce_backward" if args.separate else "flce_forward_backward",
                        "backward": "keep_logits (token chunks, 6NVD)" if keep else "recompute (8NVD)",
-                       "l2": "inputs larger than L2 (1.25 GB head), no flush"},
+                       "l2": ("inputs larger than L2 (129 MB), no flush" if flush is None else
+                              "256 MB buffer written between steps (outside the steps' events) to flush L2")},
             # executed flops: 6NVD with kept logits, 8NVD with the recompute; the metric's own
             # accounting counts 8NVD per forward + backward whatever the algorithm
             "tflops": tflops_exec,
             "tflops_8nvd_accounting": tflops,
             "flops_per_step": {"executed": exec_flops, "metric_8nvd": w.flops()},
-            "pct_of_peak": {"of_burst": tflops_exec / peak_burst, "of_sustained": tflops_exec / peak,
+            "pct_of_peak": {"of_burst": tflops_exec / peak_burst, "of_sustained": tflops_exec / peak_sus,
                             "source": peak_src, "flops": "executed"},
-            "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
-                         "peak_kind": f"bf16 sustained ({peak_src})", "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": committed_traffic(dominant, args.workload, "keep_logits" if keep else "recompute")
-                         if not (args.tokens or args.vocab or args.hidden or args.compact) else None,
-                         "launches": n_l, "avg_launch_ms": t_ms / n_l},
-            "kernels": {k: {"launches": v[0], "ms_per_step": v[1] / args.steps,
-                            "tflops": (flops_kind * args.steps / (v[1] * 1e-3) / 1e12) if k in gemm_kinds else None,
-                            "gbs": (zgrad_bytes * args.steps / (v[1] * 1e-3) / 1e9) if k == "bwd_logit_grad"
-                            else None}
-                        for k, v in sorted(per_kind.items())},
+            "roofline": dict(roof, traffic=committed_traffic(dominant, args.workload,
+                                                             "keep_logits" if keep else "recompute")
+                             if not (args.tokens or args.vocab or args.hidden or args.compact) else None),
+            "kernels": kernels,
             "gpu_launches": int(launches),
             "clocks": clock,
             "e2e": e2e,
