@@ -94,17 +94,17 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS ? FLCE_OK : FLCE_ERR_CUDA;
 }
 
-// Output map of the TMA-store epilogue: [rows][cols] bf16 or fp32, 32 x 32
-// boxes whose 64-byte (bf16) or 128-byte (fp32) rows use the matching swizzle.
+// Output map of the TMA-store epilogue: [rows][cols] fp32 in 32 x 32 boxes or
+// bf16 in 32 x 64 boxes, so that a box row is one 128-byte line, with the
+// 128-byte swizzle.
 int make_store_map(CUtensorMap* m, void* base, bool f32, uint64_t cols, uint64_t rows, uint64_t row_bytes) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {f32 ? 32u : 64u, 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FLCE_OK : FLCE_ERR_CUDA;
 }
 

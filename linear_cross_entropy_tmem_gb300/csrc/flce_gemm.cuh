@@ -207,30 +207,21 @@ __device__ __forceinline__ float max32(const float (&z)[32]) {  // 16 three-inpu
 // ============================================================================
 // Epilogue: forward statistics over one vocabulary split
 // ============================================================================
-// Stages this warp's 32 x 32 box (lane = row; r = the row's 32 values as
-// bits) in `buf` with the tensor map's swizzle, then lane 0 stores it with TMA
-// at (col, row_base).  Swizzle: 16-byte chunk j of row r lands at chunk
-// j ^ (bits 7-8 of the row offset) for 64-byte rows (bf16) and j ^ (bits 7-9)
-// for 128-byte rows (fp32).  buf: kStoreStageBytes, 1024-byte aligned.
-__device__ __forceinline__ void store_box_tma(const CUtensorMap* map, uint8_t* buf, bool f32, int64_t col,
-                                              int64_t row_base, const uint32_t (&r)[32]) {
+// Stages this warp's box of 32 rows x 128 bytes (lane = row; r = the row's 32
+// words: 32 fp32 values, or 64 bf16 values packed in pairs) in `buf` with the
+// tensor map's 128-byte swizzle (16-byte chunk j of row r lands at chunk
+// j ^ (r mod 8)), then lane 0 stores it with TMA at (col, row_base); the map
+// clips rows and columns outside the tensor.  buf: kStoreStageBytes,
+// 1024-byte aligned.
+__device__ __forceinline__ void store_box_tma(const CUtensorMap* map, uint8_t* buf, int64_t col, int64_t row_base,
+                                              const uint32_t (&r)[32]) {
   const uint32_t lane = lane_id();
   if (lane == 0) bulk_wait_read_all();  // the previous box has left this buffer
   __syncwarp();
-  if (f32) {
-    uint8_t* row = buf + lane * 128;
+  uint8_t* row = buf + lane * 128;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      st_shared_v4(row + ((j ^ (lane & 7)) * 16), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-  } else {
-    uint8_t* row = buf + lane * 64;
-    const auto f = [&](int j) { return __uint_as_float(r[j]); };
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      st_shared_v4(row + ((j ^ ((lane >> 1) & 3)) * 16), pack_bf16x2(f(8 * j), f(8 * j + 1)),
-                   pack_bf16x2(f(8 * j + 2), f(8 * j + 3)), pack_bf16x2(f(8 * j + 4), f(8 * j + 5)),
-                   pack_bf16x2(f(8 * j + 6), f(8 * j + 7)));
-  }
+  for (int j = 0; j < 8; ++j)
+    st_shared_v4(row + ((j ^ (lane & 7)) * 16), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
@@ -312,7 +303,7 @@ struct EpiFwd {
         uint32_t zb[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) zb[j] = __float_as_uint(z[j]);
-        store_box_tma(&p.z_map, zbuf, true, vc, row_base, zb);
+        store_box_tma(&p.z_map, zbuf, vc, row_base, zb);
       }
       if (ragged) {
 #pragma unroll
@@ -554,17 +545,44 @@ struct EpiStore {
     const int64_t row_base = u.row0 + (warp % kEpilogueWarps) * 32;
     if (row_base >= p.rows) return;  // this warp's 32 rows are past the output
     uint8_t* buf = warp_stage_buffer(epi_smem, grp);
-    if (u.kb_count == 0) {  // no K blocks (all tokens ignored under compaction): the product is zero
-      uint32_t zero[32];
+    if (p.out_f32) {  // 32 x 32 fp32 boxes (128-byte rows)
+      if (u.kb_count == 0) {  // no K blocks (all tokens ignored under compaction): the product is zero
+        uint32_t zero[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) zero[j] = 0u;
+        for (int j = 0; j < 32; ++j) zero[j] = 0u;
 #pragma unroll 1
-      for (int c = 0; c < nch; ++c) store_box_tma(&p.out_map, buf, p.out_f32, col_tile + c * 32, row_base, zero);
+        for (int c = 0; c < nch; ++c) store_box_tma(&p.out_map, buf, col_tile + c * 32, row_base, zero);
+        return;
+      }
+      for_each_tmem_chunk(taddr, nch, [&](const uint32_t (&r)[32], int c) {
+        store_box_tma(&p.out_map, buf, col_tile + c * 32, row_base, r);
+      });
       return;
     }
-    for_each_tmem_chunk(taddr, nch, [&](const uint32_t (&r)[32], int c) {
-      store_box_tma(&p.out_map, buf, p.out_f32, col_tile + c * 32, row_base, r);
-    });
+    // bf16: 32 x 64 boxes, so that every row of a box is one whole 128-byte line; the two TMEM
+    // chunks of a box are packed to bf16 pairs and staged like an fp32 box (128-byte rows).
+#pragma unroll 1
+    for (int q = 0; 2 * q < nch; ++q) {
+      uint32_t w[32];
+      if (u.kb_count == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = 0u;
+      } else {
+        const bool has_b = 2 * q + 1 < nch;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + q * 64, ra);
+        if (has_b) tmem_ld32(taddr + q * 64 + 32, rb);
+        tmem_ld_wait(ra);
+        if (has_b) tmem_ld_wait(rb);
+        const auto f = [](uint32_t x) { return __uint_as_float(x); };
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          w[j] = pack_bf16x2(f(ra[2 * j]), f(ra[2 * j + 1]));
+          w[16 + j] = has_b ? pack_bf16x2(f(rb[2 * j]), f(rb[2 * j + 1])) : 0u;
+        }
+      }
+      store_box_tma(&p.out_map, buf, col_tile + q * 64, row_base, w);
+    }
   }
 
   __device__ static void end_unit(const Params&, const Unit&, State&, int) {}
@@ -771,13 +789,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- producer
     if (elect_one()) {
       uint32_t stage = 0, phase = 0;
-      uint32_t issued_phase[kStages];
-      bool issued[kStages];
-#pragma unroll
-      for (int s = 0; s < kStages; ++s) {
-        issued[s] = false;
-        issued_phase[s] = 0;
-      }
+      // Stages this thread has issued copies into, and the phase of the last
+      // copy of each (bit masks: registers, not a local array).
+      uint32_t issued = 0u, issued_phase = 0u;
       for (int uu = blockIdx.x; uu < lim.total_units; uu += gridDim.x) {
         const Unit u = decode_unit(sc, uu, kBM, 0, lim);
         if (u.skip) continue;
@@ -811,8 +825,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < kBN / 64; ++j)
                   tma_load_2d(sb + j * kMnAtomBytes, mb, fb, sc.b_mn_off + n * kBN + 64 * j, sc.b_k_off + k);
               }
-              issued[stage] = true;
-              issued_phase[stage] = phase;
+              issued |= 1u << stage;
+              issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
               if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -825,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every copy this thread issued must land before the CTA may exit.
 #pragma unroll
       for (int s = 0; s < kStages; ++s)
-        if (issued[s]) mbar_wait_teardown(&sm.full[s], issued_phase[s]);
+        if ((issued >> s) & 1u) mbar_wait_teardown(&sm.full[s], (issued_phase >> s) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
@@ -1006,13 +1020,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- producers (both CTAs)
     if (elect_one()) {
       uint32_t stage = 0, phase = 0;
-      uint32_t issued_phase[kStagesPair];
-      bool issued[kStagesPair];
-#pragma unroll
-      for (int s = 0; s < kStagesPair; ++s) {
-        issued[s] = false;
-        issued_phase[s] = 0;
-      }
+      // Stages this thread has issued copies into, and the phase of the last
+      // copy of each (bit masks: registers, not a local array).
+      uint32_t issued = 0u, issued_phase = 0u;
       bool ok = true;
       for (int uu = cid; ok && uu < lim.total_units; uu += ncl) {
         const Unit u = decode_unit(sc, uu, kTileRows, rank, lim);
@@ -1048,8 +1058,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < kBN / 128; ++j)
                   tma_load_2d_pair(sb + j * kMnAtomBytes, mb, fb, b_col + 64 * j, sc.b_k_off + k);
               }
-              issued[stage] = true;
-              issued_phase[stage] = phase;
+              issued |= 1u << stage;
+              issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
               if (++stage == kStagesPair) {
                 stage = 0;
                 phase ^= 1u;
@@ -1063,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
 #pragma unroll
         for (int s = 0; s < kStagesPair; ++s)
-          if (issued[s]) mbar_wait_teardown(&sm.full[s], issued_phase[s]);
+          if ((issued >> s) & 1u) mbar_wait_teardown(&sm.full[s], (issued_phase >> s) & 1u);
       }
     }
   } else if (warp == kMmaWarp) {

@@ -165,10 +165,10 @@ struct ZGradParams {
 };
 
 // Plain store of the accumulator (dW, and the test GEMM), through TMA stores:
-// each epilogue warp stages its 32 rows x 32 columns in shared memory
+// each epilogue warp stages 32 rows x 128 bytes in shared memory
 // (kStoreStageBytes per warp) and one lane copies the box out.
 struct StoreParams {
-  CUtensorMap out_map;    // [rows][cols] in the output dtype, box 32 x 32, 64-byte (bf16) / 128-byte (fp32) swizzle
+  CUtensorMap out_map;    // [rows][cols] in the output dtype: fp32 boxes 32 x 32, bf16 boxes 32 x 64; 128-byte swizzle
   int64_t rows, cols;     // valid extent of the output
   int32_t out_f32;
 };
