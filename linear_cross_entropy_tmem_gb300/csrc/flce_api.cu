@@ -28,6 +28,12 @@ namespace {
 
 constexpr int kAbiVersion = 3;
 constexpr int kMaxSplits = 64;                     // forward vocabulary splits
+// A batch of at most two CTA-pair tiles of tokens has too few m tiles for 64
+// splits to fill the GPU; it may split the vocabulary further, so that the
+// product runs on CTA pairs (which read each head tile once per pair instead
+// of once per 128-row CTA).  Its split records stay small (<= 5 MB).
+constexpr int kMaxSplitsSmall = 256;
+constexpr int64_t kSmallBatchRows = 512;
 constexpr int kMaxKSplit = 16;                     // dh K splits
 constexpr size_t kGChunkBudget = size_t(1) << 30;  // bytes of the bf16 G chunk
 // Token-chunked backward: bytes of the kept fp32 logits + bf16 G of one chunk,
@@ -41,6 +47,8 @@ constexpr int64_t kKeepLogitsMinHidden = 1280;
 constexpr int kMaxDevices = 64;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// Largest forward split count for a product over `rows` tokens.
+int max_splits(int64_t rows) { return rows <= kSmallBatchRows ? kMaxSplitsSmall : kMaxSplits; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct DeviceInfo {
@@ -356,7 +364,7 @@ Layout make_token_layout(const flce_problem* p, bool has_bias) {
     L.c_dloss = take(size_t(N) * 4);
     L.c_chunk_rows = take(size_t(L.n_tchunks) * 4);
   }
-  const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN)) * kEpilogueGroups;
+  const int64_t splits = std::min<int64_t>(max_splits(L.nc), cdiv(V, kBN)) * kEpilogueGroups;
   const size_t part = size_t(splits) * L.nc * 4;
   L.part_m = take(part);
   L.part_s = take(part);
@@ -407,7 +415,7 @@ Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
   const size_t region = off;
   size_t end = off;
   if (kind != kBackward) {
-    const int64_t splits = std::min<int64_t>(kMaxSplits, cdiv(V, kBN)) * kEpilogueGroups;
+    const int64_t splits = std::min<int64_t>(max_splits(N), cdiv(V, kBN)) * kEpilogueGroups;
     const size_t part = size_t(splits) * N * 4;
     L.part_m = take(part);
     L.part_s = take(part);
@@ -454,12 +462,12 @@ void finish_sched(GemmSched& s) {
   s.total_units = s.m_tiles * s.n_units * s.ksplit;
 }
 
-// Forward vocabulary split: the split count (<= kMaxSplits) that best fills
+// Forward vocabulary split: the split count (<= max_s) that best fills
 // the SMs with equal units; ties go to fewer splits.
-int choose_splits(int64_t m_tiles, int64_t n_tiles, int num_sms, int* per_unit) {
+int choose_splits(int64_t m_tiles, int64_t n_tiles, int64_t max_splits, int num_sms, int* per_unit) {
   double best_eff = -1.0;
   int best_s = 1, best_per = static_cast<int>(n_tiles);
-  const int64_t max_s = std::min<int64_t>(kMaxSplits, n_tiles);
+  const int64_t max_s = std::min<int64_t>(max_splits, n_tiles);
   for (int64_t s = 1; s <= max_s; ++s) {
     const int64_t per = cdiv(n_tiles, s);
     const int64_t splits = cdiv(n_tiles, per);
@@ -486,10 +494,11 @@ struct FwdPlan {
 };
 FwdPlan plan_forward(int64_t rows, int64_t V, int num_sms) {
   FwdPlan f;
-  f.pair = use_pair(rows, std::min<int64_t>(kMaxSplits, cdiv(V, kBN)), num_sms);
+  const int max_s = max_splits(rows);
+  f.pair = use_pair(rows, std::min<int64_t>(max_s, cdiv(V, kBN)), num_sms);
   f.per_unit = 1;
-  f.splits = choose_splits(cdiv(rows, f.pair ? kPairRows : kBM), cdiv(V, kBN), f.pair ? num_sms / 2 : num_sms,
-                           &f.per_unit);
+  f.splits = choose_splits(cdiv(rows, f.pair ? kPairRows : kBM), cdiv(V, kBN), max_s,
+                           f.pair ? num_sms / 2 : num_sms, &f.per_unit);
   return f;
 }
 
@@ -821,9 +830,12 @@ struct DhPlan {
   int ctas;
   int ksplit;
 };
+// A dh product with few output tiles splits K to fill the GPU, so the units
+// per 256-row tile row count its K splits too (CTA pairs then read each W tile
+// once per pair instead of once per 128-row CTA).
 DhPlan plan_recompute_dh(const Layout& L, int64_t N, int64_t D, int num_sms) {
   DhPlan d;
-  d.pair = use_pair(N, cdiv(D, kBN), num_sms);
+  d.pair = use_pair(N, cdiv(D, kBN) * L.ksplit_max, num_sms);
   d.ctas = d.pair ? num_sms / 2 : num_sms;
   const int64_t tiles = cdiv(N, d.pair ? kPairRows : kBM) * cdiv(D, kBN);
   d.ksplit = L.ksplit_max > 1 ? choose_recompute_ksplit(tiles, d.ctas, L.ksplit_max) : 1;
@@ -831,7 +843,7 @@ DhPlan plan_recompute_dh(const Layout& L, int64_t N, int64_t D, int num_sms) {
 }
 DhPlan plan_token_dh(const Layout& L, int64_t D, int num_sms) {
   DhPlan d;
-  d.pair = use_pair(L.nc, cdiv(D, kBN), num_sms);
+  d.pair = use_pair(L.nc, cdiv(D, kBN) * L.ksplit_max, num_sms);
   d.ctas = d.pair ? num_sms / 2 : num_sms;
   d.ksplit = choose_token_ksplit(cdiv(L.nc, d.pair ? kPairRows : kBM) * cdiv(D, kBN), d.ctas, L.ksplit_max);
   return d;

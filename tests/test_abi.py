@@ -79,8 +79,10 @@ def test_workspace_size_needs_no_gpu_and_never_scales_with_n_times_v(lib):
         # its per-tile dbias sums (1/64 of it in fp32 per 128 rows), the fp32 hi/lo
         # split (4 N D bytes at most) and the fp32 dh slots (4 N D bytes each: one per
         # K split, at most 8 once the dh product has 128 tiles of 128 x 256)
-        # five 4-byte split records per token, up to 64 splits x 2 epilogue groups, + z[target]
-        assert fw <= (5 * 4 * 64 * 2 + 4) * N + (1 << 20)
+        # five 4-byte split records per token, up to 64 splits x 2 epilogue groups (256 splits for
+        # a batch of at most 512 tokens), + z[target]
+        max_splits = 256 if N <= 512 else 64
+        assert fw <= (5 * 4 * max_splits * 2 + 4) * N + (1 << 20)
         slots = 8 if -(-N // 128) * -(-D // 256) >= 128 else 16
         assert bw <= (1 << 30) + (1 << 30) // 64 + (1 + slots) * 4 * N * D + (1 << 20)
         # the G chunk covers at most about half of the vocabulary
@@ -137,7 +139,7 @@ def test_keep_logits_workspace(lib):
         # kept logits + G and the dbias partials of one chunk, fp32 dbias and dW accumulators, dh
         # K-split slots (at most 16), split records of one chunk
         bound = 6 * min(half, N) * ldz + 4 * ((half + 31) // 32) * ldz + 4 * ldz + 4 * V * D + 16 * 4 * half * D \
-            + (5 * 4 * 64 * 2 + 8) * half + (1 << 20)
+            + (5 * 4 * (256 if N <= 512 else 64) * 2 + 8) * half + (1 << 20)
         assert r < k <= bound
         if N * V >= 1 << 28:  # the chunk's kept logits + G stay within the 4 GiB budget (+ one row group)
             assert k - 4 * V * D - 16 * 4 * half * D - 4 * ((half + 31) // 32) * ldz <= (4 << 30) + 6 * 256 * ldz \
@@ -156,7 +158,8 @@ def test_keep_logits_workspace(lib):
         rows = (N + 31) // 32 * 32
         st, k = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=keep), 2)
         assert st == B.FLCE_OK
-        assert 6 * rows * ldz < k <= 6 * rows * ldz + 4 * rows * ldz // 32 + 16 * 4 * 256 * D + (1 << 20)
+        assert 6 * rows * ldz < k <= 6 * rows * ldz + 4 * rows * ldz // 32 + 16 * 4 * 256 * D \
+            + (5 * 4 * 256 * 2 + 8) * rows + (1 << 20)
         assert k < 4 * V * D  # in particular no fp32 dW accumulator
 
 
@@ -175,7 +178,8 @@ def test_keep_logits_workspace_has_no_tokens_times_vocab_term(lib):
         for flags in (keep, keep | B.FLCE_FLAG_COMPACT_VALID):
             st, k = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=flags), 2)
             assert st == B.FLCE_OK
-            chunk = 6 * nc * ldz + 4 * ldz * ((nc + 31) // 32) + 16 * 4 * nc * D + (5 * 4 * 64 * 2 + 8) * nc
+            splits = 256 if nc <= 512 else 64
+            chunk = 6 * nc * ldz + 4 * ldz * ((nc + 31) // 32) + 16 * 4 * nc * D + (5 * 4 * splits * 2 + 8) * nc
             linear = N * (20 + 2 * D) + 32 * (N // 256 + 1)
             assert k <= chunk + 4 * V * D + 4 * ldz + linear + (1 << 20), (N, flags, k)
             sizes[(N, flags)] = k

@@ -66,21 +66,25 @@ def test_qwen_like_plans(lib):
 
 
 def test_one_chunk_plan(lib):
-    """N=256, D=2048, V=248320: 16 single-CTA dh tiles on 152 SMs take 9 K splits (144 units,
-    95 % of one wave), as before the wave rule; the two 124160-column chunks stay, because a third
-    chunk costs more than the one dW wave (K = 256, ~1 us) it would save."""
+    """N=256, D=2048, V=248320: the dh product has 8 pair tiles; counted with its up to 16 K splits
+    they fill the 76 pairs, so it runs on CTA pairs, and 9 K splits (72 units, 95 % of one wave) win
+    (ahead of 8 splits at 84 %); the two 124160-column chunks stay, because a third chunk costs more
+    than the one dW wave (K = 256, ~1 us) it would save."""
     info = _plan(lib, _problem(256, 2048, 248320, reduction=B.FLCE_RED_SUM), 1)
-    assert info.keep_logits == 0 and info.dh_pair == 0
+    assert info.keep_logits == 0 and info.dh_pair == 1
     assert info.vocab_chunk_cols == 124160 and info.run_chunk_cols == 124160 and info.n_chunks == 2
     assert info.dh_ksplit == 9
 
 
 def test_one_chunk_fused_plan_keeps_logits(lib):
     """The fused call on the same shape keeps the logits of its one 256-token chunk (D = 2048 >= 1280):
-    the dh product over K = V has the same 16 single-CTA tiles and 9 K splits."""
+    the dh product over K = V runs on the same 8 pair tiles with 9 K splits.  Its forward has one
+    256-row pair tile: 64 vocabulary splits could not fill 76 pairs, so a batch this small may split
+    further, and 75 splits of 13 of the 970 vocabulary tiles fill one wave (98.2 %)."""
     info = _plan(lib, _problem(256, 2048, 248320, reduction=B.FLCE_RED_SUM), 2)
     assert info.keep_logits == 1 and info.n_chunks == 1 and info.token_chunk_rows == 256
-    assert info.dh_pair == 0 and info.dh_ksplit == 9
+    assert info.dh_pair == 1 and info.dh_ksplit == 9
+    assert (info.fwd_pair, info.fwd_splits, info.fwd_tiles_per_split) == (1, 75, 13)
     small = _plan(lib, _problem(70, 2048, 248320), 2)
     assert small.keep_logits == 1 and small.n_chunks == 1 and small.token_chunk_rows == 96
 
@@ -138,7 +142,8 @@ def test_plan_invariants(lib, sms):
             info = _plan(lib, _problem(N, D, V), fb, sms)
             assert 1 <= info.dh_ksplit <= info.dh_ksplit_max <= 16
             n_t = cdiv(V, 256)
-            assert 1 <= info.fwd_splits <= min(64, n_t)
+            fwd_rows = info.token_chunk_rows if info.keep_logits else N
+            assert 1 <= info.fwd_splits <= min(256 if fwd_rows <= 512 else 64, n_t)
             assert info.fwd_splits == cdiv(n_t, info.fwd_tiles_per_split)  # no empty split
             if info.keep_logits:
                 assert fb == 2 and D >= 1280
