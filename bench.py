@@ -356,8 +356,9 @@ def committed_traffic(kind, workload, backward):
 
 def kernel_model(w, keep, rows, launches, h_terms, grad_h_terms):
     """Algorithmic work of each launch kind over one step: flops (2 per multiply-add of the
-    product) and the bytes the kind must move to do its part (operands read, results written),
-    counting the re-reads and accumulator traffic that the chosen algorithm itself implies.
+    product) and the bytes the kind must read and write to do its part (operands read, results
+    written), counting the re-reads and accumulator traffic that the chosen algorithm itself
+    implies.  Returns {kind: (flops, bytes read, bytes written)}.
 
     rows: tokens the products run over; launches: {kind: launches per step}; h_terms: bf16 terms the
     logit products read of the hidden state (1 for bf16, 2 or 3 for fp32); grad_h_terms: those the
@@ -369,18 +370,39 @@ def kernel_model(w, keep, rows, launches, h_terms, grad_h_terms):
     prod = 2.0 * R * V * D
     if keep:
         nc = max(1, launches.get("bwd_logit_grad", 1))
-        out["fwd_logits"] = (prod, 2 * h_terms * R * D + 2 * nc * V * D + 4 * R * V)
-        out["bwd_logit_grad"] = (0.0, 6 * R * V)
-        out["bwd_dhidden"] = (prod, 2 * R * V + 2 * nc * V * D + eh * R * D)
-        acc = 2 * V * D if nc == 1 else 8 * V * D * (nc - 1) + 2 * V * D
-        out["bwd_dweight"] = (prod, 2 * R * V + 2 * grad_h_terms * R * D + acc)
+        out["fwd_logits"] = (prod, 2 * h_terms * R * D + 2 * nc * V * D, 4 * R * V)
+        out["bwd_logit_grad"] = (0.0, 4 * R * V, 2 * R * V)
+        out["bwd_dhidden"] = (prod, 2 * R * V + 2 * nc * V * D, eh * R * D)
+        out["bwd_dweight"] = (prod, 2 * R * V + 2 * grad_h_terms * R * D + 4 * V * D * (nc - 1),
+                              4 * V * D * (nc - 1) + 2 * V * D)
     else:
         nv = max(1, launches.get("bwd_recompute", 1))
-        out["fwd_logits"] = (prod, 2 * h_terms * R * D + 2 * V * D)
-        out["bwd_recompute"] = (prod, 2 * nv * h_terms * R * D + 2 * V * D + 2 * R * V)
-        out["bwd_dweight"] = (prod, 2 * R * V + 2 * nv * grad_h_terms * R * D + 2 * V * D)
-        out["bwd_dhidden"] = (prod, 2 * R * V + 2 * V * D + 4 * R * D * (2 * nv - 1) + eh * R * D)
+        out["fwd_logits"] = (prod, 2 * h_terms * R * D + 2 * V * D, 0.0)
+        out["bwd_recompute"] = (prod, 2 * nv * h_terms * R * D + 2 * V * D, 2 * R * V)
+        out["bwd_dweight"] = (prod, 2 * R * V + 2 * nv * grad_h_terms * R * D, 2 * V * D)
+        out["bwd_dhidden"] = (prod, 2 * R * V + 2 * V * D + 4 * R * D * (nv - 1), 4 * R * D * (nv - 1) + eh * R * D)
     return out
+
+
+def write_bandwidth(device):
+    """Pure HBM write bandwidth measured live: best of 5 memsets of 1 GiB (GB/s).  On GB300 it is
+    well below the copy bandwidth (writes alone do not reach the read + write rate of a copy), so
+    the floor of a kernel that mostly writes is its written bytes at this rate."""
+    import torch
+    x = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    for _ in range(3):
+        x.zero_()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        x.zero_()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del x
+    return (1 << 30) / (best * 1e-3) / 1e9
 
 
 def pick_workload(args):
@@ -494,6 +516,7 @@ def flce_arm(args):
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    write_gbs = write_bandwidth(device)
     # a kernel inside a timed region of half a second or more runs under the sustained power cap
     timed_s = ms * args.steps * 1e-3
     peak_f, peak_f_kind = (peak_sus, "sustained") if timed_s >= 0.5 else (peak_burst, "burst")
@@ -501,12 +524,17 @@ def flce_arm(args):
     for k, (n_l, t_ms) in sorted(per_kind.items()):
         e = {"launches": n_l, "ms_per_step": t_ms / args.steps}
         if k in model:
-            fl, by = model[k]
+            fl, rd, wr = model[k]
             t_s = t_ms * 1e-3 / args.steps
-            tensor = fl / (peak_f * 1e12) >= by / (peak_bw * 1e9)
-            e.update({"flops_per_step": fl, "bytes_per_step": by, "tflops": fl / t_s / 1e12 if fl else None,
-                      "gbs": by / t_s / 1e9, "bound": "tensor" if tensor else "hbm",
-                      "frac": (fl / t_s / 1e12 / peak_f) if tensor else (by / t_s / 1e9 / peak_bw)})
+            floors = {"tensor": fl / (peak_f * 1e12), "hbm": (rd + wr) / (peak_bw * 1e9),
+                      "hbm_write": wr / (write_gbs * 1e9)}
+            limit = max(floors, key=floors.get)
+            tensor = limit == "tensor"
+            e.update({"flops_per_step": fl, "bytes_per_step": rd + wr, "bytes_written_per_step": wr,
+                      "tflops": fl / t_s / 1e12 if fl else None, "gbs": (rd + wr) / t_s / 1e9,
+                      "bound": "tensor" if tensor else "hbm",
+                      "frac": (fl / t_s / 1e12 / peak_f) if tensor else ((rd + wr) / t_s / 1e9 / peak_bw),
+                      "floor": limit, "frac_of_floor": floors[limit] / t_s})
         kernels[k] = e
     dominant = max(model, key=lambda k: per_kind.get(k, [0, 0.0])[1])
     dk = kernels[dominant]
@@ -519,8 +547,11 @@ def flce_arm(args):
                 "peak_kind": f"HBM copy bandwidth ({peak_src})"}
     roof.update({"kernel": dominant, "frac": roof["achieved"] / roof["peak"],
                  "flops_per_launch": model[dominant][0] / max(1, n_l // args.steps),
-                 "bytes_per_launch": model[dominant][1] / max(1, n_l // args.steps),
-                 "launches": n_l, "avg_launch_ms": t_ms / n_l})
+                 "bytes_per_launch": (model[dominant][1] + model[dominant][2]) / max(1, n_l // args.steps),
+                 "launches": n_l, "avg_launch_ms": t_ms / n_l,
+                 # the largest of the tensor, HBM and HBM-write floors, over the measured time
+                 "floor": dk["floor"], "frac_of_floor": dk["frac_of_floor"],
+                 "hbm_write_gbs_measured": write_gbs})
 
     ms_max = max_over_ranks(dist, ms, device)
     tokens = w.n_tokens * world
