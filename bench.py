@@ -63,7 +63,7 @@ def parse_args(argv=None):
                     help="with --autograd: the separate backward instead of gradients in the forward")
     ap.add_argument("--bwd", default="auto", choices=["auto", "recompute", "keep_logits"],
                     help="backward algorithm of the fused call (FLCE_FLAG_BWD_*); auto keeps the logits of "
-                         "token chunks from D = 1280 up")
+                         "token chunks from D = 1152 up")
     ap.add_argument("--compact", action="store_true",
                     help="gather the valid tokens first (FLCE_FLAG_COMPACT_VALID)")
     ap.add_argument("--token-chunk", type=int, default=0,

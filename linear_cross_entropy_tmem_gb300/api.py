@@ -231,7 +231,7 @@ class LinearCrossEntropy(torch.autograd.Function):
 
     With ``grad_in_forward`` (the default) and a mean or sum loss, the forward already computes the
     gradients for an upstream gradient of 1 in one fused call (``flce_forward_backward``, which keeps
-    the logits of token chunks from D = 1280 up), and the backward scales them by the upstream
+    the logits of token chunks from D = 1152 up), and the backward scales them by the upstream
     gradient in place (``flce_scale_gradient``; nothing happens for the usual 1).  Gradients are linear
     in a scalar upstream gradient, so this is the same result up to one rounding.  A second backward
     through the same graph recomputes them (``flce_backward``) instead of rescaling."""

@@ -40,10 +40,10 @@ constexpr size_t kGChunkBudget = size_t(1) << 30;  // bytes of the bf16 G chunk
 // and the smallest hidden size for which the automatic choice keeps logits:
 // below it the recompute's 2*D flops per logit cost less than the 6 bytes per
 // logit of the extra pass over the kept logits (measured on GB300 at
-// N = 16384, V = 151936: the recompute is faster at D = 1152, kept logits at
-// D = 1280).
+// N = 16384, V = 151936: the recompute is faster at D = 1024, kept logits at
+// D = 1152).
 constexpr size_t kLogitChunkBudget = size_t(4) << 30;
-constexpr int64_t kKeepLogitsMinHidden = 1280;
+constexpr int64_t kKeepLogitsMinHidden = 1152;
 constexpr int kMaxDevices = 64;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }

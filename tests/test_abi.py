@@ -126,7 +126,7 @@ def test_fp32_terms_workspace(lib):
 def test_keep_logits_workspace(lib):
     """The token-chunked backward keeps fp32 logits + bf16 G for at most half of the tokens (a batch
     of at most 256 tokens is one chunk), the dbias partials of one chunk and an fp32 dbias and dW
-    accumulator; the automatic choice keeps logits from D = 1280 up."""
+    accumulator; the automatic choice keeps logits from D = 1152 up."""
     keep, rec = B.FLCE_FLAG_BWD_KEEP_LOGITS, B.FLCE_FLAG_BWD_RECOMPUTE
     for (N, D, V) in [(16384, 4096, 151936), (16384, 640, 262144), (8192, 2048, 128256), (4096, 1024, 50000),
                       (300, 200, 1000), (257, 136, 777)]:
@@ -134,7 +134,7 @@ def test_keep_logits_workspace(lib):
         ws = {f: _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=f), 2) for f in (0, keep, rec)}
         assert all(st == B.FLCE_OK for st, _ in ws.values())
         k, r, a = ws[keep][1], ws[rec][1], ws[0][1]
-        assert a == (k if D >= 1280 else r)
+        assert a == (k if D >= 1152 else r)
         half = ((N + 1) // 2 + 255) // 256 * 256
         # kept logits + G and the dbias partials of one chunk, fp32 dbias and dW accumulators, dh
         # K-split slots (at most 16), split records of one chunk

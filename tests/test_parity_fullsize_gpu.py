@@ -22,7 +22,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.fullsize]
 
 
 def _run(h, W, b, t, dloss, entry, compact, kw):
-    """The fused call (automatic backward: kept logits from D = 1280 up, else the recompute), as
+    """The fused call (automatic backward: kept logits from D = 1152 up, else the recompute), as
     bench.py times it, or flce_forward followed by flce_backward."""
     import linear_cross_entropy_tmem_gb300 as F
     if entry == "separate":

@@ -77,7 +77,7 @@ def test_one_chunk_plan(lib):
 
 
 def test_one_chunk_fused_plan_keeps_logits(lib):
-    """The fused call on the same shape keeps the logits of its one 256-token chunk (D = 2048 >= 1280):
+    """The fused call on the same shape keeps the logits of its one 256-token chunk (D = 2048 >= 1152):
     the dh product over K = V runs on the same 8 pair tiles with 9 K splits.  Its forward has one
     256-row pair tile: 64 vocabulary splits could not fill 76 pairs, so a batch this small may split
     further, and 75 splits of 13 of the 970 vocabulary tiles fill one wave (98.2 %)."""
@@ -146,7 +146,7 @@ def test_plan_invariants(lib, sms):
             assert 1 <= info.fwd_splits <= min(256 if fwd_rows <= 512 else 64, n_t)
             assert info.fwd_splits == cdiv(n_t, info.fwd_tiles_per_split)  # no empty split
             if info.keep_logits:
-                assert fb == 2 and D >= 1280
+                assert fb == 2 and D >= 1152
                 if N > 256:  # at least two chunks: the kept logits never cover the whole batch
                     assert info.token_chunk_rows % 256 == 0
                     assert info.token_chunk_rows <= cdiv(cdiv(N, 2), 256) * 256
@@ -154,7 +154,7 @@ def test_plan_invariants(lib, sms):
                 else:  # one chunk of the batch's rows, rounded up to 32
                     assert info.token_chunk_rows == cdiv(N, 32) * 32 and info.n_chunks == 1
             else:
-                assert fb == 1 or D < 1280
+                assert fb == 1 or D < 1152
                 vc, run = info.vocab_chunk_cols, info.run_chunk_cols
                 assert vc % 256 == 0 and run % 256 == 0
                 assert run <= vc and run >= max(1, vc // 256 // 2) * 256  # widths down to half the tiles
@@ -163,15 +163,15 @@ def test_plan_invariants(lib, sms):
 
 
 def test_backward_algorithm_follows_flags(lib):
-    """The fused call keeps logits from D = 1280 up (a batch of at most 256 tokens as one chunk);
+    """The fused call keeps logits from D = 1152 up (a batch of at most 256 tokens as one chunk);
     FLCE_FLAG_BWD_RECOMPUTE and FLCE_FLAG_BWD_KEEP_LOGITS force either algorithm, with and without
     valid-token compaction and fp32 hidden states.  flce_backward always recomputes."""
     rec, keep, cmp_ = B.FLCE_FLAG_BWD_RECOMPUTE, B.FLCE_FLAG_BWD_KEEP_LOGITS, B.FLCE_FLAG_COMPACT_VALID
     for extra in (0, cmp_):
         for dt in (B.FLCE_BF16, B.FLCE_F32):
             kw = dict(hidden_dtype=dt)
-            assert _plan(lib, _problem(4096, 1280, 50000, flags=extra, **kw), 2).keep_logits == 1
-            assert _plan(lib, _problem(4096, 1152, 50000, flags=extra, **kw), 2).keep_logits == 0
+            assert _plan(lib, _problem(4096, 1152, 50000, flags=extra, **kw), 2).keep_logits == 1
+            assert _plan(lib, _problem(4096, 1024, 50000, flags=extra, **kw), 2).keep_logits == 0
             assert _plan(lib, _problem(4096, 1280, 50000, flags=extra | rec, **kw), 2).keep_logits == 0
             assert _plan(lib, _problem(4096, 640, 50000, flags=extra | keep, **kw), 2).keep_logits == 1
             assert _plan(lib, _problem(256, 4096, 50000, flags=extra | keep, **kw), 2).keep_logits == 1
