@@ -372,7 +372,7 @@ Layout make_token_layout(const flce_problem* p, bool has_bias) {
   L.part_best = take(part);
   L.part_idx = take(part);
   L.z_target = take(size_t(L.nc) * 4);
-  L.blocks = take(size_t(cdiv(N, kMergeThreads)) * sizeof(BlockPartial));
+  L.blocks = take(size_t(cdiv(N, kMergeRows)) * sizeof(BlockPartial));
   L.z = take(size_t(L.nc) * L.ldz * 4);
   L.zg = take(size_t(L.nc) * L.ldz * 2);
   if (has_bias) L.dbias_part = take(size_t(cdiv(L.nc, kZGradRows)) * L.ldz * 4);
@@ -423,7 +423,7 @@ Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
     L.part_best = take(part);
     L.part_idx = take(part);
     L.z_target = take(size_t(N) * 4);
-    L.blocks = take(size_t(cdiv(N, kMergeThreads)) * sizeof(BlockPartial));
+    L.blocks = take(size_t(cdiv(N, kMergeRows)) * sizeof(BlockPartial));
     end = std::max(end, off);
   }
   if (kind != kForward) {
@@ -666,7 +666,7 @@ ReduceParams reduce_params(const flce_problem* p, const Layout& L, uint8_t* ws, 
                            int64_t* n_valid, float* entropy_sum) {
   ReduceParams rp{};
   rp.blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
-  rp.n_blocks = static_cast<int32_t>(cdiv(p->n_tokens, kMergeThreads));
+  rp.n_blocks = static_cast<int32_t>(cdiv(p->n_tokens, kMergeRows));
   rp.reduction = p->reduction;
   rp.num_items = p->num_items_in_batch;
   rp.loss = loss;
@@ -1105,7 +1105,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     mp.lse = lse + o0;
     mp.entropy = entropy ? entropy + o0 : nullptr;
     mp.loss_tok = none ? loss + o0 : nullptr;
-    mp.blocks = blocks + r0 / kMergeThreads;  // r0 % kMergeThreads == 0
+    mp.blocks = blocks + r0 / kMergeRows;  // r0 % kMergeRows == 0
     mp.row_map = rmap;
     mp.row_count = lim;
     mp.lse_compact = pr.cmp ? pr.c_lse + r0 : nullptr;

@@ -64,10 +64,12 @@ cudaError_t launch_split_f32(const float* x, uint16_t* t0, uint16_t* t1, uint16_
 }
 
 // ---------------------------------------------------------------------------
-// Merge of the split partials (one thread per token) and block partial sums.
+// Merge of the split partials and block partial sums.  One warp per token at
+// a time (kMergeRows / 8 tokens per warp); lane l takes the records l, l + 32,
+// ..., and the lanes combine their results in a fixed butterfly order.
 //   M = max_s m_s, S = sum_s s_s e^(m_s - M), A = sum_s a_s e^(m_s - M)
 //   lse = M + ln S, sum p z = A / S, entropy = lse - A / S
-//   argmax: largest best_s, the earliest split on ties (lowest index)
+//   argmax: the largest best_s, the lowest index on ties
 // ---------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ T warp_sum(T v) {
@@ -76,21 +78,32 @@ __device__ __forceinline__ T warp_sum(T v) {
   return v;
 }
 
+// Sum over the warp in a fixed butterfly order; every lane gets the result.
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p, int* status) {
-  const int64_t row = blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x;
-  double loss_d = 0.0, ent_d = 0.0;
-  long long corr = 0, val = 0;
+  constexpr int kWarps = kMergeThreads / 32;
+  constexpr int kPerWarp = kMergeRows / kWarps;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rows = p.row_count ? static_cast<int64_t>(*p.row_count) : p.n_tokens;
-  if (row < rows) {
-    const int64_t orow = p.row_map ? static_cast<int64_t>(p.row_map[row]) : row;
-    const int64_t N = p.n_tokens;
+  const int64_t N = p.n_tokens;
+  double loss_d = 0.0, ent_d = 0.0;  // this warp's tokens (lane 0)
+  long long corr = 0, val = 0;
+  for (int i = 0; i < kPerWarp; ++i) {
+    const int64_t row = blockIdx.x * static_cast<int64_t>(kMergeRows) + warp * kPerWarp + i;
+    if (row >= rows) break;  // uniform over the warp
     float M = -INFINITY;
-    for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, p.part_m[s * N + row]);
+    for (int s = lane; s < p.n_splits; s += 32) M = fmaxf(M, p.part_m[s * N + row]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float S = 0.f, A = 0.f, best = -INFINITY;
-    int32_t best_idx = 0;
-    for (int s = 0; s < p.n_splits; ++s) {
-      const float ms = p.part_m[s * N + row];
-      const float f = expf(ms - M);
+    int32_t best_idx = INT32_MAX;
+    for (int s = lane; s < p.n_splits; s += 32) {
+      const float f = expf(p.part_m[s * N + row] - M);
       S = fmaf(p.part_s[s * N + row], f, S);
       A = fmaf(p.part_a[s * N + row], f, A);
       const float b = p.part_best[s * N + row];
@@ -100,39 +113,48 @@ __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p,
         best_idx = bi;
       }
     }
-    const float lse = M + logf(S);
-    const float ent = lse - A / S;
-    const int64_t t = p.targets[row];
-    const bool in_range = t >= 0 && t < p.vocab;
-    const bool valid = in_range && t != p.ignore_index;
-    if (t != p.ignore_index && !in_range) atomicCAS(status, 0, kStatusTargetOutOfRange);
-    const float loss = valid ? lse - p.z_target[row] : 0.f;
-    p.lse[orow] = lse;
-    if (p.lse_compact) p.lse_compact[row] = lse;
-    if (p.entropy) p.entropy[orow] = ent;
-    if (p.loss_tok) p.loss_tok[orow] = loss;
-    loss_d = loss;
-    ent_d = valid ? ent : 0.0;
-    corr = (valid && best_idx == t) ? 1 : 0;
-    val = valid ? 1 : 0;
+    S = warp_allsum(S);
+    A = warp_allsum(A);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int32_t oi = __shfl_xor_sync(0xffffffffu, best_idx, o);
+      if (ob > best || (ob == best && oi < best_idx)) {
+        best = ob;
+        best_idx = oi;
+      }
+    }
+    if (lane == 0) {
+      const int64_t orow = p.row_map ? static_cast<int64_t>(p.row_map[row]) : row;
+      const float lse = M + logf(S);
+      const float ent = lse - A / S;
+      const int64_t t = p.targets[row];
+      const bool in_range = t >= 0 && t < p.vocab;
+      const bool valid = in_range && t != p.ignore_index;
+      if (t != p.ignore_index && !in_range) atomicCAS(status, 0, kStatusTargetOutOfRange);
+      const float loss = valid ? lse - p.z_target[row] : 0.f;
+      p.lse[orow] = lse;
+      if (p.lse_compact) p.lse_compact[row] = lse;
+      if (p.entropy) p.entropy[orow] = ent;
+      if (p.loss_tok) p.loss_tok[orow] = loss;
+      loss_d += loss;
+      ent_d += valid ? ent : 0.0;
+      corr += (valid && best_idx == t) ? 1 : 0;
+      val += valid ? 1 : 0;
+    }
   }
-  __shared__ double s_loss[kMergeThreads / 32], s_ent[kMergeThreads / 32];
-  __shared__ long long s_corr[kMergeThreads / 32], s_val[kMergeThreads / 32];
-  loss_d = warp_sum(loss_d);
-  ent_d = warp_sum(ent_d);
-  corr = warp_sum(corr);
-  val = warp_sum(val);
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) {
-    s_loss[w] = loss_d;
-    s_ent[w] = ent_d;
-    s_corr[w] = corr;
-    s_val[w] = val;
+  __shared__ double s_loss[kWarps], s_ent[kWarps];
+  __shared__ long long s_corr[kWarps], s_val[kWarps];
+  if (lane == 0) {
+    s_loss[warp] = loss_d;
+    s_ent[warp] = ent_d;
+    s_corr[warp] = corr;
+    s_val[warp] = val;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     BlockPartial bp{0.0, 0.0, 0, 0};
-    for (int i = 0; i < kMergeThreads / 32; ++i) {
+    for (int i = 0; i < kWarps; ++i) {
       bp.loss += s_loss[i];
       bp.entropy += s_ent[i];
       bp.correct += s_corr[i];
@@ -143,7 +165,7 @@ __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p,
 }
 
 cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream) {
-  const int64_t blocks = (p.n_tokens + kMergeThreads - 1) / kMergeThreads;
+  const int64_t blocks = (p.n_tokens + kMergeRows - 1) / kMergeRows;
   if (blocks == 0) return cudaSuccess;
   fwd_merge_kernel<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(p, status);
   return cudaGetLastError();

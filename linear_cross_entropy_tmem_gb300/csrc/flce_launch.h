@@ -51,7 +51,8 @@ struct ReduceParams {
   float* entropy_sum;
 };
 
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 256;  // threads per block of the merge: 8 warps, one token per warp at a time
+constexpr int kMergeRows = 32;      // tokens per block of the merge = per BlockPartial
 
 // GEMM launches.  `pair` selects the CTA-pair kernel (clusters of two CTAs,
 // 256-row tiles); `num_sms` bounds the persistent grid (CTAs, or 2 x clusters).
