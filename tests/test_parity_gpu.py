@@ -417,15 +417,17 @@ def test_keep_logits_with_compaction(name, ignore_every, mode):
                        oracle.backward(h, W, b, t, dloss=dloss, **kw), t, w.reduction)
 
 
+@pytest.mark.parametrize("n_tokens", [700, 200], ids=["chunks", "one-chunk"])
 @pytest.mark.parametrize("compact", [False, True], ids=["all-tokens", "compact"])
 @pytest.mark.parametrize("reduction,items", [("mean", 0.0), ("mean", 700.0), ("sum", 0.0), ("none", 0.0)])
-def test_keep_logits_reductions_and_all_ignored(reduction, items, compact):
+def test_keep_logits_reductions_and_all_ignored(reduction, items, compact, n_tokens):
     """The mean's denominator (counted before the first chunk, or num_items_in_batch), the other
-    reductions, and an all-ignored batch (zero loss, exact zero gradients) on the token path."""
+    reductions, and an all-ignored batch (zero loss, exact zero gradients) on the token path, with
+    several 256-token chunks and with a batch of at most 256 tokens as one chunk."""
     import linear_cross_entropy_tmem_gb300 as F
     from linear_cross_entropy_tmem_gb300.api import testing_set_token_chunk
     testing_set_token_chunk(256)
-    w = Workload("kl", 700, 256, 3000, sigma_w=0.1, bias=True, reduction=reduction, ignore_every=5, seed=11)
+    w = Workload("kl", n_tokens, 256, 3000, sigma_w=0.1, bias=True, reduction=reduction, ignore_every=5, seed=11)
     hc, Wc, bc, tc, dc = make_inputs(w, "cpu")
     for targets in (tc, torch.full_like(tc, -100)):
         h, W, b, t, dloss = [x.cuda() for x in (hc, Wc, bc, targets, dc)]
