@@ -24,7 +24,8 @@
  *   - Every pointer argument except `problem` and `status` is a DEVICE pointer
  *     owned by the caller.  The library allocates no device or host memory and
  *     keeps no state between calls other than a per-device cache of the SM
- *     count and kernel attributes.
+ *     count and kernel attributes (and, for flce_forward_noalloc, the address
+ *     of its static scratch array per CUDA context).
  *   - hidden, weight, dhidden, dweight and the workspace must be memory of
  *     the current device (its device memory, or managed memory): the tensor
  *     maps and the kernels address this GPU's memory only.  Host memory
