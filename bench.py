@@ -501,6 +501,21 @@ def flce_arm(args):
         if status.value != 0:
             raise RuntimeError(f"device status {status.value} during the timed region")
 
+    # The events that bracket every launch above also serialise the launches: the GEMMs, launched
+    # as programmatic dependents, cannot overlap their set-up with the previous kernel's end there.
+    # The same K steps again with events around whole steps only show what that costs (a few us
+    # per launch: visible on small heads, negligible on the large ones).
+    for k in range(args.steps):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
+        step_starts[k].record()
+        run.step()
+        step_ends[k].record()
+    torch.cuda.synchronize()
+    clean = [step_starts[k].elapsed_time(step_ends[k]) for k in range(args.steps)]
+    step_clean = {"p50": statistics.median(clean), "mean": sum(clean) / len(clean),
+                  "note": "the same K steps again, without the per-launch events of the timed region"}
+
     per_kind = {}
     for i in range(count.value):
         k = B.LAUNCH_KINDS[recs[i].kind]
@@ -648,6 +663,7 @@ def flce_arm(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "ms_per_step_quantiles": step_quantiles,
+            "ms_per_step_without_launch_events": step_clean,
             "vs_baseline": None, "dtype": "bf16" if w.hidden_dtype == torch.bfloat16 else "f32+bf16",
             "data": "synthetic",
             "config": {"workload": w.name, "n_tokens": w.n_tokens, "hidden": w.hidden, "vocab": w.vocab,

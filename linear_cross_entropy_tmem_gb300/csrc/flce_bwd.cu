@@ -35,6 +35,7 @@ cudaError_t launch_accum_gemm(bool pair, const TmaMaps& maps, const GemmSched& s
 // order.  Short tiles (32 rows) keep the last wave of blocks small.
 template <bool kSoftcap>
 __global__ void __launch_bounds__(kZGradThreads) zgrad_kernel(ZGradParams p) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   __shared__ float s_lse2[kZGradRows];  // lse * log2(e)
   __shared__ float s_wd[kZGradRows];    // w_n * s (0 at ignored rows)
   __shared__ int64_t s_t[kZGradRows];   // target column
@@ -120,17 +121,14 @@ cudaError_t launch_zgrad(const ZGradParams& p, bool softcap, cudaStream_t stream
   if (gx == 0 || row_tiles == 0) return cudaSuccess;
   if (gx > 65535) return cudaErrorInvalidConfiguration;
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(row_tiles < 65535 ? row_tiles : 65535));
-  if (softcap) {
-    zgrad_kernel<true><<<grid, kZGradThreads, 0, stream>>>(p);
-  } else {
-    zgrad_kernel<false><<<grid, kZGradThreads, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  if (softcap) return launch_plain(zgrad_kernel<true>, grid, dim3(kZGradThreads), 0, stream, p);
+  return launch_plain(zgrad_kernel<false>, grid, dim3(kZGradThreads), 0, stream, p);
 }
 
 // x[i] = rn(x[i] * s) in place (fp32 multiply, one rounding), s = *scale read
 // on the device; nothing is read or written when s == 1.
 __global__ void scale_kernel(const float* __restrict__ scale, void* x, int64_t n, int x_f32) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   const float s = __ldg(scale);
   if (s == 1.0f) return;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -147,8 +145,7 @@ __global__ void scale_kernel(const float* __restrict__ scale, void* x, int64_t n
 
 cudaError_t launch_scale(const float* scale, void* x, int64_t n, int x_f32, int grid, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
-  scale_kernel<<<grid, 256, 0, stream>>>(scale, x, n, x_f32);
-  return cudaGetLastError();
+  return launch_plain(scale_kernel, dim3(grid), dim3(256), 0, stream, scale, x, n, x_f32);
 }
 
 // dbias[j] = sum over m tiles of the per-tile column sums, in m order; with an
@@ -157,6 +154,7 @@ cudaError_t launch_scale(const float* scale, void* x, int64_t n, int x_f32, int 
 __global__ void dbias_reduce_kernel(const float* __restrict__ part, int64_t ldg, int m_tiles, int rows_per_tile,
                                     int64_t cols, void* dbias, int bias_f32, const int32_t* row_count, float* acc,
                                     int accumulate, int write_final) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (j >= cols) return;
   // Under compaction only the tiles that hold a valid token were computed.
@@ -182,9 +180,8 @@ cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int
                                 int write_final, cudaStream_t stream) {
   const int64_t blocks = (cols + 255) / 256;
   if (blocks == 0) return cudaSuccess;
-  dbias_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      part, ldg, m_tiles, rows_per_tile, cols, dbias, bias_f32, row_count, acc, accumulate, write_final);
-  return cudaGetLastError();
+  return launch_plain(dbias_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, part, ldg,
+                    m_tiles, rows_per_tile, cols, dbias, bias_f32, row_count, acc, accumulate, write_final);
 }
 
 // dh = sum over K-split slots, in slot order, cast to the output dtype; with a
@@ -193,6 +190,7 @@ cudaError_t launch_dbias_reduce(const float* part, int64_t ldg, int m_tiles, int
 __global__ void dh_finalize_kernel(const float4* __restrict__ part, int64_t stride4, int ksplit, int64_t rows,
                                    int64_t cols, void* out, int out_f32, const int32_t* row_map,
                                    const int32_t* row_count) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   const int64_t n4 = rows * cols / 4;
   const int64_t limit = row_count ? static_cast<int64_t>(*row_count) * cols / 4 : n4;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4 && i < limit;
@@ -221,9 +219,8 @@ __global__ void dh_finalize_kernel(const float4* __restrict__ part, int64_t stri
 cudaError_t launch_dh_finalize(const float* part, int64_t stride, int ksplit, int64_t rows, int64_t cols, void* out,
                                int out_f32, const int32_t* row_map, const int32_t* row_count, int grid,
                                cudaStream_t stream) {
-  dh_finalize_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(part), stride / 4, ksplit, rows, cols,
-                                               out, out_f32, row_map, row_count);
-  return cudaGetLastError();
+  return launch_plain(dh_finalize_kernel, dim3(grid), dim3(256), 0, stream, reinterpret_cast<const float4*>(part),
+                    stride / 4, ksplit, rows, cols, out, out_f32, row_map, row_count);
 }
 
 }  // namespace flce

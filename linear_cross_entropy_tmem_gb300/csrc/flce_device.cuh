@@ -25,6 +25,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// Programmatic dependent launch.  The GEMM kernels are launched so that they
+// may start while the previous kernel of the stream finishes: they set up
+// (barriers, TMEM, descriptor prefetch) and then wait until the grids they
+// depend on have completed and their writes are visible, before any access to
+// global memory.  A grid's dependents may launch once every CTA of it has
+// released or exited.  The light kernels (launched normally) release at once,
+// so that the GEMM after them launches and sets up meanwhile; the GEMMs
+// release when their CTA's work is done, overlapping the next launch with
+// their teardown.  (Launching the light kernels as dependents too was slower
+// on GB300: a 256-token step took 0.80 instead of 0.77 ms.)
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
   asm volatile(

@@ -44,6 +44,7 @@ __device__ __forceinline__ void split_terms(float4 x, uint2& t0, uint2& t1, uint
 
 __global__ void split_f32_kernel(const float4* __restrict__ x, uint2* __restrict__ t0, uint2* __restrict__ t1,
                                  uint2* __restrict__ t2, int64_t n4) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     uint2 a, b, c;
@@ -58,9 +59,8 @@ cudaError_t launch_split_f32(const float* x, uint16_t* t0, uint16_t* t1, uint16_
                              cudaStream_t stream) {
   const int64_t n4 = n / 4;
   if (n4 == 0) return cudaSuccess;
-  split_f32_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(x), reinterpret_cast<uint2*>(t0),
-                                             reinterpret_cast<uint2*>(t1), reinterpret_cast<uint2*>(t2), n4);
-  return cudaGetLastError();
+  return launch_plain(split_f32_kernel, dim3(grid), dim3(256), 0, stream, reinterpret_cast<const float4*>(x),
+                    reinterpret_cast<uint2*>(t0), reinterpret_cast<uint2*>(t1), reinterpret_cast<uint2*>(t2), n4);
 }
 
 // ---------------------------------------------------------------------------
@@ -86,6 +86,7 @@ __device__ __forceinline__ float warp_allsum(float v) {
 }
 
 __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p, int* status) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   constexpr int kWarps = kMergeThreads / 32;
   constexpr int kPerWarp = kMergeRows / kWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,14 +168,15 @@ __global__ void __launch_bounds__(kMergeThreads) fwd_merge_kernel(MergeParams p,
 cudaError_t launch_fwd_merge(const MergeParams& p, int* status, cudaStream_t stream) {
   const int64_t blocks = (p.n_tokens + kMergeRows - 1) / kMergeRows;
   if (blocks == 0) return cudaSuccess;
-  fwd_merge_kernel<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(p, status);
-  return cudaGetLastError();
+  return launch_plain(fwd_merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kMergeThreads), 0, stream, p,
+                    status);
 }
 
 // Valid-target count ahead of the forward (the token-chunked backward needs the
 // mean's denominator before the last chunk's forward has run).
 __global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* targets, int64_t n, int64_t vocab,
                                                            int64_t ignore_index, int64_t* n_valid) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   long long c = 0;
   for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
     const int64_t t = targets[i];
@@ -193,12 +195,12 @@ __global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* target
 
 cudaError_t launch_count_valid(const int64_t* targets, int64_t n, int64_t vocab, int64_t ignore_index,
                                int64_t* n_valid, cudaStream_t stream) {
-  count_valid_kernel<<<1, 1024, 0, stream>>>(targets, n, vocab, ignore_index, n_valid);
-  return cudaGetLastError();
+  return launch_plain(count_valid_kernel, dim3(1), dim3(1024), 0, stream, targets, n, vocab, ignore_index, n_valid);
 }
 
 // Rows of each token chunk under compaction: out[c] = clamp(count - c * rows_per_chunk, 0, rows_per_chunk).
 __global__ void chunk_rows_kernel(const int32_t* count, int64_t rows_per_chunk, int n_chunks, int32_t* out) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) {
     const int64_t left = static_cast<int64_t>(*count) - c * rows_per_chunk;
     out[c] = static_cast<int32_t>(left <= 0 ? 0 : (left < rows_per_chunk ? left : rows_per_chunk));
@@ -207,12 +209,12 @@ __global__ void chunk_rows_kernel(const int32_t* count, int64_t rows_per_chunk, 
 
 cudaError_t launch_chunk_rows(const int32_t* count, int64_t rows_per_chunk, int n_chunks, int32_t* out,
                               cudaStream_t stream) {
-  chunk_rows_kernel<<<1, 256, 0, stream>>>(count, rows_per_chunk, n_chunks, out);
-  return cudaGetLastError();
+  return launch_plain(chunk_rows_kernel, dim3(1), dim3(256), 0, stream, count, rows_per_chunk, n_chunks, out);
 }
 
 // Final scalars from the block partials, in a fixed order (one block).
 __global__ void __launch_bounds__(256) fwd_reduce_kernel(ReduceParams p) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   double loss_d = 0.0, ent_d = 0.0;
   long long corr = 0, val = 0;
   for (int i = threadIdx.x; i < p.n_blocks; i += blockDim.x) {
@@ -255,8 +257,7 @@ __global__ void __launch_bounds__(256) fwd_reduce_kernel(ReduceParams p) {
 }
 
 cudaError_t launch_fwd_reduce(const ReduceParams& p, cudaStream_t stream) {
-  fwd_reduce_kernel<<<1, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_plain(fwd_reduce_kernel, dim3(1), dim3(256), 0, stream, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -271,6 +272,7 @@ __device__ __forceinline__ bool target_valid(const CompactParams& p, int64_t row
 }
 
 __global__ void __launch_bounds__(kCompactBlock) compact_count_kernel(CompactParams p, int* status) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   const int64_t row = blockIdx.x * static_cast<int64_t>(kCompactBlock) + threadIdx.x;
   int valid = 0;
   if (row < p.n_tokens) {
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(kCompactBlock) compact_count_kernel(CompactPar
 }
 
 __global__ void compact_scan_kernel(CompactParams p, int n_blocks) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   if (threadIdx.x != 0) return;
   int acc = 0;
   for (int b = 0; b < n_blocks; ++b) {
@@ -329,6 +332,7 @@ __device__ __forceinline__ void zero_hidden_row(const CompactParams& p, int64_t 
 }
 
 __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactParams p) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   __shared__ int s_warp[kCompactBlock / 32];
   const int64_t base = blockIdx.x * static_cast<int64_t>(kCompactBlock);
   const int64_t row = base + threadIdx.x;
@@ -374,6 +378,7 @@ __global__ void __launch_bounds__(kCompactBlock) compact_gather_kernel(CompactPa
 // Compacted row q <- hidden row row_map[q] (q < count), or a zero row; one warp
 // per row, grid-stride, so that the copy runs on every SM.
 __global__ void __launch_bounds__(256) compact_copy_kernel(CompactParams p) {
+  griddep_release();  // lets the next kernel (a GEMM) launch and set up
   const uint32_t lane = threadIdx.x & 31u;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t count = *p.count;
@@ -390,15 +395,13 @@ __global__ void __launch_bounds__(256) compact_copy_kernel(CompactParams p) {
 cudaError_t launch_compact(const CompactParams& p, int* status, int num_sms, cudaStream_t stream) {
   const int64_t blocks = (p.n_tokens + kCompactBlock - 1) / kCompactBlock;
   if (blocks == 0) return cudaSuccess;
-  compact_count_kernel<<<static_cast<unsigned>(blocks), kCompactBlock, 0, stream>>>(p, status);
-  cudaError_t e = cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(blocks));
+  cudaError_t e = launch_plain(compact_count_kernel, grid, dim3(kCompactBlock), 0, stream, p, status);
   if (e != cudaSuccess) return e;
-  compact_scan_kernel<<<1, 32, 0, stream>>>(p, static_cast<int>(blocks));
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  compact_gather_kernel<<<static_cast<unsigned>(blocks), kCompactBlock, 0, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  compact_copy_kernel<<<num_sms * 4, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  if ((e = launch_plain(compact_scan_kernel, dim3(1), dim3(32), 0, stream, p, static_cast<int>(blocks))) != cudaSuccess)
+    return e;
+  if ((e = launch_plain(compact_gather_kernel, grid, dim3(kCompactBlock), 0, stream, p)) != cudaSuccess) return e;
+  return launch_plain(compact_copy_kernel, dim3(num_sms * 4), dim3(256), 0, stream, p);
 }
 
 }  // namespace flce

@@ -783,6 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot;
+  // The set-up above (barriers, TMEM, descriptor prefetch) may overlap the
+  // previous kernel; global memory is touched only from here on.
+  griddep_wait();
   const Limits lim = read_limits(sc, kBM);
 
   if (warp == kTmaWarp) {
@@ -930,6 +933,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     Epi::finish(ep);
   }
 
+  // The next kernel may launch once every CTA is past its work (a GEMM CTA
+  // occupies its SM: dependents released earlier would only wait beside it).
+  griddep_release();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -1011,6 +1017,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_slot;
+  // The set-up above (barriers, TMEM, descriptor prefetch) may overlap the
+  // previous kernel; global memory is touched only from here on.
+  griddep_wait();
   const Limits lim = read_limits(sc, kTileRows);
   const int cid = static_cast<int>(blockIdx.x / kCtas);
   const int ncl = static_cast<int>(gridDim.x / kCtas);
@@ -1171,6 +1180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) aborted = true;
   }
 
+  // The next kernel may launch once every CTA is past its work (a GEMM CTA
+  // occupies its SM: dependents released earlier would only wait beside it).
+  griddep_release();
   // After an abort, copies the other CTA issued may still be in flight toward
   // this CTA's shared memory or barriers: give them time to land.
   if (aborted || sm.ctl->abort) spin_ns(100000);

@@ -11,6 +11,33 @@
 
 namespace flce {
 
+// kern<<<grid, block, smem, stream>>>(args...), returning the launch error;
+// `dependent`: as a programmatic dependent of the previous kernel in the
+// stream (it may start while that kernel finishes and waits for its results in
+// griddep_wait before touching global memory).
+template <class... Params, class... Args>
+static cudaError_t launch_ex(bool dependent, void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// The light kernels: ordinary stream order.
+template <class... Params, class... Args>
+static cudaError_t launch_plain(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                Args... args) {
+  return launch_ex(false, kern, grid, block, smem, stream, args...);
+}
+
 template <class Epi>
 static cudaError_t launch_gemm_single(const TmaMaps& m, const GemmSched& sc, const typename Epi::Params& p,
                                       int* status, int num_sms, cudaStream_t stream) {
@@ -19,22 +46,26 @@ static cudaError_t launch_gemm_single(const TmaMaps& m, const GemmSched& sc, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(sc.total_units, num_sms));
-  kern<<<grid, kThreads, smem, stream>>>(m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
-  return cudaGetLastError();
+  return launch_ex(true, kern, dim3(grid), dim3(kThreads), smem, stream, m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc,
+                   p, status);
 }
 
+// Launch configuration of the pair kernel: clusters of two CTAs, and (when
+// `dependent`) a programmatic dependent of the previous kernel in the stream.
 template <class Epi>
-static cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, cudaStream_t stream) {
+static cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, cudaStream_t stream, bool dependent) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kGemmPairSmemBase + Epi::kTailBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = dependent ? 2 : 1;
   return cfg;
 }
 
@@ -52,8 +83,8 @@ static cudaError_t resident_pairs(int num_sms, int* out) {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kGemmPairSmemBase + Epi::kTailBytes)) != cudaSuccess)
       return e;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = cluster_config<Epi>(attr, nullptr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = cluster_config<Epi>(attr, nullptr, false);
     cfg.gridDim = dim3(2 * std::max(1, num_sms / 2));
     int n = 0;
     if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
@@ -70,8 +101,8 @@ static cudaError_t launch_gemm_pair(const TmaMaps& m, const GemmSched& sc, const
   int resident = 0;
   cudaError_t e = resident_pairs<Epi>(num_sms, &resident);  // also sets the smem attribute
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config<Epi>(attr, stream);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = cluster_config<Epi>(attr, stream, true);
   const int clusters = std::max(1, std::min(sc.total_units, resident));
   cfg.gridDim = dim3(2 * clusters);
   return cudaLaunchKernelEx(&cfg, kern, m.a0, m.a1, m.a2, m.b0, m.b1, m.b2, sc, p, status);
