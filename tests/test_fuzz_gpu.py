@@ -46,7 +46,7 @@ def _reset_knobs():
     testing_set_token_chunk(0)
 
 
-@pytest.mark.parametrize("seed", range(64))
+@pytest.mark.parametrize("seed", range(256))
 def test_random_case_matches_oracle(seed):
     import linear_cross_entropy_tmem_gb300 as F
     from linear_cross_entropy_tmem_gb300.api import testing_set_gemm_mode, testing_set_token_chunk, testing_set_tuning
