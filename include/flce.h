@@ -35,7 +35,11 @@
  *     targets [N] (int64), lse [N], dloss [1] or [N].
  *   - Every launch is enqueued on `stream` (0 = the legacy default stream) and
  *     is asynchronous; nothing synchronises the host except
- *     flce_read_device_status.
+ *     flce_read_device_status.  The GEMM kernels are launched with
+ *     programmatic stream serialisation: one may start its set-up (shared
+ *     memory, tensor memory) while the kernel before it on the stream is
+ *     finishing, and it waits for that kernel to complete before it reads or
+ *     writes global memory, so stream order is kept for every buffer.
  *   - Argument errors are detected on the host before anything is enqueued and
  *     are returned as a status code; nothing is launched in that case.
  *   - Errors that depend on data (a target outside [0, V) that is not the
