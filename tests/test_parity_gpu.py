@@ -230,6 +230,34 @@ def test_autograd_gradients_in_forward(D, reduction):
         assert oracle.relative_frobenius(g1.float().cpu(), x.grad.float().cpu()) <= 1e-2
 
 
+@pytest.mark.parametrize("D", [200, 1280], ids=["recompute", "keep-logits"])
+def test_autograd_none_backward_through_slices(D):
+    """Reduction 'none' through the autograd wrapper: backpropagating loss[:k].sum() (retain_graph)
+    and then loss[k:].sum() gives the gradient of loss.sum() (Liger-Kernel PR #1574, review reply
+    point 2: backward through slices of the per-token losses keeps working).  Each dhidden row
+    depends on its own token's upstream weight only, so it is the same bits as a single backward;
+    dweight and dbias add two rounded partial sums, so they match to rounding and the oracle."""
+    import linear_cross_entropy_tmem_gb300 as F
+    w = Workload("slices", 700, D, 3000, sigma_w=0.1, bias=True, softcap=10.0, reduction="none", seed=17)
+    hc, Wc, bc, tc, _ = make_inputs(w, "cpu")
+    h, W, b, t = (x.cuda() for x in (hc, Wc, bc, tc))
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction="none")
+    k = 700 // 3
+    hh, WW, bb = (x.clone().requires_grad_(True) for x in (h, W, b))
+    loss, *_ = F.linear_cross_entropy(hh, WW, t, bb, **kw)
+    loss[:k].sum().backward(retain_graph=True)
+    loss[k:].sum().backward()
+    h1, W1, b1 = (x.clone().requires_grad_(True) for x in (h, W, b))
+    loss1, *_ = F.linear_cross_entropy(h1, W1, t, b1, **kw)
+    loss1.sum().backward()
+    torch.cuda.synchronize()
+    assert torch.equal(hh.grad, h1.grad)
+    for a, c in ((WW.grad, W1.grad), (bb.grad, b1.grad)):
+        assert oracle.relative_frobenius(a.float().cpu(), c.float().cpu()) <= 5e-3
+    ref_b = oracle.backward(hc, Wc, bc, tc, dloss=torch.ones(700), **kw)
+    compare_backward((hh.grad, WW.grad, bb.grad), ref_b)
+
+
 # ---------------------------------------------------------------------------
 # num_items_in_batch and valid-token compaction
 # ---------------------------------------------------------------------------
