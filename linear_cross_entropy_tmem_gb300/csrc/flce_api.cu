@@ -1038,7 +1038,6 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
   const size_t w_elem = weight_elem(p);
   const DhPlan dhp = plan_token_dh(L, D, dev.num_sms);
   const bool pair_dh = dhp.pair;
-  const int dh_ctas = dhp.ctas;
   const int ksplit = dhp.ksplit;
   const bool pair_dw = use_pair(V, cdiv(D, kBN), dev.num_sms);
   const int dw_ctas = pair_dw ? dev.num_sms / 2 : dev.num_sms;
