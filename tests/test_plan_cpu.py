@@ -11,11 +11,6 @@ import pytest
 from linear_cross_entropy_tmem_gb300 import binding as B
 
 
-@pytest.fixture(scope="module")
-def lib():
-    return B.load()
-
-
 def _problem(N, D, V, **kw):
     base = dict(n_tokens=N, hidden=D, vocab=V, hidden_dtype=B.FLCE_BF16, weight_dtype=B.FLCE_BF16,
                 bias_dtype=B.FLCE_BF16, reduction=B.FLCE_RED_MEAN, logit_scale=1.0,
