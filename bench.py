@@ -73,6 +73,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-grads", action="store_true",
                     help="the e2e leg also reads dhidden, dweight and dbias back to pinned host memory every step "
                          "(by default only the loss and the metrics return; the gradients stay on the device)")
+    ap.add_argument("--frozen-head", action="store_true",
+                    help="the head and bias are not trained (FLCE_FLAG_FROZEN_HEAD, as in LoRA training): the "
+                         "backward forms dhidden only")
     ap.add_argument("--dh-ksplit", type=int, default=0,
                     help="force the K splits of the recompute backward's dh product (0 = automatic; tuning)")
     return ap.parse_args(argv)
@@ -256,7 +259,7 @@ class Runner:
     """Preallocated buffers and raw C-ABI calls for one forward + backward step."""
 
     def __init__(self, w, device, seed_offset=0, compact=False, fused=False, bwd="auto", autograd=False,
-                 grad_in_forward=True):
+                 grad_in_forward=True, frozen_head=False):
         import torch
 
         import linear_cross_entropy_tmem_gb300.api as api
@@ -270,7 +273,7 @@ class Runner:
         N, D, V = w.n_tokens, w.hidden, w.vocab
         self.prob = api.make_problem(N, D, V, hidden_dtype=self.h.dtype, bias_dtype=torch.bfloat16,
                                      logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction,
-                                     compact=compact, bwd=bwd)
+                                     compact=compact, bwd=bwd, frozen_head=frozen_head)
         f32 = dict(dtype=torch.float32, device=device)
         self.loss = torch.empty(N if w.reduction == "none" else 1, **f32)
         self.lse = torch.empty(N, **f32)
@@ -278,8 +281,9 @@ class Runner:
         self.n_valid = torch.empty(1, dtype=torch.int64, device=device)
         self.ent_sum = torch.empty(1, **f32)
         self.dh = torch.empty_like(self.h)
-        self.dW = torch.empty_like(self.W)
-        self.db = torch.empty_like(self.b) if self.b is not None else None
+        self.frozen_head = frozen_head  # dhidden only: no dweight / dbias buffers are passed
+        self.dW = torch.empty_like(self.W) if not frozen_head else None
+        self.db = torch.empty_like(self.b) if self.b is not None and not frozen_head else None
         self.ws_f = torch.empty(api.flce_workspace_size(self.prob, False), dtype=torch.uint8, device=device)
         self.ws_b = torch.empty(api.flce_workspace_size(self.prob, True), dtype=torch.uint8, device=device)
         self.fused = fused
@@ -297,8 +301,9 @@ class Runner:
 
         self.autograd = autograd
         self.grad_in_forward = grad_in_forward
-        if autograd:
-            self.leaves = [x.detach().requires_grad_(True) if x is not None else None for x in (self.h, self.W, self.b)]
+        if autograd:  # a frozen head: the weight and bias leaves do not require gradients
+            self.leaves = [x.detach().requires_grad_(i == 0 or not frozen_head) if x is not None else None
+                           for i, x in enumerate((self.h, self.W, self.b))]
         self.fb_args = (ctypes.byref(self.prob), p(self.h), p(self.W), p(self.b), p(self.t), p(self.dloss),
                         p(self.loss), p(self.lse), None, p(self.correct), p(self.n_valid), p(self.ent_sum),
                         p(self.dh), p(self.dW), p(self.db), p(self.ws_fb), self.ws_fb.numel(), s)
@@ -438,7 +443,7 @@ def flce_arm(args):
     B.check(lib.flce_testing_set_tuning(0, args.dh_ksplit), "dh K splits")
     B.check(lib.flce_testing_set_token_chunk(args.token_chunk), "token chunk")  # before sizing the workspace
     run = Runner(w, device, seed_offset=rank, compact=args.compact, fused=not args.separate, bwd=args.bwd,
-                 autograd=args.autograd, grad_in_forward=not args.grad_in_backward)
+                 autograd=args.autograd, grad_in_forward=not args.grad_in_backward, frozen_head=args.frozen_head)
     if args.autograd:
         if args.compact:
             raise SystemExit("--autograd does not combine with --compact")
@@ -572,7 +577,8 @@ def flce_arm(args):
     tokens = w.n_tokens * world
     value = tokens / (ms_max * 1e-3)
     tflops = w.flops() * world / (ms_max * 1e-3) / 1e12
-    exec_flops = 8.0 * rows_mult * w.vocab * w.hidden * (0.75 if keep else 1.0)
+    # executed products: 6NVD with kept logits, 8NVD with the recompute, 2NVD fewer with a frozen head
+    exec_flops = 8.0 * rows_mult * w.vocab * w.hidden * ((0.75 if keep else 1.0) - (0.25 if args.frozen_head else 0.0))
     tflops_exec = exec_flops * world / (ms_max * 1e-3) / 1e12
 
     # ---- end to end through host buffers: H2D inputs, step, D2H loss + metrics
@@ -583,7 +589,7 @@ def flce_arm(args):
         # copy of step k+1's inputs (copy stream) runs during step k's compute, as a training
         # loop that prefetches its next batch would.
         runs = [run, Runner(w, device, seed_offset=rank, compact=args.compact, fused=not args.separate,
-                            bwd=args.bwd)]
+                            bwd=args.bwd, frozen_head=args.frozen_head)]
         host = {k: getattr(run, k).to("cpu").pin_memory() for k in ("h", "W", "t", "dloss")
                 if getattr(run, k) is not None}
         if run.b is not None:
@@ -674,7 +680,9 @@ def flce_arm(args):
                                  + ("in the backward)" if args.grad_in_backward else "in the forward)"))
                        if args.autograd else
                        "flce_forward + flce_backward" if args.separate else "flce_forward_backward",
-                       "backward": "keep_logits (token chunks, 6NVD)" if keep else "recompute (8NVD)",
+                       "backward": (("keep_logits (token chunks, 4NVD: frozen head, dhidden only)" if keep else
+                                     "recompute (6NVD: frozen head, dhidden only)") if args.frozen_head else
+                                    "keep_logits (token chunks, 6NVD)" if keep else "recompute (8NVD)"),
                        "l2": ("inputs larger than L2 (129 MB), no flush" if flush is None else
                               "256 MB buffer written between steps (outside the steps' events) to flush L2")},
             # executed flops: 6NVD with kept logits, 8NVD with the recompute; the metric's own

@@ -133,7 +133,17 @@ enum {
    * (The pages' fp32 path: TRL PR #6859, review "verified" bullet 3, with the
    * head cast to the activations' dtype.)
    */
-  FLCE_FLAG_FP32_FULL = 8u
+  FLCE_FLAG_FP32_FULL = 8u,
+  /*
+   * The head (and its bias) are frozen, as in the LoRA rows of TRL PR #6859's
+   * Benchmark table, where only the adapters are trained: the backward forms
+   * dhidden alone.  flce_backward and flce_forward_backward then take NULL for
+   * dweight and dbias (a non-NULL pointer is FLCE_ERR_INVALID_ARG) and skip the
+   * dweight products and the dbias sums: 2*N*V*D flops fewer, and the
+   * workspace holds no fp32 dweight / dbias accumulators.  The bias, when
+   * given, still enters the logits.  flce_forward ignores this bit.
+   */
+  FLCE_FLAG_FROZEN_HEAD = 16u
 };
 
 /* Status codes returned by every call (and stored in the device status word). */
@@ -245,8 +255,10 @@ FLCE_API int flce_forward(const flce_problem* problem, const void* hidden, const
  *   n_valid  [1] int64 from flce_forward (the mean's denominator)
  *   dloss    fp32 upstream gradient: [1] for mean / sum, [N] for none
  *   dhidden  [N, D] in hidden_dtype (written, not accumulated), 16-byte aligned
- *   dweight  [V, D] in weight_dtype (written, not accumulated), 16-byte aligned
- *   dbias    [V] in bias_dtype; must be NULL exactly when bias is NULL
+ *   dweight  [V, D] in weight_dtype (written, not accumulated), 16-byte aligned;
+ *            NULL with FLCE_FLAG_FROZEN_HEAD (and only then)
+ *   dbias    [V] in bias_dtype; must be NULL exactly when bias is NULL, and
+ *            NULL with FLCE_FLAG_FROZEN_HEAD
  *   workspace, workspace_bytes: at least flce_workspace_size(problem, 1)
  * All-ignored batches produce exact zero gradients.
  */

@@ -34,10 +34,11 @@ def make_problem(n_tokens: int, hidden: int, vocab: int, *, hidden_dtype=torch.b
                  weight_dtype=torch.bfloat16, bias_dtype=torch.bfloat16, logit_scale: float = 1.0,
                  softcap: float = 0.0, ignore_index: int = -100, reduction: str = "mean",
                  num_items_in_batch: float = 0.0, compact: bool = False,
-                 bwd: str = "auto", fp32_full: bool = False) -> B.FlceProblem:
+                 bwd: str = "auto", fp32_full: bool = False, frozen_head: bool = False) -> B.FlceProblem:
     """``bwd`` picks the backward algorithm of the fused call: "auto", "recompute" or
     "keep_logits" (token-chunked; see FLCE_FLAG_BWD_KEEP_LOGITS in include/flce.h).
-    ``fp32_full`` splits fp32 operands into three bf16 terms (FLCE_FLAG_FP32_FULL)."""
+    ``fp32_full`` splits fp32 operands into three bf16 terms (FLCE_FLAG_FP32_FULL).
+    ``frozen_head``: the backward forms dhidden only (FLCE_FLAG_FROZEN_HEAD)."""
     if reduction not in B.REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(B.REDUCTIONS)}")
     if bwd not in B.BWD_ALGOS:
@@ -49,7 +50,7 @@ def make_problem(n_tokens: int, hidden: int, vocab: int, *, hidden_dtype=torch.b
         logit_scale=float(logit_scale), final_logit_softcapping=float(softcap), ignore_index=int(ignore_index),
         num_items_in_batch=float(num_items_in_batch),
         flags=(B.FLCE_FLAG_COMPACT_VALID if compact else 0) | B.BWD_ALGOS[bwd]
-        | (B.FLCE_FLAG_FP32_FULL if fp32_full else 0),
+        | (B.FLCE_FLAG_FP32_FULL if fp32_full else 0) | (B.FLCE_FLAG_FROZEN_HEAD if frozen_head else 0),
         reserved=0)
 
 
@@ -130,8 +131,10 @@ def flce_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Ten
                   n_valid: torch.Tensor, dloss: torch.Tensor, bias: Optional[torch.Tensor] = None, *,
                   logit_scale: float = 1.0, softcap: float = 0.0, ignore_index: int = -100,
                   reduction: str = "mean", num_items_in_batch: float = 0.0, compact: bool = False,
-                  fp32_full: bool = False, workspace: Optional[torch.Tensor] = None, outputs=None):
-    """Backward (see ``flce_backward`` in include/flce.h); returns (dhidden, dweight, dbias)."""
+                  fp32_full: bool = False, frozen_head: bool = False, workspace: Optional[torch.Tensor] = None,
+                  outputs=None):
+    """Backward (see ``flce_backward`` in include/flce.h); returns (dhidden, dweight, dbias), with
+    dweight and dbias None for a frozen head."""
     _require_cuda(hidden, weight, targets, lse, n_valid, dloss, bias)
     for t, n in ((hidden, "hidden"), (weight, "weight"), (targets, "targets"), (bias, "bias"), (lse, "lse")):
         _contig(t, n)
@@ -141,15 +144,15 @@ def flce_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Ten
                         bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
                         logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
                         reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact,
-                        fp32_full=fp32_full)
+                        fp32_full=fp32_full, frozen_head=frozen_head)
     dev = hidden.device
     ws = _workspace(flce_workspace_size(prob, True), dev, workspace)
     dloss = dloss.to(dtype=torch.float32).contiguous().reshape(-1)
     n_valid = n_valid.reshape(-1)
     if outputs is None:
         dh = torch.empty_like(hidden)
-        dW = torch.empty_like(weight)
-        db = torch.empty_like(bias) if bias is not None else None
+        dW = torch.empty_like(weight) if not frozen_head else None
+        db = torch.empty_like(bias) if bias is not None and not frozen_head else None
     else:
         dh, dW, db = outputs
     st = B.load().flce_backward(ctypes.byref(prob), _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets),
@@ -163,11 +166,13 @@ def flce_forward_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: t
                           bias: Optional[torch.Tensor] = None, *, logit_scale: float = 1.0, softcap: float = 0.0,
                           ignore_index: int = -100, reduction: str = "mean", entropy: bool = False,
                           num_items_in_batch: float = 0.0, compact: bool = False, bwd: str = "auto",
-                          fp32_full: bool = False, workspace: Optional[torch.Tensor] = None):
+                          fp32_full: bool = False, frozen_head: bool = False,
+                          workspace: Optional[torch.Tensor] = None):
     """Forward and backward in one call (see ``flce_forward_backward`` in include/flce.h);
     ``bwd`` as in :func:`make_problem`.
 
-    Returns ``(ForwardResult, (dhidden, dweight, dbias))``."""
+    Returns ``(ForwardResult, (dhidden, dweight, dbias))``, with dweight and dbias None for a frozen
+    head."""
     _require_cuda(hidden, weight, targets, dloss, bias)
     for t, n in ((hidden, "hidden"), (weight, "weight"), (targets, "targets"), (bias, "bias")):
         _contig(t, n)
@@ -179,7 +184,7 @@ def flce_forward_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: t
                         bias_dtype=bias.dtype if bias is not None else torch.bfloat16,
                         logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index,
                         reduction=reduction, num_items_in_batch=num_items_in_batch, compact=compact, bwd=bwd,
-                        fp32_full=fp32_full)
+                        fp32_full=fp32_full, frozen_head=frozen_head)
     dev = hidden.device
     ws = _workspace(flce_workspace_size(prob, 2), dev, workspace)
     f32 = dict(dtype=torch.float32, device=dev)
@@ -191,8 +196,8 @@ def flce_forward_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: t
     ent_sum = torch.empty(1, **f32)
     dloss = dloss.to(dtype=torch.float32).contiguous().reshape(-1)
     dh = torch.empty_like(hidden)
-    dW = torch.empty_like(weight)
-    db = torch.empty_like(bias) if bias is not None else None
+    dW = torch.empty_like(weight) if not frozen_head else None
+    db = torch.empty_like(bias) if bias is not None and not frozen_head else None
     st = B.load().flce_forward_backward(ctypes.byref(prob), _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets),
                                         _ptr(dloss), _ptr(loss), _ptr(lse), _ptr(ent), _ptr(correct),
                                         _ptr(n_valid), _ptr(ent_sum), _ptr(dh), _ptr(dW), _ptr(db), _ptr(ws),
@@ -234,7 +239,10 @@ class LinearCrossEntropy(torch.autograd.Function):
     the logits of token chunks from D = 1152 up), and the backward scales them by the upstream
     gradient in place (``flce_scale_gradient``; nothing happens for the usual 1).  Gradients are linear
     in a scalar upstream gradient, so this is the same result up to one rounding.  A second backward
-    through the same graph recomputes them (``flce_backward``) instead of rescaling."""
+    through the same graph recomputes them (``flce_backward``) instead of rescaling.
+
+    When neither the weight nor the bias requires a gradient (a frozen head, e.g. LoRA training),
+    only dhidden is formed (``FLCE_FLAG_FROZEN_HEAD``)."""
 
     @staticmethod
     def forward(ctx, hidden, weight, bias, targets, logit_scale, softcap, ignore_index, reduction,
@@ -242,15 +250,16 @@ class LinearCrossEntropy(torch.autograd.Function):
         kw = dict(logit_scale=logit_scale, softcap=softcap, ignore_index=ignore_index, reduction=reduction,
                   num_items_in_batch=num_items_in_batch, compact=compact, fp32_full=fp32_full)
         need = any(ctx.needs_input_grad[:3])
+        frozen = not ctx.needs_input_grad[1] and not ctx.needs_input_grad[2]
         ctx.grads = None
         if grad_in_forward and need and reduction != "none":
             ones = torch.ones(1, dtype=torch.float32, device=hidden.device)
-            r, grads = flce_forward_backward(hidden, weight, targets, ones, bias, **kw)
+            r, grads = flce_forward_backward(hidden, weight, targets, ones, bias, frozen_head=frozen, **kw)
             ctx.grads = grads
         else:
             r = flce_forward(hidden, weight, targets, bias, **kw)
         ctx.save_for_backward(hidden, weight, bias, targets, r.lse, r.n_valid)
-        ctx.cfg = kw
+        ctx.cfg = dict(kw, frozen_head=frozen)
         ctx.mark_non_differentiable(r.correct, r.n_valid, r.entropy_sum)
         return r.loss, r.correct, r.n_valid, r.entropy_sum
 

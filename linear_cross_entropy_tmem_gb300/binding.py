@@ -18,6 +18,7 @@ FLCE_FLAG_COMPACT_VALID = 1
 FLCE_FLAG_BWD_RECOMPUTE = 2
 FLCE_FLAG_BWD_KEEP_LOGITS = 4
 FLCE_FLAG_FP32_FULL = 8
+FLCE_FLAG_FROZEN_HEAD = 16
 BWD_ALGOS = {"auto": 0, "recompute": FLCE_FLAG_BWD_RECOMPUTE, "keep_logits": FLCE_FLAG_BWD_KEEP_LOGITS}
 REDUCTIONS = {"none": FLCE_RED_NONE, "sum": FLCE_RED_SUM, "mean": FLCE_RED_MEAN}
 

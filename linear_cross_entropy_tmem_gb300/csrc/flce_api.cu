@@ -151,8 +151,8 @@ int validate(const flce_problem* p) {
   if (p->weight_dtype != FLCE_BF16 && p->weight_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED_DTYPE;
   if (p->weight_dtype == FLCE_F32 && p->hidden_dtype == FLCE_BF16) return FLCE_ERR_DTYPE_MISMATCH;
   if (!std::isfinite(p->num_items_in_batch) || p->num_items_in_batch < 0.0) return FLCE_ERR_INVALID_ARG;
-  constexpr uint32_t kKnownFlags =
-      FLCE_FLAG_COMPACT_VALID | FLCE_FLAG_BWD_RECOMPUTE | FLCE_FLAG_BWD_KEEP_LOGITS | FLCE_FLAG_FP32_FULL;
+  constexpr uint32_t kKnownFlags = FLCE_FLAG_COMPACT_VALID | FLCE_FLAG_BWD_RECOMPUTE | FLCE_FLAG_BWD_KEEP_LOGITS |
+                                   FLCE_FLAG_FP32_FULL | FLCE_FLAG_FROZEN_HEAD;
   if ((p->flags & ~kKnownFlags) != 0 || p->reserved != 0) return FLCE_ERR_INVALID_ARG;
   if ((p->flags & FLCE_FLAG_BWD_RECOMPUTE) && (p->flags & FLCE_FLAG_BWD_KEEP_LOGITS)) return FLCE_ERR_INVALID_ARG;
   if (p->hidden % 8 != 0) return FLCE_ERR_MISALIGNED;
@@ -160,6 +160,8 @@ int validate(const flce_problem* p) {
 }
 
 bool compact(const flce_problem* p) { return (p->flags & FLCE_FLAG_COMPACT_VALID) != 0; }
+// The head (and bias) are not trained: the backward forms dhidden only.
+bool frozen(const flce_problem* p) { return (p->flags & FLCE_FLAG_FROZEN_HEAD) != 0; }
 
 // bf16 terms the products read of each operand: 1 for bf16, 2 for fp32 (about
 // 16 significant bits), 3 with FLCE_FLAG_FP32_FULL (all 24).
@@ -375,9 +377,10 @@ Layout make_token_layout(const flce_problem* p, bool has_bias) {
   L.blocks = take(size_t(cdiv(N, kMergeRows)) * sizeof(BlockPartial));
   L.z = take(size_t(L.nc) * L.ldz * 4);
   L.zg = take(size_t(L.nc) * L.ldz * 2);
-  if (has_bias) L.dbias_part = take(size_t(cdiv(L.nc, kZGradRows)) * L.ldz * 4);
-  if (has_bias && L.n_tchunks > 1) L.dbias_acc = take(size_t(L.ldz) * 4);
-  if (L.n_tchunks > 1) L.dw_acc = take(size_t(V) * D * 4);
+  const bool weight_grads = !frozen(p);  // a frozen head needs neither dW nor dbias scratch
+  if (has_bias && weight_grads) L.dbias_part = take(size_t(cdiv(L.nc, kZGradRows)) * L.ldz * 4);
+  if (has_bias && weight_grads && L.n_tchunks > 1) L.dbias_acc = take(size_t(L.ldz) * 4);
+  if (weight_grads && L.n_tchunks > 1) L.dw_acc = take(size_t(V) * D * 4);
   L.ksplit_max = token_dh_ksplit_bound(L.nc, D);
   L.need_dh_part = L.ksplit_max > 1;
   if (L.need_dh_part) L.dh_part = take(size_t(L.ksplit_max) * L.nc * D * 4);
@@ -432,7 +435,7 @@ Layout make_layout(const flce_problem* p, int kind, bool has_bias) {
     L.n_chunks = cdiv(V, L.vc);
     L.ksplit_max = dh_ksplit_bound(N, D, L.vc);
     L.g = take(size_t(N) * L.vc * 2);
-    if (has_bias) L.dbias_part = take(size_t(cdiv(N, kBM)) * L.vc * 4);
+    if (has_bias && !frozen(p)) L.dbias_part = take(size_t(cdiv(N, kBM)) * L.vc * 4);
     L.need_dh_part = L.n_chunks > 1 || L.ksplit_max > 1;
     if (L.need_dh_part) L.dh_part = take(size_t(L.ksplit_max) * N * D * 4);
     end = std::max(end, off);
@@ -730,8 +733,9 @@ int run_forward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, u
   fp.part_best = reinterpret_cast<float*>(ws + L.part_best);
   fp.part_idx = reinterpret_cast<int32_t*>(ws + L.part_idx);
   fp.z_target = reinterpret_cast<float*>(ws + L.z_target);
-  FLCE_TRY(logged(FLCE_LAUNCH_FWD_LOGITS, st,
-                   [&] { return launch_fwd_gemm(bias != nullptr, softcap, pair, maps, sc, fp, status, dev.num_sms, st); }));
+  FLCE_TRY(logged(FLCE_LAUNCH_FWD_LOGITS, st, [&] {
+    return launch_fwd_gemm(bias != nullptr, softcap, pair, maps, sc, fp, status, dev.num_sms, st);
+  }));
 
   MergeParams mp{};
   mp.n_tokens = N;
@@ -860,7 +864,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
   }
   const bool softcap = p->final_logit_softcapping > 0.f;
   uint16_t* g = reinterpret_cast<uint16_t*>(ws + L.g);
-  float* dbias_part = bias ? reinterpret_cast<float*>(ws + L.dbias_part) : nullptr;
+  float* dbias_part = dbias ? reinterpret_cast<float*>(ws + L.dbias_part) : nullptr;  // none with a frozen head
   float* dh_part = L.need_dh_part ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
 
   // Maps that do not change across chunks.
@@ -922,7 +926,7 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_RECOMPUTE, st, [&] {
       return launch_grad_gemm(bias != nullptr, softcap, pair_rec, rec, s1, gp, status, dev.num_sms, st);
     }));
-    if (bias) {
+    if (dbias) {
       FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
         return launch_dbias_reduce(dbias_part, L.vc, static_cast<int>(cdiv(N, kBM)), kBM, width,
                                    static_cast<uint8_t*>(dbias) + v0 * bias_elem,
@@ -930,28 +934,30 @@ int run_backward(const flce_problem* p, const Layout& L, const DeviceInfo& dev, 
       }));
     }
 
-    // (2) dW[v0 : v0+width] = G^T h    (A = G MN-major, B = h MN-major, K = N)
-    TmaMaps mw;
-    FLCE_TRY(make_map(&mw.a0, g, width, N, L.vc * 2, 64, kBK));
-    mw.a1 = mw.a2 = mw.a0;
-    mw.b0 = hmn.b0;
-    mw.b1 = hmn.b1;
-    mw.b2 = hmn.b2;
-    const bool pair_dw = use_pair(width, cdiv(D, kBN), dev.num_sms);
-    GemmSched s2 = base_sched(width, D, N, dw_nseg, dw_segs, pair_dw);
-    s2.a_mn = 1;
-    s2.b_mn = 1;
-    s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
-    s2.k_limit = pr.row_count;
-    finish_sched(s2);
-    StoreParams sp{};
-    sp.rows = width;
-    sp.cols = D;
-    sp.out_f32 = w_elem == 4 ? 1 : 0;
-    FLCE_TRY(make_store_map(&sp.out_map, static_cast<uint8_t*>(dweight) + size_t(v0) * D * w_elem, w_elem == 4, D,
-                            width, D * w_elem));
-    FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
-                    [&] { return launch_store_gemm(pair_dw, mw, s2, sp, status, dev.num_sms, st); }));
+    // (2) dW[v0 : v0+width] = G^T h    (A = G MN-major, B = h MN-major, K = N); none with a frozen head
+    if (dweight) {
+      TmaMaps mw;
+      FLCE_TRY(make_map(&mw.a0, g, width, N, L.vc * 2, 64, kBK));
+      mw.a1 = mw.a2 = mw.a0;
+      mw.b0 = hmn.b0;
+      mw.b1 = hmn.b1;
+      mw.b2 = hmn.b2;
+      const bool pair_dw = use_pair(width, cdiv(D, kBN), dev.num_sms);
+      GemmSched s2 = base_sched(width, D, N, dw_nseg, dw_segs, pair_dw);
+      s2.a_mn = 1;
+      s2.b_mn = 1;
+      s2.group_m = std::max(1, (pair_dw ? dev.num_sms / 2 : dev.num_sms) / std::max(1, s2.n_tiles));
+      s2.k_limit = pr.row_count;
+      finish_sched(s2);
+      StoreParams sp{};
+      sp.rows = width;
+      sp.cols = D;
+      sp.out_f32 = w_elem == 4 ? 1 : 0;
+      FLCE_TRY(make_store_map(&sp.out_map, static_cast<uint8_t*>(dweight) + size_t(v0) * D * w_elem, w_elem == 4, D,
+                              width, D * w_elem));
+      FLCE_TRY(logged(FLCE_LAUNCH_BWD_DWEIGHT, st,
+                      [&] { return launch_store_gemm(pair_dw, mw, s2, sp, status, dev.num_sms, st); }));
+    }
 
     // (3) dh (+)= G W[v0 : v0+width]   (A = G K-major, B = W MN-major, K = width)
     TmaMaps mh;
@@ -1009,8 +1015,8 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
   float* z = reinterpret_cast<float*>(ws + L.z);
   uint16_t* g = reinterpret_cast<uint16_t*>(ws + L.zg);
   float* dw_acc = L.dw_acc ? reinterpret_cast<float*>(ws + L.dw_acc) : nullptr;
-  float* dbias_part = bias ? reinterpret_cast<float*>(ws + L.dbias_part) : nullptr;
-  float* dbias_acc = bias && L.dbias_acc ? reinterpret_cast<float*>(ws + L.dbias_acc) : nullptr;
+  float* dbias_part = dbias ? reinterpret_cast<float*>(ws + L.dbias_part) : nullptr;  // none with a frozen head
+  float* dbias_acc = dbias && L.dbias_acc ? reinterpret_cast<float*>(ws + L.dbias_acc) : nullptr;
   float* dh_part = L.need_dh_part ? reinterpret_cast<float*>(ws + L.dh_part) : nullptr;
   BlockPartial* blocks = reinterpret_cast<BlockPartial*>(ws + L.blocks);
   // Under compaction the chunks cut the compacted tokens: chunk c holds
@@ -1130,7 +1136,7 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
     zp.num_items = static_cast<float>(p->num_items_in_batch);
     zp.dbias_part = dbias_part;
     FLCE_TRY(logged(FLCE_LAUNCH_BWD_LOGIT_GRAD, st, [&] { return launch_zgrad(zp, softcap, st); }));
-    if (bias) {  // the chunk's dbias partials, in row-tile order, into the fp32 accumulator (or dbias)
+    if (dbias) {  // the chunk's dbias partials, in row-tile order, into the fp32 accumulator (or dbias)
       FLCE_TRY(logged(FLCE_LAUNCH_OTHER, st, [&] {
         return launch_dbias_reduce(dbias_part, L.ldz, static_cast<int>(cdiv(rows, kZGradRows)), kZGradRows, V,
                                    dbias, p->bias_dtype == FLCE_F32, lim, dbias_acc, c > 0 ? 1 : 0,
@@ -1181,7 +1187,8 @@ int run_fused_tokens(const flce_problem* p, const Layout& L, const DeviceInfo& d
       }));
     }
 
-    // (4) dW (+)= G^T h[chunk]   (A = G MN-major, B = h MN-major, K = chunk rows)
+    // (4) dW (+)= G^T h[chunk]   (A = G MN-major, B = h MN-major, K = chunk rows); none with a frozen head
+    if (!dweight) continue;
     TmaMaps mw;
     FLCE_TRY(make_map(&mw.a0, g, V, rows, L.ldz * 2, 64, kBK));
     mw.a1 = mw.a2 = mw.a0;
@@ -1234,8 +1241,12 @@ int check_backward_args(const flce_problem* p, const void* hidden, const void* w
                         const int64_t* targets, const float* lse, const int64_t* n_valid, const float* dloss,
                         const void* dhidden, const void* dweight, const void* dbias, const void* workspace) {
   const int64_t N = p->n_tokens;
-  if (!weight || !dweight || !workspace || !n_valid || !dloss) return FLCE_ERR_INVALID_ARG;
-  if ((bias == nullptr) != (dbias == nullptr)) return FLCE_ERR_INVALID_ARG;
+  if (!weight || !workspace || !n_valid || !dloss) return FLCE_ERR_INVALID_ARG;
+  if (frozen(p)) {  // dhidden only: no weight or bias gradient is written
+    if (dweight || dbias) return FLCE_ERR_INVALID_ARG;
+  } else {
+    if (!dweight || (bias == nullptr) != (dbias == nullptr)) return FLCE_ERR_INVALID_ARG;
+  }
   if (N > 0 && (!hidden || !targets || !lse || !dhidden)) return FLCE_ERR_INVALID_ARG;
   if (!aligned(weight, 16) || !aligned(dweight, 16) || !aligned(workspace, 256) ||
       (N > 0 && (!aligned(hidden, 16) || !aligned(dhidden, 16))) || (targets && !aligned(targets, 8)))
@@ -1245,7 +1256,7 @@ int check_backward_args(const flce_problem* p, const void* hidden, const void* w
 
 int zero_grads_for_empty(const flce_problem* p, void* dweight, void* dbias, cudaStream_t st) {
   const size_t bias_elem = p->bias_dtype == FLCE_F32 ? 4 : 2;
-  FLCE_TRY(fail(cudaMemsetAsync(dweight, 0, size_t(p->vocab) * p->hidden * weight_elem(p), st)));
+  if (dweight) FLCE_TRY(fail(cudaMemsetAsync(dweight, 0, size_t(p->vocab) * p->hidden * weight_elem(p), st)));
   if (dbias) FLCE_TRY(fail(cudaMemsetAsync(dbias, 0, size_t(p->vocab) * bias_elem, st)));
   return FLCE_OK;
 }

@@ -503,9 +503,9 @@ struct EpiGrad {
                        pack_bf16x2(g[16 * q + 10], g[16 * q + 11]), pack_bf16x2(g[16 * q + 12], g[16 * q + 13]),
                        pack_bf16x2(g[16 * q + 14], g[16 * q + 15]));
       }
-      if (kBias) epi_smem[warp * kBN + c * 32 + lane] = warp_column_sums(g);
+      if (kBias && p.dbias_part) epi_smem[warp * kBN + c * 32 + lane] = warp_column_sums(g);
     });
-    if (kBias) {
+    if (kBias && p.dbias_part) {  // (no destination with a frozen head: the bias is not trained)
       for (int c = nch; c < kBN / 32; ++c) epi_smem[warp * kBN + c * 32 + lane] = 0.f;
       epilogue_bar_sync(1 + grp);
       // A CTA-pair tile can have its second 128-row half entirely past the

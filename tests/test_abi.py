@@ -163,6 +163,28 @@ def test_keep_logits_workspace(lib):
         assert k < 4 * V * D  # in particular no fp32 dW accumulator
 
 
+def test_frozen_head_workspace(lib):
+    """A frozen head needs neither the fp32 dweight / dbias accumulators of the token-chunked
+    backward (4 V D + 4 V bytes with more than one chunk) nor the dbias partial sums of either
+    backward; the rest of the layout is the same, and the flag changes nothing for the forward."""
+    keep, rec, frozen = B.FLCE_FLAG_BWD_KEEP_LOGITS, B.FLCE_FLAG_BWD_RECOMPUTE, B.FLCE_FLAG_FROZEN_HEAD
+    for (N, D, V) in [(16384, 4096, 151936), (8192, 2048, 128256), (256, 2048, 248320), (700, 256, 3000)]:
+        ldz = (V + 31) // 32 * 32
+        info = B.FlceTestingPlanInfo()
+        assert lib.flce_testing_plan(ctypes.byref(_problem(n_tokens=N, hidden=D, vocab=V, flags=keep)), 2, 152,
+                                     ctypes.byref(info)) == B.FLCE_OK
+        nc, chunks = info.token_chunk_rows, info.n_chunks
+        k = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=keep), 2)[1]
+        kf = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=keep | frozen), 2)[1]
+        saved = 4 * ((nc + 31) // 32) * ldz + (4 * V * D + 4 * ldz if chunks > 1 else 0)
+        assert 0 <= (k - kf) - saved <= 3 * 256, (N, D, V, k - kf, saved)
+        r = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=rec), 1)[1]
+        rf = _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=rec | frozen), 1)[1]
+        assert rf < r
+        assert _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V, flags=frozen), 0) == \
+            _ws(lib, _problem(n_tokens=N, hidden=D, vocab=V), 0)
+
+
 def test_keep_logits_workspace_has_no_tokens_times_vocab_term(lib):
     """With a bias (its partial column sums are the one per-row-tile scratch), N swept from 512 to
     131072 at V = 262144: the kept-logits workspace stays within the 4 GiB logit budget, the fp32 dW
@@ -202,7 +224,7 @@ def test_keep_logits_workspace_has_no_tokens_times_vocab_term(lib):
     (dict(logit_scale=float("nan")), B.FLCE_ERR_INVALID_ARG),
     (dict(num_items_in_batch=-1.0), B.FLCE_ERR_INVALID_ARG),
     (dict(num_items_in_batch=float("inf")), B.FLCE_ERR_INVALID_ARG),
-    (dict(flags=16), B.FLCE_ERR_INVALID_ARG),
+    (dict(flags=32), B.FLCE_ERR_INVALID_ARG),
     (dict(flags=B.FLCE_FLAG_BWD_RECOMPUTE | B.FLCE_FLAG_BWD_KEEP_LOGITS), B.FLCE_ERR_INVALID_ARG),
     (dict(reserved=1), B.FLCE_ERR_INVALID_ARG),
 ])
@@ -246,6 +268,14 @@ def test_call_validation_without_gpu(lib):
     assert bwd(ctypes.byref(p), h, w, None, t, lse, nv, loss, dh, dw, db, wsp, wsb, None) == B.FLCE_ERR_INVALID_ARG
     assert bwd(ctypes.byref(p), h, w, None, t, lse, nv, loss, dh, dw, None, wsp, wsb - 1, None) \
         == B.FLCE_ERR_WORKSPACE_TOO_SMALL
+    # a frozen head takes no dweight / dbias, and every other problem needs dweight
+    pf = _problem(flags=B.FLCE_FLAG_FROZEN_HEAD)
+    _, wsf = _ws(lib, pf, 1)
+    assert bwd(ctypes.byref(pf), h, w, None, t, lse, nv, loss, dh, dw, None, wsp, wsf, None) == B.FLCE_ERR_INVALID_ARG
+    assert bwd(ctypes.byref(pf), h, w, b, t, lse, nv, loss, dh, None, db, wsp, wsf, None) == B.FLCE_ERR_INVALID_ARG
+    assert bwd(ctypes.byref(p), h, w, None, t, lse, nv, loss, dh, None, None, wsp, wsb, None) == B.FLCE_ERR_INVALID_ARG
+    assert bwd(ctypes.byref(pf), h, w, b, t, lse, nv, loss, dh, None, None, wsp, wsf - 1, None) \
+        == B.FLCE_ERR_WORKSPACE_TOO_SMALL  # past the argument checks: only the size is left
     assert lib.flce_read_device_status(None, None, None) == B.FLCE_ERR_INVALID_ARG
     assert lib.flce_testing_set_tuning(-1, 0) == B.FLCE_ERR_INVALID_ARG
     assert lib.flce_testing_set_tuning(0, 17) == B.FLCE_ERR_INVALID_ARG

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from linear_cross_entropy_tmem_gb300.synthetic import TINY, Workload, make_inputs
-from tests.parity import TOL_LSE, compare_backward, compare_forward, launch_kinds, run_gpu
+from tests.parity import TOL_GRAD, TOL_LSE, compare_backward, compare_forward, launch_kinds, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -750,6 +750,63 @@ def test_cuda_graph_capture_replays_bitwise(entry):
             assert torch.equal(outs[k], ref[k]), k
     ref_f = oracle.forward(h.cpu(), W.cpu(), b.cpu(), t.cpu(), **kw)
     assert abs(float(outs["loss"]) - ref_f["loss"]) <= 2e-3
+
+
+@pytest.mark.parametrize("entry", ["fused-keep", "fused-recompute", "separate"])
+@pytest.mark.parametrize("variant", ["bias-softcap", "fp32h-compact"])
+def test_frozen_head_forms_dhidden_only(entry, variant):
+    """FLCE_FLAG_FROZEN_HEAD (a head that is not trained, as in LoRA): no dweight / dbias product is
+    launched and none is written; the forward outputs and dhidden are the same bits as with the head
+    trained, and dhidden matches the oracle.  Kept logits in 256-token chunks with a ragged last one."""
+    import linear_cross_entropy_tmem_gb300 as F
+    from linear_cross_entropy_tmem_gb300.api import testing_set_token_chunk
+    testing_set_token_chunk(256)
+    if variant == "bias-softcap":
+        w = Workload("fz1", 700, 1280, 3000, sigma_w=0.05, bias=True, softcap=20.0, reduction="mean", seed=51)
+        compact = False
+    else:
+        w = Workload("fz2", 600, 1280, 2600, sigma_w=0.05, hidden_dtype=torch.float32, bias=True,
+                     logit_scale=0.5, reduction="none", ignore_every=3, seed=52)
+        compact = True
+    hc, Wc, bc, tc, dc = make_inputs(w, "cpu")
+    h, W, b, t, dloss = [x.cuda() for x in (hc, Wc, bc, tc, dc)]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction, compact=compact)
+
+    def run(frozen):
+        if entry == "separate":
+            f = F.flce_forward(h, W, t, b, entropy=True, **kw)
+            return f, F.flce_backward(h, W, t, f.lse, f.n_valid, dloss, b, frozen_head=frozen, **kw)
+        bwd = "keep_logits" if entry == "fused-keep" else "recompute"
+        return F.flce_forward_backward(h, W, t, dloss, b, entropy=True, bwd=bwd, frozen_head=frozen, **kw)
+
+    (ff, gf), kinds = launch_kinds(lambda: run(True))
+    assert "bwd_dweight" not in kinds and "bwd_dhidden" in kinds
+    assert gf[1] is None and gf[2] is None
+    fa, ga = run(False)
+    torch.cuda.synchronize()
+    for x, y in zip((ff.loss, ff.lse, ff.entropy, ff.correct, ff.n_valid, ff.entropy_sum, gf[0]),
+                    (fa.loss, fa.lse, fa.entropy, fa.correct, fa.n_valid, fa.entropy_sum, ga[0])):
+        assert torch.equal(x, y)
+    ref_b = oracle.backward(hc, Wc, bc, tc, dloss=dc, **{k: v for k, v in kw.items() if k != "compact"})
+    assert oracle.relative_frobenius(gf[0], ref_b["dh"]) <= TOL_GRAD
+
+
+def test_autograd_frozen_head():
+    """The autograd wrapper forms dhidden only when neither the weight nor the bias requires a
+    gradient: the hidden gradient is the same bits as with the head trained."""
+    import linear_cross_entropy_tmem_gb300 as F
+    w = Workload("fz3", 700, 1280, 3000, sigma_w=0.05, bias=True, softcap=10.0, reduction="mean", seed=53)
+    h, W, b, t, _ = [x.cuda() for x in make_inputs(w, "cpu")]
+    kw = dict(logit_scale=w.logit_scale, softcap=w.softcap, reduction="mean")
+    h1 = h.clone().requires_grad_(True)
+    loss1, *_ = F.linear_cross_entropy(h1, W, t, b, **kw)  # W and b do not require gradients
+    loss1.backward(torch.full((), 1.5, device="cuda"))
+    h2, W2, b2 = h.clone().requires_grad_(True), W.clone().requires_grad_(True), b.clone().requires_grad_(True)
+    loss2, *_ = F.linear_cross_entropy(h2, W2, t, b2, **kw)
+    loss2.backward(torch.full((), 1.5, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(loss1, loss2) and torch.equal(h1.grad, h2.grad)
+    assert W.grad is None and b.grad is None
 
 
 def test_back_to_back_calls_on_one_stream():
