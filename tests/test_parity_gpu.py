@@ -113,6 +113,29 @@ def test_empty_batch():
         assert dh.numel() == 0 and torch.all(dW == 0) and torch.all(db == 0)
 
 
+def test_frozen_head_edge_cases():
+    """A frozen head with an empty batch, a one-word vocabulary and an all-ignored batch, through
+    every entry point: dhidden is exactly zero and nothing else is written."""
+    import linear_cross_entropy_tmem_gb300 as F
+    for N, V, ignore_all in ((0, 300, False), (33, 1, False), (700, 3000, True)):
+        W = (0.05 * torch.randn(V, 1280, device="cuda")).to(torch.bfloat16)
+        b = (0.1 * torch.randn(V, device="cuda")).to(torch.bfloat16)
+        h = torch.randn(N, 1280, device="cuda").to(torch.bfloat16)
+        t = torch.full((N,), -100, dtype=torch.int64, device="cuda") if ignore_all else \
+            torch.randint(0, V, (N,), device="cuda")
+        up = torch.ones(1, device="cuda")
+        for bwd in ("keep_logits", "recompute"):
+            f, (dh, dW, db) = F.flce_forward_backward(h, W, t, up, b, bwd=bwd, frozen_head=True)
+            torch.cuda.synchronize()
+            assert F.flce_read_device_status(f.workspace) == 0
+            assert dW is None and db is None and abs(float(f.loss)) <= 1e-6  # V = 1: lse - z rounds to ~0
+            assert dh.shape == h.shape and int(torch.count_nonzero(dh)) == 0
+        f = F.flce_forward(h, W, t, b)
+        dh, dW, db = F.flce_backward(h, W, t, f.lse, f.n_valid, up, b, frozen_head=True)
+        torch.cuda.synchronize()
+        assert dW is None and db is None and int(torch.count_nonzero(dh)) == 0
+
+
 def test_out_of_range_target_sets_status_and_is_ignored():
     w = Workload("oor", 64, 64, 300, sigma_w=0.2, seed=10, ignore_every=0)
     h, W, b, t, dloss = make_inputs(w, "cpu")
