@@ -73,6 +73,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-grads", action="store_true",
                     help="the e2e leg also reads dhidden, dweight and dbias back to pinned host memory every step "
                          "(by default only the loss and the metrics return; the gradients stay on the device)")
+    ap.add_argument("--valid-frac", type=float, default=0.0,
+                    help="prompt-completion batches: only the last fraction of every 2048-token sequence has a "
+                         "target (the prompt before it is ignored); 0 keeps the workload's own ignore pattern")
     ap.add_argument("--frozen-head", action="store_true",
                     help="the head and bias are not trained (FLCE_FLAG_FROZEN_HEAD, as in LoRA training): the "
                          "backward forms dhidden only")
@@ -259,7 +262,7 @@ class Runner:
     """Preallocated buffers and raw C-ABI calls for one forward + backward step."""
 
     def __init__(self, w, device, seed_offset=0, compact=False, fused=False, bwd="auto", autograd=False,
-                 grad_in_forward=True, frozen_head=False):
+                 grad_in_forward=True, frozen_head=False, valid_frac=0.0):
         import torch
 
         import linear_cross_entropy_tmem_gb300.api as api
@@ -271,6 +274,9 @@ class Runner:
         self.device = device
         self.h, self.W, self.b, self.t, self.dloss = make_inputs(w.scaled(seed=w.seed + seed_offset), device)
         N, D, V = w.n_tokens, w.hidden, w.vocab
+        if valid_frac > 0.0:  # prompt-completion batches: each 2048-token sequence's prompt is ignored
+            pos = torch.arange(N, device=device) % 2048
+            self.t[pos < round((1.0 - valid_frac) * 2048)] = -100
         self.prob = api.make_problem(N, D, V, hidden_dtype=self.h.dtype, bias_dtype=torch.bfloat16,
                                      logit_scale=w.logit_scale, softcap=w.softcap, reduction=w.reduction,
                                      compact=compact, bwd=bwd, frozen_head=frozen_head)
@@ -443,7 +449,8 @@ def flce_arm(args):
     B.check(lib.flce_testing_set_tuning(0, args.dh_ksplit), "dh K splits")
     B.check(lib.flce_testing_set_token_chunk(args.token_chunk), "token chunk")  # before sizing the workspace
     run = Runner(w, device, seed_offset=rank, compact=args.compact, fused=not args.separate, bwd=args.bwd,
-                 autograd=args.autograd, grad_in_forward=not args.grad_in_backward, frozen_head=args.frozen_head)
+                 autograd=args.autograd, grad_in_forward=not args.grad_in_backward, frozen_head=args.frozen_head,
+                 valid_frac=args.valid_frac)
     if args.autograd:
         if args.compact:
             raise SystemExit("--autograd does not combine with --compact")
@@ -589,7 +596,7 @@ def flce_arm(args):
         # copy of step k+1's inputs (copy stream) runs during step k's compute, as a training
         # loop that prefetches its next batch would.
         runs = [run, Runner(w, device, seed_offset=rank, compact=args.compact, fused=not args.separate,
-                            bwd=args.bwd, frozen_head=args.frozen_head)]
+                            bwd=args.bwd, frozen_head=args.frozen_head, valid_frac=args.valid_frac)]
         host = {k: getattr(run, k).to("cpu").pin_memory() for k in ("h", "W", "t", "dloss")
                 if getattr(run, k) is not None}
         if run.b is not None:
@@ -676,6 +683,7 @@ def flce_arm(args):
                        "reduction": w.reduction, "parallelism": f"replicas x{world}" if world > 1 else "none",
                        "gemm_mode": ["auto", "single-cta", "cta-pair"][args.gemm_mode],
                        "compact_valid_tokens": bool(args.compact),
+                       "valid_tokens": None if args.autograd else int(run.n_valid.item()),
                        "entry": ("linear_cross_entropy + backward (autograd, gradients "
                                  + ("in the backward)" if args.grad_in_backward else "in the forward)"))
                        if args.autograd else
