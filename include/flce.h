@@ -49,6 +49,9 @@
  *     flce_read_device_status.
  *   - Results are deterministic: no floating-point atomics; every reduction
  *     runs in a fixed order.
+ *   - Host threads may call at once (on their own streams and workspaces): the
+ *     library's per-device caches are synchronised.  The flce_testing_* hooks
+ *     are process-wide switches and are not.
  *   - flce_forward, flce_backward and flce_forward_backward enqueue only
  *     kernels and asynchronous memsets, so a step built from them can be
  *     captured into a CUDA graph once the device's one-time set-up has run

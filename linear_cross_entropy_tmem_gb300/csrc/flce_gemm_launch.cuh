@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "flce_gemm.cuh"
 #include "flce_launch.h"
@@ -70,27 +71,30 @@ static cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, cudaStream_t
 }
 
 // CTA pairs of the pair kernel that can be resident at once on the current
-// device, one CTA per SM; cached per device.
+// device, one CTA per SM.  The kernel's shared-memory attribute is set on every
+// call (it belongs to the current context); the occupancy query is cached per
+// device, in atomics, so that host threads may call at once.
 template <class Epi>
 static cudaError_t resident_pairs(int num_sms, int* out) {
   auto kern = gemm_pair_kernel<Epi>;
-  static int resident[64] = {0};
+  static std::atomic<int> resident[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (resident[dev] == 0) {
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kGemmPairSmemBase + Epi::kTailBytes)) != cudaSuccess)
-      return e;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kGemmPairSmemBase + Epi::kTailBytes)) != cudaSuccess)
+    return e;
+  int n = resident[dev].load(std::memory_order_relaxed);
+  if (n == 0) {  // every thread that gets here computes the same value
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = cluster_config<Epi>(attr, nullptr, false);
     cfg.gridDim = dim3(2 * std::max(1, num_sms / 2));
-    int n = 0;
     if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
-    resident[dev] = std::max(1, n);
+    n = std::max(1, n);
+    resident[dev].store(n, std::memory_order_relaxed);
   }
-  *out = std::min(resident[dev], std::max(1, num_sms / 2));
+  *out = std::min(n, std::max(1, num_sms / 2));
   return cudaSuccess;
 }
 

@@ -832,6 +832,51 @@ def test_autograd_frozen_head():
     assert W.grad is None and b.grad is None
 
 
+def test_two_host_threads_at_once():
+    """Two host threads call the library at once, each on its own stream with its own problem (one
+    kept-logits, one recompute): every result is the same bits as the same call made alone."""
+    import threading
+
+    import linear_cross_entropy_tmem_gb300 as F
+    ws_ = [Workload("th1", 900, 1280, 3000, sigma_w=0.05, bias=True, softcap=15.0, seed=61),
+           Workload("th2", 500, 512, 5000, sigma_w=0.05, reduction="sum", seed=62)]
+    inputs = [[x.cuda() if x is not None else None for x in make_inputs(w, "cpu")] for w in ws_]
+
+    def call(i):
+        h, W, b, t, dloss = inputs[i]
+        w = ws_[i]
+        f, g = F.flce_forward_backward(h, W, t, dloss, b, entropy=True, logit_scale=w.logit_scale,
+                                       softcap=w.softcap, reduction=w.reduction)
+        return [f.loss, f.lse, f.entropy, f.correct, f.n_valid, f.entropy_sum, *[x for x in g if x is not None]]
+
+    alone = []
+    for i in range(2):
+        alone.append([x.clone() for x in call(i)])
+        torch.cuda.synchronize()
+    out, errors = [None, None], []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                res = [call(i) for _ in range(3)]
+            s.synchronize()
+            out[i] = res
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for i in range(2):
+        for res in out[i]:
+            for x, y in zip(res, alone[i]):
+                assert torch.equal(x, y), i
+
+
 def test_back_to_back_calls_on_one_stream():
     """The GEMMs are launched as programmatic dependents (they set up while the kernel before them
     finishes, and wait for its results before touching global memory).  Calls of different shapes
